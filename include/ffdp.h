@@ -1,0 +1,186 @@
+/*
+ * ffdp.h -- C ABI of libffdp: the fused registration objective of FFDP on one
+ * GPU (sm_103a).
+ *
+ * Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
+ * Registration" (ICLR 2026).  The entry points follow its "Key designs":
+ *   item 1  fused_grid_sampler(I; A, t, [u], S, x_bounds)(x) = I(Ax + t + Su(x)),
+ *           coordinates computed in registers, identity grid implicit in
+ *           x_bounds, backward pass to u, A and t;
+ *   item 2  Mattes mutual information with an implicit Parzen window (the
+ *           B x N Parzen block is never formed; histogram entries and partial
+ *           gradients accumulate in shared memory) and fused LNCC;
+ *   "Background"  the objective L = C(F, M o phi) with phi(x) = Ax + t + u(x).
+ *
+ * Conventions shared by every call
+ *   Volumes are [D][H][W] (W fastest).  Coordinates follow the PyTorch
+ *   grid_sample convention: normalised [-1, 1], align_corners = true, vector
+ *   components in (x, y, z) = (W, H, D) order.  Trilinear samples read 0 for
+ *   taps outside the moving image.  The identity-grid coordinate of fixed
+ *   voxel i along axis c is x_min[c] + (x_max[c] - x_min[c]) * i_c / (n_c - 1).
+ *   A displacement u is [D][H][W][3] float32 in normalised units of M.
+ *
+ *   Memory: every pointer named F, M, J, u, gJ, du, dJ, dA, dt, loss, ws is a
+ *   DEVICE pointer owned by the caller; the library never allocates or frees
+ *   device memory.  ffdp_transform and the *_params structs are HOST structs
+ *   read during the call.  Float and half volumes and u/du/J/dJ must be 16-byte
+ *   aligned (FFDP_ERR_INVALID_ARGUMENT otherwise).  Outputs are overwritten,
+ *   never accumulated into.
+ *
+ *   Streams: every call only enqueues work on `stream` (a cudaStream_t passed
+ *   as void*, NULL = legacy default stream) and returns; results are ready
+ *   when the stream is.  Calls on different streams may run concurrently if
+ *   their workspaces and outputs are distinct.
+ *
+ *   Errors: arguments are validated on the host before anything is enqueued;
+ *   a rejected call returns a non-zero status, launches nothing and writes
+ *   nothing.  FFDP_ERR_CUDA reports a failed launch (ffdp_last_error() holds
+ *   the CUDA message).  No exception crosses this interface.  No call blocks
+ *   on the device.
+ *
+ *   Limits: each dimension in [2, 2^20]; D*H*W < 2^32 voxels; bins in [8, 64];
+ *   LNCC window odd in [3, 9].
+ */
+#ifndef FFDP_H
+#define FFDP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FFDP_OK = 0,
+  FFDP_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size or parameter */
+  FFDP_ERR_UNSUPPORTED = 2,      /* valid request outside the built limits */
+  FFDP_ERR_WORKSPACE = 3,        /* workspace missing or smaller than ffdp_workspace_bytes */
+  FFDP_ERR_CUDA = 4,             /* a CUDA launch or query failed */
+  FFDP_ERR_INTERNAL = 5
+} ffdp_status;
+
+typedef enum { FFDP_F32 = 0, FFDP_F16 = 1 } ffdp_dtype;
+
+typedef struct { int64_t d, h, w; } ffdp_dims;
+
+/* Host struct.  A and S row-major 3x3 with rows/columns in (x, y, z) order;
+ * xmin/xmax are the normalised coordinates of the first and last fixed voxel
+ * per axis (x_bounds; (-1, 1) for the whole moving domain). */
+typedef struct {
+  float A[9];
+  float t[3];
+  float S[9];
+  float xmin[3];
+  float xmax[3];
+} ffdp_transform;
+
+/* Parzen-window MI.  bins in [8, 64].  Intensities map to bin coordinates
+ * c = 2 + (clamp(v, lo, hi) - lo) / (hi - lo) * (bins - 5) with the cubic
+ * B-spline kernel; f_* is the fixed image's range, m_* the moving image's
+ * (i.e. J's).  hi > lo required. */
+typedef struct {
+  int bins;
+  float f_lo, f_hi, m_lo, m_hi;
+} ffdp_mi_params;
+
+/* LNCC: odd window in [3, 9]; cc = cross^2 / (varF varJ + eps) with
+ * zero-padded window sums and divisor window^3. */
+typedef struct {
+  int window;
+  float eps;
+} ffdp_lncc_params;
+
+/* Objective L = w_mi * (-MI) + w_lncc * (-LNCC).  A weight of 0 disables (does
+ * not evaluate) that term; at least one weight must be non-zero. */
+typedef struct {
+  float w_mi, w_lncc;
+  ffdp_mi_params mi;
+  ffdp_lncc_params lncc;
+} ffdp_objective_params;
+
+/* Operation codes for ffdp_workspace_bytes. */
+enum {
+  FFDP_OP_GRID_SAMPLE_BWD = 1, /* params: NULL */
+  FFDP_OP_MI = 2,              /* params: const ffdp_mi_params* */
+  FFDP_OP_LNCC = 3,            /* params: const ffdp_lncc_params* */
+  FFDP_OP_OBJECTIVE = 4        /* params: const ffdp_objective_params* */
+};
+
+/* Bytes of device workspace a call of `op` on fixed grid `fixed` needs (0 for
+ * an invalid request).  MI and the sampler need O(bins^2 + #SMs) bytes,
+ * independent of the volume size.  An objective with LNCC enabled also holds
+ * the warped image J (4 bytes per voxel) so that window sums can read their
+ * halo instead of re-sampling it; the paper's fused LNCC keeps five such
+ * intermediates.  Queries the current device's SM count. */
+size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void *params);
+
+/* Design 1, forward: J[i] = M(A x_i + t + S u_i) for every fixed voxel i.
+ * M: [md] volume of dtype mt; u: [out_dims][3] float32 or NULL (u = 0);
+ * J_out: [out_dims] float32.  No workspace. */
+ffdp_status ffdp_grid_sample_fwd(const void *M, ffdp_dtype mt, ffdp_dims mdims, ffdp_dims out_dims,
+                                 const float *u, const ffdp_transform *T, float *J_out,
+                                 void *stream);
+
+/* Design 1, backward: given gJ = dL/dJ ([out_dims] float32),
+ *   du_i = S^T (gJ_i dJ/dp_i),  dA = sum_i gJ_i dJ/dp_i x_i^T,  dt = sum_i gJ_i dJ/dp_i,
+ * where p = A x + t + S u.  du ([out_dims][3]), dA (9, row-major) and dt (3)
+ * are float32 device outputs; each may be NULL to skip it.  Workspace:
+ * ffdp_workspace_bytes(FFDP_OP_GRID_SAMPLE_BWD, out_dims, NULL). */
+ffdp_status ffdp_grid_sample_bwd(const void *M, ffdp_dtype mt, ffdp_dims mdims, ffdp_dims out_dims,
+                                 const float *u, const ffdp_transform *T, const float *gJ,
+                                 float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
+                                 void *stream);
+
+/* Design 2, MI on a materialised J: loss[0] = -MI(F, J); dJ = d(-MI)/dJ
+ * ([dims] float32, may be NULL).  F has dtype ft; J is float32. */
+ffdp_status ffdp_mi_fwd_bwd(const void *F, ffdp_dtype ft, const float *J, ffdp_dims dims,
+                            const ffdp_mi_params *p, float *loss, float *dJ, void *ws,
+                            size_t ws_bytes, void *stream);
+
+/* Design 2, LNCC on a materialised J: loss[0] = -LNCC(F, J); dJ = d(-LNCC)/dJ
+ * ([dims] float32, may be NULL). */
+ffdp_status ffdp_lncc_fwd_bwd(const void *F, ffdp_dtype ft, const float *J, ffdp_dims dims,
+                              const ffdp_lncc_params *p, float *loss, float *dJ, void *ws,
+                              size_t ws_bytes, void *stream);
+
+/* The fused objective: J = M(Ax + t + Su) is never stored for MI; the
+ * histogram sweep, the MI table, the LNCC window sums and the sampler
+ * backward run as one pipeline on `stream`.
+ *   loss[3] (device float32) = { w_mi*(-MI) + w_lncc*(-LNCC), -MI, -LNCC }
+ *   (a disabled term reports 0);  du [fdims][3], dA[9], dt[3] as in
+ *   ffdp_grid_sample_bwd (each may be NULL).  F: [fdims] of dtype ft;
+ *   M: [mdims] of dtype mt. */
+ffdp_status ffdp_objective(const void *F, ffdp_dtype ft, ffdp_dims fdims, const void *M,
+                           ffdp_dtype mt, ffdp_dims mdims, const float *u,
+                           const ffdp_transform *T, const ffdp_objective_params *p, float *loss,
+                           float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/* Human-readable name of a status. */
+const char *ffdp_status_string(ffdp_status s);
+
+/* Detail of the last failed call on this host thread ("" if none). */
+const char *ffdp_last_error(void);
+
+/* ---- instrumentation (not part of the method) -------------------------
+ * Kernel launch accounting for benchmarks: every kernel the library enqueues
+ * increments a process-wide counter; when timing is enabled the library also
+ * records a CUDA event pair around each launch, on the launch's own stream,
+ * so per-kernel device time can be read back afterwards. */
+uint64_t ffdp_launch_count(void);
+/* Enable (capacity > 0: number of launches to record) or disable (0) event
+ * timing.  Enabling resets previous records.  Not thread-safe with
+ * concurrent library calls. */
+ffdp_status ffdp_timing_enable(int capacity);
+/* Synchronises the recorded events and writes, for up to `max` kernels in
+ * first-launch order: a NUL-terminated name (names[k*64 ... k*64+63]), the
+ * number of launches and the summed device milliseconds.  Returns the number
+ * of distinct kernels (may exceed max). */
+int ffdp_timing_read(char *names, int *counts, double *ms, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FFDP_H */

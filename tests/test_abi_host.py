@@ -1,0 +1,112 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for
+sm_103a, loads, exports every entry point include/ffdp.h declares, and
+rejects invalid arguments with a status before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ffdp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from voxel_grid_sampler_gb300 import build, ffdp
+    build.build()
+    return ffdp.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ffdp_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "ffdp_objective" in names and "ffdp_grid_sample_fwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    from voxel_grid_sampler_gb300 import ffdp
+    for code, name in ffdp.STATUS.items():
+        assert lib.ffdp_status_string(code).decode() == name
+
+
+# The calls below only ever pass arguments that validation rejects; they are
+# skipped where a GPU is present (the GPU suite exercises real calls there).
+nogpu = pytest.mark.skipif(torch.cuda.is_available(), reason="host-only validation checks")
+
+
+@nogpu
+def test_invalid_arguments_are_rejected_before_launch(lib):
+    from voxel_grid_sampler_gb300 import ffdp
+    n0 = lib.ffdp_launch_count()
+    T = ffdp.transform()
+    good = ffdp.dims_of((8, 8, 8))
+    fake = ctypes.c_void_p(0x1000)       # never dereferenced: every call below is invalid
+    odd = ctypes.c_void_p(0x1004)        # misaligned
+    P = ffdp.objective_params(1.0, 1.0, 32, (0, 1), (0, 1), 5)
+    ws = ctypes.c_void_p(0x2000)
+    st = lib.ffdp_objective(None, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(P), fake,
+                            fake, fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    st = lib.ffdp_objective(odd, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(P), fake,
+                            fake, fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    st = lib.ffdp_grid_sample_fwd(fake, 0, good, ffdp.dims_of((1, 8, 8)), None, ctypes.byref(T), fake, None)
+    assert st == 1
+    st = lib.ffdp_grid_sample_fwd(fake, 7, good, good, None, ctypes.byref(T), fake, None)
+    assert st == 1
+    bad = ffdp.objective_params(1.0, 0.0, 65, (0, 1), (0, 1), 5)
+    st = lib.ffdp_objective(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(bad), fake,
+                            fake, fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    bad = ffdp.objective_params(0.0, 1.0, 32, (0, 1), (0, 1), 4)
+    st = lib.ffdp_objective(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(bad), fake,
+                            fake, fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    bad = ffdp.objective_params(1.0, 0.0, 32, (1, 1), (0, 1), 5)
+    st = lib.ffdp_objective(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(bad), fake,
+                            fake, fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    zero = ffdp.objective_params(0.0, 0.0, 32, (0, 1), (0, 1), 5)
+    st = lib.ffdp_objective(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(zero), fake,
+                            fake, fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    # workspace too small / missing
+    st = lib.ffdp_objective(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(P), fake,
+                            fake, fake, fake, ws, 16, None)
+    assert st == 3
+    st = lib.ffdp_objective(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), ctypes.byref(P), fake,
+                            fake, fake, fake, None, 0, None)
+    assert st == 3
+    mp = ffdp.mi_params(32, (0, 1), (2, 1))
+    st = lib.ffdp_mi_fwd_bwd(fake, 0, fake, good, ctypes.byref(mp), fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    lp = ffdp.lncc_params(11)
+    st = lib.ffdp_lncc_fwd_bwd(fake, 0, fake, good, ctypes.byref(lp), fake, fake, ws, 1 << 30, None)
+    assert st == 1
+    assert lib.ffdp_launch_count() == n0
+    assert len(lib.ffdp_last_error()) > 0
+
+
+def test_workspace_is_o1_for_mi_and_sampler(lib):
+    from voxel_grid_sampler_gb300 import ffdp
+    p = ffdp.mi_params(64, (0, 1), (0, 1))
+    small = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_MI, (16, 16, 16), p)
+    large = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_MI, (1024, 1024, 1024), p)
+    assert small == large > 0
+    a = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_GRID_SAMPLE_BWD, (16, 16, 16))
+    b = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_GRID_SAMPLE_BWD, (1024, 1024, 1024))
+    assert a == b > 0
+    # with LNCC the objective keeps J (4 bytes per voxel)
+    q = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 5)
+    c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (64, 64, 64), q)
+    assert c >= 4 * 64 ** 3
+    assert ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (1, 64, 64), q) == 0

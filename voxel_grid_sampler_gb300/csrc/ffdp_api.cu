@@ -1,0 +1,658 @@
+// ffdp_api.cu -- the C ABI of libffdp (declared in include/ffdp.h): argument
+// validation, transform pre-computation, workspace layout and the launch
+// pipeline of each entry point.
+//
+// Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
+// Registration", Key designs items 1 (fused_grid_sampler(I; A, t, [u], S,
+// x_bounds)) and 2 (implicit-Parzen MI, fused LNCC); "Background" for the
+// objective L = C(F, M o phi), phi(x) = Ax + t + u(x).
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/ffdp.h"
+#include "ffdp_internal.h"
+
+using namespace ffdp;
+
+// ------------------------------------------------------------ error detail
+static thread_local char g_err[512] = "";
+
+static ffdp_status fail(ffdp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+static ffdp_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(FFDP_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+extern "C" const char* ffdp_last_error(void) { return g_err; }
+
+extern "C" const char* ffdp_status_string(ffdp_status s) {
+  switch (s) {
+    case FFDP_OK: return "FFDP_OK";
+    case FFDP_ERR_INVALID_ARGUMENT: return "FFDP_ERR_INVALID_ARGUMENT";
+    case FFDP_ERR_UNSUPPORTED: return "FFDP_ERR_UNSUPPORTED";
+    case FFDP_ERR_WORKSPACE: return "FFDP_ERR_WORKSPACE";
+    case FFDP_ERR_CUDA: return "FFDP_ERR_CUDA";
+    case FFDP_ERR_INTERNAL: return "FFDP_ERR_INTERNAL";
+  }
+  return "FFDP_ERR_UNKNOWN";
+}
+
+// -------------------------------------------------- launch accounting
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+struct TimingRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_tmu;
+std::vector<cudaEvent_t> g_events;  // pool, 2 per record
+std::vector<TimingRec> g_recs;
+int g_cap = 0;
+thread_local int g_open = -1;  // record index opened by note_launch_begin
+}  // namespace
+
+void ffdp::note_launch_begin(const char* name, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  g_open = -1;
+  if (g_cap == 0) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  const int i = (int)g_recs.size();
+  if (i >= g_cap) return;
+  TimingRec r{name, g_events[2 * i], g_events[2 * i + 1]};
+  cudaEventRecord(r.a, s);
+  g_recs.push_back(r);
+  g_open = i;
+}
+
+void ffdp::note_launch_end(cudaStream_t s) {
+  if (g_open < 0) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  cudaEventRecord(g_recs[g_open].b, s);
+  g_open = -1;
+}
+
+extern "C" uint64_t ffdp_launch_count(void) { return g_launches.load(); }
+
+extern "C" ffdp_status ffdp_timing_enable(int capacity) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  g_recs.clear();
+  if (capacity < 0) return fail(FFDP_ERR_INVALID_ARGUMENT, "timing capacity < 0");
+  const size_t need = 2 * (size_t)capacity;
+  while (g_events.size() < need) {
+    cudaEvent_t e;
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaEventCreate");
+    g_events.push_back(e);
+  }
+  g_cap = capacity;
+  return FFDP_OK;
+}
+
+extern "C" int ffdp_timing_read(char* names, int* counts, double* ms, int max) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  std::vector<std::string> keys;
+  std::vector<int> cnt;
+  std::vector<double> tot;
+  for (const TimingRec& r : g_recs) {
+    cudaEventSynchronize(r.b);
+    float t = 0.0f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) t = 0.0f;
+    size_t k = 0;
+    while (k < keys.size() && keys[k] != r.name) ++k;
+    if (k == keys.size()) {
+      keys.push_back(r.name);
+      cnt.push_back(0);
+      tot.push_back(0.0);
+    }
+    cnt[k] += 1;
+    tot[k] += t;
+  }
+  for (size_t k = 0; k < keys.size() && (int)k < max; ++k) {
+    if (names) {
+      std::strncpy(names + 64 * k, keys[k].c_str(), 63);
+      names[64 * k + 63] = '\0';
+    }
+    if (counts) counts[k] = cnt[k];
+    if (ms) ms[k] = tot[k];
+  }
+  return (int)keys.size();
+}
+
+// --------------------------------------------------------- helpers
+namespace {
+
+constexpr int64_t kMaxDim = 1 << 20;
+constexpr uint64_t kMaxVoxels = (1ull << 32) - (1ull << 16);
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+ffdp_status check_dims(ffdp_dims d, const char* what) {
+  if (d.d < 2 || d.h < 2 || d.w < 2)
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "%s dims must be >= 2 (got %lld x %lld x %lld)", what,
+                (long long)d.d, (long long)d.h, (long long)d.w);
+  if (d.d > kMaxDim || d.h > kMaxDim || d.w > kMaxDim)
+    return fail(FFDP_ERR_UNSUPPORTED, "%s dims above 2^20", what);
+  if ((uint64_t)d.d * (uint64_t)d.h * (uint64_t)d.w > kMaxVoxels)
+    return fail(FFDP_ERR_UNSUPPORTED, "%s has more than 2^32 - 2^16 voxels", what);
+  return FFDP_OK;
+}
+
+ffdp_status check_dtype(ffdp_dtype t, const char* what) {
+  if (t != FFDP_F32 && t != FFDP_F16) return fail(FFDP_ERR_INVALID_ARGUMENT, "%s dtype must be F32 or F16", what);
+  return FFDP_OK;
+}
+
+uint64_t nvox(ffdp_dims d) { return (uint64_t)d.d * (uint64_t)d.h * (uint64_t)d.w; }
+
+// magic numbers for fast_div (round-up method): s = ceil(log2 d),
+// m = floor(2^32 (2^s - d) / d) + 1, q = (umulhi(n, m) + n) >> s.
+void fast_div_magic(uint32_t d, unsigned& m, int& s) {
+  int l = 0;
+  while ((1ull << l) < d) ++l;
+  const unsigned __int128 num = ((unsigned __int128)1 << 32) * (((unsigned __int128)1 << l) - d);
+  m = (unsigned)(num / d + 1);
+  s = l;
+}
+
+ffdp_status make_geom(ffdp_dims f, ffdp_dims m, const ffdp_transform* T, Geom& g) {
+  const double nf[3] = {(double)f.w, (double)f.h, (double)f.d};
+  const double nm[3] = {(double)m.w, (double)m.h, (double)m.d};
+  for (int k = 0; k < 9; ++k)
+    if (!std::isfinite(T->A[k]) || !std::isfinite(T->S[k]))
+      return fail(FFDP_ERR_INVALID_ARGUMENT, "non-finite A or S");
+  for (int k = 0; k < 3; ++k)
+    if (!std::isfinite(T->t[k]) || !std::isfinite(T->xmin[k]) || !std::isfinite(T->xmax[k]))
+      return fail(FFDP_ERR_INVALID_ARGUMENT, "non-finite t or x_bounds");
+  double dx[3], hM[3];
+  for (int c = 0; c < 3; ++c) {
+    dx[c] = ((double)T->xmax[c] - (double)T->xmin[c]) / (nf[c] - 1.0);
+    hM[c] = (nm[c] - 1.0) / 2.0;
+  }
+  const double two32 = 4294967296.0;
+  for (int r = 0; r < 3; ++r) {
+    double g0 = (double)T->t[r] + 1.0;
+    for (int c = 0; c < 3; ++c) {
+      const double G = hM[r] * (double)T->A[r * 3 + c] * dx[c];
+      if (std::fabs(G) > 1048576.0) return fail(FFDP_ERR_UNSUPPORTED, "affine scale too large");
+      g.Gq[r * 3 + c] = (long long)llround(G * two32);
+      g0 += (double)T->A[r * 3 + c] * (double)T->xmin[c];
+      g.K[r * 3 + c] = (float)(hM[r] * (double)T->S[r * 3 + c]);
+    }
+    g0 *= hM[r];
+    if (std::fabs(g0) > 268435456.0) return fail(FFDP_ERR_UNSUPPORTED, "translation too large");
+    g.g0q[r] = (long long)llround(g0 * two32);
+    g.hM[r] = (float)hM[r];
+    g.ctr[r] = (float)((nf[r] - 1.0) / 2.0);
+  }
+  g.k_diag = (T->S[1] == 0.f && T->S[2] == 0.f && T->S[3] == 0.f && T->S[5] == 0.f && T->S[6] == 0.f &&
+              T->S[7] == 0.f)
+                 ? 1
+                 : 0;
+  g.fW = (int)f.w;
+  g.fH = (int)f.h;
+  g.fD = (int)f.d;
+  g.mW = (int)m.w;
+  g.mH = (int)m.h;
+  g.mD = (int)m.d;
+  g.mHW = (long long)m.w * m.h;
+  g.N = (unsigned)nvox(f);
+  fast_div_magic((uint32_t)f.w, g.divW_m, g.divW_s);
+  fast_div_magic((uint32_t)(f.w * f.h), g.divHW_m, g.divHW_s);
+  return FFDP_OK;
+}
+
+// Extents only (for ops without a sampler).
+void make_grid_only(ffdp_dims f, Geom& g) {
+  std::memset(&g, 0, sizeof(g));
+  g.fW = (int)f.w;
+  g.fH = (int)f.h;
+  g.fD = (int)f.d;
+  g.N = (unsigned)nvox(f);
+  fast_div_magic((uint32_t)f.w, g.divW_m, g.divW_s);
+  fast_div_magic((uint32_t)(f.w * f.h), g.divHW_m, g.divHW_s);
+}
+
+ffdp_status check_mi(const ffdp_mi_params* p) {
+  if (!p) return fail(FFDP_ERR_INVALID_ARGUMENT, "null MI params");
+  if (p->bins < 8 || p->bins > 64) return fail(FFDP_ERR_INVALID_ARGUMENT, "bins must be in [8, 64]");
+  if (!std::isfinite(p->f_lo) || !std::isfinite(p->f_hi) || !(p->f_hi > p->f_lo))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "fixed intensity range needs finite f_lo < f_hi");
+  if (!std::isfinite(p->m_lo) || !std::isfinite(p->m_hi) || !(p->m_hi > p->m_lo))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "moving intensity range needs finite m_lo < m_hi");
+  return FFDP_OK;
+}
+
+ffdp_status check_lncc(const ffdp_lncc_params* p) {
+  if (!p) return fail(FFDP_ERR_INVALID_ARGUMENT, "null LNCC params");
+  if (p->window < 3 || p->window > 9 || (p->window & 1) == 0)
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "window must be odd in [3, 9]");
+  if (!std::isfinite(p->eps) || p->eps < 0.0f) return fail(FFDP_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
+  return FFDP_OK;
+}
+
+BinMap bin_map(float lo, float hi, int B) {
+  BinMap m;
+  const double sc = (double)(B - 5) / ((double)hi - (double)lo);
+  m.lo = lo;
+  m.hi = hi;
+  m.sc = (float)sc;
+  m.off = (float)(2.0 - (double)lo * sc);
+  return m;
+}
+
+int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
+
+// Workspace layout (byte offsets, 256-aligned).
+struct Ws {
+  size_t hist, table, scalars, partials, J, total;
+};
+
+size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
+  Ws w;
+  size_t o = 0;
+  w.hist = o;
+  if (mi) o = al(o + (size_t)bmax * bmax * sizeof(unsigned long long));
+  w.table = o;
+  if (mi) o = al(o + (size_t)bmax * bmax * 4 * sizeof(float));
+  w.scalars = o;
+  o = al(o + 16 * sizeof(double));
+  w.partials = o;
+  o = al(o + max_parts * kPartialStride * sizeof(double));
+  w.J = o;
+  if (needJ) o = al(o + (size_t)N * sizeof(float));
+  w.total = o;
+  return w;
+}
+
+size_t max_parts() { return (size_t)(sm_count() > 0 ? sm_count() : 1) * kMaxCtasPerSm; }
+
+ffdp_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (need == 0) return FFDP_OK;
+  if (!ws) return fail(FFDP_ERR_WORKSPACE, "workspace of %zu bytes required, got NULL", need);
+  if (ws_bytes < need) return fail(FFDP_ERR_WORKSPACE, "workspace of %zu bytes required, got %zu", need, ws_bytes);
+  if (!aligned16(ws)) return fail(FFDP_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+  return FFDP_OK;
+}
+
+int persistent_grid(unsigned nIter, int per_sm) {
+  long long g = (long long)sm_count() * per_sm;
+  if (g < 1) g = 1;
+  if ((long long)nIter < g) g = nIter;
+  return (int)(g < 1 ? 1 : g);
+}
+
+unsigned n_iter(uint64_t N) { return (unsigned)((N + (uint64_t)(kThreads * kVPT) - 1) / (kThreads * kVPT)); }
+
+#define FFDP_TRY(x)                    \
+  do {                                 \
+    ffdp_status _st = (x);             \
+    if (_st != FFDP_OK) return _st;    \
+  } while (0)
+
+#define FFDP_CUDA(x, where)                          \
+  do {                                               \
+    cudaError_t _e = (x);                            \
+    if (_e != cudaSuccess) return cuda_fail(_e, where); \
+  } while (0)
+
+// LNCC tiling for a fixed grid: persistent CTAs over (32 x TY) columns x z-chunks.
+void lncc_tiling(ffdp_dims f, int R, LnccArgs& a, int per_sm, int& grid) {
+  const int TY = R <= 2 ? 16 : 8;
+  a.tilesX = (int)((f.w + kLnccTX - 1) / kLnccTX);
+  a.tilesY = (int)((f.h + TY - 1) / TY);
+  const long long cols = (long long)a.tilesX * a.tilesY;
+  const long long slots = (long long)sm_count() * per_sm;
+  // z chunks: enough tiles to fill every resident CTA twice, >= 32 planes each
+  int tz = (int)f.d;
+  while (cols * ((f.d + tz - 1) / tz) < 2 * slots && tz > 32) tz = (tz + 1) / 2;
+  a.tz = tz;
+  const long long ntiles = cols * ((f.d + tz - 1) / tz);
+  grid = (int)(ntiles < slots ? ntiles : slots);
+  if (grid < 1) grid = 1;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- ABI
+extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* params) {
+  if (check_dims(fixed, "fixed") != FFDP_OK) return 0;
+  const uint64_t N = nvox(fixed);
+  switch (op) {
+    case FFDP_OP_GRID_SAMPLE_BWD:
+      return ws_layout(false, 32, max_parts(), false, N).total;
+    case FFDP_OP_MI: {
+      const ffdp_mi_params* p = static_cast<const ffdp_mi_params*>(params);
+      if (check_mi(p) != FFDP_OK) return 0;
+      return ws_layout(true, bmax_of(p->bins), max_parts(), false, N).total;
+    }
+    case FFDP_OP_LNCC: {
+      const ffdp_lncc_params* p = static_cast<const ffdp_lncc_params*>(params);
+      if (check_lncc(p) != FFDP_OK) return 0;
+      return ws_layout(false, 32, max_parts(), false, N).total;
+    }
+    case FFDP_OP_OBJECTIVE: {
+      const ffdp_objective_params* p = static_cast<const ffdp_objective_params*>(params);
+      if (!p) return 0;
+      const bool mi = p->w_mi != 0.0f, ln = p->w_lncc != 0.0f;
+      if (mi && check_mi(&p->mi) != FFDP_OK) return 0;
+      if (ln && check_lncc(&p->lncc) != FFDP_OK) return 0;
+      return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln, N).total;
+    }
+  }
+  return 0;
+}
+
+extern "C" ffdp_status ffdp_grid_sample_fwd(const void* M, ffdp_dtype mt, ffdp_dims mdims, ffdp_dims out_dims,
+                                            const float* u, const ffdp_transform* T, float* J_out,
+                                            void* stream) {
+  g_err[0] = '\0';
+  if (!M || !T || !J_out) return fail(FFDP_ERR_INVALID_ARGUMENT, "null M, T or J_out");
+  FFDP_TRY(check_dtype(mt, "M"));
+  FFDP_TRY(check_dims(mdims, "moving"));
+  FFDP_TRY(check_dims(out_dims, "output"));
+  if (!aligned16(J_out) || (u && !aligned16(u))) return fail(FFDP_ERR_INVALID_ARGUMENT, "J_out and u must be 16-byte aligned");
+  Sweep1Args a{};
+  FFDP_TRY(make_geom(out_dims, mdims, T, a.g));
+  a.M = M;
+  a.u = u;
+  a.Jout = J_out;
+  a.nIter = n_iter(a.g.N);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = persistent_grid(a.nIter, sweep1_ctas_per_sm(S1_WRITEJ, 0, mt, 32));
+  FFDP_CUDA(launch_sweep1(S1_WRITEJ, 0, mt, 32, a, grid, s), "grid_sample_fwd launch");
+  return FFDP_OK;
+}
+
+extern "C" ffdp_status ffdp_grid_sample_bwd(const void* M, ffdp_dtype mt, ffdp_dims mdims, ffdp_dims out_dims,
+                                            const float* u, const ffdp_transform* T, const float* gJ,
+                                            float* du, float* dA, float* dt, void* ws, size_t ws_bytes,
+                                            void* stream) {
+  g_err[0] = '\0';
+  if (!M || !T || !gJ) return fail(FFDP_ERR_INVALID_ARGUMENT, "null M, T or gJ");
+  FFDP_TRY(check_dtype(mt, "M"));
+  FFDP_TRY(check_dims(mdims, "moving"));
+  FFDP_TRY(check_dims(out_dims, "output"));
+  if ((u && !aligned16(u)) || !aligned16(gJ) || (du && !aligned16(du)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "u, gJ and du must be 16-byte aligned");
+  const Ws w = ws_layout(false, 32, max_parts(), false, nvox(out_dims));
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  Sweep2Args a{};
+  FFDP_TRY(make_geom(out_dims, mdims, T, a.g));
+  a.M = M;
+  a.u = u;
+  a.gbuf = gJ;
+  a.du = du;
+  a.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
+  a.nIter = n_iter(a.g.N);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int grid = persistent_grid(a.nIter, sweep2_ctas_per_sm(S2_GBUF, 0, mt, 32));
+  FFDP_CUDA(launch_sweep2(S2_GBUF, 0, mt, 32, a, grid, s), "grid_sample_bwd launch");
+  if (dA || dt) {
+    FinishArgs f{};
+    f.partials = a.partials;
+    f.nparts = grid;
+    f.dA = dA;
+    f.dt = dt;
+    f.has_affine = 1;
+    for (int c = 0; c < 3; ++c) {
+      const double nf = c == 0 ? (double)out_dims.w : (c == 1 ? (double)out_dims.h : (double)out_dims.d);
+      const double nmv = c == 0 ? (double)mdims.w : (c == 1 ? (double)mdims.h : (double)mdims.d);
+      f.hM[c] = (nmv - 1.0) / 2.0;
+      f.dx[c] = ((double)T->xmax[c] - (double)T->xmin[c]) / (nf - 1.0);
+      f.xc[c] = (double)T->xmin[c] + f.dx[c] * (nf - 1.0) / 2.0;
+    }
+    FFDP_CUDA(launch_finish(f, s), "finish launch");
+  }
+  return FFDP_OK;
+}
+
+extern "C" ffdp_status ffdp_mi_fwd_bwd(const void* F, ffdp_dtype ft, const float* J, ffdp_dims dims,
+                                       const ffdp_mi_params* p, float* loss, float* dJ, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!F || !J || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null F, J or loss");
+  FFDP_TRY(check_dtype(ft, "F"));
+  FFDP_TRY(check_dims(dims, "image"));
+  FFDP_TRY(check_mi(p));
+  if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
+  const int bmax = bmax_of(p->bins);
+  const Ws w = ws_layout(true, bmax, max_parts(), false, nvox(dims));
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  char* wb = static_cast<char*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Geom g;
+  make_grid_only(dims, g);
+  unsigned long long* hist = reinterpret_cast<unsigned long long*>(wb + w.hist);
+  FFDP_CUDA(launch_zero_u64(hist, bmax * bmax, s), "zero launch");
+  Sweep1Args a1{};
+  a1.g = g;
+  a1.F = F;
+  a1.Jin = J;
+  a1.ghist = hist;
+  a1.bf = bin_map(p->f_lo, p->f_hi, p->bins);
+  a1.bj = bin_map(p->m_lo, p->m_hi, p->bins);
+  a1.B = p->bins;
+  a1.nIter = n_iter(g.N);
+  FFDP_CUDA(launch_sweep1(S1_HIST_JBUF, ft, 0, bmax,
+                          a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(S1_HIST_JBUF, ft, 0, bmax)), s),
+            "MI histogram launch");
+  FinalizeArgs fa{};
+  fa.ghist = hist;
+  fa.T = reinterpret_cast<float*>(wb + w.table);
+  fa.scalars = reinterpret_cast<double*>(wb + w.scalars);
+  fa.B = p->bins;
+  fa.N = (double)g.N;
+  fa.tscale = (double)(p->bins - 5) / ((double)p->m_hi - (double)p->m_lo) / (double)g.N;
+  FFDP_CUDA(launch_finalize(bmax, fa, s), "MI finalize launch");
+  if (dJ) {
+    Sweep2Args a2{};
+    a2.g = g;
+    a2.F = F;
+    a2.Jin = J;
+    a2.dJ = dJ;
+    a2.T = fa.T;
+    a2.bf = a1.bf;
+    a2.bj = a1.bj;
+    a2.B = p->bins;
+    a2.nIter = a1.nIter;
+    FFDP_CUDA(launch_sweep2(S2_MI_JBUF, ft, 0, bmax, a2,
+                            persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MI_JBUF, ft, 0, bmax)), s),
+              "MI gradient launch");
+  }
+  FinishArgs f{};
+  f.scalars = fa.scalars;
+  f.nparts = 0;
+  f.partials = reinterpret_cast<double*>(wb + w.partials);
+  f.loss = loss;
+  f.nloss = 1;
+  f.has_mi = 1;
+  f.N = (double)g.N;
+  FFDP_CUDA(launch_finish(f, s), "finish launch");
+  return FFDP_OK;
+}
+
+extern "C" ffdp_status ffdp_lncc_fwd_bwd(const void* F, ffdp_dtype ft, const float* J, ffdp_dims dims,
+                                         const ffdp_lncc_params* p, float* loss, float* dJ, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!F || !J || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null F, J or loss");
+  FFDP_TRY(check_dtype(ft, "F"));
+  FFDP_TRY(check_dims(dims, "image"));
+  FFDP_TRY(check_lncc(p));
+  if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
+  const Ws w = ws_layout(false, 32, max_parts(), false, nvox(dims));
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  char* wb = static_cast<char*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LnccArgs a{};
+  make_grid_only(dims, a.g);
+  a.F = F;
+  a.J = J;
+  a.dJ = dJ;
+  a.partials = reinterpret_cast<double*>(wb + w.partials);
+  a.R = (p->window - 1) / 2;
+  a.eps = p->eps;
+  a.inv_n = (float)(1.0 / ((double)p->window * p->window * p->window));
+  a.gscale = (float)(-1.0 / (double)a.g.N);
+  int grid = 1;
+  lncc_tiling(dims, a.R, a, lncc_ctas_per_sm(LN_DJ, ft, 0, 0, a.R), grid);
+  FFDP_CUDA(launch_lncc(LN_DJ, ft, 0, 0, a, grid, s), "LNCC launch");
+  FinishArgs f{};
+  f.partials = a.partials;
+  f.nparts = grid;
+  f.loss = loss;
+  f.nloss = 1;
+  f.has_lncc = 1;
+  f.N = (double)a.g.N;
+  FFDP_CUDA(launch_finish(f, s), "finish launch");
+  return FFDP_OK;
+}
+
+extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M,
+                                      ffdp_dtype mt, ffdp_dims mdims, const float* u,
+                                      const ffdp_transform* T, const ffdp_objective_params* p, float* loss,
+                                      float* du, float* dA, float* dt, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  g_err[0] = '\0';
+  if (!F || !M || !T || !p || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null F, M, T, params or loss");
+  FFDP_TRY(check_dtype(ft, "F"));
+  FFDP_TRY(check_dtype(mt, "M"));
+  FFDP_TRY(check_dims(fdims, "fixed"));
+  FFDP_TRY(check_dims(mdims, "moving"));
+  if (!std::isfinite(p->w_mi) || !std::isfinite(p->w_lncc))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "non-finite loss weights");
+  const bool mi = p->w_mi != 0.0f, ln = p->w_lncc != 0.0f;
+  if (!mi && !ln) return fail(FFDP_ERR_INVALID_ARGUMENT, "both loss weights are zero");
+  if (mi) FFDP_TRY(check_mi(&p->mi));
+  if (ln) FFDP_TRY(check_lncc(&p->lncc));
+  if (!aligned16(F) || (u && !aligned16(u)) || (du && !aligned16(du)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "F, u and du must be 16-byte aligned");
+  const int bmax = mi ? bmax_of(p->mi.bins) : 32;
+  const uint64_t N = nvox(fdims);
+  const Ws w = ws_layout(mi, bmax, max_parts(), ln, N);
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  char* wb = static_cast<char*>(ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Geom g;
+  FFDP_TRY(make_geom(fdims, mdims, T, g));
+  unsigned long long* hist = reinterpret_cast<unsigned long long*>(wb + w.hist);
+  float* table = reinterpret_cast<float*>(wb + w.table);
+  double* scalars = reinterpret_cast<double*>(wb + w.scalars);
+  double* partials = reinterpret_cast<double*>(wb + w.partials);
+  float* Jbuf = ln ? reinterpret_cast<float*>(wb + w.J) : nullptr;
+  const BinMap bf = mi ? bin_map(p->mi.f_lo, p->mi.f_hi, p->mi.bins) : BinMap{0, 1, 1, 0};
+  const BinMap bj = mi ? bin_map(p->mi.m_lo, p->mi.m_hi, p->mi.bins) : BinMap{0, 1, 1, 0};
+
+  // sweep 1: histogram (MI) and/or the materialised J (LNCC)
+  if (mi) FFDP_CUDA(launch_zero_u64(hist, bmax * bmax, s), "zero launch");
+  Sweep1Args a1{};
+  a1.g = g;
+  a1.F = F;
+  a1.M = M;
+  a1.u = u;
+  a1.Jout = Jbuf;
+  a1.ghist = hist;
+  a1.bf = bf;
+  a1.bj = bj;
+  a1.B = mi ? p->mi.bins : 32;
+  a1.nIter = n_iter(N);
+  const int m1 = mi ? (ln ? S1_HIST_WRITEJ : S1_HIST) : S1_WRITEJ;
+  FFDP_CUDA(launch_sweep1(m1, ft, mt, bmax, a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(m1, ft, mt, bmax)), s),
+            "sweep 1 launch");
+  if (mi) {
+    FinalizeArgs fa{};
+    fa.ghist = hist;
+    fa.T = table;
+    fa.scalars = scalars;
+    fa.B = p->mi.bins;
+    fa.N = (double)N;
+    fa.tscale = (double)p->w_mi * (double)(p->mi.bins - 5) / ((double)p->mi.m_hi - (double)p->mi.m_lo) / (double)N;
+    FFDP_CUDA(launch_finalize(bmax, fa, s), "MI finalize launch");
+  }
+  int nparts = 0;
+  if (ln) {
+    LnccArgs a{};
+    a.g = g;
+    a.F = F;
+    a.J = Jbuf;
+    a.M = M;
+    a.u = u;
+    a.du = du;
+    a.T = table;
+    a.partials = partials;
+    a.bf = bf;
+    a.bj = bj;
+    a.B = mi ? p->mi.bins : 0;
+    a.R = (p->lncc.window - 1) / 2;
+    a.eps = p->lncc.eps;
+    a.inv_n = (float)(1.0 / ((double)p->lncc.window * p->lncc.window * p->lncc.window));
+    a.gscale = (float)(-(double)p->w_lncc / (double)N);
+    const int bm = mi ? bmax : 0;
+    int grid = 1;
+    lncc_tiling(fdims, a.R, a, lncc_ctas_per_sm(LN_BWD, ft, mt, bm, a.R), grid);
+    FFDP_CUDA(launch_lncc(LN_BWD, ft, mt, bm, a, grid, s), "LNCC sweep launch");
+    nparts = grid;
+  } else {
+    Sweep2Args a2{};
+    a2.g = g;
+    a2.F = F;
+    a2.M = M;
+    a2.u = u;
+    a2.du = du;
+    a2.T = table;
+    a2.partials = partials;
+    a2.bf = bf;
+    a2.bj = bj;
+    a2.B = p->mi.bins;
+    a2.nIter = n_iter(N);
+    const int grid = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MI, ft, mt, bmax));
+    FFDP_CUDA(launch_sweep2(S2_MI, ft, mt, bmax, a2, grid, s), "sweep 2 launch");
+    nparts = grid;
+  }
+  FinishArgs f{};
+  f.partials = partials;
+  f.nparts = nparts;
+  f.scalars = scalars;
+  f.dA = dA;
+  f.dt = dt;
+  f.loss = loss;
+  f.nloss = 3;
+  f.N = (double)N;
+  f.w_mi = p->w_mi;
+  f.w_lncc = p->w_lncc;
+  f.has_mi = mi;
+  f.has_lncc = ln;
+  f.has_affine = 1;
+  for (int c = 0; c < 3; ++c) {
+    const double nf = c == 0 ? (double)fdims.w : (c == 1 ? (double)fdims.h : (double)fdims.d);
+    const double nmv = c == 0 ? (double)mdims.w : (c == 1 ? (double)mdims.h : (double)mdims.d);
+    f.hM[c] = (nmv - 1.0) / 2.0;
+    f.dx[c] = ((double)T->xmax[c] - (double)T->xmin[c]) / (nf - 1.0);
+    f.xc[c] = (double)T->xmin[c] + f.dx[c] * (nf - 1.0) / 2.0;
+  }
+  FFDP_CUDA(launch_finish(f, s), "finish launch");
+  return FFDP_OK;
+}

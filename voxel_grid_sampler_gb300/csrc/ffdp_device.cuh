@@ -1,0 +1,242 @@
+// ffdp_device.cuh -- device building blocks shared by the libffdp kernels.
+//
+// Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
+// Registration", Key designs item 1 (coordinates of I(Ax+t+Su(x)) computed in
+// registers from x_bounds; nothing grid-sized is materialised) and item 2
+// (Parzen-window MI with a shared-memory histogram; LNCC window sums).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ffdp {
+
+// ---------------------------------------------------------------- constants
+constexpr int kThreads = 256;           // threads per CTA of every sweep kernel
+constexpr int kVPT = 4;                 // voxels per thread per iteration (x-contiguous)
+constexpr int kHistFrac = 20;           // fixed-point fraction bits of histogram weights
+constexpr float kHistOne = 1048576.0f;  // 2^kHistFrac
+constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic holds round(x) in its low bits
+constexpr unsigned kMagicBits = 0x4B400000u;
+constexpr int kPartialStride = 16;      // doubles per CTA partial record
+
+// Per-CTA partial record layout (doubles), reduced by the finish kernel:
+//   [0..2]  s_r   = sum g dJ/dq_r
+//   [3..11] m_rc  = sum g dJ/dq_r (i_c - c_c)   (c_c: grid centre index)
+//   [12]    sum cc (LNCC)
+enum { kPS = 0, kPM = 3, kPCC = 12 };
+
+// ------------------------------------------------------------ geometry
+// Fixed-grid index i = (ix, iy, iz) maps to moving-image voxel coordinates
+//   q = G i + g0 + K u,   G = diag(hM) A diag(dx),  g0 = hM (A x_min + t + 1),
+//   K = diag(hM) S,       hM = (n_M - 1)/2,          dx = (x_max - x_min)/(n_F - 1).
+// G i + g0 is carried in 64-bit fixed point with 32 fraction bits, so the
+// integer cell index and the in-cell fraction stay exact to ~1e-7 voxel even
+// on 1024^3 grids (a float32 q would round at 6e-5 voxel there).
+struct Geom {
+  long long Gq[9];  // [r][c], 2^-32 units
+  long long g0q[3];
+  float K[9];       // [r][c]
+  float hM[3];
+  float ctr[3];     // grid centre index (n_F - 1)/2 per axis (x, y, z)
+  int fW, fH, fD;   // fixed grid extents
+  int mW, mH, mD;   // moving grid extents
+  long long mHW;
+  unsigned N;       // fixed voxels
+  unsigned divW_m, divHW_m;  // fast division magic numbers for W and H*W
+  int divW_s, divHW_s;
+  int k_diag;       // K is diagonal (S diagonal): u enters q component-wise
+};
+
+// Unsigned division by a runtime-invariant divisor (round-up method).
+__device__ __forceinline__ unsigned fast_div(unsigned n, unsigned m, int s) {
+  return (unsigned)(((unsigned long long)__umulhi(n, m) + n) >> s);
+}
+
+__device__ __forceinline__ void lin_to_xyz(const Geom& g, unsigned lin, int& ix, int& iy, int& iz) {
+  unsigned z = fast_div(lin, g.divHW_m, g.divHW_s);
+  unsigned rem = lin - z * ((unsigned)g.fW * (unsigned)g.fH);
+  unsigned y = fast_div(rem, g.divW_m, g.divW_s);
+  iz = (int)z;
+  iy = (int)y;
+  ix = (int)(rem - y * (unsigned)g.fW);
+}
+
+// 64-bit fixed-point anchor P = G i + g0 (no displacement).
+__device__ __forceinline__ void anchor(const Geom& g, int ix, int iy, int iz, long long P[3]) {
+#pragma unroll
+  for (int r = 0; r < 3; ++r)
+    P[r] = g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
+}
+
+// floor(t) and t - floor(t) for |t| < 2^21 with full-rate float/int ops:
+// x + 1.5*2^23 rounds to the nearest integer, corrected by one when it
+// rounded up.
+__device__ __forceinline__ void floor_split(float t, int& fi, float& fr) {
+  float a = t + kMagic;
+  float fl = a - kMagic;
+  int i = (int)(__float_as_uint(a) - kMagicBits);
+  if (fl > t) {
+    fl -= 1.0f;
+    i -= 1;
+  }
+  fi = i;
+  fr = t - fl;
+}
+
+// Cell of the moving image containing q = P + K u: integer corner b (clamped
+// to [-2, n] so that far-away points keep every tap outside) and fractions r.
+__device__ __forceinline__ void cell_of(const Geom& g, const long long P[3], float u0, float u1,
+                                        float u2, int b[3], float r[3]) {
+  const int nm[3] = {g.mW, g.mH, g.mD};
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    const int k = (int)(P[c] >> 32);
+    const unsigned lo = (unsigned)(P[c] & 0xffffffffll);
+    const float f = __uint_as_float(0x3f800000u | (lo >> 9)) - 1.0f;  // [0, 1)
+    float t;
+    if (g.k_diag) {
+      t = fmaf(g.K[c * 4], c == 0 ? u0 : (c == 1 ? u1 : u2), f);
+    } else {
+      t = fmaf(g.K[c * 3 + 0], u0, fmaf(g.K[c * 3 + 1], u1, fmaf(g.K[c * 3 + 2], u2, f)));
+    }
+    t = fminf(fmaxf(t, -1048576.0f), 1048576.0f);
+    int fi;
+    float fr;
+    floor_split(t, fi, fr);
+    long long bb = (long long)k + fi;
+    bb = bb < -2 ? -2 : (bb > nm[c] ? nm[c] : bb);
+    b[c] = (int)bb;
+    r[c] = fr;
+  }
+}
+
+// ------------------------------------------------------------- M access
+template <typename T>
+__device__ __forceinline__ float ldg_f(const T* p);
+template <>
+__device__ __forceinline__ float ldg_f<float>(const float* p) {
+  return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float ldg_f<__half>(const __half* p) {
+  return __half2float(__ldg(p));
+}
+
+// Trilinear sample of M at cell (b, r) with zero padding per tap; optionally
+// the slope dJ/dq from the same 8 taps (cell [b, b+1] on every axis).
+template <typename MT, bool GRAD>
+__device__ __forceinline__ float trilinear(const MT* __restrict__ M, const Geom& g, const int b[3],
+                                           const float r[3], float& gx, float& gy, float& gz) {
+  float m000, m001, m010, m011, m100, m101, m110, m111;  // m[z][y][x]
+  const int bx = b[0], by = b[1], bz = b[2];
+  if ((unsigned)bx < (unsigned)(g.mW - 1) && (unsigned)by < (unsigned)(g.mH - 1) &&
+      (unsigned)bz < (unsigned)(g.mD - 1)) {
+    const MT* p = M + ((long long)bz * g.mH + by) * g.mW + bx;
+    const MT* q = p + g.mW;
+    m000 = ldg_f(p);
+    m001 = ldg_f(p + 1);
+    m010 = ldg_f(q);
+    m011 = ldg_f(q + 1);
+    p += g.mHW;
+    q += g.mHW;
+    m100 = ldg_f(p);
+    m101 = ldg_f(p + 1);
+    m110 = ldg_f(q);
+    m111 = ldg_f(q + 1);
+  } else {
+    const bool x0 = (unsigned)bx < (unsigned)g.mW, x1 = (unsigned)(bx + 1) < (unsigned)g.mW;
+    const bool y0 = (unsigned)by < (unsigned)g.mH, y1 = (unsigned)(by + 1) < (unsigned)g.mH;
+    const bool z0 = (unsigned)bz < (unsigned)g.mD, z1 = (unsigned)(bz + 1) < (unsigned)g.mD;
+    auto at = [&](int dz, int dy, int dx, bool ok) -> float {
+      return ok ? ldg_f(M + ((long long)(bz + dz) * g.mH + (by + dy)) * g.mW + (bx + dx)) : 0.0f;
+    };
+    m000 = at(0, 0, 0, z0 && y0 && x0);
+    m001 = at(0, 0, 1, z0 && y0 && x1);
+    m010 = at(0, 1, 0, z0 && y1 && x0);
+    m011 = at(0, 1, 1, z0 && y1 && x1);
+    m100 = at(1, 0, 0, z1 && y0 && x0);
+    m101 = at(1, 0, 1, z1 && y0 && x1);
+    m110 = at(1, 1, 0, z1 && y1 && x0);
+    m111 = at(1, 1, 1, z1 && y1 && x1);
+  }
+  const float rx = r[0], ry = r[1], rz = r[2];
+  const float dx00 = m001 - m000, dx01 = m011 - m010, dx10 = m101 - m100, dx11 = m111 - m110;
+  const float c00 = fmaf(rx, dx00, m000), c01 = fmaf(rx, dx01, m010);
+  const float c10 = fmaf(rx, dx10, m100), c11 = fmaf(rx, dx11, m110);
+  const float dy0 = c01 - c00, dy1 = c11 - c10;
+  const float c0 = fmaf(ry, dy0, c00), c1 = fmaf(ry, dy1, c10);
+  const float dz = c1 - c0;
+  if (GRAD) {
+    gz = dz;
+    gy = fmaf(rz, dy1 - dy0, dy0);
+    const float e0 = fmaf(ry, dx01 - dx00, dx00);
+    const float e1 = fmaf(ry, dx11 - dx10, dx10);
+    gx = fmaf(rz, e1 - e0, e0);
+  }
+  return fmaf(rz, dz, c0);
+}
+
+// ------------------------------------------------------- Parzen window
+// Cubic B-spline weights of the four bins floor(c)-1 .. floor(c)+2 for
+// fraction t = c - floor(c), each multiplied by `scale`.
+__device__ __forceinline__ void bspline4(float t, float scale, float w[4]) {
+  const float u = 1.0f - t;
+  const float t2 = t * t, u2 = u * u;
+  const float t3 = t2 * t, u3 = u2 * u;
+  const float s6 = scale * (1.0f / 6.0f), s23 = scale * (2.0f / 3.0f), sh = 0.5f * scale;
+  w[0] = u3 * s6;
+  w[1] = fmaf(t3, sh, fmaf(-t2, scale, s23));
+  w[2] = fmaf(u3, sh, fmaf(-u2, scale, s23));
+  w[3] = t3 * s6;
+}
+
+// d beta(s)/ds at s = bin - c for the same four bins.
+__device__ __forceinline__ void bspline4_deriv(float t, float d[4]) {
+  const float u = 1.0f - t;
+  d[0] = 0.5f * u * u;
+  d[1] = t * fmaf(-1.5f, t, 2.0f);
+  d[2] = u * fmaf(1.5f, u, -2.0f);
+  d[3] = -0.5f * t * t;
+}
+
+// Bin coordinate c = clamp(v, lo, hi) * sc + off  (sc = (B-5)/(hi-lo), off = 2 - lo*sc).
+struct BinMap {
+  float lo, hi, sc, off;
+};
+
+__device__ __forceinline__ float bin_coord(const BinMap& m, float v) {
+  return fmaf(fminf(fmaxf(v, m.lo), m.hi), m.sc, m.off);
+}
+
+// c lies in [2, B-3]: a non-negative value below 2^21, so floor_split applies.
+
+// --------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Loads of 4 consecutive fixed-image values as float.
+__device__ __forceinline__ void load4(const float* __restrict__ p, float v[4]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  v[0] = a.x;
+  v[1] = a.y;
+  v[2] = a.z;
+  v[3] = a.w;
+}
+__device__ __forceinline__ void load4(const __half* __restrict__ p, float v[4]) {
+  const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&a.x));
+  const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&a.y));
+  v[0] = lo.x;
+  v[1] = lo.y;
+  v[2] = hi.x;
+  v[3] = hi.y;
+}
+__device__ __forceinline__ float load1(const float* __restrict__ p) { return __ldg(p); }
+__device__ __forceinline__ float load1(const __half* __restrict__ p) { return __half2float(__ldg(p)); }
+
+}  // namespace ffdp

@@ -1,0 +1,124 @@
+// ffdp_internal.h -- argument records and launcher declarations shared by the
+// host ABI (ffdp_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "ffdp_device.cuh"
+
+// Instantiate a body for the float (code 0) or half (code 1) element type.
+#define FFDP_DT_SWITCH(code, T, ...)      \
+  do {                                    \
+    if ((code) == 0) {                    \
+      using T = float;                    \
+      __VA_ARGS__;                        \
+    } else {                              \
+      using T = __half;                   \
+      __VA_ARGS__;                        \
+    }                                     \
+  } while (0)
+
+namespace ffdp {
+
+enum Sweep1Mode { S1_HIST = 0, S1_HIST_WRITEJ = 1, S1_WRITEJ = 2, S1_HIST_JBUF = 3 };
+enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2 };
+enum LnccMode { LN_DJ = 0, LN_BWD = 1 };
+
+// Histogram sweep / forward sampler.
+struct Sweep1Args {
+  const void* F;
+  const void* M;
+  const float* u;
+  const float* Jin;
+  float* Jout;
+  unsigned long long* ghist;  // [B*B] fixed-point (kHistFrac) joint histogram
+  Geom g;
+  BinMap bf, bj;
+  int B;
+  unsigned nIter;             // CTA iterations of kThreads*kVPT voxels
+};
+
+// Gradient sweep: MI table lookups and/or a given dL/dJ, sampler backward.
+struct Sweep2Args {
+  const void* F;
+  const void* M;
+  const float* u;
+  const float* Jin;   // S2_MI_JBUF
+  const float* gbuf;  // S2_GBUF
+  float* du;
+  float* dJ;          // S2_MI_JBUF
+  const float* T;     // packed MI table (scaled by w_mi * c' / N)
+  double* partials;   // [gridDim.x][kPartialStride]
+  Geom g;
+  BinMap bf, bj;
+  int B;
+  unsigned nIter;
+};
+
+// MI table: normalise the histogram, MI value, packed T = ln P - ln P_F - ln P_J.
+struct FinalizeArgs {
+  const unsigned long long* ghist;
+  float* T;        // packed table
+  double* scalars; // [0] = MI
+  int B;
+  double N;
+  double tscale;   // multiplies T (w_mi * (B-5)/(m_hi-m_lo) / N)
+};
+
+// LNCC window kernel (J materialised), optional MI gradient and sampler backward.
+struct LnccArgs {
+  const void* F;
+  const float* J;
+  const void* M;
+  const float* u;
+  float* du;
+  float* dJ;
+  const float* T;
+  double* partials;
+  Geom g;          // fixed-grid extents always valid; sampler fields for LN_BWD
+  BinMap bf, bj;
+  int B;
+  int R;           // window radius
+  float eps;
+  float inv_n;     // 1 / window^3
+  float gscale;    // -w_lncc / N
+  int tilesX, tilesY, tz;  // tile grid and z planes per CTA
+};
+
+// Reduction of per-CTA partials into dA, dt and the loss values.
+struct FinishArgs {
+  const double* partials;
+  int nparts;
+  const double* scalars;  // [0] = MI (if MI on)
+  float* dA;
+  float* dt;
+  float* loss;            // NULL or [nloss]
+  int nloss;              // 1 (single-term ops) or 3 (objective)
+  double hM[3], xc[3], dx[3];
+  double N;
+  double w_mi, w_lncc;
+  int has_mi, has_lncc, has_affine;
+};
+
+// Launchers (return cudaGetLastError() after the launch).
+cudaError_t launch_zero_u64(unsigned long long* p, int n, cudaStream_t s);
+cudaError_t launch_sweep1(int mode, int ft, int mt, int bmax, const Sweep1Args& a, int grid, cudaStream_t s);
+cudaError_t launch_sweep2(int mode, int ft, int mt, int bmax, const Sweep2Args& a, int grid, cudaStream_t s);
+cudaError_t launch_finalize(int bmax, const FinalizeArgs& a, cudaStream_t s);
+cudaError_t launch_lncc(int mode, int ft, int mt, int bmax_or0, const LnccArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s);
+
+// Occupancy-derived persistent grid sizes (CTAs per SM), cached.
+int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax);
+int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax);
+size_t lncc_smem_bytes(int R, int bmax_or0);
+int lncc_ctas_per_sm(int mode, int ft, int mt, int bmax_or0, int R);
+
+// Timing / launch-count hooks implemented in ffdp_api.cu.
+void note_launch_begin(const char* name, cudaStream_t s);
+void note_launch_end(cudaStream_t s);
+
+constexpr int kMaxCtasPerSm = 8;
+constexpr int kLnccTX = 32;
+
+}  // namespace ffdp

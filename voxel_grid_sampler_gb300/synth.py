@@ -163,12 +163,12 @@ def _norm_axes(shape, device, z0=0, z1=None):
 def _random_ellipsoids(rng: np.random.Generator, nested: bool, count: int):
     """Ellipsoids in normalised coordinates: (centre[3], semi-axes[3], rotation 3x3)."""
     out = []
-    scale = 0.75
-    centre = rng.uniform(-0.08, 0.08, 3)
+    scale = 0.9
+    centre = rng.uniform(-0.05, 0.05, 3)
     for i in range(count):
         if nested:
             axes = np.array([scale, scale * rng.uniform(0.8, 1.0), scale * rng.uniform(0.7, 0.95)])
-            scale *= rng.uniform(0.55, 0.7)
+            scale *= rng.uniform(0.7, 0.8)
             c = centre + rng.uniform(-0.05, 0.05, 3) * i
         else:
             axes = rng.uniform(0.08, 0.3, 3)
