@@ -1,0 +1,375 @@
+"""Benchmark of the fused registration objective (MI + LNCC, forward + backward).
+
+One step = one ffdp_objective call on the 512^3 fp32 phantom pair (MI with 64
+bins + LNCC with a 5^3 window, gradients to u, A and t): every row of the hot
+path -- implicit sampler, histogram sweep, MI table, LNCC window sums, MI and
+LNCC gradients, sampler backward, affine reductions.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4|5] [--impl reference]
+
+Under torch.distributed.run each rank evaluates its own independent pair
+(weak scaling, no collective on the data path); the step time is the maximum
+over ranks.  Rank 0 prints one JSON line.  --impl reference times the CPU
+oracle (double precision, all host cores) on a bounded z-slab of the same
+workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Gvoxels/s fused warp+MI/LNCC fwd+bwd on 1 GB300; % of HBM roofline"
+UNIT = "Gvoxels/s"
+# Algorithmic bytes per voxel (inputs read once per sweep, du written once):
+# MI needs two sweeps because the histogram is a global dependency.
+ALGO_BYTES = {4: 2 * (4 + 12 + 4) + 12, 5: 2 * (2 + 12 + 2) + 12}
+# Dominant kernel's algorithmic bytes per voxel (the gradient sweep reads
+# F, u and M and writes du).
+SWEEP2_BYTES = {4: 4 + 12 + 4 + 12, 5: 2 + 12 + 2 + 12}
+HBM_NOMINAL_GBS = 8000.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _crop_transform(pair, ds):
+    """x_bounds of the first ds planes of the fixed grid (same sample points)."""
+    D = pair.F.shape[0]
+    xmax = pair.xmax.copy()
+    xmax[2] = pair.xmin[2] + (pair.xmax[2] - pair.xmin[2]) * (ds - 1) / (D - 1)
+    return xmax
+
+
+def oracle_sample(pair, ds, threads=None):
+    """Time the CPU oracle on the first ds planes of the workload (one fwd+bwd)."""
+    import oracle
+    wl = pair.workload
+    if threads:
+        oracle.set_threads(threads)
+    F = pair.F[:ds].float().cpu().numpy()
+    M = pair.M.float().cpu().numpy()
+    u = pair.u[:ds].cpu().numpy()
+    xmax = _crop_transform(pair, ds)
+    T = oracle.Transform(pair.A.astype(np.float64), pair.t.astype(np.float64), pair.S.astype(np.float64),
+                         pair.xmin.astype(np.float64), xmax.astype(np.float32).astype(np.float64))
+    P = oracle.ObjectiveParams(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    t0 = time.perf_counter()
+    if wl.w_lncc != 0.0:
+        oracle.objective(F, M, u, T, P)
+    else:
+        oracle.objective_mi_slabs(F, M, u, T, P, slab=8)
+    dt = time.perf_counter() - t0
+    return F.size, dt, oracle.max_threads()
+
+
+def _sample_planes(pair, budget_s=12.0):
+    """Planes of the bounded CPU sample: ~budget_s seconds of oracle work."""
+    import oracle
+    n1, t1, _ = oracle_sample(pair, 2)
+    per_plane = t1 / 2.0
+    ds = int(max(2, min(pair.F.shape[0], budget_s / max(per_plane, 1e-3))))
+    return ds
+
+
+def run_reference(args, ws, rank, local):
+    from voxel_grid_sampler_gb300 import synth
+    if rank != 0:
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    pair = synth.make_pair(args.workload, device=dev)
+    pair.F, pair.M, pair.u = pair.F.cpu(), pair.M.cpu(), pair.u.cpu()
+    ds = _sample_planes(pair, budget_s=args.ref_step_s)
+    for _ in range(args.warmup):
+        oracle_sample(pair, ds)
+    times = []
+    cores = 1
+    for _ in range(args.steps):
+        n, t, cores = oracle_sample(pair, ds)
+        times.append(t)
+    t = sum(times) / len(times)
+    value = n / t / 1e9
+    wl = pair.workload
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "shape": list(pair.F.shape), "sample_planes": ds},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "oracle objective on fixed planes z<%d of the %s pair (%d voxels)"
+                                   % (ds, "x".join(map(str, pair.F.shape)), n)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def _traffic_per_launch(kernel, workload, N):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        import hashlib
+        with open(p) as f:
+            d = json.load(f)
+        rec = d.get(kernel)
+        if not rec or rec.get("workload") != workload:
+            return None
+        src = "".join(open(os.path.join(ROOT, "voxel_grid_sampler_gb300", "csrc", s)).read()
+                      for s in sorted(rec["sources"]))
+        if hashlib.sha256(src.encode()).hexdigest()[:16] != rec["source_sha"]:
+            return None
+        return rec["bytes_per_voxel"] * N
+    except Exception:
+        return None
+
+
+def run_gpu(args, ws, rank, local):
+    from voxel_grid_sampler_gb300 import build, ffdp, synth
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    pair = synth.make_pair(args.workload, device=dev, seed=1000 + args.workload + 100 * rank)
+    wl = pair.workload
+    F, M, u = pair.F, pair.M, pair.u
+    N = F.numel()
+    T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    wsbuf = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P, dev)
+    loss = torch.empty(3, device=dev)
+    du = torch.empty(tuple(F.shape) + (3,), device=dev)
+    dA = torch.empty(9, device=dev)
+    dt = torch.empty(3, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, wsbuf, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # ---- device-resident timed region (per-kernel events recorded live)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    ffdp.timing_enable(args.steps * 8)
+    n0 = ffdp.launch_count()
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.15)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    clk = clocks.stop()
+    launches = ffdp.launch_count() - n0
+    kern = ffdp.timing_read()
+    ffdp.timing_enable(0)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = _max_over_ranks(ms, ws, dev)
+    value = N * ws / (ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    Fh = F.cpu().pin_memory()
+    Mh = M.cpu().pin_memory()
+    uh = u.cpu().pin_memory()
+    duh = torch.empty(du.shape, dtype=du.dtype).pin_memory()
+    outh = torch.empty(15, dtype=torch.float32).pin_memory()
+    Fd, Md, ud = torch.empty_like(F), torch.empty_like(M), torch.empty_like(u)
+    small = torch.empty(15, device=dev)
+
+    def e2e_step():
+        Fd.copy_(Fh, non_blocking=True)
+        Md.copy_(Mh, non_blocking=True)
+        ud.copy_(uh, non_blocking=True)
+        ffdp.ffdp_objective(Fd, Md, ud, T, P, loss, du, dA, dt, wsbuf, stream)
+        small[0:3].copy_(loss)
+        small[3:12].copy_(dA)
+        small[12:15].copy_(dt)
+        duh.copy_(du, non_blocking=True)
+        outh.copy_(small, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    ms_e2e = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, dev)
+    h2d = F.numel() * F.element_size() + M.numel() * M.element_size() + u.numel() * u.element_size()
+    d2h = du.numel() * du.element_size() + 15 * 4
+    del Fh, Mh, uh, duh, Fd, Md, ud
+
+    # ---- roofline of the dominant kernel (algorithmic bytes / its own time)
+    peak, peak_kind = _peaks()
+    dom = max(kern.items(), key=lambda kv: kv[1][1]) if kern else ("?", (1, ms))
+    dom_name, (dom_n, dom_ms) = dom
+    dom_avg = dom_ms / max(dom_n, 1)
+    per_launch_voxels = N
+    algo = {"k_lncc": SWEEP2_BYTES, "k_sweep2": SWEEP2_BYTES}.get(dom_name, {4: 20, 5: 16})
+    achieved = algo[args.workload] * per_launch_voxels / (dom_avg * 1e-3) / 1e9
+    traffic = _traffic_per_launch(dom_name, wl.name, N)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,
+                "algorithmic_bytes_per_voxel": algo[args.workload], "peak_source": peak_kind}
+    step_gbs = ALGO_BYTES[args.workload] * N / (ms * 1e-3) / 1e9
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if wl.dtype == "f32" else "f32 (f16 storage)",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "shape": list(F.shape), "voxels": N,
+                   "l2": "inputs larger than L2 (%.2f GB algorithmic bytes per step)"
+                         % (ALGO_BYTES[args.workload] * N / 1e9),
+                   "parallelism": "independent pair per rank" if ws > 1 else "single GPU"},
+        "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs,
+                             "of_8tbs": step_gbs / HBM_NOMINAL_GBS,
+                             "of_measured": step_gbs / peak,
+                             "bytes_per_voxel": ALGO_BYTES[args.workload]},
+        "roofline": roofline,
+        "kernels_ms_per_launch": {k: v[1] / max(v[0], 1) for k, v in kern.items()},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": {"value": N * ws / (ms_e2e * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e},
+        "loss": [float(x) for x in loss.tolist()],
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        ds = _sample_planes(pair, budget_s=args.cpu_budget_s)
+        n, t, cores = oracle_sample(pair, ds)
+        out["cpu_baseline"] = {"value": n / t / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": "oracle objective on fixed planes z<%d of the %s pair "
+                                         "(%d voxels, %.1f s)" % (ds, "x".join(map(str, F.shape)), n, t)}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=4, choices=[4, 5])
+    ap.add_argument("--impl", default="ffdp", choices=["ffdp", "reference"])
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=6.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = _dist()
+    if ws > 1:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ws, rank, local)
+        else:
+            run_gpu(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

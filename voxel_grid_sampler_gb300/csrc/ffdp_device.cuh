@@ -201,16 +201,17 @@ __device__ __forceinline__ void bspline4_deriv(float t, float d[4]) {
   d[3] = -0.5f * t * t;
 }
 
-// Bin coordinate c = clamp(v, lo, hi) * sc + off  (sc = (B-5)/(hi-lo), off = 2 - lo*sc).
+// Bin coordinate c = 2 + (clamp(v, lo, hi) - lo) * sc, sc = (B-5)/(hi-lo).
+// Subtracting lo first keeps c inside [2, B-3] up to one rounding of
+// (hi-lo)*sc, whatever the magnitude of lo, so every histogram / table
+// address derived from floor(c) stays in range (NaN clamps to lo).
 struct BinMap {
   float lo, hi, sc, off;
 };
 
 __device__ __forceinline__ float bin_coord(const BinMap& m, float v) {
-  return fmaf(fminf(fmaxf(v, m.lo), m.hi), m.sc, m.off);
+  return fmaf(fminf(fmaxf(v, m.lo), m.hi) - m.lo, m.sc, 2.0f);
 }
-
-// c lies in [2, B-3]: a non-negative value below 2^21, so floor_split applies.
 
 // --------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {
