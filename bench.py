@@ -172,7 +172,9 @@ def run_reference(args, ws, rank, local):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     pair = synth.make_pair(args.workload, device=dev)
     pair.F, pair.M, pair.u = pair.F.cpu(), pair.M.cpu(), pair.u.cpu()
-    ds = _sample_planes(pair, budget_s=args.ref_step_s)
+    # each step a bounded sample so that warm-up + timed steps end within ~3 minutes
+    budget = min(args.ref_step_s, 150.0 / max(1, args.steps + args.warmup))
+    ds = _sample_planes(pair, budget_s=budget)
     for _ in range(args.warmup):
         oracle_sample(pair, ds)
     times = []
@@ -221,7 +223,8 @@ def run_gpu(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    pair = synth.make_pair(args.workload, device=dev, seed=1000 + args.workload + 100 * rank)
+    shape = None if not args.shape else (args.shape,) * 3
+    pair = synth.make_pair(args.workload, device=dev, shape=shape, seed=1000 + args.workload + 100 * rank)
     wl = pair.workload
     F, M, u = pair.F, pair.M, pair.u
     N = F.numel()
@@ -266,6 +269,17 @@ def run_gpu(args, ws, rank, local):
     value = N * ws / (ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with host buffers
+    if args.no_e2e:
+        ms_e2e, h2d, d2h = float("nan"), 0, 0
+    else:
+        ms_e2e, h2d, d2h = _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws)
+    _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h)
+
+
+def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
+    from voxel_grid_sampler_gb300 import ffdp
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     Fh = F.cpu().pin_memory()
     Mh = M.cpu().pin_memory()
     uh = u.cpu().pin_memory()
@@ -300,7 +314,10 @@ def run_gpu(args, ws, rank, local):
     h2d = F.numel() * F.element_size() + M.numel() * M.element_size() + u.numel() * u.element_size()
     d2h = du.numel() * du.element_size() + 15 * 4
     del Fh, Mh, uh, duh, Fd, Md, ud
+    return ms_e2e, h2d, d2h
 
+
+def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h):
     # ---- roofline of the dominant kernel (algorithmic bytes / its own time)
     peak, peak_kind = _peaks()
     dom = max(kern.items(), key=lambda kv: kv[1][1]) if kern else ("?", (1, ms))
@@ -333,8 +350,9 @@ def run_gpu(args, ws, rank, local):
         "kernels_ms_per_launch": {k: v[1] / max(v[0], 1) for k, v in kern.items()},
         "gpu_launches": int(launches),
         "clocks": clk,
-        "e2e": {"value": N * ws / (ms_e2e * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e},
+        "e2e": None if args.no_e2e else {
+            "value": N * ws / (ms_e2e * 1e-3) / 1e9, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms_e2e},
         "loss": [float(x) for x in loss.tolist()],
     }
     if ws == 1 and not args.no_cpu_baseline:
@@ -356,6 +374,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--shape", type=int, default=0, help="cube edge overriding the workload size (profiling)")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if ws > 1:

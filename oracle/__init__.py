@@ -314,6 +314,7 @@ def objective_mi_slabs(F, M, u, T: Transform, p: ObjectiveParams, slab: int = 16
     dt = np.zeros(3, np.float64)
     idx = None if du_index is None else np.asarray(du_index, np.int64)
     du_s = None if idx is None else np.zeros((idx.size, 3), np.float64)
+    J_s = None if idx is None else np.zeros(idx.size, np.float64)
     plane = H * W
     for z0 in range(0, D, slab):
         z1 = min(D, z0 + slab)
@@ -324,5 +325,7 @@ def objective_mi_slabs(F, M, u, T: Transform, p: ObjectiveParams, slab: int = 16
         if idx is not None:
             sel = (idx >= z0 * plane) & (idx < z1 * plane)
             du_s[sel] = du.reshape(-1, 3)[idx[sel] - z0 * plane]
+            J_s[sel] = J.reshape(-1)[idx[sel] - z0 * plane]
     loss = np.array([p.w_mi * -mi_v, -mi_v, 0.0])
-    return dict(loss=loss, dA=dA.reshape(3, 3), dt=dt, du_samples=du_s, mi=mi_v, P=P, PF=PF, PJ=PJ)
+    return dict(loss=loss, dA=dA.reshape(3, 3), dt=dt, du_samples=du_s, J_samples=J_s, mi=mi_v, P=P,
+                PF=PF, PJ=PJ)

@@ -49,3 +49,9 @@ def random_transform(rng, scale=0.1, s_offdiag=True):
     xmin = np.array([-0.95, -1.0, -0.9], np.float32)
     xmax = np.array([1.0, 0.92, 0.97], np.float32)
     return A, t, S, xmin, xmax
+
+
+def report(name, **errs):
+    """Print measured errors next to their tolerances (visible with pytest -s)."""
+    parts = ["%s=%.3g" % (k, float(v)) for k, v in errs.items()]
+    print("[parity] %s: %s" % (name, " ".join(parts)))

@@ -1,0 +1,93 @@
+"""Full-size parity on the five benchmark workloads, in the launch
+configuration bench.py times (one ffdp_objective call on the whole volume).
+
+Workloads 1-4 are compared element by element against the oracle on whole
+arrays (du in full, dA, dt, all three loss values, and the sampled image J);
+workload 5 (1024^3, ~1.07e9 voxels) streams the oracle slab by slab and
+compares the losses, dA and dt in full and du / J at 4096 sampled voxels.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import TOL_GRAD, TOL_J, TOL_LOSS, oracle_T_of, rel_err, rel_l2, report
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def ffdp():
+    from voxel_grid_sampler_gb300 import build, ffdp as f
+    build.build()
+    return f
+
+
+def _run_gpu(ffdp, pair):
+    wl = pair.workload
+    T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    loss, du, dA, dt = ffdp.ffdp_objective(pair.F, pair.M, pair.u, T, P)
+    J = ffdp.ffdp_grid_sample_fwd(pair.M, pair.F.shape, pair.u, T)
+    torch.cuda.synchronize()
+    return loss.cpu().numpy(), du, dA.cpu().numpy(), dt.cpu().numpy(), J
+
+
+def _oparams(pair):
+    wl = pair.workload
+    return oracle.ObjectiveParams(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window,
+                                  wl.eps)
+
+
+def _check_losses(l, ref):
+    for k in range(3):
+        if ref[k] != 0.0:
+            assert rel_err(l[k], ref[k]) <= TOL_LOSS, (k, l, ref)
+        else:
+            assert l[k] == 0.0
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 4])
+def test_workload_full_arrays(ffdp, k):
+    from voxel_grid_sampler_gb300 import synth
+    pair = synth.make_pair(k, device="cuda")
+    l, du, dA, dt, J = _run_gpu(ffdp, pair)
+    F = pair.F.cpu().float().numpy()
+    M = pair.M.cpu().float().numpy()
+    u = pair.u.cpu().numpy()
+    du = du.cpu().numpy()
+    J = J.cpu().numpy()
+    del pair.F, pair.M, pair.u
+    torch.cuda.empty_cache()
+    ref = oracle.objective(F, M, u, oracle_T_of(pair), _oparams(pair))
+    report("workload %d" % k, J=np.max(np.abs(J - ref["J"])),
+           loss=max(rel_err(l[i], ref["loss"][i]) for i in range(3) if ref["loss"][i] != 0),
+           du=rel_l2(du, ref["du"]), dAdt=rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]))
+    assert np.max(np.abs(J - ref["J"])) <= TOL_J
+    _check_losses(l, ref["loss"])
+    assert rel_l2(du, ref["du"]) <= TOL_GRAD
+    assert rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
+
+
+def test_workload5_gigavoxel_streamed(ffdp):
+    from voxel_grid_sampler_gb300 import synth
+    pair = synth.make_pair(5, device="cuda")
+    l, du, dA, dt, J = _run_gpu(ffdp, pair)
+    N = pair.F.numel()
+    idx = np.sort(np.random.default_rng(5).choice(N, 4096, replace=False))
+    it = torch.from_numpy(idx).cuda()
+    du_s = du.view(-1, 3)[it].cpu().numpy()
+    J_s = J.view(-1)[it].cpu().numpy()
+    del du, J
+    F = pair.F.cpu().float().numpy()
+    M = pair.M.cpu().float().numpy()
+    u = pair.u.cpu().numpy()
+    del pair.F, pair.M, pair.u
+    torch.cuda.empty_cache()
+    ref = oracle.objective_mi_slabs(F, M, u, oracle_T_of(pair), _oparams(pair), slab=16, du_index=idx)
+    report("workload 5", J=np.max(np.abs(J_s - ref["J_samples"])), loss=rel_err(l[0], ref["loss"][0]),
+           du=rel_l2(du_s, ref["du_samples"]), dAdt=rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]))
+    assert np.max(np.abs(J_s - ref["J_samples"])) <= TOL_J
+    _check_losses(l, ref["loss"])
+    assert rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
+    assert rel_l2(du_s, ref["du_samples"]) <= TOL_GRAD

@@ -188,21 +188,27 @@ ffdp_status make_geom(ffdp_dims f, ffdp_dims m, const ffdp_transform* T, Geom& g
     hM[c] = (nm[c] - 1.0) / 2.0;
   }
   const double two32 = 4294967296.0;
+  if ((uint64_t)m.d * (uint64_t)m.h * (uint64_t)m.w >= (1ull << 31))
+    return fail(FFDP_ERR_UNSUPPORTED, "moving image has 2^31 or more voxels");
   for (int r = 0; r < 3; ++r) {
     double g0 = (double)T->t[r] + 1.0;
+    double reach = 0.0;  // largest |G i| over the fixed grid
     for (int c = 0; c < 3; ++c) {
       const double G = hM[r] * (double)T->A[r * 3 + c] * dx[c];
-      if (std::fabs(G) > 1048576.0) return fail(FFDP_ERR_UNSUPPORTED, "affine scale too large");
+      reach += std::fabs(G) * (nf[c] - 1.0);
       g.Gq[r * 3 + c] = (long long)llround(G * two32);
       g0 += (double)T->A[r * 3 + c] * (double)T->xmin[c];
       g.K[r * 3 + c] = (float)(hM[r] * (double)T->S[r * 3 + c]);
     }
     g0 *= hM[r];
-    if (std::fabs(g0) > 268435456.0) return fail(FFDP_ERR_UNSUPPORTED, "translation too large");
+    // keeps the integer part of every anchor below 2^25 voxels
+    if (reach + std::fabs(g0) > 16777216.0) return fail(FFDP_ERR_UNSUPPORTED, "affine maps the grid beyond 2^24 voxels");
     g.g0q[r] = (long long)llround(g0 * two32);
+    g.Gx[r] = (float)(hM[r] * (double)T->A[r * 3 + 0] * dx[0]);
     g.hM[r] = (float)hM[r];
     g.ctr[r] = (float)((nf[r] - 1.0) / 2.0);
   }
+  g.w4 = (f.w % 4) == 0 ? 1 : 0;
   g.k_diag = (T->S[1] == 0.f && T->S[2] == 0.f && T->S[3] == 0.f && T->S[5] == 0.f && T->S[6] == 0.f &&
               T->S[7] == 0.f)
                  ? 1
@@ -227,6 +233,7 @@ void make_grid_only(ffdp_dims f, Geom& g) {
   g.fH = (int)f.h;
   g.fD = (int)f.d;
   g.N = (unsigned)nvox(f);
+  g.w4 = (f.w % 4) == 0 ? 1 : 0;
   fast_div_magic((uint32_t)f.w, g.divW_m, g.divW_s);
   fast_div_magic((uint32_t)(f.w * f.h), g.divHW_m, g.divHW_s);
 }
@@ -263,7 +270,7 @@ int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
 
 // Workspace layout (byte offsets, 256-aligned).
 struct Ws {
-  size_t hist, table, scalars, partials, J, total;
+  size_t hist, table, table2, scalars, partials, J, total;
 };
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -274,7 +281,9 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
   w.hist = o;
   if (mi) o = al(o + (size_t)bmax * bmax * sizeof(unsigned long long));
   w.table = o;
-  if (mi) o = al(o + (size_t)bmax * bmax * 4 * sizeof(float));
+  if (mi) o = al(o + mi_table_bytes(bmax));
+  w.table2 = o;
+  if (mi && needJ) o = al(o + (size_t)bmax * bmax * 2 * sizeof(float));
   w.scalars = o;
   o = al(o + 16 * sizeof(double));
   w.partials = o;
@@ -560,6 +569,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   FFDP_TRY(make_geom(fdims, mdims, T, g));
   unsigned long long* hist = reinterpret_cast<unsigned long long*>(wb + w.hist);
   float* table = reinterpret_cast<float*>(wb + w.table);
+  float* table2 = (mi && ln) ? reinterpret_cast<float*>(wb + w.table2) : nullptr;
   double* scalars = reinterpret_cast<double*>(wb + w.scalars);
   double* partials = reinterpret_cast<double*>(wb + w.partials);
   float* Jbuf = ln ? reinterpret_cast<float*>(wb + w.J) : nullptr;
@@ -586,6 +596,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     FinalizeArgs fa{};
     fa.ghist = hist;
     fa.T = table;
+    fa.T2 = table2;
     fa.scalars = scalars;
     fa.B = p->mi.bins;
     fa.N = (double)N;
@@ -601,7 +612,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a.M = M;
     a.u = u;
     a.du = du;
-    a.T = table;
+    a.T = table2;
     a.partials = partials;
     a.bf = bf;
     a.bj = bj;

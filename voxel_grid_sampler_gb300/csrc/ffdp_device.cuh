@@ -37,6 +37,7 @@ enum { kPS = 0, kPM = 3, kPCC = 12 };
 struct Geom {
   long long Gq[9];  // [r][c], 2^-32 units
   long long g0q[3];
+  float Gx[3];      // G[r][0]: q step per fixed voxel along x (float)
   float K[9];       // [r][c]
   float hM[3];
   float ctr[3];     // grid centre index (n_F - 1)/2 per axis (x, y, z)
@@ -47,7 +48,19 @@ struct Geom {
   unsigned divW_m, divHW_m;  // fast division magic numbers for W and H*W
   int divW_s, divHW_s;
   int k_diag;       // K is diagonal (S diagonal): u enters q component-wise
+  int w4;           // fW % 4 == 0: a 4-voxel group never crosses a row
 };
+
+// Integer part k and fraction f in [0, 1) of the fixed-point anchor of voxel
+// (ix, iy, iz); |k| < 2^25 is guaranteed by the host-side range check.
+__device__ __forceinline__ void anchor_kf(const Geom& g, int ix, int iy, int iz, int k[3], float f[3]) {
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const long long P = g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
+    k[r] = (int)(P >> 32);
+    f[r] = __uint_as_float(0x3f800000u | ((unsigned)(P & 0xffffffffll) >> 9)) - 1.0f;
+  }
+}
 
 // Unsigned division by a runtime-invariant divisor (round-up method).
 __device__ __forceinline__ unsigned fast_div(unsigned n, unsigned m, int s) {
@@ -105,9 +118,30 @@ __device__ __forceinline__ void cell_of(const Geom& g, const long long P[3], flo
     int fi;
     float fr;
     floor_split(t, fi, fr);
-    long long bb = (long long)k + fi;
-    bb = bb < -2 ? -2 : (bb > nm[c] ? nm[c] : bb);
-    b[c] = (int)bb;
+    b[c] = min(max(k + fi, -2), nm[c]);
+    r[c] = fr;
+  }
+}
+
+// Cell of voxel v (0..3) of a 4-voxel group in one row: q = k + f + v Gx + K u.
+// The small part f + v Gx + K u stays below ~2^21 in magnitude, so float
+// rounding there is ~1e-7 voxel while k carries the large part exactly.
+__device__ __forceinline__ void cell_v(const Geom& g, const int k[3], const float f[3], float v, float u0,
+                                       float u1, float u2, int b[3], float r[3]) {
+  const int nm[3] = {g.mW, g.mH, g.mD};
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    float t = fmaf(v, g.Gx[c], f[c]);
+    if (g.k_diag) {
+      t = fmaf(g.K[c * 4], c == 0 ? u0 : (c == 1 ? u1 : u2), t);
+    } else {
+      t = fmaf(g.K[c * 3 + 0], u0, fmaf(g.K[c * 3 + 1], u1, fmaf(g.K[c * 3 + 2], u2, t)));
+    }
+    t = fminf(fmaxf(t, -1048576.0f), 1048576.0f);
+    int fi;
+    float fr;
+    floor_split(t, fi, fr);
+    b[c] = min(max(k[c] + fi, -2), nm[c]);
     r[c] = fr;
   }
 }

@@ -58,7 +58,8 @@ struct Sweep2Args {
 // MI table: normalise the histogram, MI value, packed T = ln P - ln P_F - ln P_J.
 struct FinalizeArgs {
   const unsigned long long* ghist;
-  float* T;        // packed table
+  float* T;        // gradient table of the linear sweep (polynomial cells for 32 bins)
+  float* T2;       // optional: T rows packed as float2 pairs (LNCC-fused gradient)
   double* scalars; // [0] = MI
   int B;
   double N;
@@ -112,6 +113,7 @@ cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s);
 int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax);
 int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax);
 size_t lncc_smem_bytes(int R, int bmax_or0);
+size_t mi_table_bytes(int bmax);
 int lncc_ctas_per_sm(int mode, int ft, int mt, int bmax_or0, int R);
 
 // Timing / launch-count hooks implemented in ffdp_api.cu.

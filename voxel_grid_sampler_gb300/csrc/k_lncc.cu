@@ -46,13 +46,14 @@ __host__ __device__ inline LnccLayout lncc_layout(int R, int bmax) {
   L.off_xb = L.off_zb + imax(5 * L.E2, 3 * L.E1);
   L.off_gr = L.off_xb + imax(5 * L.E2H * L.E1W, 3 * L.E1H * kTX);
   L.off_T = ((L.off_gr + L.W_ * 3 * L.E1) + 3) & ~3;
-  const int tf = bmax == 32 ? 32 * 32 * 4 : (bmax == 64 ? 64 * 64 * 2 : 0);
+  const int tf = bmax * bmax * 2;
   L.total = L.off_T + tf;
   return L;
 }
 
 size_t lncc_smem_bytes(int R, int bmax_or0) { return (size_t)lncc_layout(R, bmax_or0).total * sizeof(float); }
 
+// MI partial gradient from T rows packed as float2 pairs (any bin count).
 template <int BMAX>
 __device__ __forceinline__ float mi_grad_ln(const float* tsm, const BinMap& bf, const BinMap& bj, float f,
                                             float j) {
@@ -64,20 +65,11 @@ __device__ __forceinline__ float mi_grad_ln(const float* tsm, const BinMap& bf, 
   bspline4(tf, 1.0f, wf);
   bspline4_deriv(tj, d);
   float s = 0.0f;
-  if (BMAX == 32) {
-    const float4* t4 = reinterpret_cast<const float4*>(tsm) + (af - 1) * BMAX + (aj - 1);
+  const float2* t2 = reinterpret_cast<const float2*>(tsm) + (af - 1) * BMAX + (aj - 1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 t = t4[i * BMAX];
-      s = fmaf(wf[i], fmaf(t.x, d[0], fmaf(t.y, d[1], fmaf(t.z, d[2], t.w * d[3]))), s);
-    }
-  } else {
-    const float2* t2 = reinterpret_cast<const float2*>(tsm) + (af - 1) * BMAX + (aj - 1);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 p = t2[i * BMAX], q = t2[i * BMAX + 2];
-      s = fmaf(wf[i], fmaf(p.x, d[0], fmaf(p.y, d[1], fmaf(q.x, d[2], q.y * d[3]))), s);
-    }
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = t2[i * BMAX], q = t2[i * BMAX + 2];
+    s = fmaf(wf[i], fmaf(p.x, d[0], fmaf(p.y, d[1], fmaf(q.x, d[2], q.y * d[3]))), s);
   }
   return (j >= bj.lo && j <= bj.hi) ? s : 0.0f;
 }
@@ -100,7 +92,7 @@ __global__ void __launch_bounds__(kThreads) k_lncc(const LnccArgs a) {
   float* tsm = sm + L.off_T;
   const int tid = threadIdx.x;
   if (MI) {
-    const int n4 = (BMAX == 32 ? 32 * 32 * 4 : 64 * 64 * 2) / 4;
+    const int n4 = BMAX * BMAX * 2 / 4;
     const float4* src = reinterpret_cast<const float4*>(a.T);
     for (int i = tid; i < n4; i += kThreads) reinterpret_cast<float4*>(tsm)[i] = __ldg(src + i);
   }
