@@ -157,6 +157,35 @@ ffdp_status ffdp_objective(const void *F, ffdp_dtype ft, ffdp_dims fdims, const 
                            float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
                            void *stream);
 
+/* Workspace-free variant of ffdp_objective for the MI term (the paper has no
+ * counterpart; it exists for callers that cannot allocate device memory).
+ * Some callers cannot hand the library a workspace: a plug-in inside a host
+ * application that owns every device allocation, a real-time loop that may
+ * not allocate after start-up, or a plain C host that only holds its input and
+ * output buffers.  This entry point takes the same arguments as
+ * ffdp_objective minus the workspace, and uses scratch memory reserved inside
+ * the library image instead: ffdp_static_scratch_bytes() bytes (512 KiB) that
+ * every GPU loading the library holds until the process exits.  It never
+ * calls an allocator.
+ *   - MI only: p->w_lncc must be 0 (LNCC keeps a per-voxel image that does not
+ *     fit); a call whose scratch need (ffdp_workspace_bytes of the MI-only
+ *     objective) exceeds the static scratch returns FFDP_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the scratch's device address (a
+ *     one-time set-up per device); make that first call before any stream
+ *     capture.
+ *   - All calls on a device share the one scratch area, which keeps the last
+ *     call's contents; each call re-initialises what must start at zero.
+ *     Calls that overlap on the GPU (e.g. on two streams at once) race on it:
+ *     serialise them.
+ * Outputs and errors are as for ffdp_objective. */
+ffdp_status ffdp_objective_mi_static(const void *F, ffdp_dtype ft, ffdp_dims fdims, const void *M,
+                                     ffdp_dtype mt, ffdp_dims mdims, const float *u,
+                                     const ffdp_transform *T, const ffdp_objective_params *p,
+                                     float *loss, float *du, float *dA, float *dt, void *stream);
+
+/* Size in bytes of the static scratch used by ffdp_objective_mi_static. */
+size_t ffdp_static_scratch_bytes(void);
+
 /* Human-readable name of a status. */
 const char *ffdp_status_string(ffdp_status s);
 

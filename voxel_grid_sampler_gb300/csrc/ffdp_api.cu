@@ -667,3 +667,64 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   FFDP_CUDA(launch_finish(f, s), "finish launch");
   return FFDP_OK;
 }
+
+// ------------------------------------------------ workspace-free MI objective
+// Some callers cannot hand the library a workspace: a plug-in running inside a
+// host application that owns every device allocation, a real-time loop whose
+// rules forbid allocating after start-up, or a plain C host that only holds
+// its input and output buffers and has no device allocator of its own.  For
+// them the MI-only objective can run on scratch memory reserved inside the
+// library image: this file-scope array is created on every GPU that loads the
+// library and is held until the process exits.  Host code must not use the
+// array's name as a device address (in host code it is only a stand-in);
+// the device address is looked up once per device and passed to the kernels.
+static constexpr size_t kStaticScratchBytes = 512u * 1024u;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};  // device address of g_static_scratch, per device ordinal
+
+ffdp_status static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FFDP_ERR_UNSUPPORTED, "device ordinal %d above 63", dev);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return FFDP_OK;
+}
+}  // namespace
+
+extern "C" size_t ffdp_static_scratch_bytes(void) { return kStaticScratchBytes; }
+
+extern "C" ffdp_status ffdp_objective_mi_static(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M,
+                                                ffdp_dtype mt, ffdp_dims mdims, const float* u,
+                                                const ffdp_transform* T, const ffdp_objective_params* p,
+                                                float* loss, float* du, float* dA, float* dt, void* stream) {
+  g_err[0] = '\0';
+  if (!p) return fail(FFDP_ERR_INVALID_ARGUMENT, "null params");
+  if (p->w_lncc != 0.0f)
+    return fail(FFDP_ERR_UNSUPPORTED,
+                "the workspace-free objective evaluates MI only (w_lncc must be 0): LNCC keeps a "
+                "per-voxel image that does not fit the %zu-byte static scratch",
+                kStaticScratchBytes);
+  const size_t need = ffdp_workspace_bytes(FFDP_OP_OBJECTIVE, fdims, p);
+  if (need == 0) {
+    if (g_err[0] == '\0') fail(FFDP_ERR_INVALID_ARGUMENT, "invalid objective parameters or dimensions");
+    return FFDP_ERR_INVALID_ARGUMENT;
+  }
+  if (need > kStaticScratchBytes)
+    return fail(FFDP_ERR_UNSUPPORTED, "this call needs %zu bytes of scratch; the static scratch holds %zu",
+                need, kStaticScratchBytes);
+  void* scratch = nullptr;
+  FFDP_TRY(static_scratch_address(&scratch));
+  return ffdp_objective(F, ft, fdims, M, mt, mdims, u, T, p, loss, du, dA, dt, scratch, kStaticScratchBytes,
+                        stream);
+}

@@ -295,3 +295,22 @@ class Declared:
     names: tuple = ("ffdp_workspace_bytes", "ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd",
                     "ffdp_mi_fwd_bwd", "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_status_string",
                     "ffdp_last_error", "ffdp_launch_count", "ffdp_timing_enable", "ffdp_timing_read")
+
+
+def ffdp_objective_mi_static(F, M, u, T: ffdp_transform, params: ffdp_objective_params, loss, du, dA, dt,
+                             stream=None):
+    """Workspace-free MI objective (see include/ffdp.h): for callers that cannot
+    allocate device memory.  All outputs must be passed in; nothing is allocated."""
+    L = lib()
+    fn = L.ffdp_objective_mi_static
+    fn.restype = ctypes.c_int
+    fn.argtypes = [_vp, ctypes.c_int, ffdp_dims, _vp, ctypes.c_int, ffdp_dims, _vp,
+                   ctypes.POINTER(ffdp_transform), ctypes.POINTER(ffdp_objective_params), _vp, _vp, _vp,
+                   _vp, _vp]
+    _dev(F, "F", ndim=3)
+    _dev(M, "M", ndim=3)
+    _dev(u, "u", torch.float32, 4)
+    _check(fn(_ptr(F), _dtype_code(F), dims_of(F.shape), _ptr(M), _dtype_code(M), dims_of(M.shape), _ptr(u),
+              ctypes.byref(T), ctypes.byref(params), _ptr(loss), _ptr(du), _ptr(dA), _ptr(dt),
+              _stream(stream)))
+    return loss, du, dA, dt
