@@ -557,6 +557,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   if (!mi && !ln) return fail(FFDP_ERR_INVALID_ARGUMENT, "both loss weights are zero");
   if (mi) FFDP_TRY(check_mi(&p->mi));
   if (ln) FFDP_TRY(check_lncc(&p->lncc));
+  if (ln && ft != mt) return fail(FFDP_ERR_UNSUPPORTED, "LNCC objective needs F and M of the same dtype");
   if (!aligned16(F) || (u && !aligned16(u)) || (du && !aligned16(du)))
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, u and du must be 16-byte aligned");
   const int bmax = mi ? bmax_of(p->mi.bins) : 32;

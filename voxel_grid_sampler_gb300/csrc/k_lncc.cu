@@ -11,52 +11,74 @@
 //   s = -w_lncc / N:  g_FJ = s A1,  g_JJ = -s A2,  g_J = s (2 A2 S_J - A1 S_F) / n,
 //   dJ_m = sum_{k in window(m)} g_J(k) + 2 J_m g_JJ(k) + F_m g_FJ(k).
 //
-// Work layout: a CTA owns a 32 x TY column of output voxels and streams a
-// z-range of planes through shared memory.  Per incoming plane: the (J, F)
-// plane with a 2R halo enters a ring of w planes; the 5 products are summed
-// over the ring (z), then along x and y, giving the window sums one plane
-// behind; the three g-terms enter a second ring, are summed the same way and
-// give dJ 2R planes behind the incoming plane.  CTAs are persistent over
-// tiles, so the per-CTA partial records stay O(#SMs).
+// Work layout.  A CTA owns a 32 x TY column of output voxels and streams a
+// z-range of planes.  (J, F) planes with a 2R halo sit in a ring of w planes
+// in shared memory as interleaved pairs, so that the five window sums run on
+// packed fp32 pairs ((S_J, S_F), (S_JJ, S_FF)) plus S_FJ.  Per incoming plane:
+//   [B] z sums of the products over the ring (direct, w terms),
+//   [C] x sums (runs of 4 outputs per thread, sliding),
+//   [D] y sums (runs of 4 rows per thread, sliding) -> cc and the g-terms of
+//       plane zc = zi - R on the R-halo region,
+//   [E] x sums and [F] y sums of the g-terms -> their 2-D window sums at the
+//       output columns, kept in a ring of w planes,
+//   [G] z sums over that ring give dJ at plane zo = zi - 2R, then the
+//       epilogue (dJ store, or MI gradient + sampler backward).
+// The next plane is fetched into registers during a step and written to the
+// ring after [B], so global latency overlaps the shared-memory work.  The
+// first window pass uses direct fp32 sums in z (no sliding add/subtract) to
+// keep rounding low in flat regions.  CTAs are persistent over tiles, so the
+// per-CTA partial records stay O(#SMs).
 #include "ffdp_internal.h"
 
 namespace ffdp {
 
 constexpr int kTX = kLnccTX;
 
-struct LnccLayout {
-  int W_, TY, E2W, E2H, E1W, E1H, E2, E1;
-  int off_jf, off_zb, off_xb, off_gr, off_T, total;
+template <int R>
+struct LT {
+  static constexpr int W = 2 * R + 1;
+  static constexpr int TY = R <= 2 ? 16 : 8;
+  static constexpr int E2W = kTX + 4 * R;  // multiple of 4
+  static constexpr int E2H = TY + 4 * R;
+  static constexpr int E1W = kTX + 2 * R;
+  static constexpr int E1H = TY + 2 * R;
+  static constexpr int E1S = (E1W + 3) & ~3;
+  static constexpr int E2S = E2W;
+  static constexpr int NIN = ((4 + 2 * R) + 3) & ~3;  // inputs of a 4-output sliding run, rounded to 4
+  static constexpr int RING = W * E2H * E2S * 2;
+  static constexpr int ZB = E2H * E2S * 5;
+  static constexpr int XB = E2H * E1S * 5;
+  static constexpr int GR = W * TY * kTX * 3;
+  static constexpr int PAD = 32;
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_Z = OFF_RING + RING + PAD;
+  static constexpr int OFF_X = OFF_Z + ZB + PAD;
+  static constexpr int OFF_G = OFF_X + XB + PAD;
+  static constexpr int TOTAL = OFF_G + GR + PAD;
+  static_assert(E1H * E1S * 3 <= ZB, "g-term plane must fit in the z buffer");
+  static_assert(E1H * kTX * 3 <= XB, "g-term x buffer must fit in the x buffer");
+  static_assert((OFF_Z % 4) == 0 && (OFF_X % 4) == 0 && (OFF_G % 4) == 0, "16-byte alignment");
+  static_assert((TY % 4) == 0, "TY multiple of 4");
 };
 
-__host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
-
-__host__ __device__ inline LnccLayout lncc_layout(int R, int bmax) {
-  LnccLayout L;
-  L.W_ = 2 * R + 1;
-  L.TY = R <= 2 ? 16 : 8;
-  L.E2W = kTX + 4 * R;
-  L.E2H = L.TY + 4 * R;
-  L.E1W = kTX + 2 * R;
-  L.E1H = L.TY + 2 * R;
-  L.E2 = L.E2W * L.E2H;
-  L.E1 = L.E1W * L.E1H;
-  L.off_jf = 0;
-  L.off_zb = L.off_jf + L.W_ * L.E2 * 2;
-  L.off_xb = L.off_zb + imax(5 * L.E2, 3 * L.E1);
-  L.off_gr = L.off_xb + imax(5 * L.E2H * L.E1W, 3 * L.E1H * kTX);
-  L.off_T = ((L.off_gr + L.W_ * 3 * L.E1) + 3) & ~3;
-  const int tf = bmax * bmax * 2;
-  L.total = L.off_T + tf;
-  return L;
+template <int R>
+static size_t smem_of() {
+  return (size_t)LT<R>::TOTAL * sizeof(float);
 }
 
-size_t lncc_smem_bytes(int R, int bmax_or0) { return (size_t)lncc_layout(R, bmax_or0).total * sizeof(float); }
+size_t lncc_smem_bytes(int R, int /*bmax*/) {
+  switch (R) {
+    case 1: return smem_of<1>();
+    case 2: return smem_of<2>();
+    case 3: return smem_of<3>();
+    default: return smem_of<4>();
+  }
+}
 
-// MI partial gradient from T rows packed as float2 pairs (any bin count).
+// MI partial gradient from T rows packed as float2 pairs (global, read through L1).
 template <int BMAX>
-__device__ __forceinline__ float mi_grad_ln(const float* tsm, const BinMap& bf, const BinMap& bj, float f,
-                                            float j) {
+__device__ __forceinline__ float mi_grad_ln(const float* __restrict__ T, const BinMap& bf, const BinMap& bj,
+                                            float f, float j) {
   int af, aj;
   float tf, tj;
   floor_split(bin_coord(bf, f), af, tf);
@@ -65,47 +87,89 @@ __device__ __forceinline__ float mi_grad_ln(const float* tsm, const BinMap& bf, 
   bspline4(tf, 1.0f, wf);
   bspline4_deriv(tj, d);
   float s = 0.0f;
-  const float2* t2 = reinterpret_cast<const float2*>(tsm) + (af - 1) * BMAX + (aj - 1);
+  const float2* t2 = reinterpret_cast<const float2*>(T) + (af - 1) * BMAX + (aj - 1);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 p = t2[i * BMAX], q = t2[i * BMAX + 2];
+    const float2 p = __ldg(t2 + i * BMAX), q = __ldg(t2 + i * BMAX + 2);
     s = fmaf(wf[i], fmaf(p.x, d[0], fmaf(p.y, d[1], fmaf(q.x, d[2], q.y * d[3]))), s);
   }
   return (j >= bj.lo && j <= bj.hi) ? s : 0.0f;
 }
 
-template <typename FT, typename MT, int MODE, int BMAX>
-__global__ void __launch_bounds__(kThreads) k_lncc(const LnccArgs a) {
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+template <typename FT, typename MT, int MODE, int BMAX, int R>
+__global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArgs a) {
+  using L = LT<R>;
+  constexpr int W = L::W, TY = L::TY, E2H = L::E2H, E2W = L::E2W, E2S = L::E2S;
+  constexpr int E1W = L::E1W, E1H = L::E1H, E1S = L::E1S, NIN = L::NIN;
   constexpr bool MI = BMAX != 0;
+  constexpr int NSTG = (E2H * E2W + kThreads - 1) / kThreads;
+  constexpr int NOUT = (kTX * TY) / kThreads;  // output positions per thread (2 or 1)
+  static_assert(NOUT >= 1 && NOUT * kThreads == kTX * TY, "tile / thread mismatch");
+
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   __shared__ double wsum[kThreads / 32][13];
-  const int R = a.R;
-  const LnccLayout L = lncc_layout(R, BMAX);
+  float2* ring = reinterpret_cast<float2*>(sm + L::OFF_RING);
+  float2* zP = reinterpret_cast<float2*>(sm + L::OFF_Z);
+  float2* zQ = zP + E2H * E2S;
+  float* zX = sm + L::OFF_Z + 4 * E2H * E2S;
+  float2* xP = reinterpret_cast<float2*>(sm + L::OFF_X);
+  float2* xQ = xP + E2H * E1S;
+  float* xX = sm + L::OFF_X + 4 * E2H * E1S;
+  float2* gP = reinterpret_cast<float2*>(sm + L::OFF_Z);
+  float* gX = sm + L::OFF_Z + 2 * E1H * E1S;
+  float2* gxP = reinterpret_cast<float2*>(sm + L::OFF_X);
+  float* gxX = sm + L::OFF_X + 2 * E1H * kTX;
+  float2* grP = reinterpret_cast<float2*>(sm + L::OFF_G);
+  float* grX = sm + L::OFF_G + W * TY * kTX * 2;
+
   const Geom& g = a.g;
-  const int W_ = L.W_, TY = L.TY, E2W = L.E2W, E2H = L.E2H, E1W = L.E1W, E1H = L.E1H;
-  const int E2 = L.E2, E1 = L.E1;
-  float2* jf = reinterpret_cast<float2*>(sm + L.off_jf);
-  float* zb = sm + L.off_zb;
-  float* xb = sm + L.off_xb;
-  float* gr = sm + L.off_gr;
-  float* tsm = sm + L.off_T;
   const int tid = threadIdx.x;
-  if (MI) {
-    const int n4 = BMAX * BMAX * 2 / 4;
-    const float4* src = reinterpret_cast<const float4*>(a.T);
-    for (int i = tid; i < n4; i += kThreads) reinterpret_cast<float4*>(tsm)[i] = __ldg(src + i);
-  }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
   const MT* __restrict__ M = static_cast<const MT*>(a.M);
   const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
+  const float2 ninv2 = make_float2(-inv_n, -inv_n);
   float cc_acc = 0.0f;
   float acc[12];
 #pragma unroll
   for (int k = 0; k < 12; ++k) acc[k] = 0.0f;
-  double dacc[13];
+  if ((tid & 31) == 0)
 #pragma unroll
-  for (int k = 0; k < 13; ++k) dacc[k] = 0.0;
+    for (int k = 0; k < 13; ++k) wsum[tid >> 5][k] = 0.0;
+
+  float2 stg[NSTG];
+  auto load_plane = [&](int zp, int x0, int y0) {
+    const bool zin = zp >= 0 && zp < g.fD;
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      const int e = tid + i * kThreads;
+      float2 v = make_float2(0.0f, 0.0f);
+      if (e < E2H * E2W) {
+        const int ey = e / E2W, ex = e - ey * E2W;
+        const int x = x0 - 2 * R + ex, y = y0 - 2 * R + ey;
+        if (zin && (unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) {
+          const size_t lin = ((size_t)zp * g.fH + y) * g.fW + x;
+          v.x = __ldg(a.J + lin);
+          v.y = load1(F + lin);
+        }
+      }
+      stg[i] = v;
+    }
+  };
+  auto store_plane = [&](int slot) {
+    float2* dst = ring + slot * (E2H * E2S);
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      const int e = tid + i * kThreads;
+      if (e < E2H * E2W) dst[e] = stg[i];
+    }
+  };
 
   const int chunksZ = (g.fD + a.tz - 1) / a.tz;
   const int ntiles = a.tilesX * a.tilesY * chunksZ;
@@ -118,206 +182,379 @@ __global__ void __launch_bounds__(kThreads) k_lncc(const LnccArgs a) {
     const int x0 = tx * kTX, y0 = ty * TY, z0 = tzc * a.tz;
     const int z1 = min(z0 + a.tz, g.fD);
     const int nsteps = (z1 - z0) + 4 * R;
+
+    // epilogue positions and their fixed-point anchors at plane z0
+    int oX[NOUT], oY[NOUT];
+    long long P[NOUT][3];
+#pragma unroll
+    for (int k = 0; k < NOUT; ++k) {
+      const int e = tid + k * kThreads;
+      oY[k] = y0 + e / kTX;
+      oX[k] = x0 + (e % kTX);
+      if (MODE == LN_BWD) anchor(g, oX[k], oY[k], z0, P[k]);
+    }
+
+    __syncthreads();  // previous tile finished with every buffer
+    load_plane(z0 - 2 * R, x0, y0);
+    store_plane(0);
+    if (nsteps > 1) load_plane(z0 - 2 * R + 1, x0, y0);
+    __syncthreads();
+
     for (int s = 0; s < nsteps; ++s) {
       const int zi = z0 - 2 * R + s;
-      // [A] incoming (J, F) plane with a 2R halo; zero outside the grid.
-      {
-        float2* slot = jf + (s % W_) * E2;
-        const bool zin = zi >= 0 && zi < g.fD;
-        for (int e = tid; e < E2; e += kThreads) {
-          const int ey = e / E2W, ex = e - ey * E2W;
-          const int x = x0 - 2 * R + ex, y = y0 - 2 * R + ey;
-          float2 v = make_float2(0.0f, 0.0f);
-          if (zin && (unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) {
-            const size_t lin = ((size_t)zi * g.fH + y) * g.fW + x;
-            v.x = __ldg(a.J + lin);
-            v.y = load1(F + lin);
+      const bool pass1 = s >= 2 * R;
+      const bool pass2 = s >= 4 * R;
+      // (J, F) at this thread's outputs of plane zo = zi - 2R: the ring slot
+      // about to be overwritten.
+      float2 jfo[NOUT];
+      if (pass2) {
+        const float2* src = ring + ((s + 1) % W) * (E2H * E2S);
+#pragma unroll
+        for (int k = 0; k < NOUT; ++k) {
+          const int e = tid + k * kThreads;
+          jfo[k] = src[(e / kTX + 2 * R) * E2S + (e % kTX) + 2 * R];
+        }
+      }
+      // [B] z sums over the ring: (S_J, S_F), (S_JJ, S_FF), S_FJ
+      if (pass1) {
+        constexpr int BG = E2W / 4;
+        for (int it = tid; it < E2H * BG; it += kThreads) {
+          const int row = it / BG, c4 = it - row * BG;
+          float2 sP[4], sQ[4];
+          float sX[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            sP[i] = make_float2(0.f, 0.f);
+            sQ[i] = make_float2(0.f, 0.f);
+            sX[i] = 0.f;
           }
-          slot[e] = v;
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            const float4* src = reinterpret_cast<const float4*>(ring + k * (E2H * E2S) + row * E2S + 4 * c4);
+            const float4 v0 = src[0], v1 = src[1];
+            const float2 p[4] = {make_float2(v0.x, v0.y), make_float2(v0.z, v0.w), make_float2(v1.x, v1.y),
+                                 make_float2(v1.z, v1.w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              sP[i] = add2(sP[i], p[i]);
+              sQ[i] = fma2(p[i], p[i], sQ[i]);
+              sX[i] = fmaf(p[i].x, p[i].y, sX[i]);
+            }
+          }
+          float4* dP = reinterpret_cast<float4*>(zP + row * E2S + 4 * c4);
+          float4* dQ = reinterpret_cast<float4*>(zQ + row * E2S + 4 * c4);
+          dP[0] = make_float4(sP[0].x, sP[0].y, sP[1].x, sP[1].y);
+          dP[1] = make_float4(sP[2].x, sP[2].y, sP[3].x, sP[3].y);
+          dQ[0] = make_float4(sQ[0].x, sQ[0].y, sQ[1].x, sQ[1].y);
+          dQ[1] = make_float4(sQ[2].x, sQ[2].y, sQ[3].x, sQ[3].y);
+          *reinterpret_cast<float4*>(zX + row * E2S + 4 * c4) = make_float4(sX[0], sX[1], sX[2], sX[3]);
         }
       }
       __syncthreads();
-      if (s >= 2 * R) {
-        // [B] z sums of F, J, F^2, J^2, FJ over the ring (planes zi-2R .. zi).
-        for (int e = tid; e < E2; e += kThreads) {
-          float sF = 0.f, sJ = 0.f, sFF = 0.f, sJJ = 0.f, sFJ = 0.f;
-          for (int k = 0; k < W_; ++k) {
-            const float2 v = jf[k * E2 + e];
-            sJ += v.x;
-            sF += v.y;
-            sJJ = fmaf(v.x, v.x, sJJ);
-            sFF = fmaf(v.y, v.y, sFF);
-            sFJ = fmaf(v.x, v.y, sFJ);
-          }
-          zb[0 * E2 + e] = sF;
-          zb[1 * E2 + e] = sJ;
-          zb[2 * E2 + e] = sFF;
-          zb[3 * E2 + e] = sJJ;
-          zb[4 * E2 + e] = sFJ;
-        }
-        __syncthreads();
-        // [C] x sums: E2H rows, E1W outputs per row.
-        for (int e = tid; e < E2H * E1W; e += kThreads) {
-          const int row = e / E1W, x1 = e - row * E1W;
-#pragma unroll
-          for (int q = 0; q < 5; ++q) {
-            const float* src = zb + q * E2 + row * E2W + x1;
-            float sacc = 0.0f;
-            for (int k = 0; k <= 2 * R; ++k) sacc += src[k];
-            xb[q * E2H * E1W + e] = sacc;
-          }
-        }
-        __syncthreads();
-        // [D] y sums give the window sums at plane zc on the R-halo region;
-        // cc and the three g-terms (zero outside the grid).
-        {
-          const int zc = zi - R;
-          float* gslot = gr + (s % W_) * 3 * E1;
-          const bool zin = zc >= 0 && zc < g.fD;
-          const bool zown = zc >= z0 && zc < z1;
-          for (int e = tid; e < E1; e += kThreads) {
-            const int y1 = e / E1W, x1 = e - y1 * E1W;
-            float S[5];
-#pragma unroll
-            for (int q = 0; q < 5; ++q) {
-              const float* src = xb + q * E2H * E1W + y1 * E1W + x1;
-              float sacc = 0.0f;
-              for (int k = 0; k <= 2 * R; ++k) sacc += src[k * E1W];
-              S[q] = sacc;
-            }
-            const int x = x0 - R + x1, y = y0 - R + y1;
-            float gJ = 0.f, gJJ = 0.f, gFJ = 0.f;
-            if (zin && (unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) {
-              const float cross = fmaf(-S[0] * S[1], inv_n, S[4]);
-              const float vF = fmaf(-S[0] * S[0], inv_n, S[2]);
-              const float vJ = fmaf(-S[1] * S[1], inv_n, S[3]);
-              const float D = fmaf(vF, vJ, eps);
-              const float rD = 1.0f / D;
-              const float A1 = 2.0f * cross * rD;
-              const float cc = cross * cross * rD;
-              const float A2 = cc * vF * rD;
-              gFJ = gs * A1;
-              gJJ = -gs * A2;
-              gJ = gs * (2.0f * A2 * S[1] - A1 * S[0]) * inv_n;
-              if (zown && x1 >= R && x1 < R + kTX && y1 >= R && y1 < R + TY) cc_acc += cc;
-            }
-            gslot[e] = gJ;
-            gslot[E1 + e] = gJJ;
-            gslot[2 * E1 + e] = gFJ;
-          }
-        }
-        __syncthreads();
+      // the oldest ring slot is free: write the staged plane, fetch the next
+      if (s + 1 < nsteps) {
+        store_plane((s + 1) % W);
+        if (s + 2 < nsteps) load_plane(zi + 2, x0, y0);
       }
-      if (s >= 4 * R) {
-        // [E] z sums of the g-terms over their ring.
-        float* gz = zb;
-        for (int e = tid; e < E1; e += kThreads) {
-#pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            float sacc = 0.0f;
-            for (int k = 0; k < W_; ++k) sacc += gr[k * 3 * E1 + c * E1 + e];
-            gz[c * E1 + e] = sacc;
-          }
-        }
+      if (!pass1) {
         __syncthreads();
-        // [F] x sums onto the 32 output columns.
-        float* gx = xb;
-        for (int e = tid; e < E1H * kTX; e += kThreads) {
-          const int row = e / kTX, x = e - row * kTX;
+        continue;
+      }
+      // [C] x sums, 4 outputs per item (sliding)
+      {
+        constexpr int XG = E1S / 4;
+        for (int it = tid; it < E2H * XG; it += kThreads) {
+          const int row = it / XG, g4 = it - row * XG;
+          float2 vP[NIN], vQ[NIN];
+          float vX[NIN];
+          const float4* sP4 = reinterpret_cast<const float4*>(zP + row * E2S + 4 * g4);
+          const float4* sQ4 = reinterpret_cast<const float4*>(zQ + row * E2S + 4 * g4);
+          const float4* sX4 = reinterpret_cast<const float4*>(zX + row * E2S + 4 * g4);
 #pragma unroll
-          for (int c = 0; c < 3; ++c) {
-            const float* src = gz + c * E1 + row * E1W + x;
-            float sacc = 0.0f;
-            for (int k = 0; k <= 2 * R; ++k) sacc += src[k];
-            gx[c * E1H * kTX + e] = sacc;
+          for (int k = 0; k < NIN / 2; ++k) {
+            const float4 p = sP4[k], q = sQ4[k];
+            vP[2 * k] = make_float2(p.x, p.y);
+            vP[2 * k + 1] = make_float2(p.z, p.w);
+            vQ[2 * k] = make_float2(q.x, q.y);
+            vQ[2 * k + 1] = make_float2(q.z, q.w);
           }
-        }
-        __syncthreads();
-        // [G] y sums at the outputs of plane zo, then the epilogue.
-        {
-          const int zo = zi - 2 * R;
-          const float2* jfo = jf + ((s - 2 * R) % W_) * E2;
-          for (int e = tid; e < kTX * TY; e += kThreads) {
-            const int yy = e / kTX, xx = e - yy * kTX;
-            const int X = x0 + xx, Y = y0 + yy;
-            if (X < g.fW && Y < g.fH) {
-              float bg[3];
 #pragma unroll
-              for (int c = 0; c < 3; ++c) {
-                const float* src = gx + c * E1H * kTX + yy * kTX + xx;
-                float sacc = 0.0f;
-                for (int k = 0; k <= 2 * R; ++k) sacc += src[k * kTX];
-                bg[c] = sacc;
+          for (int k = 0; k < NIN / 4; ++k) {
+            const float4 x = sX4[k];
+            vX[4 * k] = x.x;
+            vX[4 * k + 1] = x.y;
+            vX[4 * k + 2] = x.z;
+            vX[4 * k + 3] = x.w;
+          }
+          float2 aP = vP[0], aQ = vQ[0];
+          float aX = vX[0];
+#pragma unroll
+          for (int k = 1; k <= 2 * R; ++k) {
+            aP = add2(aP, vP[k]);
+            aQ = add2(aQ, vQ[k]);
+            aX += vX[k];
+          }
+          float2 oP[4], oQ[4];
+          float oXv[4];
+          oP[0] = aP;
+          oQ[0] = aQ;
+          oXv[0] = aX;
+#pragma unroll
+          for (int j = 1; j < 4; ++j) {
+            aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
+            aQ = sub2(add2(aQ, vQ[2 * R + j]), vQ[j - 1]);
+            aX = (aX + vX[2 * R + j]) - vX[j - 1];
+            oP[j] = aP;
+            oQ[j] = aQ;
+            oXv[j] = aX;
+          }
+          float4* dP = reinterpret_cast<float4*>(xP + row * E1S + 4 * g4);
+          float4* dQ = reinterpret_cast<float4*>(xQ + row * E1S + 4 * g4);
+          dP[0] = make_float4(oP[0].x, oP[0].y, oP[1].x, oP[1].y);
+          dP[1] = make_float4(oP[2].x, oP[2].y, oP[3].x, oP[3].y);
+          dQ[0] = make_float4(oQ[0].x, oQ[0].y, oQ[1].x, oQ[1].y);
+          dQ[1] = make_float4(oQ[2].x, oQ[2].y, oQ[3].x, oQ[3].y);
+          *reinterpret_cast<float4*>(xX + row * E1S + 4 * g4) = make_float4(oXv[0], oXv[1], oXv[2], oXv[3]);
+        }
+      }
+      __syncthreads();
+      // [D] y sums -> window sums at plane zc on the R-halo region; cc and g-terms
+      {
+        constexpr int YR = (E1H + 3) / 4;
+        const int zc = zi - R;
+        const bool zin = zc >= 0 && zc < g.fD;
+        const bool zown = zc >= z0 && zc < z1;
+        for (int it = tid; it < E1W * YR; it += kThreads) {
+          const int x1 = it % E1W, r4 = it / E1W;
+          const int ys = 4 * r4;
+          float2 vP[4 + 2 * R], vQ[4 + 2 * R];
+          float vX[4 + 2 * R];
+#pragma unroll
+          for (int k = 0; k < 4 + 2 * R; ++k) {
+            const int row = ys + k;
+            if (row < E2H) {
+              vP[k] = xP[row * E1S + x1];
+              vQ[k] = xQ[row * E1S + x1];
+              vX[k] = xX[row * E1S + x1];
+            } else {
+              vP[k] = vQ[k] = make_float2(0.f, 0.f);
+              vX[k] = 0.f;
+            }
+          }
+          float2 aP = vP[0], aQ = vQ[0];
+          float aX = vX[0];
+#pragma unroll
+          for (int k = 1; k <= 2 * R; ++k) {
+            aP = add2(aP, vP[k]);
+            aQ = add2(aQ, vQ[k]);
+            aX += vX[k];
+          }
+          const int x = x0 - R + x1;
+          const bool xin = (unsigned)x < (unsigned)g.fW;
+          const bool xown = x1 >= R && x1 < R + kTX;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j > 0) {
+              aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
+              aQ = sub2(add2(aQ, vQ[2 * R + j]), vQ[j - 1]);
+              aX = (aX + vX[2 * R + j]) - vX[j - 1];
+            }
+            const int y1 = ys + j;
+            if (y1 < E1H) {
+              const int y = y0 - R + y1;
+              float2 gpair = make_float2(0.f, 0.f);
+              float gfj = 0.f;
+              if (zin && xin && (unsigned)y < (unsigned)g.fH) {
+                // aP = (S_J, S_F), aQ = (S_JJ, S_FF), aX = S_FJ
+                const float2 v = fma2(mul2(aP, aP), ninv2, aQ);  // (vJ, vF)
+                const float cross = fmaf(-aP.x * aP.y, inv_n, aX);
+                const float D = fmaf(v.x, v.y, eps);
+                const float rD = rcp_approx(D);
+                const float A1 = 2.0f * cross * rD;
+                const float cc = cross * cross * rD;
+                const float A2 = cc * v.y * rD;
+                gfj = gs * A1;
+                gpair.y = -gs * A2;
+                gpair.x = gs * (2.0f * A2 * aP.x - A1 * aP.y) * inv_n;
+                if (zown && xown && y1 >= R && y1 < R + TY) cc_acc += cc;
               }
-              const float2 v = jfo[(yy + 2 * R) * E2W + (xx + 2 * R)];
-              float gv = fmaf(v.y, bg[2], fmaf(2.0f * v.x, bg[1], bg[0]));
-              if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(tsm, a.bf, a.bj, v.y, v.x);
-              const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
-              if (MODE == LN_DJ) {
-                if (a.dJ) a.dJ[lin] = gv;
-              } else {
-                long long P[3];
-                anchor(g, X, Y, zo, P);
-                float u0 = 0.f, u1 = 0.f, u2 = 0.f;
-                if (a.u) {
-                  u0 = __ldg(a.u + 3 * lin + 0);
-                  u1 = __ldg(a.u + 3 * lin + 1);
-                  u2 = __ldg(a.u + 3 * lin + 2);
-                }
-                int b[3];
-                float r[3], gq0, gq1, gq2;
-                cell_of(g, P, u0, u1, u2, b, r);
-                trilinear<MT, true>(M, g, b, r, gq0, gq1, gq2);
-                const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
-                if (a.du) {
-                  if (g.k_diag) {
-                    a.du[3 * lin + 0] = g.K[0] * e0;
-                    a.du[3 * lin + 1] = g.K[4] * e1;
-                    a.du[3 * lin + 2] = g.K[8] * e2;
-                  } else {
-                    a.du[3 * lin + 0] = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
-                    a.du[3 * lin + 1] = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
-                    a.du[3 * lin + 2] = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
-                  }
-                }
-                const float cx = (float)X - g.ctr[0], cy = (float)Y - g.ctr[1], cz = (float)zo - g.ctr[2];
-                acc[kPS + 0] += e0;
-                acc[kPS + 1] += e1;
-                acc[kPS + 2] += e2;
-                acc[kPM + 0] = fmaf(e0, cx, acc[kPM + 0]);
-                acc[kPM + 1] = fmaf(e0, cy, acc[kPM + 1]);
-                acc[kPM + 2] = fmaf(e0, cz, acc[kPM + 2]);
-                acc[kPM + 3] = fmaf(e1, cx, acc[kPM + 3]);
-                acc[kPM + 4] = fmaf(e1, cy, acc[kPM + 4]);
-                acc[kPM + 5] = fmaf(e1, cz, acc[kPM + 5]);
-                acc[kPM + 6] = fmaf(e2, cx, acc[kPM + 6]);
-                acc[kPM + 7] = fmaf(e2, cy, acc[kPM + 7]);
-                acc[kPM + 8] = fmaf(e2, cz, acc[kPM + 8]);
-              }
+              gP[y1 * E1S + x1] = gpair;
+              gX[y1 * E1S + x1] = gfj;
             }
           }
         }
-        __syncthreads();
+      }
+      __syncthreads();
+      // [E] x sums of the g-terms onto the 32 output columns
+      {
+        constexpr int XG2 = kTX / 4;
+        for (int it = tid; it < E1H * XG2; it += kThreads) {
+          const int row = it / XG2, g4 = it - row * XG2;
+          float2 vP[NIN];
+          float vX[NIN];
+          const float4* sP4 = reinterpret_cast<const float4*>(gP + row * E1S + 4 * g4);
+          const float4* sX4 = reinterpret_cast<const float4*>(gX + row * E1S + 4 * g4);
+#pragma unroll
+          for (int k = 0; k < NIN / 2; ++k) {
+            const float4 p = sP4[k];
+            vP[2 * k] = make_float2(p.x, p.y);
+            vP[2 * k + 1] = make_float2(p.z, p.w);
+          }
+#pragma unroll
+          for (int k = 0; k < NIN / 4; ++k) {
+            const float4 x = sX4[k];
+            vX[4 * k] = x.x;
+            vX[4 * k + 1] = x.y;
+            vX[4 * k + 2] = x.z;
+            vX[4 * k + 3] = x.w;
+          }
+          float2 aP = vP[0];
+          float aX = vX[0];
+#pragma unroll
+          for (int k = 1; k <= 2 * R; ++k) {
+            aP = add2(aP, vP[k]);
+            aX += vX[k];
+          }
+          float2 oP[4];
+          float oXv[4];
+          oP[0] = aP;
+          oXv[0] = aX;
+#pragma unroll
+          for (int j = 1; j < 4; ++j) {
+            aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
+            aX = (aX + vX[2 * R + j]) - vX[j - 1];
+            oP[j] = aP;
+            oXv[j] = aX;
+          }
+          float4* dP = reinterpret_cast<float4*>(gxP + row * kTX + 4 * g4);
+          dP[0] = make_float4(oP[0].x, oP[0].y, oP[1].x, oP[1].y);
+          dP[1] = make_float4(oP[2].x, oP[2].y, oP[3].x, oP[3].y);
+          *reinterpret_cast<float4*>(gxX + row * kTX + 4 * g4) = make_float4(oXv[0], oXv[1], oXv[2], oXv[3]);
+        }
+      }
+      __syncthreads();
+      // [F] y sums of the g-terms -> 2-D window sums at the outputs, into the ring
+      {
+        float2* rP = grP + (s % W) * (TY * kTX);
+        float* rX = grX + (s % W) * (TY * kTX);
+        for (int it = tid; it < kTX * (TY / 4); it += kThreads) {
+          const int x = it % kTX, r4 = it / kTX;
+          const int ys = 4 * r4;
+          float2 vP[4 + 2 * R];
+          float vX[4 + 2 * R];
+#pragma unroll
+          for (int k = 0; k < 4 + 2 * R; ++k) {
+            vP[k] = gxP[(ys + k) * kTX + x];
+            vX[k] = gxX[(ys + k) * kTX + x];
+          }
+          float2 aP = vP[0];
+          float aX = vX[0];
+#pragma unroll
+          for (int k = 1; k <= 2 * R; ++k) {
+            aP = add2(aP, vP[k]);
+            aX += vX[k];
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j > 0) {
+              aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
+              aX = (aX + vX[2 * R + j]) - vX[j - 1];
+            }
+            rP[(ys + j) * kTX + x] = aP;
+            rX[(ys + j) * kTX + x] = aX;
+          }
+        }
+      }
+      __syncthreads();
+      // [G] z sums over the g-term ring -> dJ at plane zo, then the epilogue
+      if (pass2) {
+        const int zo = zi - 2 * R;
+#pragma unroll
+        for (int k = 0; k < NOUT; ++k) {
+          const int e = tid + k * kThreads;
+          float2 bP = grP[e];
+          float bX = grX[e];
+#pragma unroll
+          for (int q = 1; q < W; ++q) {
+            bP = add2(bP, grP[q * (TY * kTX) + e]);
+            bX += grX[q * (TY * kTX) + e];
+          }
+          const float jv = jfo[k].x, fv = jfo[k].y;
+          const int X = oX[k], Y = oY[k];
+          if (X < g.fW && Y < g.fH) {
+            float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
+            if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
+            const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
+            if (MODE == LN_DJ) {
+              if (a.dJ) a.dJ[lin] = gv;
+            } else {
+              float u0 = 0.f, u1 = 0.f, u2 = 0.f;
+              if (a.u) {
+                u0 = __ldg(a.u + 3 * lin + 0);
+                u1 = __ldg(a.u + 3 * lin + 1);
+                u2 = __ldg(a.u + 3 * lin + 2);
+              }
+              int b[3];
+              float r[3], gq0, gq1, gq2;
+              cell_of(g, P[k], u0, u1, u2, b, r);
+              trilinear<MT, true>(M, g, b, r, gq0, gq1, gq2);
+              const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
+              if (a.du) {
+                if (g.k_diag) {
+                  a.du[3 * lin + 0] = g.K[0] * e0;
+                  a.du[3 * lin + 1] = g.K[4] * e1;
+                  a.du[3 * lin + 2] = g.K[8] * e2;
+                } else {
+                  a.du[3 * lin + 0] = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
+                  a.du[3 * lin + 1] = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
+                  a.du[3 * lin + 2] = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
+                }
+              }
+              const float cx = (float)X - g.ctr[0], cy = (float)Y - g.ctr[1], cz = (float)zo - g.ctr[2];
+              acc[kPS + 0] += e0;
+              acc[kPS + 1] += e1;
+              acc[kPS + 2] += e2;
+              acc[kPM + 0] = fmaf(e0, cx, acc[kPM + 0]);
+              acc[kPM + 1] = fmaf(e0, cy, acc[kPM + 1]);
+              acc[kPM + 2] = fmaf(e0, cz, acc[kPM + 2]);
+              acc[kPM + 3] = fmaf(e1, cx, acc[kPM + 3]);
+              acc[kPM + 4] = fmaf(e1, cy, acc[kPM + 4]);
+              acc[kPM + 5] = fmaf(e1, cz, acc[kPM + 5]);
+              acc[kPM + 6] = fmaf(e2, cx, acc[kPM + 6]);
+              acc[kPM + 7] = fmaf(e2, cy, acc[kPM + 7]);
+              acc[kPM + 8] = fmaf(e2, cz, acc[kPM + 8]);
+            }
+          }
+          if (MODE == LN_BWD) {
+            P[k][0] += g.Gq[2];
+            P[k][1] += g.Gq[5];
+            P[k][2] += g.Gq[8];
+          }
+        }
       }
       // fold the fp32 partials into fp64 every 8 planes (uniform across the CTA)
       if ((s & 7) == 7) {
 #pragma unroll
         for (int k = 0; k < 12; ++k) {
-          dacc[k] += (double)warp_sum(acc[k]);
+          const float v = warp_sum(acc[k]);
+          if ((tid & 31) == 0) wsum[tid >> 5][k] += (double)v;
           acc[k] = 0.0f;
         }
-        dacc[12] += (double)warp_sum(cc_acc);
+        const float v = warp_sum(cc_acc);
+        if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
         cc_acc = 0.0f;
       }
     }
   }
 #pragma unroll
-  for (int k = 0; k < 12; ++k) dacc[k] += (double)warp_sum(acc[k]);
-  dacc[12] += (double)warp_sum(cc_acc);
-  const int w = tid >> 5;
-  if ((tid & 31) == 0)
-#pragma unroll
-    for (int k = 0; k < 13; ++k) wsum[w][k] = dacc[k];
+  for (int k = 0; k < 12; ++k) {
+    const float v = warp_sum(acc[k]);
+    if ((tid & 31) == 0) wsum[tid >> 5][k] += (double)v;
+  }
+  {
+    const float v = warp_sum(cc_acc);
+    if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
+  }
   __syncthreads();
   if (tid < kPartialStride) {
     double s = 0.0;
@@ -328,10 +565,10 @@ __global__ void __launch_bounds__(kThreads) k_lncc(const LnccArgs a) {
 }
 
 // occ != nullptr: report resident CTAs per SM instead of launching.
-template <typename FT, typename MT, int MODE, int BMAX>
-static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int R, int* occ) {
-  auto k = k_lncc<FT, MT, MODE, BMAX>;
-  const size_t smem = lncc_smem_bytes(R, BMAX);
+template <typename FT, typename MT, int MODE, int BMAX, int R>
+static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
+  auto k = k_lncc<FT, MT, MODE, BMAX, R>;
+  const size_t smem = smem_of<R>();
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kThreads, smem);
@@ -341,21 +578,34 @@ static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int R, 
   return cudaGetLastError();
 }
 
+template <int R>
+static cudaError_t dispatch_r(int mode, int ft, int mt, int bmax, const LnccArgs& a, int grid, cudaStream_t s,
+                              int* occ) {
+  cudaError_t e = cudaErrorInvalidValue;
+  FFDP_DT_SWITCH(ft, FT, {
+    if (mode == LN_DJ) {
+      e = run_lncc<FT, float, LN_DJ, 0, R>(a, grid, s, occ);
+    } else if (ft == mt) {
+      if (bmax == 0)
+        e = run_lncc<FT, FT, LN_BWD, 0, R>(a, grid, s, occ);
+      else if (bmax == 32)
+        e = run_lncc<FT, FT, LN_BWD, 32, R>(a, grid, s, occ);
+      else
+        e = run_lncc<FT, FT, LN_BWD, 64, R>(a, grid, s, occ);
+    }
+  });
+  return e;
+}
+
 static cudaError_t dispatch_lncc(int mode, int ft, int mt, int bmax, const LnccArgs& a, int grid,
                                  cudaStream_t s, int R, int* occ) {
-  cudaError_t e = cudaErrorInvalidValue;
-  FFDP_DT_SWITCH(ft, FT, FFDP_DT_SWITCH(mt, MT, {
-    if (mode == LN_DJ) {
-      e = run_lncc<FT, float, LN_DJ, 0>(a, grid, s, R, occ);
-    } else if (bmax == 0) {
-      e = run_lncc<FT, MT, LN_BWD, 0>(a, grid, s, R, occ);
-    } else if (bmax == 32) {
-      e = run_lncc<FT, MT, LN_BWD, 32>(a, grid, s, R, occ);
-    } else {
-      e = run_lncc<FT, MT, LN_BWD, 64>(a, grid, s, R, occ);
-    }
-  }));
-  return e;
+  switch (R) {
+    case 1: return dispatch_r<1>(mode, ft, mt, bmax, a, grid, s, occ);
+    case 2: return dispatch_r<2>(mode, ft, mt, bmax, a, grid, s, occ);
+    case 3: return dispatch_r<3>(mode, ft, mt, bmax, a, grid, s, occ);
+    case 4: return dispatch_r<4>(mode, ft, mt, bmax, a, grid, s, occ);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_lncc(int mode, int ft, int mt, int bmax, const LnccArgs& a, int grid, cudaStream_t s) {
