@@ -318,6 +318,7 @@ def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
 
 
 def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h):
+    value = N * ws / (ms * 1e-3) / 1e9
     # ---- roofline of the dominant kernel (algorithmic bytes / its own time)
     peak, peak_kind = _peaks()
     dom = max(kern.items(), key=lambda kv: kv[1][1]) if kern else ("?", (1, ms))

@@ -29,8 +29,10 @@ def _nvcc() -> str:
 
 
 def _flags(extra=()):
+    # FFDP_NVCC_DEFINES: extra -D tuning macros (e.g. "FFDP_SWEEP_MINB=3"), for tuning runs
+    defs = ["-D" + d for d in os.environ.get("FFDP_NVCC_DEFINES", "").split() if d]
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-                   "-I" + os.path.join(HERE, "..", "include")] + list(extra)
+                   "-I" + os.path.join(HERE, "..", "include")] + defs + list(extra)
 
 
 def _stale() -> bool:

@@ -209,6 +209,7 @@ ffdp_status make_geom(ffdp_dims f, ffdp_dims m, const ffdp_transform* T, Geom& g
     g.ctr[r] = (float)((nf[r] - 1.0) / 2.0);
   }
   g.w4 = (f.w % 4) == 0 ? 1 : 0;
+  g.a_diag = (g.Gq[1] == 0 && g.Gq[2] == 0 && g.Gq[3] == 0 && g.Gq[5] == 0 && g.Gq[6] == 0 && g.Gq[7] == 0) ? 1 : 0;
   g.k_diag = (T->S[1] == 0.f && T->S[2] == 0.f && T->S[3] == 0.f && T->S[5] == 0.f && T->S[6] == 0.f &&
               T->S[7] == 0.f)
                  ? 1
@@ -270,7 +271,7 @@ int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
 
 // Workspace layout (byte offsets, 256-aligned).
 struct Ws {
-  size_t hist, table, table2, scalars, partials, J, total;
+  size_t hist, table, table2, scalars, partials, J, G, total;
 };
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -286,9 +287,12 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
   if (mi && needJ) o = al(o + (size_t)bmax * bmax * 2 * sizeof(float));
   w.scalars = o;
   o = al(o + 16 * sizeof(double));
+  // two partial-record sets: the LNCC kernel's and the gradient sweep's
   w.partials = o;
-  o = al(o + max_parts * kPartialStride * sizeof(double));
+  o = al(o + 2 * max_parts * kPartialStride * sizeof(double));
   w.J = o;
+  if (needJ) o = al(o + (size_t)N * sizeof(float));
+  w.G = o;
   if (needJ) o = al(o + (size_t)N * sizeof(float));
   w.total = o;
   return w;
@@ -606,13 +610,13 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   }
   int nparts = 0;
   if (ln) {
+    // LNCC window kernel: g = dL/dJ (LNCC term + MI term from on-chip J, F)
+    float* Gbuf = reinterpret_cast<float*>(wb + w.G);
     LnccArgs a{};
     a.g = g;
     a.F = F;
     a.J = Jbuf;
-    a.M = M;
-    a.u = u;
-    a.du = du;
+    a.dJ = Gbuf;
     a.T = table2;
     a.partials = partials;
     a.bf = bf;
@@ -624,9 +628,20 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a.gscale = (float)(-(double)p->w_lncc / (double)N);
     const int bm = mi ? bmax : 0;
     int grid = 1;
-    lncc_tiling(fdims, a.R, a, lncc_ctas_per_sm(LN_BWD, ft, mt, bm, a.R), grid);
-    FFDP_CUDA(launch_lncc(LN_BWD, ft, mt, bm, a, grid, s), "LNCC sweep launch");
-    nparts = grid;
+    lncc_tiling(fdims, a.R, a, lncc_ctas_per_sm(LN_DJ, ft, 0, bm, a.R), grid);
+    FFDP_CUDA(launch_lncc(LN_DJ, ft, 0, bm, a, grid, s), "LNCC window launch");
+    // sampler backward of g: du, affine partials
+    Sweep2Args a2{};
+    a2.g = g;
+    a2.M = M;
+    a2.u = u;
+    a2.gbuf = Gbuf;
+    a2.du = du;
+    a2.partials = partials + (size_t)grid * kPartialStride;
+    a2.nIter = n_iter(N);
+    const int grid2 = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_GBUF, 0, mt, 32));
+    FFDP_CUDA(launch_sweep2(S2_GBUF, 0, mt, 32, a2, grid2, s), "sampler backward launch");
+    nparts = grid + grid2;
   } else {
     Sweep2Args a2{};
     a2.g = g;

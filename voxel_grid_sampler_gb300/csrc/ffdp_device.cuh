@@ -48,15 +48,19 @@ struct Geom {
   unsigned divW_m, divHW_m;  // fast division magic numbers for W and H*W
   int divW_s, divHW_s;
   int k_diag;       // K is diagonal (S diagonal): u enters q component-wise
+  int a_diag;       // G is diagonal (A diagonal)
   int w4;           // fW % 4 == 0: a 4-voxel group never crosses a row
 };
 
 // Integer part k and fraction f in [0, 1) of the fixed-point anchor of voxel
 // (ix, iy, iz); |k| < 2^25 is guaranteed by the host-side range check.
 __device__ __forceinline__ void anchor_kf(const Geom& g, int ix, int iy, int iz, int k[3], float f[3]) {
+  const int idx[3] = {ix, iy, iz};
 #pragma unroll
   for (int r = 0; r < 3; ++r) {
-    const long long P = g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
+    // a diagonal affine part (the common case) needs one product per axis
+    const long long P = g.a_diag ? g.g0q[r] + g.Gq[r * 4] * idx[r]
+                                 : g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
     k[r] = (int)(P >> 32);
     f[r] = __uint_as_float(0x3f800000u | ((unsigned)(P & 0xffffffffll) >> 9)) - 1.0f;
   }
@@ -87,6 +91,12 @@ __device__ __forceinline__ void anchor(const Geom& g, int ix, int iy, int iz, lo
 // x + 1.5*2^23 rounds to the nearest integer, corrected by one when it
 // rounded up.
 __device__ __forceinline__ void floor_split(float t, int& fi, float& fr) {
+#ifndef FFDP_FLOOR_MAGIC_ONLY
+  // round-down instruction, then the exact integer through the same trick
+  const float fl = floorf(t);
+  fi = (int)(__float_as_uint(fl + kMagic) - kMagicBits);
+  fr = t - fl;
+#else
   float a = t + kMagic;
   float fl = a - kMagic;
   int i = (int)(__float_as_uint(a) - kMagicBits);
@@ -96,6 +106,7 @@ __device__ __forceinline__ void floor_split(float t, int& fi, float& fr) {
   }
   fi = i;
   fr = t - fl;
+#endif
 }
 
 // Cell of the moving image containing q = P + K u: integer corner b (clamped
@@ -144,6 +155,40 @@ __device__ __forceinline__ void cell_v(const Geom& g, const int k[3], const floa
     b[c] = min(max(k[c] + fi, -2), nm[c]);
     r[c] = fr;
   }
+}
+
+// ------------------------------------------------- packed fp32 pairs
+// Blackwell executes add/sub/mul/fma on a pair of fp32 values held in a
+// 64-bit register pair as one instruction (PTX .f32x2, sm_100 and later).
+__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+  return bits_f2(d);
 }
 
 // ------------------------------------------------------------- M access
@@ -195,21 +240,23 @@ __device__ __forceinline__ float trilinear(const MT* __restrict__ M, const Geom&
     m110 = at(1, 1, 0, z1 && y1 && x0);
     m111 = at(1, 1, 1, z1 && y1 && x1);
   }
-  const float rx = r[0], ry = r[1], rz = r[2];
-  const float dx00 = m001 - m000, dx01 = m011 - m010, dx10 = m101 - m100, dx11 = m111 - m110;
-  const float c00 = fmaf(rx, dx00, m000), c01 = fmaf(rx, dx01, m010);
-  const float c10 = fmaf(rx, dx10, m100), c11 = fmaf(rx, dx11, m110);
-  const float dy0 = c01 - c00, dy1 = c11 - c10;
-  const float c0 = fmaf(ry, dy0, c00), c1 = fmaf(ry, dy1, c10);
-  const float dz = c1 - c0;
+  // the two z planes of the cell run as packed pairs (z0, z1)
+  const float rz = r[2];
+  const float2 rx2 = make_float2(r[0], r[0]), ry2 = make_float2(r[1], r[1]);
+  const float2 a0 = make_float2(m000, m100), a1 = make_float2(m001, m101);
+  const float2 b0 = make_float2(m010, m110), b1 = make_float2(m011, m111);
+  const float2 dxa = sub2(a1, a0), dxb = sub2(b1, b0);           // x differences at y0, y1
+  const float2 ca = fma2(rx2, dxa, a0), cb = fma2(rx2, dxb, b0);  // x-lerped at y0, y1
+  const float2 dy = sub2(cb, ca);
+  const float2 c = fma2(ry2, dy, ca);                             // (c0, c1)
+  const float dz = c.y - c.x;
   if (GRAD) {
     gz = dz;
-    gy = fmaf(rz, dy1 - dy0, dy0);
-    const float e0 = fmaf(ry, dx01 - dx00, dx00);
-    const float e1 = fmaf(ry, dx11 - dx10, dx10);
-    gx = fmaf(rz, e1 - e0, e0);
+    gy = fmaf(rz, dy.y - dy.x, dy.x);
+    const float2 e = fma2(ry2, sub2(dxb, dxa), dxa);
+    gx = fmaf(rz, e.y - e.x, e.x);
   }
-  return fmaf(rz, dz, c0);
+  return fmaf(rz, dz, c.x);
 }
 
 // ------------------------------------------------------- Parzen window
@@ -245,40 +292,6 @@ struct BinMap {
 
 __device__ __forceinline__ float bin_coord(const BinMap& m, float v) {
   return fmaf(fminf(fmaxf(v, m.lo), m.hi) - m.lo, m.sc, 2.0f);
-}
-
-// ------------------------------------------------- packed fp32 pairs
-// Blackwell executes add/sub/mul/fma on a pair of fp32 values held in a
-// 64-bit register pair as one instruction (PTX .f32x2, sm_100 and later).
-__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
-  return r;
-}
-__device__ __forceinline__ float2 bits_f2(unsigned long long r) {
-  float2 v;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
-  return v;
-}
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)));
-  return bits_f2(d);
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
-  return bits_f2(d);
 }
 
 // --------------------------------------------------------- reductions

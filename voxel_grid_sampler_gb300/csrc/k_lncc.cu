@@ -1,5 +1,6 @@
 // k_lncc.cu -- fused LNCC forward + backward on a materialised warped image J,
-// optionally fused with the MI partial gradient and the sampler backward.
+// optionally adding the MI partial gradient: writes g = dL/dJ per voxel (the
+// sampler backward of g runs in the linear gradient sweep).
 //
 // Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
 // Registration", Key designs item 2: all LNCC intermediates (the window sums
@@ -21,8 +22,8 @@
 //       plane zc = zi - R on the R-halo region,
 //   [E] x sums and [F] y sums of the g-terms -> their 2-D window sums at the
 //       output columns, kept in a ring of w planes,
-//   [G] z sums over that ring give dJ at plane zo = zi - 2R, then the
-//       epilogue (dJ store, or MI gradient + sampler backward).
+//   [G] z sums over that ring give dJ at plane zo = zi - 2R; the MI term
+//       (from the on-chip J and F) is added and g is stored.
 // The next plane is fetched into registers during a step and written to the
 // ring after [B], so global latency overlaps the shared-memory work.  The
 // first window pass uses direct fp32 sums in z (no sliding add/subtract) to
@@ -102,7 +103,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
-template <typename FT, typename MT, int MODE, int BMAX, int R>
+template <typename FT, int BMAX, int R>
 __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArgs a) {
   using L = LT<R>;
   constexpr int W = L::W, TY = L::TY, E2H = L::E2H, E2W = L::E2W, E2S = L::E2S;
@@ -132,32 +133,25 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   const Geom& g = a.g;
   const int tid = threadIdx.x;
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
-  const MT* __restrict__ M = static_cast<const MT*>(a.M);
   const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
   const float2 ninv2 = make_float2(-inv_n, -inv_n);
+  const size_t plane = (size_t)g.fW * g.fH;
   float cc_acc = 0.0f;
-  float acc[12];
-#pragma unroll
-  for (int k = 0; k < 12; ++k) acc[k] = 0.0f;
-  if ((tid & 31) == 0)
-#pragma unroll
-    for (int k = 0; k < 13; ++k) wsum[tid >> 5][k] = 0.0;
+  if ((tid & 31) == 0) wsum[tid >> 5][12] = 0.0;
 
+  // this thread's staged elements of a halo plane: in-plane offset, or -1
+  // where the element lies outside the grid (read as zero)
   float2 stg[NSTG];
-  auto load_plane = [&](int zp, int x0, int y0) {
+  int soff[NSTG];
+  auto load_plane = [&](int zp) {
     const bool zin = zp >= 0 && zp < g.fD;
+    const size_t base = (size_t)zp * plane;
 #pragma unroll
     for (int i = 0; i < NSTG; ++i) {
-      const int e = tid + i * kThreads;
       float2 v = make_float2(0.0f, 0.0f);
-      if (e < E2H * E2W) {
-        const int ey = e / E2W, ex = e - ey * E2W;
-        const int x = x0 - 2 * R + ex, y = y0 - 2 * R + ey;
-        if (zin && (unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) {
-          const size_t lin = ((size_t)zp * g.fH + y) * g.fW + x;
-          v.x = __ldg(a.J + lin);
-          v.y = load1(F + lin);
-        }
+      if (zin && soff[i] >= 0) {
+        v.x = __ldg(a.J + base + soff[i]);
+        v.y = load1(F + base + soff[i]);
       }
       stg[i] = v;
     }
@@ -183,21 +177,26 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
     const int z1 = min(z0 + a.tz, g.fD);
     const int nsteps = (z1 - z0) + 4 * R;
 
-    // epilogue positions and their fixed-point anchors at plane z0
+    // output positions of this thread
     int oX[NOUT], oY[NOUT];
-    long long P[NOUT][3];
 #pragma unroll
     for (int k = 0; k < NOUT; ++k) {
       const int e = tid + k * kThreads;
       oY[k] = y0 + e / kTX;
       oX[k] = x0 + (e % kTX);
-      if (MODE == LN_BWD) anchor(g, oX[k], oY[k], z0, P[k]);
+    }
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      const int e = tid + i * kThreads;
+      const int ey = e / E2W, ex = e - ey * E2W;
+      const int x = x0 - 2 * R + ex, y = y0 - 2 * R + ey;
+      soff[i] = (e < E2H * E2W && (unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) ? y * g.fW + x : -1;
     }
 
     __syncthreads();  // previous tile finished with every buffer
-    load_plane(z0 - 2 * R, x0, y0);
+    load_plane(z0 - 2 * R);
     store_plane(0);
-    if (nsteps > 1) load_plane(z0 - 2 * R + 1, x0, y0);
+    if (nsteps > 1) load_plane(z0 - 2 * R + 1);
     __syncthreads();
 
     for (int s = 0; s < nsteps; ++s) {
@@ -254,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
       // the oldest ring slot is free: write the staged plane, fetch the next
       if (s + 1 < nsteps) {
         store_plane((s + 1) % W);
-        if (s + 2 < nsteps) load_plane(zi + 2, x0, y0);
+        if (s + 2 < nsteps) load_plane(zi + 2);
       }
       if (!pass1) {
         __syncthreads();
@@ -484,72 +483,17 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
           if (X < g.fW && Y < g.fH) {
             float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
             if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
-            const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
-            if (MODE == LN_DJ) {
-              if (a.dJ) a.dJ[lin] = gv;
-            } else {
-              float u0 = 0.f, u1 = 0.f, u2 = 0.f;
-              if (a.u) {
-                u0 = __ldg(a.u + 3 * lin + 0);
-                u1 = __ldg(a.u + 3 * lin + 1);
-                u2 = __ldg(a.u + 3 * lin + 2);
-              }
-              int b[3];
-              float r[3], gq0, gq1, gq2;
-              cell_of(g, P[k], u0, u1, u2, b, r);
-              trilinear<MT, true>(M, g, b, r, gq0, gq1, gq2);
-              const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
-              if (a.du) {
-                if (g.k_diag) {
-                  a.du[3 * lin + 0] = g.K[0] * e0;
-                  a.du[3 * lin + 1] = g.K[4] * e1;
-                  a.du[3 * lin + 2] = g.K[8] * e2;
-                } else {
-                  a.du[3 * lin + 0] = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
-                  a.du[3 * lin + 1] = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
-                  a.du[3 * lin + 2] = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
-                }
-              }
-              const float cx = (float)X - g.ctr[0], cy = (float)Y - g.ctr[1], cz = (float)zo - g.ctr[2];
-              acc[kPS + 0] += e0;
-              acc[kPS + 1] += e1;
-              acc[kPS + 2] += e2;
-              acc[kPM + 0] = fmaf(e0, cx, acc[kPM + 0]);
-              acc[kPM + 1] = fmaf(e0, cy, acc[kPM + 1]);
-              acc[kPM + 2] = fmaf(e0, cz, acc[kPM + 2]);
-              acc[kPM + 3] = fmaf(e1, cx, acc[kPM + 3]);
-              acc[kPM + 4] = fmaf(e1, cy, acc[kPM + 4]);
-              acc[kPM + 5] = fmaf(e1, cz, acc[kPM + 5]);
-              acc[kPM + 6] = fmaf(e2, cx, acc[kPM + 6]);
-              acc[kPM + 7] = fmaf(e2, cy, acc[kPM + 7]);
-              acc[kPM + 8] = fmaf(e2, cz, acc[kPM + 8]);
-            }
-          }
-          if (MODE == LN_BWD) {
-            P[k][0] += g.Gq[2];
-            P[k][1] += g.Gq[5];
-            P[k][2] += g.Gq[8];
+            if (a.dJ) a.dJ[((size_t)zo * g.fH + Y) * g.fW + X] = gv;
           }
         }
       }
-      // fold the fp32 partials into fp64 every 8 planes (uniform across the CTA)
-      if ((s & 7) == 7) {
-#pragma unroll
-        for (int k = 0; k < 12; ++k) {
-          const float v = warp_sum(acc[k]);
-          if ((tid & 31) == 0) wsum[tid >> 5][k] += (double)v;
-          acc[k] = 0.0f;
-        }
+      // fold the fp32 cc partial into fp64 every 32 planes (uniform across the CTA)
+      if ((s & 31) == 31) {
         const float v = warp_sum(cc_acc);
         if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
         cc_acc = 0.0f;
       }
     }
-  }
-#pragma unroll
-  for (int k = 0; k < 12; ++k) {
-    const float v = warp_sum(acc[k]);
-    if ((tid & 31) == 0) wsum[tid >> 5][k] += (double)v;
   }
   {
     const float v = warp_sum(cc_acc);
@@ -558,16 +502,16 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   __syncthreads();
   if (tid < kPartialStride) {
     double s = 0.0;
-    if (tid < 13)
-      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][tid];
+    if (tid == kPCC)
+      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][kPCC];
     a.partials[(size_t)blockIdx.x * kPartialStride + tid] = s;
   }
 }
 
 // occ != nullptr: report resident CTAs per SM instead of launching.
-template <typename FT, typename MT, int MODE, int BMAX, int R>
+template <typename FT, int BMAX, int R>
 static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
-  auto k = k_lncc<FT, MT, MODE, BMAX, R>;
+  auto k = k_lncc<FT, BMAX, R>;
   const size_t smem = smem_of<R>();
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -579,20 +523,16 @@ static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* oc
 }
 
 template <int R>
-static cudaError_t dispatch_r(int mode, int ft, int mt, int bmax, const LnccArgs& a, int grid, cudaStream_t s,
-                              int* occ) {
+static cudaError_t dispatch_r(int mode, int ft, int bmax, const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
   cudaError_t e = cudaErrorInvalidValue;
+  if (mode != LN_DJ) return e;
   FFDP_DT_SWITCH(ft, FT, {
-    if (mode == LN_DJ) {
-      e = run_lncc<FT, float, LN_DJ, 0, R>(a, grid, s, occ);
-    } else if (ft == mt) {
-      if (bmax == 0)
-        e = run_lncc<FT, FT, LN_BWD, 0, R>(a, grid, s, occ);
-      else if (bmax == 32)
-        e = run_lncc<FT, FT, LN_BWD, 32, R>(a, grid, s, occ);
-      else
-        e = run_lncc<FT, FT, LN_BWD, 64, R>(a, grid, s, occ);
-    }
+    if (bmax == 0)
+      e = run_lncc<FT, 0, R>(a, grid, s, occ);
+    else if (bmax == 32)
+      e = run_lncc<FT, 32, R>(a, grid, s, occ);
+    else
+      e = run_lncc<FT, 64, R>(a, grid, s, occ);
   });
   return e;
 }
@@ -600,10 +540,10 @@ static cudaError_t dispatch_r(int mode, int ft, int mt, int bmax, const LnccArgs
 static cudaError_t dispatch_lncc(int mode, int ft, int mt, int bmax, const LnccArgs& a, int grid,
                                  cudaStream_t s, int R, int* occ) {
   switch (R) {
-    case 1: return dispatch_r<1>(mode, ft, mt, bmax, a, grid, s, occ);
-    case 2: return dispatch_r<2>(mode, ft, mt, bmax, a, grid, s, occ);
-    case 3: return dispatch_r<3>(mode, ft, mt, bmax, a, grid, s, occ);
-    case 4: return dispatch_r<4>(mode, ft, mt, bmax, a, grid, s, occ);
+    case 1: return dispatch_r<1>(mode, ft, bmax, a, grid, s, occ);
+    case 2: return dispatch_r<2>(mode, ft, bmax, a, grid, s, occ);
+    case 3: return dispatch_r<3>(mode, ft, bmax, a, grid, s, occ);
+    case 4: return dispatch_r<4>(mode, ft, bmax, a, grid, s, occ);
   }
   return cudaErrorInvalidValue;
 }

@@ -253,7 +253,13 @@ __device__ __forceinline__ void walk_cell(const Geom& g, GroupWalk& w, int v, fl
 // ------------------------------------------------------------------ sweep 1
 // Sampling (or reading J) plus, per mode, the histogram and/or a J store.
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kThreads) k_sweep1(const Sweep1Args a) {
+#ifndef FFDP_SWEEP1_MINB
+#define FFDP_SWEEP1_MINB 1
+#endif
+#ifndef FFDP_SWEEP2_MINB
+#define FFDP_SWEEP2_MINB 1
+#endif
+__global__ void __launch_bounds__(kThreads, FFDP_SWEEP1_MINB) k_sweep1(const Sweep1Args a) {
   constexpr bool HIST = MODE != S1_WRITEJ;
   constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
   constexpr bool WRITEJ = (MODE == S1_WRITEJ) || (MODE == S1_HIST_WRITEJ);
@@ -270,12 +276,23 @@ __global__ void __launch_bounds__(kThreads) k_sweep1(const Sweep1Args a) {
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
   const MT* __restrict__ M = static_cast<const MT*>(a.M);
   int pending = 0;
+  // the F / u group of the next iteration is fetched while this one is processed
+  Group Gnext;
+  {
+    const unsigned l0 = (blockIdx.x * kThreads + threadIdx.x) * kVPT;
+    if (blockIdx.x < a.nIter && l0 < g.N)
+      load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, l0, min(g.N - l0, (unsigned)kVPT), Gnext);
+  }
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x) {
     const unsigned lin0 = (it * kThreads + threadIdx.x) * kVPT;
+    Group G = Gnext;
+    {
+      const unsigned itn = it + gridDim.x, ln = (itn * kThreads + threadIdx.x) * kVPT;
+      if (itn < a.nIter && ln < g.N)
+        load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, ln, min(g.N - ln, (unsigned)kVPT), Gnext);
+    }
     if (lin0 < g.N) {
       const unsigned nv = min(g.N - lin0, (unsigned)kVPT);
-      Group G;
-      load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, lin0, nv, G);
       if (SAMPLE) {
         GroupWalk w;
         walk_begin(g, lin0, w);
@@ -399,7 +416,7 @@ __global__ void __launch_bounds__(1024) k_mi_finalize(const FinalizeArgs a) {
 // materialised J) or the sampler backward: du = K^T (g dJ/dq) and the affine
 // partial sums, reduced per CTA in fp64.
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kThreads) k_sweep2(const Sweep2Args a) {
+__global__ void __launch_bounds__(kThreads, FFDP_SWEEP2_MINB) k_sweep2(const Sweep2Args a) {
   constexpr bool MI = MODE != S2_GBUF;
   constexpr bool SAMPLE = MODE != S2_MI_JBUF;
   constexpr bool BWD = MODE != S2_MI_JBUF;
@@ -423,12 +440,22 @@ __global__ void __launch_bounds__(kThreads) k_sweep2(const Sweep2Args a) {
 #pragma unroll
   for (int k = 0; k < 12; ++k) acc[k] = 0.0f;
   int pending = 0;
+  Group Gnext;
+  {
+    const unsigned l0 = (blockIdx.x * kThreads + threadIdx.x) * kVPT;
+    if (blockIdx.x < a.nIter && l0 < g.N)
+      load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, l0, min(g.N - l0, (unsigned)kVPT), Gnext);
+  }
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x) {
     const unsigned lin0 = (it * kThreads + threadIdx.x) * kVPT;
+    Group G = Gnext;
+    {
+      const unsigned itn = it + gridDim.x, ln = (itn * kThreads + threadIdx.x) * kVPT;
+      if (itn < a.nIter && ln < g.N)
+        load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, ln, min(g.N - ln, (unsigned)kVPT), Gnext);
+    }
     if (lin0 < g.N) {
       const unsigned nv = min(g.N - lin0, (unsigned)kVPT);
-      Group G;
-      load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, lin0, nv, G);
       float out[3 * kVPT];
       if (SAMPLE) {
         GroupWalk w;
