@@ -203,6 +203,66 @@ __device__ __forceinline__ float ldg_f<__half>(const __half* p) {
   return __half2float(__ldg(p));
 }
 
+// The 8 taps of cell b (m[z][y][x] order: 000,001,010,011,100,101,110,111),
+// zero outside M.  Split from the interpolation so callers can issue the
+// loads of several voxels before using any of them.
+template <typename MT>
+__device__ __forceinline__ void gather8(const MT* __restrict__ M, const Geom& g, const int b[3], float m[8]) {
+  const int bx = b[0], by = b[1], bz = b[2];
+  if ((unsigned)bx < (unsigned)(g.mW - 1) && (unsigned)by < (unsigned)(g.mH - 1) &&
+      (unsigned)bz < (unsigned)(g.mD - 1)) {
+    const unsigned off = ((unsigned)bz * (unsigned)g.mH + (unsigned)by) * (unsigned)g.mW + (unsigned)bx;
+    const MT* p = M + off;
+    const MT* q = M + (off + (unsigned)g.mW);
+    const MT* p2 = M + (off + (unsigned)g.mHW);
+    const MT* q2 = M + (off + (unsigned)g.mHW + (unsigned)g.mW);
+    m[0] = ldg_f(p);
+    m[1] = ldg_f(p + 1);
+    m[2] = ldg_f(q);
+    m[3] = ldg_f(q + 1);
+    m[4] = ldg_f(p2);
+    m[5] = ldg_f(p2 + 1);
+    m[6] = ldg_f(q2);
+    m[7] = ldg_f(q2 + 1);
+  } else {
+    const bool x0 = (unsigned)bx < (unsigned)g.mW, x1 = (unsigned)(bx + 1) < (unsigned)g.mW;
+    const bool y0 = (unsigned)by < (unsigned)g.mH, y1 = (unsigned)(by + 1) < (unsigned)g.mH;
+    const bool z0 = (unsigned)bz < (unsigned)g.mD, z1 = (unsigned)(bz + 1) < (unsigned)g.mD;
+    auto at = [&](int dz, int dy, int dx, bool ok) -> float {
+      return ok ? ldg_f(M + ((long long)(bz + dz) * g.mH + (by + dy)) * g.mW + (bx + dx)) : 0.0f;
+    };
+    m[0] = at(0, 0, 0, z0 && y0 && x0);
+    m[1] = at(0, 0, 1, z0 && y0 && x1);
+    m[2] = at(0, 1, 0, z0 && y1 && x0);
+    m[3] = at(0, 1, 1, z0 && y1 && x1);
+    m[4] = at(1, 0, 0, z1 && y0 && x0);
+    m[5] = at(1, 0, 1, z1 && y0 && x1);
+    m[6] = at(1, 1, 0, z1 && y1 && x0);
+    m[7] = at(1, 1, 1, z1 && y1 && x1);
+  }
+}
+
+// Trilinear value (and optionally dJ/dq) from the 8 taps and fractions r.
+template <bool GRAD>
+__device__ __forceinline__ float interp8(const float m[8], const float r[3], float& gx, float& gy, float& gz) {
+  const float rz = r[2];
+  const float2 rx2 = make_float2(r[0], r[0]), ry2 = make_float2(r[1], r[1]);
+  const float2 a0 = make_float2(m[0], m[4]), a1 = make_float2(m[1], m[5]);
+  const float2 b0 = make_float2(m[2], m[6]), b1 = make_float2(m[3], m[7]);
+  const float2 dxa = sub2(a1, a0), dxb = sub2(b1, b0);
+  const float2 ca = fma2(rx2, dxa, a0), cb = fma2(rx2, dxb, b0);
+  const float2 dy = sub2(cb, ca);
+  const float2 c = fma2(ry2, dy, ca);
+  const float dz = c.y - c.x;
+  if (GRAD) {
+    gz = dz;
+    gy = fmaf(rz, dy.y - dy.x, dy.x);
+    const float2 e = fma2(ry2, sub2(dxb, dxa), dxa);
+    gx = fmaf(rz, e.y - e.x, e.x);
+  }
+  return fmaf(rz, dz, c.x);
+}
+
 // Trilinear sample of M at cell (b, r) with zero padding per tap; optionally
 // the slope dJ/dq from the same 8 taps (cell [b, b+1] on every axis).
 template <typename MT, bool GRAD>

@@ -42,6 +42,12 @@ static_assert(flush_every<32>() >= 16 && flush_every<64>() >= 16, "histogram flu
 // fp32 per-thread gradient partials are folded into fp64 every this many iterations.
 constexpr int kFoldEvery = 16;
 
+// Fetch the next iteration's F / u group while processing the current one.
+#ifndef FFDP_PREFETCH
+#define FFDP_PREFETCH 0
+#endif
+constexpr bool kPrefetch = FFDP_PREFETCH != 0;
+
 __global__ void k_zero_u64(unsigned long long* p, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0ull;
 }
@@ -250,15 +256,17 @@ __device__ __forceinline__ void walk_cell(const Geom& g, GroupWalk& w, int v, fl
   }
 }
 
+// Minimum resident CTAs per SM requested from the register allocator.
+#ifndef FFDP_SWEEP1_MINB
+#define FFDP_SWEEP1_MINB 2
+#endif
+#ifndef FFDP_SWEEP2_MINB
+#define FFDP_SWEEP2_MINB 2
+#endif
+
 // ------------------------------------------------------------------ sweep 1
 // Sampling (or reading J) plus, per mode, the histogram and/or a J store.
 template <typename FT, typename MT, int BMAX, int MODE>
-#ifndef FFDP_SWEEP1_MINB
-#define FFDP_SWEEP1_MINB 1
-#endif
-#ifndef FFDP_SWEEP2_MINB
-#define FFDP_SWEEP2_MINB 1
-#endif
 __global__ void __launch_bounds__(kThreads, FFDP_SWEEP1_MINB) k_sweep1(const Sweep1Args a) {
   constexpr bool HIST = MODE != S1_WRITEJ;
   constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
@@ -280,28 +288,37 @@ __global__ void __launch_bounds__(kThreads, FFDP_SWEEP1_MINB) k_sweep1(const Swe
   Group Gnext;
   {
     const unsigned l0 = (blockIdx.x * kThreads + threadIdx.x) * kVPT;
-    if (blockIdx.x < a.nIter && l0 < g.N)
+    if (kPrefetch && blockIdx.x < a.nIter && l0 < g.N)
       load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, l0, min(g.N - l0, (unsigned)kVPT), Gnext);
   }
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x) {
     const unsigned lin0 = (it * kThreads + threadIdx.x) * kVPT;
     Group G = Gnext;
-    {
+    if (kPrefetch) {
       const unsigned itn = it + gridDim.x, ln = (itn * kThreads + threadIdx.x) * kVPT;
       if (itn < a.nIter && ln < g.N)
         load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, ln, min(g.N - ln, (unsigned)kVPT), Gnext);
+    } else if (lin0 < g.N) {
+      load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, lin0, min(g.N - lin0, (unsigned)kVPT), G);
     }
     if (lin0 < g.N) {
       const unsigned nv = min(g.N - lin0, (unsigned)kVPT);
       if (SAMPLE) {
+        // all 32 tap loads of the group are issued before any interpolation
         GroupWalk w;
         walk_begin(g, lin0, w);
+        float taps[kVPT][8], rr[kVPT][3];
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
           int b[3], ix, iy, iz;
-          float r[3], d0, d1, d2;
-          walk_cell(g, w, v, G.u[3 * v], G.u[3 * v + 1], G.u[3 * v + 2], b, r, ix, iy, iz);
-          if ((unsigned)v < nv) G.j[v] = trilinear<MT, false>(M, g, b, r, d0, d1, d2);
+          walk_cell(g, w, v, G.u[3 * v], G.u[3 * v + 1], G.u[3 * v + 2], b, rr[v], ix, iy, iz);
+          if ((unsigned)v >= nv) b[0] = -2;  // past the end: no loads
+          gather8<MT>(M, g, b, taps[v]);
+        }
+#pragma unroll
+        for (int v = 0; v < kVPT; ++v) {
+          float d0, d1, d2;
+          G.j[v] = interp8<false>(taps[v], rr[v], d0, d1, d2);
         }
       }
       if (HIST) {
@@ -443,32 +460,42 @@ __global__ void __launch_bounds__(kThreads, FFDP_SWEEP2_MINB) k_sweep2(const Swe
   Group Gnext;
   {
     const unsigned l0 = (blockIdx.x * kThreads + threadIdx.x) * kVPT;
-    if (blockIdx.x < a.nIter && l0 < g.N)
+    if (kPrefetch && blockIdx.x < a.nIter && l0 < g.N)
       load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, l0, min(g.N - l0, (unsigned)kVPT), Gnext);
   }
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x) {
     const unsigned lin0 = (it * kThreads + threadIdx.x) * kVPT;
     Group G = Gnext;
-    {
+    if (kPrefetch) {
       const unsigned itn = it + gridDim.x, ln = (itn * kThreads + threadIdx.x) * kVPT;
       if (itn < a.nIter && ln < g.N)
         load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, ln, min(g.N - ln, (unsigned)kVPT), Gnext);
+    } else if (lin0 < g.N) {
+      load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, lin0, min(g.N - lin0, (unsigned)kVPT), G);
     }
     if (lin0 < g.N) {
       const unsigned nv = min(g.N - lin0, (unsigned)kVPT);
       float out[3 * kVPT];
       if (SAMPLE) {
+        // all 32 tap loads of the group are issued before any interpolation
         GroupWalk w;
         walk_begin(g, lin0, w);
+        float taps[kVPT][8], rr[kVPT][3];
+        int ixv[kVPT], iyv[kVPT], izv[kVPT];
+#pragma unroll
+        for (int v = 0; v < kVPT; ++v) {
+          int b[3];
+          walk_cell(g, w, v, G.u[3 * v], G.u[3 * v + 1], G.u[3 * v + 2], b, rr[v], ixv[v], iyv[v], izv[v]);
+          if ((unsigned)v >= nv) b[0] = -2;  // past the end: no loads
+          gather8<MT>(M, g, b, taps[v]);
+        }
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
           out[3 * v + 0] = out[3 * v + 1] = out[3 * v + 2] = 0.0f;
-          int b[3], ix, iy, iz;
-          float r[3];
-          walk_cell(g, w, v, G.u[3 * v], G.u[3 * v + 1], G.u[3 * v + 2], b, r, ix, iy, iz);
+          const int ix = ixv[v], iy = iyv[v], iz = izv[v];
           if ((unsigned)v < nv) {
             float gq0, gq1, gq2;
-            const float j = trilinear<MT, true>(M, g, b, r, gq0, gq1, gq2);
+            const float j = interp8<true>(taps[v], rr[v], gq0, gq1, gq2);
             const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, G.f[v], j) : G.gb[v];
             const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
             if (g.k_diag) {
