@@ -186,6 +186,16 @@ ffdp_status ffdp_objective_mi_static(const void *F, ffdp_dtype ft, ffdp_dims fdi
 /* Size in bytes of the static scratch used by ffdp_objective_mi_static. */
 size_t ffdp_static_scratch_bytes(void);
 
+/* Device-side failure report.  The sweep kernels stream their per-voxel
+ * inputs into shared memory with asynchronous bulk copies and wait for each
+ * with a time limit (1 s).  A wait that runs out marks the current device's
+ * error word, the kernel finishes without touching the copies' data, and the
+ * losses of that call are written as NaN (its other outputs are invalid).
+ * This call synchronises the current device (the one exception to "no call
+ * blocks on the device"), stores 1 in *flag if the word was marked since the
+ * last call and 0 otherwise, and clears the word. */
+ffdp_status ffdp_device_error(int *flag);
+
 /* Human-readable name of a status. */
 const char *ffdp_status_string(ffdp_status s);
 

@@ -23,10 +23,10 @@ def ffdp():
     return f
 
 
-def _vol(shape, seed, lo=0.0, hi=1.0, dtype=np.float32):
+def _vol(shape, seed, lo=0.0, hi=1.0, dtype=np.float32, sigma=1.0):
     from voxel_grid_sampler_gb300 import synth
     g = torch.Generator().manual_seed(seed)
-    v = synth.gaussian_smooth(torch.rand(shape, generator=g), 1.0)
+    v = synth.gaussian_smooth(torch.rand(shape, generator=g), sigma)
     v = (v - v.min()) / (v.max() - v.min()) * (hi - lo) + lo
     return v.numpy().astype(dtype)
 
@@ -166,6 +166,43 @@ def test_objective(ffdp, fs, ms, dt_, wmi, wln, B, w):
     assert rel_l2(np.r_[host(dA), host(dt)], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
 
 
+# Larger grids: several CTA iterations per persistent CTA (the streamed-input
+# ring wraps), rows that are not a multiple of 32 voxels and a ragged last
+# chunk.  M is an intensity remap of F (as in the registration workloads), so
+# MI is of order 1 instead of the near-zero MI of two independent volumes,
+# whose relative error is ill-conditioned.
+LARGE_CASES = [
+    # shape, dtype, w_mi, w_lncc, bins, window
+    ((41, 199, 257), np.float32, 1.0, 1.0, 64, 5),
+    ((41, 199, 257), np.float16, 1.0, 0.0, 32, 5),
+]
+
+
+@pytest.mark.parametrize("fs,dt_,wmi,wln,B,w", LARGE_CASES)
+def test_objective_large(ffdp, fs, dt_, wmi, wln, B, w):
+    rng = np.random.default_rng(sum(fs) + B)
+    base = _vol(fs, 23, sigma=2.0)
+    F = base.astype(dt_)
+    M = (1.0 - base ** 2 + rng.normal(size=fs) * 0.01).astype(dt_)
+    u = (rng.normal(size=fs + (3,)) * 0.002).astype(np.float32)
+    A, t, S, _, _ = random_transform(rng, 0.003)
+    xmin, xmax = np.full(3, -1.0, np.float32), np.full(3, 1.0, np.float32)  # grids aligned
+    fr = (float(F.min()), float(F.max()))
+    mr = (float(M.min()), float(M.max()))
+    T = ffdp.transform(A, t, S, xmin, xmax)
+    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5)
+    loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P)
+    ref = oracle.objective(F, M, u, oracle_T(A, t, S, xmin, xmax),
+                           oracle.ObjectiveParams(wmi, wln, B, fr, mr, w, 1e-5))
+    l = host(loss)
+    assert abs(ref["loss"][1]) > 0.05  # MI of order 1
+    for k in range(3):
+        if ref["loss"][k] != 0.0:
+            assert rel_err(l[k], ref["loss"][k]) <= TOL_LOSS, (k, l, ref["loss"])
+    assert rel_l2(host(du), ref["du"]) <= TOL_GRAD
+    assert rel_l2(np.r_[host(dA), host(dt)], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
+
+
 def test_objective_is_deterministic(ffdp):
     rng = np.random.default_rng(3)
     fs = (16, 20, 24)
@@ -185,3 +222,8 @@ def test_workspace_is_independent_of_volume_size_for_mi(ffdp):
     a = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (64, 64, 64), p)
     b = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), p)
     assert a == b and a < (1 << 20)
+
+
+def test_no_device_error_after_runs(ffdp):
+    # every bounded wait of the sweeps above completed
+    assert not ffdp.device_error()

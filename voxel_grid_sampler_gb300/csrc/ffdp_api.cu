@@ -85,6 +85,15 @@ void ffdp::note_launch_end(cudaStream_t s) {
 
 extern "C" uint64_t ffdp_launch_count(void) { return g_launches.load(); }
 
+extern "C" ffdp_status ffdp_device_error(int* flag) {
+  if (!flag) return fail(FFDP_ERR_INVALID_ARGUMENT, "flag is NULL");
+  unsigned v = 0;
+  const cudaError_t e = ffdp::take_device_error(&v);
+  if (e != cudaSuccess) return cuda_fail(e, "device error word");
+  *flag = v ? 1 : 0;
+  return FFDP_OK;
+}
+
 extern "C" ffdp_status ffdp_timing_enable(int capacity) {
   std::lock_guard<std::mutex> lk(g_tmu);
   g_recs.clear();
@@ -315,7 +324,9 @@ int persistent_grid(unsigned nIter, int per_sm) {
   return (int)(g < 1 ? 1 : g);
 }
 
-unsigned n_iter(uint64_t N) { return (unsigned)((N + (uint64_t)(kThreads * kVPT) - 1) / (kThreads * kVPT)); }
+unsigned n_iter(uint64_t N) {
+  return (unsigned)((N + (uint64_t)(kSweepThreads * kVPT) - 1) / (kSweepThreads * kVPT));
+}
 
 #define FFDP_TRY(x)                    \
   do {                                 \

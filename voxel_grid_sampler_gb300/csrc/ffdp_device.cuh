@@ -13,8 +13,9 @@
 namespace ffdp {
 
 // ---------------------------------------------------------------- constants
-constexpr int kThreads = 256;           // threads per CTA of every sweep kernel
-constexpr int kVPT = 4;                 // voxels per thread per iteration (x-contiguous)
+constexpr int kThreads = 256;           // threads per CTA of the LNCC kernel
+constexpr int kSweepThreads = 512;      // threads per CTA of the voxel sweeps (one CTA per SM)
+constexpr int kVPT = 4;                 // voxels per sweep thread per iteration (32 apart)
 constexpr int kHistFrac = 20;           // fixed-point fraction bits of histogram weights
 constexpr float kHistOne = 1048576.0f;  // 2^kHistFrac
 constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic holds round(x) in its low bits
@@ -82,9 +83,15 @@ __device__ __forceinline__ void lin_to_xyz(const Geom& g, unsigned lin, int& ix,
 
 // 64-bit fixed-point anchor P = G i + g0 (no displacement).
 __device__ __forceinline__ void anchor(const Geom& g, int ix, int iy, int iz, long long P[3]) {
+  if (g.a_diag) {
+    P[0] = g.g0q[0] + g.Gq[0] * ix;
+    P[1] = g.g0q[1] + g.Gq[4] * iy;
+    P[2] = g.g0q[2] + g.Gq[8] * iz;
+  } else {
 #pragma unroll
-  for (int r = 0; r < 3; ++r)
-    P[r] = g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
+    for (int r = 0; r < 3; ++r)
+      P[r] = g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
+  }
 }
 
 // floor(t) and t - floor(t) for |t| < 2^21 with full-rate float/int ops:

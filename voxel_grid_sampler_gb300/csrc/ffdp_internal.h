@@ -35,7 +35,7 @@ struct Sweep1Args {
   Geom g;
   BinMap bf, bj;
   int B;
-  unsigned nIter;             // CTA iterations of kThreads*kVPT voxels
+  unsigned nIter;             // CTA iterations of kSweepThreads*kVPT voxels
 };
 
 // Gradient sweep: MI table lookups and/or a given dL/dJ, sampler backward.
@@ -110,6 +110,8 @@ cudaError_t launch_lncc(int mode, int ft, int mt, int bmax_or0, const LnccArgs& 
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s);
 
 // Occupancy-derived persistent grid sizes (CTAs per SM), cached.
+// Reads the device error word of the current device (synchronous) and clears it.
+cudaError_t take_device_error(unsigned* v);
 int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax);
 int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax);
 size_t lncc_smem_bytes(int R, int bmax_or0);

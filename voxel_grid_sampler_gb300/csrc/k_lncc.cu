@@ -365,7 +365,10 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
               float gfj = 0.f;
               if (zin && xin && (unsigned)y < (unsigned)g.fH) {
                 // aP = (S_J, S_F), aQ = (S_JJ, S_FF), aX = S_FJ
-                const float2 v = fma2(mul2(aP, aP), ninv2, aQ);  // (vJ, vF)
+                // (vJ, vF), clamped at 0 (exact variances are; fp32 cancellation in
+                // flat windows can leave small negatives) so that vF vJ + eps >= eps
+                float2 v = fma2(mul2(aP, aP), ninv2, aQ);
+                v = make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f));
                 const float cross = fmaf(-aP.x * aP.y, inv_n, aX);
                 const float D = fmaf(v.x, v.y, eps);
                 const float rD = rcp_approx(D);

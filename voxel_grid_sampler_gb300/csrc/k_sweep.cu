@@ -7,32 +7,37 @@
 // Parzen window -- histogram entries accumulate per voxel in shared memory and
 // the per-voxel partial gradient reads a small table, so no B x N block exists.
 //
-// Layout of the work: a CTA iteration covers kThreads*kVPT consecutive voxels
-// of the flattened [D][H][W] grid; each thread owns kVPT x-consecutive voxels
-// so F, J and dJ move as 16-byte vectors and u/du as three 16-byte vectors.
-// Grids are persistent (a few CTAs per SM striding over iterations).
+// Layout of the work: a CTA iteration covers kSweepThreads*kVPT consecutive
+// voxels of the flattened [D][H][W] grid; each warp owns 32*kVPT of them and
+// each lane every 32nd (see the lane walk).  Grids are persistent (one CTA per
+// SM striding over iterations).
 #include "ffdp_internal.h"
 
 namespace ffdp {
 
 // ----------------------------------------------------- histogram layout
-// Bin (a, b) of the joint histogram has R lane copies: lane l adds into copy
-// c = l mod R and visits the four kernel rows rotated by q = (l / R) mod 4.
-// Word address = a * SR + b * R + c with row stride SR = BMAX * R + 8
-// (8 mod 32), so lanes whose voxels share a base bin always hit distinct words
-// in distinct banks, and same-address serialisation cannot occur.
+// Bin (a, b) of the joint histogram has R = 8 lane copies.  Lane l adds into
+// copy c = l mod 8, and its group ga = l / 8 (0..3) fixes the order in which
+// it visits a voxel's four kernel rows: at step i it takes the row a of the
+// four with a = i + ga (mod 4).  The word address
+//   word(a, b, c) = (a / 4) * 32 B + 32 b + 8 (a mod 4) + c
+// lies in bank 8 (a mod 4) + c, so at every step the 32 lanes of a warp hit
+// 32 distinct banks whatever their bins: each shared atomic instruction is
+// one wavefront and no two lanes ever share an address.
 template <int BMAX>
 struct HistLayout {
-  static constexpr int R = 256 / BMAX;            // 8 copies for 32 bins, 4 for 64
-  static constexpr int SR = BMAX * R + 8;          // row stride in words
-  static constexpr int WORDS = BMAX * SR;
+  static constexpr int R = 8;
+  static constexpr int COL = 4 * R;             // word stride of b
+  static constexpr int QROW = COL * BMAX;       // words per group of four rows
+  static constexpr int WORDS = BMAX * BMAX * R;
   // voxels reaching one word per CTA iteration: lanes sharing a copy
-  static constexpr int VOX_PER_ITER = kThreads * kVPT / R;
+  static constexpr int VOX_PER_ITER = kSweepThreads * kVPT / R;
+  __host__ __device__ static constexpr int word(int a, int b) { return (a >> 2) * QROW + COL * b + R * (a & 3); }
 };
 
 // u32 fixed-point counts (kHistFrac fraction bits): one voxel adds at most
 // (2/3)^2 to a word, so a CTA flushes its copies to the u64 global histogram
-// at least every kFlush<BMAX> iterations.
+// at least every flush_every<BMAX>() iterations.
 template <int BMAX>
 __host__ __device__ constexpr int flush_every() {
   return (int)(4294967295.0 / (HistLayout<BMAX>::VOX_PER_ITER * (4.0 / 9.0) * kHistOne)) - 1;
@@ -42,63 +47,58 @@ static_assert(flush_every<32>() >= 16 && flush_every<64>() >= 16, "histogram flu
 // fp32 per-thread gradient partials are folded into fp64 every this many iterations.
 constexpr int kFoldEvery = 16;
 
-// Fetch the next iteration's F / u group while processing the current one.
-#ifndef FFDP_PREFETCH
-#define FFDP_PREFETCH 0
-#endif
-constexpr bool kPrefetch = FFDP_PREFETCH != 0;
-
 __global__ void k_zero_u64(unsigned long long* p, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0ull;
 }
 
+// Sums the R copies of every bin into the u64 histogram and clears them.
+// Thread i reads bin (a, b) with a mod 4 = i mod 4 and takes its two 16-byte
+// halves in lane-dependent order, so the 8 lanes of each quarter-warp read 8
+// different bank quads.  Rows run to B rounded up to a multiple of 4.
 template <int BMAX>
 __device__ __forceinline__ void hist_flush(unsigned* hist, unsigned long long* gh, int B) {
   using L = HistLayout<BMAX>;
+  static_assert(L::R == 8, "flush reads two uint4 per bin");
   __syncthreads();
-  for (int i = threadIdx.x; i < B * B; i += kThreads) {
-    const int ra = i / B, rb = i - ra * B;
-    uint4* w = reinterpret_cast<uint4*>(hist + ra * L::SR + rb * L::R);
-    unsigned long long s = 0ull;
-#pragma unroll
-    for (int k = 0; k < L::R / 4; ++k) {
-      const uint4 v = w[k];
-      s += (unsigned long long)v.x + v.y + (unsigned long long)v.z + v.w;
-      w[k] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (s) atomicAdd(gh + i, s);
+  const int h = (threadIdx.x >> 2) & 1;
+  const int n = ((B + 3) & ~3) * B;
+  for (int i = threadIdx.x; i < n; i += kSweepThreads) {
+    const int rest = i >> 2, rb = rest % B, ra = ((rest / B) << 2) | (i & 3);
+    if (ra >= B) continue;
+    uint4* w = reinterpret_cast<uint4*>(hist + L::word(ra, rb));
+    const uint4 v0 = w[h], v1 = w[h ^ 1];
+    w[h] = make_uint4(0u, 0u, 0u, 0u);
+    w[h ^ 1] = make_uint4(0u, 0u, 0u, 0u);
+    const unsigned long long s = (unsigned long long)v0.x + v0.y + (unsigned long long)v0.z + v0.w +
+                                 (unsigned long long)v1.x + v1.y + (unsigned long long)v1.z + v1.w;
+    if (s) atomicAdd(gh + ra * B + rb, s);
   }
   __syncthreads();
 }
 
-// Per-lane constants of the rotated histogram accumulation: polynomial
-// coefficients (in t, scaled by 2^kHistFrac) of the cubic B-spline weight of
-// kernel row (i + q) mod 4, and that row's word offset.
+// Per-lane constants of the histogram accumulation.
 struct HistLane {
-  float c[4][4];
-  int rowoff[4];
-  int copy;
+  int rowoff[4];  // R ((i + ga) mod 4) + c for step i
+  int ga;
 };
 
 template <int BMAX>
 __device__ __forceinline__ void hist_lane_init(HistLane& h) {
   using L = HistLayout<BMAX>;
-  // w_j(t) = sum_p W[j][p] t^p for the taps floor(c)-1+j, j = 0..3:
-  //   w0 = (1-t)^3/6, w1 = 2/3 - t^2 + t^3/2, w2 = 1/6 + t/2 + t^2/2 - t^3/2, w3 = t^3/6
-  const float W[4][4] = {{1.f / 6, -0.5f, 0.5f, -1.f / 6},
-                         {2.f / 3, 0.f, -1.f, 0.5f},
-                         {1.f / 6, 0.5f, 0.5f, -0.5f},
-                         {0.f, 0.f, 0.f, 1.f / 6}};
   const int lane = threadIdx.x & 31;
-  const int q = (lane / L::R) & 3;
-  h.copy = lane & (L::R - 1);
+  h.ga = lane / L::R;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int j = (i + q) & 3;
+  for (int i = 0; i < 4; ++i) h.rowoff[i] = L::R * ((i + h.ga) & 3) + (lane & (L::R - 1));
+}
+
+// r[i] = w[(i + s) mod 4].
+__device__ __forceinline__ void rotate4(const float w[4], int s, float r[4]) {
+  const bool s1 = (s & 1) != 0, s2 = (s & 2) != 0;
+  float t[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) h.c[i][p] = W[j][p] * kHistOne;
-    h.rowoff[i] = j * L::SR;
-  }
+  for (int i = 0; i < 4; ++i) t[i] = s1 ? w[(i + 1) & 3] : w[i];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[i] = s2 ? t[(i + 2) & 3] : t[i];
 }
 
 // Parzen contribution of one voxel: beta(a - cF) beta(b - cJ) on the 4x4 bins
@@ -111,15 +111,21 @@ __device__ __forceinline__ void hist_add(unsigned* hist, const HistLane& h, cons
   float tf, tj;
   floor_split(bin_coord(bf, f), af, tf);
   floor_split(bin_coord(bj, j), aj, tj);
-  float wj[4];
+  float wf[4], wj[4], wr[4];
+  bspline4(tf, kHistOne, wf);
   bspline4(tj, 1.0f, wj);
-  unsigned* base = hist + (af - 1) * L::SR + (aj - 1) * L::R + h.copy;
+  // step i takes kernel row a_i = af - 1 + ((i + s) mod 4), s = ga - af + 1,
+  // so that a_i = i + ga (mod 4)
+  const int s = h.ga - af + 1;
+  rotate4(wf, s, wr);
+  unsigned* col = hist + L::COL * (aj - 1);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float wf = fmaf(fmaf(fmaf(h.c[i][3], tf, h.c[i][2]), tf, h.c[i][1]), tf, h.c[i][0]);
-    unsigned* row = base + h.rowoff[i];
+    const int ai = af - 1 + ((i + s) & 3);
+    unsigned* row = col + (ai >> 2) * L::QROW + h.rowoff[i];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) atomicAdd(row + k * L::R, __float_as_uint(fmaf(wf, wj[k], kMagic)) - kMagicBits);
+    for (int k = 0; k < 4; ++k)
+      atomicAdd(row + k * L::COL, __float_as_uint(fmaf(wr[i], wj[k], kMagic)) - kMagicBits);
   }
 }
 
@@ -170,169 +176,338 @@ __device__ __forceinline__ float mi_grad(const float* tsm, const BinMap& bf, con
   return (j >= bj.lo && j <= bj.hi) ? s : 0.0f;
 }
 
-// ----------------------------------------------------------- group loads
-struct Group {
-  float f[kVPT], j[kVPT], gb[kVPT], u[3 * kVPT];
-};
-
-template <typename FT, bool LOADF, bool LOADU, bool LOADJ, bool LOADG>
-__device__ __forceinline__ void load_group(const FT* __restrict__ F, const float* __restrict__ u,
-                                           const float* __restrict__ J, const float* __restrict__ gbuf,
-                                           unsigned lin0, unsigned nv, Group& G) {
-#pragma unroll
-  for (int k = 0; k < kVPT; ++k) {
-    G.f[k] = 0.f;
-    G.j[k] = 0.f;
-    G.gb[k] = 0.f;
-  }
-#pragma unroll
-  for (int k = 0; k < 3 * kVPT; ++k) G.u[k] = 0.f;
-  if (nv == kVPT) {
-    if (LOADF) load4(F + lin0, G.f);
-    if (LOADU && u) {
-      const float4* up = reinterpret_cast<const float4*>(u + 3ull * lin0);
-      const float4 q0 = __ldg(up), q1 = __ldg(up + 1), q2 = __ldg(up + 2);
-      G.u[0] = q0.x; G.u[1] = q0.y; G.u[2] = q0.z; G.u[3] = q0.w;
-      G.u[4] = q1.x; G.u[5] = q1.y; G.u[6] = q1.z; G.u[7] = q1.w;
-      G.u[8] = q2.x; G.u[9] = q2.y; G.u[10] = q2.z; G.u[11] = q2.w;
-    }
-    if (LOADJ) load4(J + lin0, G.j);
-    if (LOADG) load4(gbuf + lin0, G.gb);
-  } else {
-#pragma unroll
-    for (int v = 0; v < kVPT; ++v) {
-      if ((unsigned)v < nv) {
-        if (LOADF) G.f[v] = load1(F + lin0 + v);
-        if (LOADU && u) {
-          G.u[3 * v + 0] = __ldg(u + 3ull * (lin0 + v) + 0);
-          G.u[3 * v + 1] = __ldg(u + 3ull * (lin0 + v) + 1);
-          G.u[3 * v + 2] = __ldg(u + 3ull * (lin0 + v) + 2);
-        }
-        if (LOADJ) G.j[v] = __ldg(J + lin0 + v);
-        if (LOADG) G.gb[v] = __ldg(gbuf + lin0 + v);
-      }
-    }
-  }
-}
-
-// Walks the voxels of a 4-voxel group.  Fast path (the group lies in one
-// row, always when W % 4 == 0): one fixed-point anchor serves all four.
-struct GroupWalk {
-  int k[3];
-  float f[3];
+// ------------------------------------------------------------- lane walk
+// Lane l of warp w handles, in CTA iteration it, the voxels
+//   lin = it * kSweepThreads * kVPT + w * 32 * kVPT + l + 32 v,  v = 0..kVPT-1.
+// Every load, gather and store instruction of a warp covers 32 consecutive
+// voxels, so F, J, g and dJ move in whole 128-byte lines and the trilinear
+// taps of 32 neighbouring points share one or two lines per M row.
+struct LaneWalk {
+  long long P[3];  // fixed-point anchor G i + g0 of the current voxel
   int x, y, z;
-  bool row;  // whole group in one row
 };
 
-__device__ __forceinline__ void walk_begin(const Geom& g, unsigned lin0, GroupWalk& w) {
-  lin_to_xyz(g, lin0, w.x, w.y, w.z);
-  w.row = g.w4 || (w.x + kVPT <= g.fW);
-  anchor_kf(g, w.x, w.y, w.z, w.k, w.f);
+__device__ __forceinline__ void lw_seek(const Geom& g, unsigned lin, LaneWalk& w) {
+  lin_to_xyz(g, lin, w.x, w.y, w.z);
+  anchor(g, w.x, w.y, w.z, w.P);
 }
 
-// Cell of voxel v of the group and its grid index.
-__device__ __forceinline__ void walk_cell(const Geom& g, GroupWalk& w, int v, float u0, float u1, float u2,
-                                          int b[3], float r[3], int& ix, int& iy, int& iz) {
-  if (w.row) {
-    cell_v(g, w.k, w.f, (float)v, u0, u1, u2, b, r);
-    ix = w.x + v;
-    iy = w.y;
-    iz = w.z;
-  } else {
-    if (v > 0) {
-      if (++w.x == g.fW) {
-        w.x = 0;
-        if (++w.y == g.fH) {
-          w.y = 0;
-          ++w.z;
-        }
-      }
-      anchor_kf(g, w.x, w.y, w.z, w.k, w.f);
+// Moves to voxel lin = previous + 32: inside the row the anchor advances by
+// the exact fixed-point step 32 G e_x, otherwise it is recomputed.
+__device__ __forceinline__ void lw_step(const Geom& g, unsigned lin, LaneWalk& w) {
+  if (w.x + 32 < g.fW) {
+    w.x += 32;
+    w.P[0] += g.Gq[0] * 32;
+    if (!g.a_diag) {
+      w.P[1] += g.Gq[3] * 32;
+      w.P[2] += g.Gq[6] * 32;
     }
-    cell_v(g, w.k, w.f, 0.0f, u0, u1, u2, b, r);
-    ix = w.x;
-    iy = w.y;
-    iz = w.z;
+  } else {
+    lw_seek(g, lin, w);
   }
 }
 
-// Minimum resident CTAs per SM requested from the register allocator.
-#ifndef FFDP_SWEEP1_MINB
-#define FFDP_SWEEP1_MINB 2
-#endif
-#ifndef FFDP_SWEEP2_MINB
-#define FFDP_SWEEP2_MINB 2
-#endif
+// Number of the lane's kVPT voxels (32 apart from lin0) inside the grid.
+__device__ __forceinline__ int lane_count(unsigned lin0, unsigned N) {
+  return lin0 >= N ? 0 : min((int)((N - lin0 + 31u) >> 5), kVPT);
+}
+
+// ------------------------------------------------------ streamed inputs
+// The per-voxel inputs of a warp's chunk of 32*kVPT voxels (u: 12 B, F: 2 or
+// 4 B, J or g: 4 B per voxel) reach shared memory through 1-D bulk
+// asynchronous copies that lane 0 of the warp issues NST chunks ahead into a
+// per-warp ring of NST slots; each slot's completion is counted in bytes on
+// its own mbarrier.  HBM therefore always holds several chunks per warp in
+// flight, independent of the warp's instruction stream.  Only whole chunks
+// are streamed; the one ragged chunk at the end of the grid is read directly.
+
+// Set when a bounded wait for a ring slot gave up; outputs of that call are
+// invalid (the finish kernel then writes NaN losses).
+__device__ unsigned g_ffdp_device_error;
+
+constexpr unsigned long long kWaitNs = 1000000000ull;  // a ring wait gives up after 1 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Waits for the completion of phase `parity`; false after kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, unsigned parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitNs) return false;
+  return true;
+}
+
+// Streamed inputs are read once: mark them first for eviction from L2, which
+// keeps the randomly gathered moving image resident.
+__device__ __forceinline__ unsigned long long policy_evict_first() {
+  unsigned long long p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, unsigned bytes, uint32_t bar,
+                                         unsigned long long pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// Ring geometry: per slot [u][F][X] for one chunk; NST slots per warp, then
+// one 8-byte mbarrier per slot after all warps' slots.
+template <typename FT, bool SU, bool SF, bool SX, int NST>
+struct Ring {
+  static constexpr int kChunk = 32 * kVPT;
+  static constexpr int kU = SU ? kChunk * 12 : 0;
+  static constexpr int kF = SF ? kChunk * (int)sizeof(FT) : 0;
+  static constexpr int kX = SX ? kChunk * 4 : 0;
+  static constexpr int kSlot = kU + kF + kX;
+  static constexpr int kWarps = kSweepThreads / 32;
+  static constexpr size_t kBytes = (size_t)kWarps * NST * (kSlot + 8);
+  static_assert(kU % 16 == 0 && kF % 16 == 0 && kX % 16 == 0, "bulk copies move multiples of 16 bytes");
+};
+
+// Per-warp view of the ring.
+template <class RG, int NST>
+struct WarpRing {
+  char* slots;    // this warp's NST slots
+  uint32_t bars;  // shared address of this warp's first mbarrier
+  unsigned tx;    // bytes per chunk (0: nothing streamed)
+  bool has_u;
+
+  __device__ __forceinline__ void init(char* ring, bool has_u_) {
+    const int warp = threadIdx.x >> 5;
+    slots = ring + (size_t)warp * NST * RG::kSlot;
+    bars = smem_u32(ring + (size_t)RG::kWarps * NST * RG::kSlot) + warp * NST * 8;
+    has_u = has_u_ && RG::kU > 0;
+    tx = (has_u ? RG::kU : 0) + RG::kF + RG::kX;
+    if (tx && (threadIdx.x & 31) == 0) {
+#pragma unroll
+      for (int s = 0; s < NST; ++s) mbar_init(bars + 8 * s, 1);
+      mbar_fence_init();
+    }
+    __syncwarp();
+  }
+
+  // lane 0: copy chunk ch into slot s
+  template <typename FT>
+  __device__ __forceinline__ void issue(int s, unsigned ch, const float* u, const FT* F, const float* X,
+                                        unsigned long long pol) const {
+    const size_t v0 = (size_t)ch * RG::kChunk;
+    char* slot = slots + s * RG::kSlot;
+    const uint32_t bar = bars + 8 * s;
+    mbar_expect_tx(bar, tx);
+    if (RG::kU && has_u) bulk_g2s(smem_u32(slot), u + 3 * v0, RG::kU, bar, pol);
+    if (RG::kF) bulk_g2s(smem_u32(slot + RG::kU), F + v0, RG::kF, bar, pol);
+    if (RG::kX) bulk_g2s(smem_u32(slot + RG::kU + RG::kF), X + v0, RG::kX, bar, pol);
+  }
+
+  __device__ __forceinline__ const float* u_of(int s) const { return reinterpret_cast<const float*>(slots + s * RG::kSlot); }
+  template <typename FT>
+  __device__ __forceinline__ const FT* f_of(int s) const {
+    return reinterpret_cast<const FT*>(slots + s * RG::kSlot + RG::kU);
+  }
+  __device__ __forceinline__ const float* x_of(int s) const {
+    return reinterpret_cast<const float*>(slots + s * RG::kSlot + RG::kU + RG::kF);
+  }
+};
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+
+// The ring schedule of one warp: iteration k of the CTA loop (it = blockIdx.x
+// + k gridDim.x) takes chunk it * kWarps + warp from slot k mod NST, whose
+// (k / NST)-th completion has parity (k / NST) & 1.  A wait that gives up
+// sets the device error word; the warp then stops streaming (its later
+// chunks read nothing) and, before exiting, waits (bounded) for the copies it
+// still has in flight.
+template <class WR, int NST>
+struct RingSched {
+  unsigned nIter, nFull;  // CTA iterations; whole chunks in the grid
+  int kfail;              // first iteration whose wait gave up (-1: none)
+
+  __device__ __forceinline__ unsigned chunk(unsigned it) const { return it * (kSweepThreads / 32) + (threadIdx.x >> 5); }
+  __device__ __forceinline__ bool streamed(unsigned it) const { return it < nIter && chunk(it) < nFull; }
+
+  template <typename FT>
+  __device__ __forceinline__ void prologue(const WR& r, const float* u, const FT* F, const float* X,
+                                           unsigned long long pol) const {
+    if (r.tx != 0 && (threadIdx.x & 31) == 0) {
+#pragma unroll
+      for (int s = 0; s < NST; ++s) {
+        const unsigned it = blockIdx.x + s * gridDim.x;
+        if (streamed(it)) r.template issue<FT>(s, chunk(it), u, F, X, pol);
+      }
+    }
+    __syncwarp();
+  }
+
+  // Waits for slot k mod NST; false (uniform over the warp) if it gave up.
+  __device__ __forceinline__ bool wait(const WR& r, unsigned k) {
+    if (kfail >= 0) return false;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(r.bars + 8 * (k % NST), (k / NST) & 1));
+    if (!ok) {
+      kfail = (int)k;
+      if ((threadIdx.x & 31) == 0) atomicExch(&g_ffdp_device_error, 1u);
+    }
+    return ok;
+  }
+
+  // After the warp has read slot k mod NST: refill it with the chunk NST iterations ahead.
+  template <typename FT>
+  __device__ __forceinline__ void refill(const WR& r, unsigned k, unsigned it, const float* u, const FT* F,
+                                         const float* X, unsigned long long pol) const {
+    __syncwarp();
+    const unsigned it2 = it + NST * gridDim.x;
+    if (kfail < 0 && (threadIdx.x & 31) == 0 && streamed(it2)) r.template issue<FT>(k % NST, chunk(it2), u, F, X, pol);
+    __syncwarp();
+  }
+
+  // Bounded drain of the copies still in flight after a failed wait.
+  __device__ __forceinline__ void drain(const WR& r) const {
+    if (kfail < 0 || (threadIdx.x & 31) != 0) return;
+    for (unsigned k = (unsigned)kfail; k < (unsigned)kfail + NST; ++k)
+      if (streamed(blockIdx.x + k * gridDim.x)) mbar_wait(r.bars + 8 * (k % NST), (k / NST) & 1);
+  }
+};
 
 // ------------------------------------------------------------------ sweep 1
 // Sampling (or reading J) plus, per mode, the histogram and/or a J store.
+// Streams: u (sampling), F (histogram), J (histogram of a given J).
+template <typename FT, int BMAX, int MODE>
+struct S1Cfg {
+  static constexpr bool HIST = MODE != S1_WRITEJ;
+  static constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
+  static constexpr int NST = (HIST && BMAX == 64) ? 2 : 4;
+  using RG = Ring<FT, SAMPLE, HIST, !SAMPLE, NST>;
+  static constexpr size_t kHistBytes = HIST ? (size_t)HistLayout<BMAX>::WORDS * sizeof(unsigned) : 0;
+  static constexpr size_t kSmem = kHistBytes + RG::kBytes;
+};
+
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kThreads, FFDP_SWEEP1_MINB) k_sweep1(const Sweep1Args a) {
-  constexpr bool HIST = MODE != S1_WRITEJ;
-  constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
+__global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a) {
+  using C = S1Cfg<FT, BMAX, MODE>;
+  constexpr bool HIST = C::HIST;
+  constexpr bool SAMPLE = C::SAMPLE;
   constexpr bool WRITEJ = (MODE == S1_WRITEJ) || (MODE == S1_HIST_WRITEJ);
+  constexpr int NST = C::NST;
   using L = HistLayout<BMAX>;
-  extern __shared__ uint4 hist_sm4[];
-  unsigned* hist_sm = reinterpret_cast<unsigned*>(hist_sm4);
+  using RG = typename C::RG;
+  using WR = WarpRing<RG, NST>;
+  extern __shared__ uint4 smem4[];
+  unsigned* hist_sm = reinterpret_cast<unsigned*>(smem4);
   const Geom& g = a.g;
   HistLane hl;
   if (HIST) {
     hist_lane_init<BMAX>(hl);
-    for (int i = threadIdx.x; i < L::WORDS / 4; i += kThreads) hist_sm4[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < L::WORDS / 4; i += kSweepThreads) smem4[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
   const MT* __restrict__ M = static_cast<const MT*>(a.M);
+  const float* X = a.Jin;
+  WR wr;
+  wr.init(reinterpret_cast<char*>(smem4) + C::kHistBytes, SAMPLE && a.u != nullptr);
+  RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
+  const unsigned long long pol = policy_evict_first();
+  rs.template prologue<FT>(wr, a.u, F, X, pol);
+  const int lane = threadIdx.x & 31;
   int pending = 0;
-  // the F / u group of the next iteration is fetched while this one is processed
-  Group Gnext;
-  {
-    const unsigned l0 = (blockIdx.x * kThreads + threadIdx.x) * kVPT;
-    if (kPrefetch && blockIdx.x < a.nIter && l0 < g.N)
-      load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, l0, min(g.N - l0, (unsigned)kVPT), Gnext);
-  }
-  for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x) {
-    const unsigned lin0 = (it * kThreads + threadIdx.x) * kVPT;
-    Group G = Gnext;
-    if (kPrefetch) {
-      const unsigned itn = it + gridDim.x, ln = (itn * kThreads + threadIdx.x) * kVPT;
-      if (itn < a.nIter && ln < g.N)
-        load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, ln, min(g.N - ln, (unsigned)kVPT), Gnext);
-    } else if (lin0 < g.N) {
-      load_group<FT, HIST, SAMPLE, !SAMPLE, false>(F, a.u, a.Jin, nullptr, lin0, min(g.N - lin0, (unsigned)kVPT), G);
-    }
-    if (lin0 < g.N) {
-      const unsigned nv = min(g.N - lin0, (unsigned)kVPT);
+  unsigned k = 0;
+  for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
+    const unsigned ch = rs.chunk(it);
+    const unsigned lin0 = ch * RG::kChunk + lane;
+    const int nv = lane_count(lin0, g.N);
+    if (nv > 0) {
+      float f[kVPT], j[kVPT], u[3 * kVPT];
+#pragma unroll
+      for (int v = 0; v < kVPT; ++v) f[v] = j[v] = u[3 * v] = u[3 * v + 1] = u[3 * v + 2] = 0.0f;
+      if (wr.tx && ch < rs.nFull) {
+        const int s = k % NST;
+        if (rs.wait(wr, k)) {
+#pragma unroll
+          for (int v = 0; v < kVPT; ++v) {
+            const int e = lane + 32 * v;
+            if (HIST) f[v] = to_f(wr.template f_of<FT>(s)[e]);
+            if (SAMPLE && wr.has_u) {
+              u[3 * v + 0] = wr.u_of(s)[3 * e + 0];
+              u[3 * v + 1] = wr.u_of(s)[3 * e + 1];
+              u[3 * v + 2] = wr.u_of(s)[3 * e + 2];
+            }
+            if (!SAMPLE) j[v] = wr.x_of(s)[e];
+          }
+        }
+        rs.template refill<FT>(wr, k, it, a.u, F, X, pol);
+      } else {
+#pragma unroll
+        for (int v = 0; v < kVPT; ++v) {
+          const unsigned lin = lin0 + 32u * v;
+          if (v < nv) {
+            if (HIST) f[v] = load1(F + lin);
+            if (SAMPLE && a.u) {
+              u[3 * v + 0] = __ldg(a.u + 3ull * lin + 0);
+              u[3 * v + 1] = __ldg(a.u + 3ull * lin + 1);
+              u[3 * v + 2] = __ldg(a.u + 3ull * lin + 2);
+            }
+            if (!SAMPLE) j[v] = __ldg(a.Jin + lin);
+          }
+        }
+      }
       if (SAMPLE) {
-        // all 32 tap loads of the group are issued before any interpolation
-        GroupWalk w;
-        walk_begin(g, lin0, w);
+        // all tap loads of the lane's voxels are issued before any interpolation
+        LaneWalk w;
+        lw_seek(g, lin0, w);
         float taps[kVPT][8], rr[kVPT][3];
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
-          int b[3], ix, iy, iz;
-          walk_cell(g, w, v, G.u[3 * v], G.u[3 * v + 1], G.u[3 * v + 2], b, rr[v], ix, iy, iz);
-          if ((unsigned)v >= nv) b[0] = -2;  // past the end: no loads
+          int b[3];
+          if (v > 0 && v < nv) lw_step(g, lin0 + 32u * v, w);
+          cell_of(g, w.P, u[3 * v], u[3 * v + 1], u[3 * v + 2], b, rr[v]);
+          if (v >= nv) b[0] = -2;  // past the end: no loads
           gather8<MT>(M, g, b, taps[v]);
         }
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
           float d0, d1, d2;
-          G.j[v] = interp8<false>(taps[v], rr[v], d0, d1, d2);
+          j[v] = interp8<false>(taps[v], rr[v], d0, d1, d2);
         }
       }
-      if (HIST) {
 #pragma unroll
-        for (int v = 0; v < kVPT; ++v)
-          if ((unsigned)v < nv) hist_add<BMAX>(hist_sm, hl, a.bf, a.bj, G.f[v], G.j[v]);
-      }
-      if (WRITEJ) {
-        if (nv == kVPT) {
-          *reinterpret_cast<float4*>(a.Jout + lin0) = make_float4(G.j[0], G.j[1], G.j[2], G.j[3]);
-        } else {
-#pragma unroll
-          for (int v = 0; v < kVPT; ++v)
-            if ((unsigned)v < nv) a.Jout[lin0 + v] = G.j[v];
+      for (int v = 0; v < kVPT; ++v) {
+        if (v < nv) {
+          if (HIST) hist_add<BMAX>(hist_sm, hl, a.bf, a.bj, f[v], j[v]);
+          if (WRITEJ) a.Jout[lin0 + 32u * v] = j[v];
         }
       }
     }
@@ -341,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, FFDP_SWEEP1_MINB) k_sweep1(const Swe
       pending = 0;
     }
   }
+  rs.drain(wr);
   if (HIST) hist_flush<BMAX>(hist_sm, a.ghist, a.B);
 }
 
@@ -431,83 +607,134 @@ __global__ void __launch_bounds__(1024) k_mi_finalize(const FinalizeArgs a) {
 // ------------------------------------------------------------------ sweep 2
 // Per voxel g = dL/dJ (MI table or a given buffer), then either dJ (MI on a
 // materialised J) or the sampler backward: du = K^T (g dJ/dq) and the affine
-// partial sums, reduced per CTA in fp64.
+// partial sums, reduced per CTA in fp64.  Streams: u (sampling), F (MI), and
+// g (given gradient) or J (MI on a given J).
+template <typename FT, int BMAX, int MODE>
+struct S2Cfg {
+  static constexpr bool MI = MODE != S2_GBUF;
+  static constexpr bool SAMPLE = MODE != S2_MI_JBUF;
+  static constexpr int NST = 4;
+  using RG = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, NST>;
+  static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
+  static constexpr size_t kSmem = kTableBytes + RG::kBytes;
+};
+
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kThreads, FFDP_SWEEP2_MINB) k_sweep2(const Sweep2Args a) {
-  constexpr bool MI = MODE != S2_GBUF;
-  constexpr bool SAMPLE = MODE != S2_MI_JBUF;
-  constexpr bool BWD = MODE != S2_MI_JBUF;
+__global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a) {
+  using C = S2Cfg<FT, BMAX, MODE>;
+  constexpr bool MI = C::MI;
+  constexpr bool SAMPLE = C::SAMPLE;
+  constexpr bool BWD = SAMPLE;
+  constexpr int NST = C::NST;
+  using RG = typename C::RG;
+  using WR = WarpRing<RG, NST>;
   extern __shared__ float4 tsm4[];
   float* tsm = reinterpret_cast<float*>(tsm4);
-  __shared__ double wsum[kThreads / 32][12];
+  __shared__ double wsum[kSweepThreads / 32][12];
   const Geom& g = a.g;
   if (MI) {
     constexpr int n4 = table_floats<BMAX>() / 4;
     const float4* src = reinterpret_cast<const float4*>(a.T);
-    for (int i = threadIdx.x; i < n4; i += kThreads) tsm4[i] = __ldg(src + i);
+    for (int i = threadIdx.x; i < n4; i += kSweepThreads) tsm4[i] = __ldg(src + i);
     __syncthreads();
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
   const MT* __restrict__ M = static_cast<const MT*>(a.M);
-  const int warp = threadIdx.x >> 5;
-  if (BWD && (threadIdx.x & 31) == 0)
+  const float* X = SAMPLE ? a.gbuf : a.Jin;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (BWD && lane == 0)
 #pragma unroll
     for (int k = 0; k < 12; ++k) wsum[warp][k] = 0.0;
   float acc[12];
 #pragma unroll
   for (int k = 0; k < 12; ++k) acc[k] = 0.0f;
+  WR wr;
+  wr.init(reinterpret_cast<char*>(tsm4) + C::kTableBytes, SAMPLE && a.u != nullptr);
+  RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
+  const unsigned long long pol = policy_evict_first();
+  rs.template prologue<FT>(wr, a.u, F, X, pol);
   int pending = 0;
-  Group Gnext;
-  {
-    const unsigned l0 = (blockIdx.x * kThreads + threadIdx.x) * kVPT;
-    if (kPrefetch && blockIdx.x < a.nIter && l0 < g.N)
-      load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, l0, min(g.N - l0, (unsigned)kVPT), Gnext);
-  }
-  for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x) {
-    const unsigned lin0 = (it * kThreads + threadIdx.x) * kVPT;
-    Group G = Gnext;
-    if (kPrefetch) {
-      const unsigned itn = it + gridDim.x, ln = (itn * kThreads + threadIdx.x) * kVPT;
-      if (itn < a.nIter && ln < g.N)
-        load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, ln, min(g.N - ln, (unsigned)kVPT), Gnext);
-    } else if (lin0 < g.N) {
-      load_group<FT, MI, SAMPLE, !SAMPLE, !MI>(F, a.u, a.Jin, a.gbuf, lin0, min(g.N - lin0, (unsigned)kVPT), G);
-    }
-    if (lin0 < g.N) {
-      const unsigned nv = min(g.N - lin0, (unsigned)kVPT);
-      float out[3 * kVPT];
+  unsigned k = 0;
+  for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
+    const unsigned ch = rs.chunk(it);
+    const unsigned lin0 = ch * RG::kChunk + lane;
+    const int nv = lane_count(lin0, g.N);
+    if (nv > 0) {
+      float f[kVPT], x[kVPT], u[3 * kVPT];
+#pragma unroll
+      for (int v = 0; v < kVPT; ++v) f[v] = x[v] = u[3 * v] = u[3 * v + 1] = u[3 * v + 2] = 0.0f;
+      if (wr.tx && ch < rs.nFull) {
+        const int s = k % NST;
+        if (rs.wait(wr, k)) {
+#pragma unroll
+          for (int v = 0; v < kVPT; ++v) {
+            const int e = lane + 32 * v;
+            if (MI) f[v] = to_f(wr.template f_of<FT>(s)[e]);
+            if (SAMPLE && wr.has_u) {
+              u[3 * v + 0] = wr.u_of(s)[3 * e + 0];
+              u[3 * v + 1] = wr.u_of(s)[3 * e + 1];
+              u[3 * v + 2] = wr.u_of(s)[3 * e + 2];
+            }
+            if (!MI || !SAMPLE) x[v] = wr.x_of(s)[e];
+          }
+        }
+        rs.template refill<FT>(wr, k, it, a.u, F, X, pol);
+      } else {
+#pragma unroll
+        for (int v = 0; v < kVPT; ++v) {
+          const unsigned lin = lin0 + 32u * v;
+          if (v < nv) {
+            if (MI) f[v] = load1(F + lin);
+            if (SAMPLE && a.u) {
+              u[3 * v + 0] = __ldg(a.u + 3ull * lin + 0);
+              u[3 * v + 1] = __ldg(a.u + 3ull * lin + 1);
+              u[3 * v + 2] = __ldg(a.u + 3ull * lin + 2);
+            }
+            if (!MI || !SAMPLE) x[v] = __ldg(X + lin);
+          }
+        }
+      }
       if (SAMPLE) {
-        // all 32 tap loads of the group are issued before any interpolation
-        GroupWalk w;
-        walk_begin(g, lin0, w);
+        // all tap loads of the lane's voxels are issued before any interpolation
+        LaneWalk w;
+        lw_seek(g, lin0, w);
         float taps[kVPT][8], rr[kVPT][3];
         int ixv[kVPT], iyv[kVPT], izv[kVPT];
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
           int b[3];
-          walk_cell(g, w, v, G.u[3 * v], G.u[3 * v + 1], G.u[3 * v + 2], b, rr[v], ixv[v], iyv[v], izv[v]);
-          if ((unsigned)v >= nv) b[0] = -2;  // past the end: no loads
+          if (v > 0 && v < nv) lw_step(g, lin0 + 32u * v, w);
+          cell_of(g, w.P, u[3 * v], u[3 * v + 1], u[3 * v + 2], b, rr[v]);
+          ixv[v] = w.x;
+          iyv[v] = w.y;
+          izv[v] = w.z;
+          if (v >= nv) b[0] = -2;  // past the end: no loads
           gather8<MT>(M, g, b, taps[v]);
         }
 #pragma unroll
         for (int v = 0; v < kVPT; ++v) {
-          out[3 * v + 0] = out[3 * v + 1] = out[3 * v + 2] = 0.0f;
-          const int ix = ixv[v], iy = iyv[v], iz = izv[v];
-          if ((unsigned)v < nv) {
+          if (v < nv) {
             float gq0, gq1, gq2;
             const float j = interp8<true>(taps[v], rr[v], gq0, gq1, gq2);
-            const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, G.f[v], j) : G.gb[v];
+            const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, f[v], j) : x[v];
             const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
-            if (g.k_diag) {
-              out[3 * v + 0] = g.K[0] * e0;
-              out[3 * v + 1] = g.K[4] * e1;
-              out[3 * v + 2] = g.K[8] * e2;
-            } else {
-              out[3 * v + 0] = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
-              out[3 * v + 1] = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
-              out[3 * v + 2] = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
+            if (a.du) {
+              float o0, o1, o2;
+              if (g.k_diag) {
+                o0 = g.K[0] * e0;
+                o1 = g.K[4] * e1;
+                o2 = g.K[8] * e2;
+              } else {
+                o0 = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
+                o1 = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
+                o2 = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
+              }
+              float* dp = a.du + 3ull * (lin0 + 32u * v);
+              dp[0] = o0;
+              dp[1] = o1;
+              dp[2] = o2;
             }
-            const float cx = (float)ix - g.ctr[0], cy = (float)iy - g.ctr[1], cz = (float)iz - g.ctr[2];
+            const float cx = (float)ixv[v] - g.ctr[0], cy = (float)iyv[v] - g.ctr[1], cz = (float)izv[v] - g.ctr[2];
             acc[kPS + 0] += e0;
             acc[kPS + 1] += e1;
             acc[kPS + 2] += e2;
@@ -522,55 +749,34 @@ __global__ void __launch_bounds__(kThreads, FFDP_SWEEP2_MINB) k_sweep2(const Swe
             acc[kPM + 8] = fmaf(e2, cz, acc[kPM + 8]);
           }
         }
-        if (a.du) {
-          if (nv == kVPT) {
-            float4* dp = reinterpret_cast<float4*>(a.du + 3ull * lin0);
-            dp[0] = make_float4(out[0], out[1], out[2], out[3]);
-            dp[1] = make_float4(out[4], out[5], out[6], out[7]);
-            dp[2] = make_float4(out[8], out[9], out[10], out[11]);
-          } else {
-#pragma unroll
-            for (int v = 0; v < kVPT; ++v)
-              if ((unsigned)v < nv) {
-                a.du[3ull * (lin0 + v) + 0] = out[3 * v + 0];
-                a.du[3ull * (lin0 + v) + 1] = out[3 * v + 1];
-                a.du[3ull * (lin0 + v) + 2] = out[3 * v + 2];
-              }
-          }
-        }
       } else {
 #pragma unroll
-        for (int v = 0; v < kVPT; ++v) out[v] = mi_grad<BMAX>(tsm, a.bf, a.bj, G.f[v], G.j[v]);
-        if (nv == kVPT) {
-          *reinterpret_cast<float4*>(a.dJ + lin0) = make_float4(out[0], out[1], out[2], out[3]);
-        } else {
-#pragma unroll
-          for (int v = 0; v < kVPT; ++v)
-            if ((unsigned)v < nv) a.dJ[lin0 + v] = out[v];
-        }
+        for (int v = 0; v < kVPT; ++v)
+          if (v < nv) a.dJ[lin0 + 32u * v] = mi_grad<BMAX>(tsm, a.bf, a.bj, f[v], x[v]);
       }
     }
     if (BWD && ++pending == kFoldEvery) {
 #pragma unroll
-      for (int k = 0; k < 12; ++k) {
-        const float s = warp_sum(acc[k]);
-        if ((threadIdx.x & 31) == 0) wsum[warp][k] += (double)s;
-        acc[k] = 0.0f;
+      for (int k2 = 0; k2 < 12; ++k2) {
+        const float s = warp_sum(acc[k2]);
+        if (lane == 0) wsum[warp][k2] += (double)s;
+        acc[k2] = 0.0f;
       }
       pending = 0;
     }
   }
+  rs.drain(wr);
   if (BWD) {
 #pragma unroll
-    for (int k = 0; k < 12; ++k) {
-      const float s = warp_sum(acc[k]);
-      if ((threadIdx.x & 31) == 0) wsum[warp][k] += (double)s;
+    for (int k2 = 0; k2 < 12; ++k2) {
+      const float s = warp_sum(acc[k2]);
+      if (lane == 0) wsum[warp][k2] += (double)s;
     }
     __syncthreads();
     if (threadIdx.x < kPartialStride) {
       double s = 0.0;
       if (threadIdx.x < 12)
-        for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][threadIdx.x];
+        for (int w = 0; w < kSweepThreads / 32; ++w) s += wsum[w][threadIdx.x];
       a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = s;
     }
   }
@@ -603,7 +809,9 @@ __global__ void __launch_bounds__(256) k_finish(const FinishArgs a) {
             a.dA[r * 3 + cc] = (float)(a.hM[r] * (a.xc[cc] * sr + a.dx[cc] * sm[kPM + r * 3 + cc][16]));
       }
     }
-    if (a.loss) {
+    if (a.loss && g_ffdp_device_error) {
+      for (int i = 0; i < a.nloss; ++i) a.loss[i] = __int_as_float(0x7fc00000);  // a ring wait gave up: NaN
+    } else if (a.loss) {
       const double mi = a.has_mi ? a.scalars[0] : 0.0;
       const double lncc = a.has_lncc ? sm[kPCC][16] / a.N : 0.0;
       if (a.nloss == 3) {
@@ -625,20 +833,15 @@ cudaError_t launch_zero_u64(unsigned long long* p, int n, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int BMAX, int MODE>
-static size_t sweep1_smem() {
-  return MODE == S1_WRITEJ ? 0 : (size_t)HistLayout<BMAX>::WORDS * sizeof(unsigned);
-}
-
 template <typename FT, typename MT, int BMAX, int MODE>
 static cudaError_t run_sweep1(const Sweep1Args& a, int grid, cudaStream_t s, int* occ) {
   auto k = k_sweep1<FT, MT, BMAX, MODE>;
-  const size_t smem = sweep1_smem<BMAX, MODE>();
+  const size_t smem = S1Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kThreads, smem);
+  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweepThreads, smem);
   note_launch_begin("k_sweep1", s);
-  k<<<grid, kThreads, smem, s>>>(a);
+  k<<<grid, kSweepThreads, smem, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
@@ -685,12 +888,12 @@ int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax) {
 template <typename FT, typename MT, int BMAX, int MODE>
 static cudaError_t run_sweep2(const Sweep2Args& a, int grid, cudaStream_t s, int* occ) {
   auto k = k_sweep2<FT, MT, BMAX, MODE>;
-  const size_t smem = MODE == S2_GBUF ? 0 : (size_t)table_floats<BMAX>() * sizeof(float);
+  const size_t smem = S2Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kThreads, smem);
+  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweepThreads, smem);
   note_launch_begin("k_sweep2", s);
-  k<<<grid, kThreads, smem, s>>>(a);
+  k<<<grid, kSweepThreads, smem, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
@@ -747,6 +950,15 @@ cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s) {
   k_finish<<<1, 256, 0, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
+}
+
+cudaError_t take_device_error(unsigned* v) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_ffdp_device_error, sizeof(unsigned));
+  if (e == cudaSuccess && *v) {
+    const unsigned zero = 0u;
+    e = cudaMemcpyToSymbol(g_ffdp_device_error, &zero, sizeof(unsigned));
+  }
+  return e;
 }
 
 size_t mi_table_bytes(int bmax) { return (size_t)(bmax == 32 ? table_floats<32>() : table_floats<64>()) * sizeof(float); }

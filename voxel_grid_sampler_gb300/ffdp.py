@@ -94,6 +94,8 @@ def lib() -> ctypes.CDLL:
         L.ffdp_timing_read.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int),
                                        ctypes.POINTER(ctypes.c_double), ctypes.c_int]
         L.ffdp_timing_read.restype = ctypes.c_int
+        L.ffdp_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+        L.ffdp_device_error.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -273,6 +275,14 @@ def launch_count() -> int:
     return int(lib().ffdp_launch_count())
 
 
+def device_error() -> bool:
+    """True if a sweep kernel gave up a bounded wait since the last call
+    (synchronises the current device and clears the flag)."""
+    flag = ctypes.c_int(0)
+    _check(lib().ffdp_device_error(ctypes.byref(flag)))
+    return bool(flag.value)
+
+
 def timing_enable(capacity: int) -> None:
     _check(lib().ffdp_timing_enable(int(capacity)))
 
@@ -294,7 +304,8 @@ class Declared:
     """Entry points declared in include/ffdp.h (for the symbol check)."""
     names: tuple = ("ffdp_workspace_bytes", "ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd",
                     "ffdp_mi_fwd_bwd", "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_status_string",
-                    "ffdp_last_error", "ffdp_launch_count", "ffdp_timing_enable", "ffdp_timing_read")
+                    "ffdp_last_error", "ffdp_launch_count", "ffdp_timing_enable", "ffdp_timing_read",
+                    "ffdp_device_error")
 
 
 def ffdp_objective_mi_static(F, M, u, T: ffdp_transform, params: ffdp_objective_params, loss, du, dA, dt,
