@@ -14,7 +14,10 @@ namespace ffdp {
 
 // ---------------------------------------------------------------- constants
 constexpr int kThreads = 256;           // threads per CTA of the LNCC kernel
-constexpr int kSweepThreads = 512;      // threads per CTA of the voxel sweeps (one CTA per SM)
+#ifndef FFDP_SWEEP_THREADS
+#define FFDP_SWEEP_THREADS 512
+#endif
+constexpr int kSweepThreads = FFDP_SWEEP_THREADS;  // threads per CTA of the voxel sweeps (one CTA per SM)
 constexpr int kVPT = 4;                 // voxels per sweep thread per iteration (32 apart)
 constexpr int kHistFrac = 20;           // fixed-point fraction bits of histogram weights
 constexpr float kHistOne = 1048576.0f;  // 2^kHistFrac

@@ -9,30 +9,38 @@
 //
 // Layout of the work: a CTA iteration covers kSweepThreads*kVPT consecutive
 // voxels of the flattened [D][H][W] grid; each warp owns 32*kVPT of them and
-// each lane every 32nd (see the lane walk).  Grids are persistent (one CTA per
-// SM striding over iterations).
+// each lane every 32nd (see the lane walk), taken two at a time through a
+// two-stage gather pipeline.  Grids are persistent (one CTA per SM striding
+// over iterations).
 #include "ffdp_internal.h"
 
 namespace ffdp {
 
 // ----------------------------------------------------- histogram layout
-// Bin (a, b) of the joint histogram has R = 8 lane copies.  Lane l adds into
-// copy c = l mod 8, and its group ga = l / 8 (0..3) fixes the order in which
-// it visits a voxel's four kernel rows: at step i it takes the row a of the
-// four with a = i + ga (mod 4).  The word address
-//   word(a, b, c) = (a / 4) * 32 B + 32 b + 8 (a mod 4) + c
-// lies in bank 8 (a mod 4) + c, so at every step the 32 lanes of a warp hit
-// 32 distinct banks whatever their bins: each shared atomic instruction is
-// one wavefront and no two lanes ever share an address.
+// Shared atomic instructions of a warp are conflict-free by construction:
+//
+// * BMAX = 32: every lane owns a private copy of the joint histogram, word
+//   (a * 32 + b) * 32 + lane; all 32 lanes of an instruction hit 32 banks and
+//   the 16 words of a voxel sit at compile-time offsets from one base.
+// * BMAX = 64 (a private copy per lane would not fit): R = 8 lane copies per
+//   bin.  Lane l adds into copy c = l mod 8, and its group ga = l / 8 (0..3)
+//   fixes the order in which it visits a voxel's four kernel rows: at step i
+//   the row a of the four with a = i + ga (mod 4).  The word address
+//     word(a, b, c) = (a / 4) * 32 B + 32 b + 8 (a mod 4) + c
+//   lies in bank 8 (a mod 4) + c, so at every step the 32 lanes use 32
+//   distinct banks whatever their bins.
 template <int BMAX>
 struct HistLayout {
-  static constexpr int R = 8;
-  static constexpr int COL = 4 * R;             // word stride of b
-  static constexpr int QROW = COL * BMAX;       // words per group of four rows
+  static constexpr bool PRIVATE = BMAX <= 32;
+  static constexpr int R = PRIVATE ? 32 : 8;      // copies per bin
+  static constexpr int COL = PRIVATE ? 32 : 4 * R;  // word stride of b
+  static constexpr int QROW = COL * BMAX;         // words per row (private) / per group of four rows
   static constexpr int WORDS = BMAX * BMAX * R;
   // voxels reaching one word per CTA iteration: lanes sharing a copy
   static constexpr int VOX_PER_ITER = kSweepThreads * kVPT / R;
-  __host__ __device__ static constexpr int word(int a, int b) { return (a >> 2) * QROW + COL * b + R * (a & 3); }
+  __host__ __device__ static constexpr int word(int a, int b) {
+    return PRIVATE ? (a * BMAX + b) * 32 : (a >> 2) * QROW + COL * b + R * (a & 3);
+  }
 };
 
 // u32 fixed-point counts (kHistFrac fraction bits): one voxel adds at most
@@ -52,33 +60,51 @@ __global__ void k_zero_u64(unsigned long long* p, int n) {
 }
 
 // Sums the R copies of every bin into the u64 histogram and clears them.
-// Thread i reads bin (a, b) with a mod 4 = i mod 4 and takes its two 16-byte
-// halves in lane-dependent order, so the 8 lanes of each quarter-warp read 8
-// different bank quads.  Rows run to B rounded up to a multiple of 4.
+// Private copies: a thread reads the 32 words of its bin starting at its own
+// lane's bank.  Shared copies: thread i reads bin (a, b) with a mod 4 = i mod 4
+// and takes its two 16-byte halves in lane-dependent order, so the 8 lanes of
+// each quarter-warp read 8 different bank quads (rows run to B rounded up to
+// a multiple of 4).
 template <int BMAX>
 __device__ __forceinline__ void hist_flush(unsigned* hist, unsigned long long* gh, int B) {
   using L = HistLayout<BMAX>;
-  static_assert(L::R == 8, "flush reads two uint4 per bin");
   __syncthreads();
-  const int h = (threadIdx.x >> 2) & 1;
-  const int n = ((B + 3) & ~3) * B;
-  for (int i = threadIdx.x; i < n; i += kSweepThreads) {
-    const int rest = i >> 2, rb = rest % B, ra = ((rest / B) << 2) | (i & 3);
-    if (ra >= B) continue;
-    uint4* w = reinterpret_cast<uint4*>(hist + L::word(ra, rb));
-    const uint4 v0 = w[h], v1 = w[h ^ 1];
-    w[h] = make_uint4(0u, 0u, 0u, 0u);
-    w[h ^ 1] = make_uint4(0u, 0u, 0u, 0u);
-    const unsigned long long s = (unsigned long long)v0.x + v0.y + (unsigned long long)v0.z + v0.w +
-                                 (unsigned long long)v1.x + v1.y + (unsigned long long)v1.z + v1.w;
-    if (s) atomicAdd(gh + ra * B + rb, s);
+  if (L::PRIVATE) {
+    const int lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < B * B; i += kSweepThreads) {
+      const int ra = i / B, rb = i - ra * B;
+      unsigned* w = hist + L::word(ra, rb);
+      unsigned long long s = 0ull;
+#pragma unroll 8
+      for (int j = 0; j < 32; ++j) {
+        const int c = (lane + j) & 31;
+        s += w[c];
+        w[c] = 0u;
+      }
+      if (s) atomicAdd(gh + i, s);
+    }
+  } else {
+    static_assert(L::PRIVATE || L::R == 8, "flush reads two uint4 per bin");
+    const int h = (threadIdx.x >> 2) & 1;
+    const int n = ((B + 3) & ~3) * B;
+    for (int i = threadIdx.x; i < n; i += kSweepThreads) {
+      const int rest = i >> 2, rb = rest % B, ra = ((rest / B) << 2) | (i & 3);
+      if (ra >= B) continue;
+      uint4* w = reinterpret_cast<uint4*>(hist + L::word(ra, rb));
+      const uint4 v0 = w[h], v1 = w[h ^ 1];
+      w[h] = make_uint4(0u, 0u, 0u, 0u);
+      w[h ^ 1] = make_uint4(0u, 0u, 0u, 0u);
+      const unsigned long long s = (unsigned long long)v0.x + v0.y + (unsigned long long)v0.z + v0.w +
+                                   (unsigned long long)v1.x + v1.y + (unsigned long long)v1.z + v1.w;
+      if (s) atomicAdd(gh + ra * B + rb, s);
+    }
   }
   __syncthreads();
 }
 
 // Per-lane constants of the histogram accumulation.
 struct HistLane {
-  int rowoff[4];  // R ((i + ga) mod 4) + c for step i
+  int rowoff[4];  // shared copies: R ((i + ga) mod 4) + c for step i; private: lane
   int ga;
 };
 
@@ -86,9 +112,9 @@ template <int BMAX>
 __device__ __forceinline__ void hist_lane_init(HistLane& h) {
   using L = HistLayout<BMAX>;
   const int lane = threadIdx.x & 31;
-  h.ga = lane / L::R;
+  h.ga = lane / 8;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) h.rowoff[i] = L::R * ((i + h.ga) & 3) + (lane & (L::R - 1));
+  for (int i = 0; i < 4; ++i) h.rowoff[i] = L::PRIVATE ? lane : 8 * ((i + h.ga) & 3) + (lane & 7);
 }
 
 // r[i] = w[(i + s) mod 4].
@@ -111,21 +137,31 @@ __device__ __forceinline__ void hist_add(unsigned* hist, const HistLane& h, cons
   float tf, tj;
   floor_split(bin_coord(bf, f), af, tf);
   floor_split(bin_coord(bj, j), aj, tj);
-  float wf[4], wj[4], wr[4];
+  float wf[4], wj[4];
   bspline4(tf, kHistOne, wf);
   bspline4(tj, 1.0f, wj);
-  // step i takes kernel row a_i = af - 1 + ((i + s) mod 4), s = ga - af + 1,
-  // so that a_i = i + ga (mod 4)
-  const int s = h.ga - af + 1;
-  rotate4(wf, s, wr);
-  unsigned* col = hist + L::COL * (aj - 1);
+  if (L::PRIVATE) {
+    unsigned* base = hist + L::word(af - 1, aj - 1) + h.rowoff[0];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int ai = af - 1 + ((i + s) & 3);
-    unsigned* row = col + (ai >> 2) * L::QROW + h.rowoff[i];
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      atomicAdd(row + k * L::COL, __float_as_uint(fmaf(wr[i], wj[k], kMagic)) - kMagicBits);
+      for (int k = 0; k < 4; ++k)
+        atomicAdd(base + i * L::QROW + k * L::COL, __float_as_uint(fmaf(wf[i], wj[k], kMagic)) - kMagicBits);
+  } else {
+    // step i takes kernel row a_i = af - 1 + ((i + s) mod 4), s = ga - af + 1,
+    // so that a_i = i + ga (mod 4)
+    const int s = h.ga - af + 1;
+    float wr[4];
+    rotate4(wf, s, wr);
+    unsigned* col = hist + L::COL * (aj - 1);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ai = af - 1 + ((i + s) & 3);
+      unsigned* row = col + (ai >> 2) * L::QROW + h.rowoff[i];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        atomicAdd(row + k * L::COL, __float_as_uint(fmaf(wr[i], wj[k], kMagic)) - kMagicBits);
+    }
   }
 }
 
@@ -402,6 +438,90 @@ struct RingSched {
   }
 };
 
+// ------------------------------------------------------ half-chunk pipeline
+// A lane's kVPT = 4 voxels of a chunk are taken two at a time ("halves").
+// While one half is interpolated and accumulated, the 16 trilinear taps of the
+// next half (the second half of this chunk, or the first half of the warp's
+// next chunk) are already in flight, so gather latency overlaps arithmetic.
+static_assert(kVPT == 4, "the pipeline takes a lane's four voxels as two halves");
+
+struct Half {
+  float taps[2][8];
+  float rr[2][3];
+  float f[2];       // F (histogram / MI)
+  float x[2];       // J (MI on a given J) or g = dL/dJ (given gradient)
+  int ix[2], iy[2], iz[2];
+  unsigned lin;     // linear index of the half's first voxel (this lane)
+  int nv;           // voxels of the half inside the grid (0..2)
+};
+
+// Prepares half h (0 or 1) of iteration k (CTA iteration it): reads u, F and
+// J/g (from the ring slot of a streamed chunk, else from global memory),
+// walks the coordinates and issues the gathers.  Half 0 waits for the chunk's
+// slot; half 1 releases the slot for refilling.
+template <typename FT, typename MT, bool LF, bool LU, bool LX, class WR, int NST>
+__device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __restrict__ M, const FT* __restrict__ F,
+                                        const float* u, const float* X, WR& wr, RingSched<WR, NST>& rs,
+                                        LaneWalk& w, unsigned it, unsigned k, int h, unsigned long long pol) {
+  const int lane = threadIdx.x & 31;
+  const unsigned ch = rs.chunk(it);
+  const unsigned lin0 = ch * (32 * kVPT) + lane;
+  const int nvc = it < rs.nIter ? lane_count(lin0, g.N) : 0;
+  H.lin = lin0 + 64u * h;
+  H.nv = min(max(nvc - 2 * h, 0), 2);
+  const bool streamed = wr.tx && it < rs.nIter && ch < rs.nFull;
+  bool ok = true;
+  if (streamed && h == 0) ok = rs.wait(wr, k);
+  const int s = k % NST;
+  float uu[2][3];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int v = 2 * h + j;
+    const unsigned lin = lin0 + 32u * v;
+    H.f[j] = H.x[j] = uu[j][0] = uu[j][1] = uu[j][2] = 0.0f;
+    if (streamed) {
+      if (ok) {
+        const int e = lane + 32 * v;
+        if (LF) H.f[j] = to_f(wr.template f_of<FT>(s)[e]);
+        if (LU && wr.has_u) {
+          uu[j][0] = wr.u_of(s)[3 * e + 0];
+          uu[j][1] = wr.u_of(s)[3 * e + 1];
+          uu[j][2] = wr.u_of(s)[3 * e + 2];
+        }
+        if (LX) H.x[j] = wr.x_of(s)[e];
+      }
+    } else if (v < nvc) {
+      if (LF) H.f[j] = load1(F + lin);
+      if (LU && u) {
+        uu[j][0] = __ldg(u + 3ull * lin + 0);
+        uu[j][1] = __ldg(u + 3ull * lin + 1);
+        uu[j][2] = __ldg(u + 3ull * lin + 2);
+      }
+      if (LX) H.x[j] = __ldg(X + lin);
+    }
+  }
+  if (streamed && h == 1) rs.template refill<FT>(wr, k, it, u, F, X, pol);
+  if (LU) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int v = 2 * h + j;
+      int b[3];
+      if (v < nvc) {
+        if (v == 0)
+          lw_seek(g, lin0, w);
+        else
+          lw_step(g, lin0 + 32u * v, w);
+      }
+      cell_of(g, w.P, uu[j][0], uu[j][1], uu[j][2], b, H.rr[j]);
+      H.ix[j] = w.x;
+      H.iy[j] = w.y;
+      H.iz[j] = w.z;
+      if (v >= nvc) b[0] = -2;  // past the end: no loads
+      gather8<MT>(M, g, b, H.taps[j]);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ sweep 1
 // Sampling (or reading J) plus, per mode, the histogram and/or a J store.
 // Streams: u (sampling), F (histogram), J (histogram of a given J).
@@ -409,11 +529,29 @@ template <typename FT, int BMAX, int MODE>
 struct S1Cfg {
   static constexpr bool HIST = MODE != S1_WRITEJ;
   static constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
-  static constexpr int NST = (HIST && BMAX == 64) ? 2 : 4;
-  using RG = Ring<FT, SAMPLE, HIST, !SAMPLE, NST>;
   static constexpr size_t kHistBytes = HIST ? (size_t)HistLayout<BMAX>::WORDS * sizeof(unsigned) : 0;
+  using RG1 = Ring<FT, SAMPLE, HIST, !SAMPLE, 1>;
+  // as many ring slots (up to 4) as fit next to the histogram in 220 KiB
+  static constexpr int NST_FIT = (int)((220 * 1024 - kHistBytes) / ((kSweepThreads / 32) * (RG1::kSlot + 8)));
+  static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
+  static_assert(NST >= 2, "ring needs two slots");
+  using RG = Ring<FT, SAMPLE, HIST, !SAMPLE, NST>;
   static constexpr size_t kSmem = kHistBytes + RG::kBytes;
 };
+
+template <int BMAX, bool HIST, bool WRITEJ>
+__device__ __forceinline__ void sweep1_half(const Half& H, unsigned* hist, const HistLane& hl, const Sweep1Args& a,
+                                            bool sample) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (j < H.nv) {
+      float d0, d1, d2;
+      const float jv = sample ? interp8<false>(H.taps[j], H.rr[j], d0, d1, d2) : H.x[j];
+      if (HIST) hist_add<BMAX>(hist, hl, a.bf, a.bj, H.f[j], jv);
+      if (WRITEJ) a.Jout[H.lin + 32u * j] = jv;
+    }
+  }
+}
 
 template <typename FT, typename MT, int BMAX, int MODE>
 __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a) {
@@ -442,75 +580,16 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a)
   RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
   const unsigned long long pol = policy_evict_first();
   rs.template prologue<FT>(wr, a.u, F, X, pol);
-  const int lane = threadIdx.x & 31;
-  int pending = 0;
+  LaneWalk w;
+  Half A, B;
   unsigned k = 0;
+  prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
-    const unsigned ch = rs.chunk(it);
-    const unsigned lin0 = ch * RG::kChunk + lane;
-    const int nv = lane_count(lin0, g.N);
-    if (nv > 0) {
-      float f[kVPT], j[kVPT], u[3 * kVPT];
-#pragma unroll
-      for (int v = 0; v < kVPT; ++v) f[v] = j[v] = u[3 * v] = u[3 * v + 1] = u[3 * v + 2] = 0.0f;
-      if (wr.tx && ch < rs.nFull) {
-        const int s = k % NST;
-        if (rs.wait(wr, k)) {
-#pragma unroll
-          for (int v = 0; v < kVPT; ++v) {
-            const int e = lane + 32 * v;
-            if (HIST) f[v] = to_f(wr.template f_of<FT>(s)[e]);
-            if (SAMPLE && wr.has_u) {
-              u[3 * v + 0] = wr.u_of(s)[3 * e + 0];
-              u[3 * v + 1] = wr.u_of(s)[3 * e + 1];
-              u[3 * v + 2] = wr.u_of(s)[3 * e + 2];
-            }
-            if (!SAMPLE) j[v] = wr.x_of(s)[e];
-          }
-        }
-        rs.template refill<FT>(wr, k, it, a.u, F, X, pol);
-      } else {
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          const unsigned lin = lin0 + 32u * v;
-          if (v < nv) {
-            if (HIST) f[v] = load1(F + lin);
-            if (SAMPLE && a.u) {
-              u[3 * v + 0] = __ldg(a.u + 3ull * lin + 0);
-              u[3 * v + 1] = __ldg(a.u + 3ull * lin + 1);
-              u[3 * v + 2] = __ldg(a.u + 3ull * lin + 2);
-            }
-            if (!SAMPLE) j[v] = __ldg(a.Jin + lin);
-          }
-        }
-      }
-      if (SAMPLE) {
-        // all tap loads of the lane's voxels are issued before any interpolation
-        LaneWalk w;
-        lw_seek(g, lin0, w);
-        float taps[kVPT][8], rr[kVPT][3];
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          int b[3];
-          if (v > 0 && v < nv) lw_step(g, lin0 + 32u * v, w);
-          cell_of(g, w.P, u[3 * v], u[3 * v + 1], u[3 * v + 2], b, rr[v]);
-          if (v >= nv) b[0] = -2;  // past the end: no loads
-          gather8<MT>(M, g, b, taps[v]);
-        }
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          float d0, d1, d2;
-          j[v] = interp8<false>(taps[v], rr[v], d0, d1, d2);
-        }
-      }
-#pragma unroll
-      for (int v = 0; v < kVPT; ++v) {
-        if (v < nv) {
-          if (HIST) hist_add<BMAX>(hist_sm, hl, a.bf, a.bj, f[v], j[v]);
-          if (WRITEJ) a.Jout[lin0 + 32u * v] = j[v];
-        }
-      }
-    }
+    prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
+    sweep1_half<BMAX, HIST, WRITEJ>(A, hist_sm, hl, a, SAMPLE);
+    prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+    sweep1_half<BMAX, HIST, WRITEJ>(B, hist_sm, hl, a, SAMPLE);
     if (HIST && ++pending == flush_every<BMAX>()) {
       hist_flush<BMAX>(hist_sm, a.ghist, a.B);
       pending = 0;
@@ -613,11 +692,63 @@ template <typename FT, int BMAX, int MODE>
 struct S2Cfg {
   static constexpr bool MI = MODE != S2_GBUF;
   static constexpr bool SAMPLE = MODE != S2_MI_JBUF;
-  static constexpr int NST = 4;
-  using RG = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, NST>;
   static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
+  using RG1 = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, 1>;
+  // as many ring slots (up to 4) as fit next to the table in 220 KiB
+  static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (kSweepThreads / 32) * 96) /
+                                       ((kSweepThreads / 32) * (RG1::kSlot + 8)));
+  static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
+  static_assert(NST >= 2, "ring needs two slots");
+  using RG = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, NST>;
   static constexpr size_t kSmem = kTableBytes + RG::kBytes;
 };
+
+template <int BMAX, bool MI, bool SAMPLE>
+__device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, const Sweep2Args& a, float acc[12]) {
+  const Geom& g = a.g;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    if (j >= H.nv) continue;
+    const unsigned lin = H.lin + 32u * j;
+    if (!SAMPLE) {
+      a.dJ[lin] = mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], H.x[j]);
+      continue;
+    }
+    float gq0, gq1, gq2;
+    const float jv = interp8<true>(H.taps[j], H.rr[j], gq0, gq1, gq2);
+    const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
+    const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
+    if (a.du) {
+      float o0, o1, o2;
+      if (g.k_diag) {
+        o0 = g.K[0] * e0;
+        o1 = g.K[4] * e1;
+        o2 = g.K[8] * e2;
+      } else {
+        o0 = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
+        o1 = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
+        o2 = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
+      }
+      float* dp = a.du + 3ull * lin;
+      dp[0] = o0;
+      dp[1] = o1;
+      dp[2] = o2;
+    }
+    const float cx = (float)H.ix[j] - g.ctr[0], cy = (float)H.iy[j] - g.ctr[1], cz = (float)H.iz[j] - g.ctr[2];
+    acc[kPS + 0] += e0;
+    acc[kPS + 1] += e1;
+    acc[kPS + 2] += e2;
+    acc[kPM + 0] = fmaf(e0, cx, acc[kPM + 0]);
+    acc[kPM + 1] = fmaf(e0, cy, acc[kPM + 1]);
+    acc[kPM + 2] = fmaf(e0, cz, acc[kPM + 2]);
+    acc[kPM + 3] = fmaf(e1, cx, acc[kPM + 3]);
+    acc[kPM + 4] = fmaf(e1, cy, acc[kPM + 4]);
+    acc[kPM + 5] = fmaf(e1, cz, acc[kPM + 5]);
+    acc[kPM + 6] = fmaf(e2, cx, acc[kPM + 6]);
+    acc[kPM + 7] = fmaf(e2, cy, acc[kPM + 7]);
+    acc[kPM + 8] = fmaf(e2, cz, acc[kPM + 8]);
+  }
+}
 
 template <typename FT, typename MT, int BMAX, int MODE>
 __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a) {
@@ -644,123 +775,31 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (BWD && lane == 0)
 #pragma unroll
-    for (int k = 0; k < 12; ++k) wsum[warp][k] = 0.0;
+    for (int q = 0; q < 12; ++q) wsum[warp][q] = 0.0;
   float acc[12];
 #pragma unroll
-  for (int k = 0; k < 12; ++k) acc[k] = 0.0f;
+  for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
   WR wr;
   wr.init(reinterpret_cast<char*>(tsm4) + C::kTableBytes, SAMPLE && a.u != nullptr);
   RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
   const unsigned long long pol = policy_evict_first();
   rs.template prologue<FT>(wr, a.u, F, X, pol);
-  int pending = 0;
+  LaneWalk w;
+  Half A, B;
   unsigned k = 0;
+  prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
-    const unsigned ch = rs.chunk(it);
-    const unsigned lin0 = ch * RG::kChunk + lane;
-    const int nv = lane_count(lin0, g.N);
-    if (nv > 0) {
-      float f[kVPT], x[kVPT], u[3 * kVPT];
-#pragma unroll
-      for (int v = 0; v < kVPT; ++v) f[v] = x[v] = u[3 * v] = u[3 * v + 1] = u[3 * v + 2] = 0.0f;
-      if (wr.tx && ch < rs.nFull) {
-        const int s = k % NST;
-        if (rs.wait(wr, k)) {
-#pragma unroll
-          for (int v = 0; v < kVPT; ++v) {
-            const int e = lane + 32 * v;
-            if (MI) f[v] = to_f(wr.template f_of<FT>(s)[e]);
-            if (SAMPLE && wr.has_u) {
-              u[3 * v + 0] = wr.u_of(s)[3 * e + 0];
-              u[3 * v + 1] = wr.u_of(s)[3 * e + 1];
-              u[3 * v + 2] = wr.u_of(s)[3 * e + 2];
-            }
-            if (!MI || !SAMPLE) x[v] = wr.x_of(s)[e];
-          }
-        }
-        rs.template refill<FT>(wr, k, it, a.u, F, X, pol);
-      } else {
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          const unsigned lin = lin0 + 32u * v;
-          if (v < nv) {
-            if (MI) f[v] = load1(F + lin);
-            if (SAMPLE && a.u) {
-              u[3 * v + 0] = __ldg(a.u + 3ull * lin + 0);
-              u[3 * v + 1] = __ldg(a.u + 3ull * lin + 1);
-              u[3 * v + 2] = __ldg(a.u + 3ull * lin + 2);
-            }
-            if (!MI || !SAMPLE) x[v] = __ldg(X + lin);
-          }
-        }
-      }
-      if (SAMPLE) {
-        // all tap loads of the lane's voxels are issued before any interpolation
-        LaneWalk w;
-        lw_seek(g, lin0, w);
-        float taps[kVPT][8], rr[kVPT][3];
-        int ixv[kVPT], iyv[kVPT], izv[kVPT];
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          int b[3];
-          if (v > 0 && v < nv) lw_step(g, lin0 + 32u * v, w);
-          cell_of(g, w.P, u[3 * v], u[3 * v + 1], u[3 * v + 2], b, rr[v]);
-          ixv[v] = w.x;
-          iyv[v] = w.y;
-          izv[v] = w.z;
-          if (v >= nv) b[0] = -2;  // past the end: no loads
-          gather8<MT>(M, g, b, taps[v]);
-        }
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v) {
-          if (v < nv) {
-            float gq0, gq1, gq2;
-            const float j = interp8<true>(taps[v], rr[v], gq0, gq1, gq2);
-            const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, f[v], j) : x[v];
-            const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
-            if (a.du) {
-              float o0, o1, o2;
-              if (g.k_diag) {
-                o0 = g.K[0] * e0;
-                o1 = g.K[4] * e1;
-                o2 = g.K[8] * e2;
-              } else {
-                o0 = fmaf(g.K[0], e0, fmaf(g.K[3], e1, g.K[6] * e2));
-                o1 = fmaf(g.K[1], e0, fmaf(g.K[4], e1, g.K[7] * e2));
-                o2 = fmaf(g.K[2], e0, fmaf(g.K[5], e1, g.K[8] * e2));
-              }
-              float* dp = a.du + 3ull * (lin0 + 32u * v);
-              dp[0] = o0;
-              dp[1] = o1;
-              dp[2] = o2;
-            }
-            const float cx = (float)ixv[v] - g.ctr[0], cy = (float)iyv[v] - g.ctr[1], cz = (float)izv[v] - g.ctr[2];
-            acc[kPS + 0] += e0;
-            acc[kPS + 1] += e1;
-            acc[kPS + 2] += e2;
-            acc[kPM + 0] = fmaf(e0, cx, acc[kPM + 0]);
-            acc[kPM + 1] = fmaf(e0, cy, acc[kPM + 1]);
-            acc[kPM + 2] = fmaf(e0, cz, acc[kPM + 2]);
-            acc[kPM + 3] = fmaf(e1, cx, acc[kPM + 3]);
-            acc[kPM + 4] = fmaf(e1, cy, acc[kPM + 4]);
-            acc[kPM + 5] = fmaf(e1, cz, acc[kPM + 5]);
-            acc[kPM + 6] = fmaf(e2, cx, acc[kPM + 6]);
-            acc[kPM + 7] = fmaf(e2, cy, acc[kPM + 7]);
-            acc[kPM + 8] = fmaf(e2, cz, acc[kPM + 8]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < kVPT; ++v)
-          if (v < nv) a.dJ[lin0 + 32u * v] = mi_grad<BMAX>(tsm, a.bf, a.bj, f[v], x[v]);
-      }
-    }
+    prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
+    sweep2_half<BMAX, MI, SAMPLE>(A, tsm, a, acc);
+    prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+    sweep2_half<BMAX, MI, SAMPLE>(B, tsm, a, acc);
     if (BWD && ++pending == kFoldEvery) {
 #pragma unroll
-      for (int k2 = 0; k2 < 12; ++k2) {
-        const float s = warp_sum(acc[k2]);
-        if (lane == 0) wsum[warp][k2] += (double)s;
-        acc[k2] = 0.0f;
+      for (int q = 0; q < 12; ++q) {
+        const float s = warp_sum(acc[q]);
+        if (lane == 0) wsum[warp][q] += (double)s;
+        acc[q] = 0.0f;
       }
       pending = 0;
     }
@@ -768,15 +807,15 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a)
   rs.drain(wr);
   if (BWD) {
 #pragma unroll
-    for (int k2 = 0; k2 < 12; ++k2) {
-      const float s = warp_sum(acc[k2]);
-      if (lane == 0) wsum[warp][k2] += (double)s;
+    for (int q = 0; q < 12; ++q) {
+      const float s = warp_sum(acc[q]);
+      if (lane == 0) wsum[warp][q] += (double)s;
     }
     __syncthreads();
     if (threadIdx.x < kPartialStride) {
       double s = 0.0;
       if (threadIdx.x < 12)
-        for (int w = 0; w < kSweepThreads / 32; ++w) s += wsum[w][threadIdx.x];
+        for (int q = 0; q < kSweepThreads / 32; ++q) s += wsum[q][threadIdx.x];
       a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = s;
     }
   }
