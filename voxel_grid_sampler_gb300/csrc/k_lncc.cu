@@ -63,9 +63,10 @@ struct LT {
 };
 
 template <int R>
-static size_t smem_of() {
-  return (size_t)LT<R>::TOTAL * sizeof(float);
-}
+struct LTR;
+
+template <int R>
+static size_t smem_of();
 
 size_t lncc_smem_bytes(int R, int /*bmax*/) {
   switch (R) {
@@ -511,10 +512,428 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   }
 }
 
+// ------------------------------------------------- register-history variant
+// Same mathematics and tiling, for R <= 3.  Each thread stages NSTG fixed
+// positions of the 2R-halo plane (its own NOUT output voxels first) and keeps
+// their (J, F) for the last w planes in registers, so the z window sums need
+// no shared memory; the z sums of the g-terms run over a register ring of the
+// thread's own outputs.  Shared memory carries only the x and y passes:
+//   [B] z sums (registers) -> zbuf,        [C] x sums zbuf -> xbuf,
+//   [D] y sums, cc and g-terms -> gbuf,    [E] x sums gbuf -> gxbuf,
+//   [F] y sums at the thread's outputs -> register ring, [G] z sums, dJ.
+// The plane loop is unrolled by w so that every register slot index is a
+// compile-time constant.
+template <int R>
+struct LTR {
+  using L = LT<R>;
+  static constexpr int W = L::W, TY = L::TY, E2W = L::E2W, E2H = L::E2H;
+  static constexpr int NOUT = TY * kTX / kThreads;       // outputs per thread
+  static constexpr int NCORE = TY * kTX;
+  static constexpr int NHALO = E2H * E2W - NCORE;        // halo positions outside the outputs
+  static constexpr int NEXTRA = (NHALO + kThreads - 1) / kThreads;
+  static constexpr int NSTG = NOUT + NEXTRA;
+  static_assert(NOUT * kThreads == NCORE, "outputs per thread");
+  // shared memory: zbuf (z sums, later the g-terms) and xbuf (x sums, later
+  // the x-summed g-terms); no plane ring
+  static constexpr int OFF_Z = 0;
+  static constexpr int OFF_X = L::ZB + L::PAD;
+  static constexpr int TOTAL = OFF_X + L::XB + L::PAD;
+};
+
+// Halo position h (outside the output core) of a tile: the top and bottom 2R
+// rows in full, then the 2R columns on either side of the core rows.
+template <int R>
+__device__ __forceinline__ void halo_pos(int h, int& row, int& col) {
+  using L = LT<R>;
+  constexpr int STRIP = 2 * R * L::E2W;
+  if (h < STRIP) {
+    row = h / L::E2W;
+    col = h - row * L::E2W;
+  } else if (h < 2 * STRIP) {
+    h -= STRIP;
+    row = 2 * R + L::TY + h / L::E2W;
+    col = h % L::E2W;
+  } else {
+    h -= 2 * STRIP;
+    row = 2 * R + h / (4 * R);
+    const int c = h % (4 * R);
+    col = c < 2 * R ? c : kTX + c;
+  }
+}
+
+template <typename FT, int BMAX, int R>
+__global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
+  using L = LT<R>;
+  using Q = LTR<R>;
+  constexpr int W = L::W, TY = L::TY, E2S = L::E2S;
+  constexpr int E1W = L::E1W, E1H = L::E1H, E1S = L::E1S, NIN = L::NIN;
+  constexpr int NOUT = Q::NOUT, NSTG = Q::NSTG;
+  constexpr bool MI = BMAX != 0;
+
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  __shared__ double wsum[kThreads / 32][13];
+  float2* zP = reinterpret_cast<float2*>(sm + Q::OFF_Z);
+  float2* zQ = zP + L::E2H * E2S;
+  float* zX = sm + Q::OFF_Z + 4 * L::E2H * E2S;
+  float2* xP = reinterpret_cast<float2*>(sm + Q::OFF_X);
+  float2* xQ = xP + L::E2H * E1S;
+  float* xX = sm + Q::OFF_X + 4 * L::E2H * E1S;
+  float2* gP = reinterpret_cast<float2*>(sm + Q::OFF_Z);
+  float* gX = sm + Q::OFF_Z + 2 * E1H * E1S;
+  float2* gxP = reinterpret_cast<float2*>(sm + Q::OFF_X);
+  float* gxX = sm + Q::OFF_X + 2 * E1H * kTX;
+
+  const Geom& g = a.g;
+  const int tid = threadIdx.x;
+  const FT* __restrict__ F = static_cast<const FT*>(a.F);
+  const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
+  const float2 ninv2 = make_float2(-inv_n, -inv_n);
+  const size_t plane = (size_t)g.fW * g.fH;
+  float cc_acc = 0.0f;
+  if ((tid & 31) == 0) wsum[tid >> 5][12] = 0.0;
+
+  // staged positions: shared-memory index in the halo plane and in-plane
+  // global offset (-1: outside the grid, read as zero; -2: no position)
+  const int ox = tid & 31, oy0 = (tid >> 5) * NOUT;
+  int sidx[NSTG];
+#pragma unroll
+  for (int i = 0; i < NSTG; ++i) {
+    int row, col;
+    if (i < NOUT) {
+      row = oy0 + i + 2 * R;
+      col = ox + 2 * R;
+    } else {
+      const int h = tid + (i - NOUT) * kThreads;
+      if (h < Q::NHALO) {
+        halo_pos<R>(h, row, col);
+      } else {
+        row = -1;
+        col = 0;
+      }
+    }
+    sidx[i] = row < 0 ? -1 : row * E2S + col;
+  }
+
+  float2 hist[W][NSTG];  // (J, F) of the last w planes at the staged positions
+  float2 grP[W][NOUT];   // g-term 2-D window sums at the own outputs, last w planes
+  float grX[W][NOUT];
+  float2 nxt[NSTG];      // next plane, fetched one step ahead
+  int soff[NSTG];
+
+  auto load_plane = [&](int zp) {
+    const bool zin = zp >= 0 && zp < g.fD;
+    const size_t base = (size_t)zp * plane;
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      float2 v = make_float2(0.0f, 0.0f);
+      if (zin && soff[i] >= 0) {
+        v.x = __ldg(a.J + base + soff[i]);
+        v.y = load1(F + base + soff[i]);
+      }
+      nxt[i] = v;
+    }
+  };
+
+  const int chunksZ = (g.fD + a.tz - 1) / a.tz;
+  const int ntiles = a.tilesX * a.tilesY * chunksZ;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    int t = tile;
+    const int tx = t % a.tilesX;
+    t /= a.tilesX;
+    const int ty = t % a.tilesY;
+    const int tzc = t / a.tilesY;
+    const int x0 = tx * kTX, y0 = ty * TY, z0 = tzc * a.tz;
+    const int z1 = min(z0 + a.tz, g.fD);
+    const int nsteps = (z1 - z0) + 4 * R;
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      soff[i] = -2;
+      if (sidx[i] >= 0) {
+        const int row = sidx[i] / E2S, col = sidx[i] - row * E2S;
+        const int x = x0 - 2 * R + col, y = y0 - 2 * R + row;
+        soff[i] = ((unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) ? y * g.fW + x : -1;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < W; ++q) {
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) {
+        grP[q][k] = make_float2(0.f, 0.f);
+        grX[q][k] = 0.f;
+      }
+    }
+    load_plane(z0 - 2 * R);
+
+    for (int s0 = 0; s0 < nsteps; s0 += W) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const int s = s0 + j;
+        if (s < nsteps) {
+          const int zi = z0 - 2 * R + s;
+          const bool pass1 = s >= 2 * R;
+          const bool pass2 = s >= 4 * R;
+          // the fetched plane becomes the newest history slot j; fetch the next
+#pragma unroll
+          for (int i = 0; i < NSTG; ++i) hist[j][i] = nxt[i];
+          if (s + 1 < nsteps) load_plane(zi + 1);
+          if (pass1) {
+            // [B] z sums over the register history -> zbuf
+#pragma unroll
+            for (int i = 0; i < NSTG; ++i) {
+              if (sidx[i] >= 0) {
+                float2 sP = hist[0][i];
+                float2 sQ = mul2(hist[0][i], hist[0][i]);
+                float sX = hist[0][i].x * hist[0][i].y;
+#pragma unroll
+                for (int q = 1; q < W; ++q) {
+                  sP = add2(sP, hist[q][i]);
+                  sQ = fma2(hist[q][i], hist[q][i], sQ);
+                  sX = fmaf(hist[q][i].x, hist[q][i].y, sX);
+                }
+                zP[sidx[i]] = sP;
+                zQ[sidx[i]] = sQ;
+                zX[sidx[i]] = sX;
+              }
+            }
+          }
+          __syncthreads();
+          if (pass1) {
+            // [C] x sums, 2 outputs per item: neighbouring lanes read
+            // neighbouring 16-byte vectors (no bank conflicts)
+            constexpr int XG = E1S / 2;
+            constexpr int NI = 2 + 2 * R;  // inputs of a 2-output run
+            for (int it = tid; it < L::E2H * XG; it += kThreads) {
+              const int row = it / XG, g2 = it - row * XG;
+              float2 vP[NI], vQ[NI];
+              float vX[NI];
+              const float4* sP4 = reinterpret_cast<const float4*>(zP + row * E2S + 2 * g2);
+              const float4* sQ4 = reinterpret_cast<const float4*>(zQ + row * E2S + 2 * g2);
+              const float2* sX2 = reinterpret_cast<const float2*>(zX + row * E2S + 2 * g2);
+#pragma unroll
+              for (int k = 0; k < NI / 2; ++k) {
+                const float4 p = sP4[k], q = sQ4[k];
+                const float2 x = sX2[k];
+                vP[2 * k] = make_float2(p.x, p.y);
+                vP[2 * k + 1] = make_float2(p.z, p.w);
+                vQ[2 * k] = make_float2(q.x, q.y);
+                vQ[2 * k + 1] = make_float2(q.z, q.w);
+                vX[2 * k] = x.x;
+                vX[2 * k + 1] = x.y;
+              }
+              float2 aP = vP[0], aQ = vQ[0];
+              float aX = vX[0];
+#pragma unroll
+              for (int k = 1; k <= 2 * R; ++k) {
+                aP = add2(aP, vP[k]);
+                aQ = add2(aQ, vQ[k]);
+                aX += vX[k];
+              }
+              const float2 bP = sub2(add2(aP, vP[2 * R + 1]), vP[0]);
+              const float2 bQ = sub2(add2(aQ, vQ[2 * R + 1]), vQ[0]);
+              const float bX = (aX + vX[2 * R + 1]) - vX[0];
+              *reinterpret_cast<float4*>(xP + row * E1S + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
+              *reinterpret_cast<float4*>(xQ + row * E1S + 2 * g2) = make_float4(aQ.x, aQ.y, bQ.x, bQ.y);
+              *reinterpret_cast<float2*>(xX + row * E1S + 2 * g2) = make_float2(aX, bX);
+            }
+          }
+          __syncthreads();
+          if (pass1) {
+            // [D] y sums -> window sums at plane zc on the R-halo region; cc and g-terms
+            constexpr int YR = (E1H + 3) / 4;
+            const int zc = zi - R;
+            const bool zin = zc >= 0 && zc < g.fD;
+            const bool zown = zc >= z0 && zc < z1;
+            for (int it = tid; it < E1W * YR; it += kThreads) {
+              const int x1 = it % E1W, r4 = it / E1W;
+              const int ys = 4 * r4;
+              float2 vP[4 + 2 * R], vQ[4 + 2 * R];
+              float vX[4 + 2 * R];
+#pragma unroll
+              for (int k = 0; k < 4 + 2 * R; ++k) {
+                const int row = ys + k;
+                if (row < L::E2H) {
+                  vP[k] = xP[row * E1S + x1];
+                  vQ[k] = xQ[row * E1S + x1];
+                  vX[k] = xX[row * E1S + x1];
+                } else {
+                  vP[k] = vQ[k] = make_float2(0.f, 0.f);
+                  vX[k] = 0.f;
+                }
+              }
+              float2 aP = vP[0], aQ = vQ[0];
+              float aX = vX[0];
+#pragma unroll
+              for (int k = 1; k <= 2 * R; ++k) {
+                aP = add2(aP, vP[k]);
+                aQ = add2(aQ, vQ[k]);
+                aX += vX[k];
+              }
+              const int x = x0 - R + x1;
+              const bool xin = (unsigned)x < (unsigned)g.fW;
+              const bool xown = x1 >= R && x1 < R + kTX;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if (k > 0) {
+                  aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
+                  aQ = sub2(add2(aQ, vQ[2 * R + k]), vQ[k - 1]);
+                  aX = (aX + vX[2 * R + k]) - vX[k - 1];
+                }
+                const int y1 = ys + k;
+                if (y1 < E1H) {
+                  const int y = y0 - R + y1;
+                  float2 gpair = make_float2(0.f, 0.f);
+                  float gfj = 0.f;
+                  if (zin && xin && (unsigned)y < (unsigned)g.fH) {
+                    // aP = (S_J, S_F), aQ = (S_JJ, S_FF), aX = S_FJ; variances clamped at 0
+                    float2 v = fma2(mul2(aP, aP), ninv2, aQ);
+                    v = make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f));
+                    const float cross = fmaf(-aP.x * aP.y, inv_n, aX);
+                    const float D = fmaf(v.x, v.y, eps);
+                    const float rD = rcp_approx(D);
+                    const float A1 = 2.0f * cross * rD;
+                    const float cc = cross * cross * rD;
+                    const float A2 = cc * v.y * rD;
+                    gfj = gs * A1;
+                    gpair.y = -gs * A2;
+                    gpair.x = gs * (2.0f * A2 * aP.x - A1 * aP.y) * inv_n;
+                    if (zown && xown && y1 >= R && y1 < R + TY) cc_acc += cc;
+                  }
+                  gP[y1 * E1S + x1] = gpair;
+                  gX[y1 * E1S + x1] = gfj;
+                }
+              }
+            }
+          }
+          __syncthreads();
+          if (pass1) {
+            // [E] x sums of the g-terms onto the 32 output columns, 2 per item
+            constexpr int XG2 = kTX / 2;
+            constexpr int NI = 2 + 2 * R;
+            for (int it = tid; it < E1H * XG2; it += kThreads) {
+              const int row = it / XG2, g2 = it - row * XG2;
+              float2 vP[NI];
+              float vX[NI];
+              const float4* sP4 = reinterpret_cast<const float4*>(gP + row * E1S + 2 * g2);
+              const float2* sX2 = reinterpret_cast<const float2*>(gX + row * E1S + 2 * g2);
+#pragma unroll
+              for (int k = 0; k < NI / 2; ++k) {
+                const float4 p = sP4[k];
+                const float2 x = sX2[k];
+                vP[2 * k] = make_float2(p.x, p.y);
+                vP[2 * k + 1] = make_float2(p.z, p.w);
+                vX[2 * k] = x.x;
+                vX[2 * k + 1] = x.y;
+              }
+              float2 aP = vP[0];
+              float aX = vX[0];
+#pragma unroll
+              for (int k = 1; k <= 2 * R; ++k) {
+                aP = add2(aP, vP[k]);
+                aX += vX[k];
+              }
+              const float2 bP = sub2(add2(aP, vP[2 * R + 1]), vP[0]);
+              const float bX = (aX + vX[2 * R + 1]) - vX[0];
+              *reinterpret_cast<float4*>(gxP + row * kTX + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
+              *reinterpret_cast<float2*>(gxX + row * kTX + 2 * g2) = make_float2(aX, bX);
+            }
+          }
+          __syncthreads();
+          // [F] y sums of the g-terms at the own outputs -> register ring slot j
+          if (pass1) {
+            float2 vP[NOUT + 2 * R];
+            float vX[NOUT + 2 * R];
+#pragma unroll
+            for (int k = 0; k < NOUT + 2 * R; ++k) {
+              vP[k] = gxP[(oy0 + k) * kTX + ox];
+              vX[k] = gxX[(oy0 + k) * kTX + ox];
+            }
+            float2 aP = vP[0];
+            float aX = vX[0];
+#pragma unroll
+            for (int k = 1; k <= 2 * R; ++k) {
+              aP = add2(aP, vP[k]);
+              aX += vX[k];
+            }
+#pragma unroll
+            for (int k = 0; k < NOUT; ++k) {
+              if (k > 0) {
+                aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
+                aX = (aX + vX[2 * R + k]) - vX[k - 1];
+              }
+              grP[j][k] = aP;
+              grX[j][k] = aX;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < NOUT; ++k) {
+              grP[j][k] = make_float2(0.f, 0.f);
+              grX[j][k] = 0.f;
+            }
+          }
+          // [G] z sums over the register ring -> dJ at plane zo = zi - 2R
+          if (pass2) {
+            const int zo = zi - 2 * R;
+            const int OLD = (j + 1) % W;  // history slot of plane zo
+#pragma unroll
+            for (int k = 0; k < NOUT; ++k) {
+              float2 bP = grP[0][k];
+              float bX = grX[0][k];
+#pragma unroll
+              for (int q = 1; q < W; ++q) {
+                bP = add2(bP, grP[q][k]);
+                bX += grX[q][k];
+              }
+              const float jv = hist[OLD][k].x, fv = hist[OLD][k].y;
+              const int X = x0 + ox, Y = y0 + oy0 + k;
+              if (X < g.fW && Y < g.fH) {
+                float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
+                if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
+                if (a.dJ) a.dJ[((size_t)zo * g.fH + Y) * g.fW + X] = gv;
+              }
+            }
+          }
+          // fold the fp32 cc partial into fp64 every 32 planes (uniform across the CTA)
+          if ((s & 31) == 31) {
+            const float v = warp_sum(cc_acc);
+            if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
+            cc_acc = 0.0f;
+          }
+        }
+      }
+    }
+  }
+  {
+    const float v = warp_sum(cc_acc);
+    if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
+  }
+  __syncthreads();
+  if (tid < kPartialStride) {
+    double s = 0.0;
+    if (tid == kPCC)
+      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][kPCC];
+    a.partials[(size_t)blockIdx.x * kPartialStride + tid] = s;
+  }
+}
+
+template <int R>
+static size_t smem_of() {
+  if constexpr (R <= 3)
+    return (size_t)LTR<R>::TOTAL * sizeof(float);
+  else
+    return (size_t)LT<R>::TOTAL * sizeof(float);
+}
+
 // occ != nullptr: report resident CTAs per SM instead of launching.
 template <typename FT, int BMAX, int R>
 static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
-  auto k = k_lncc<FT, BMAX, R>;
+  // radius <= 3: register-history kernel; radius 4: shared-memory plane ring
+  auto k = [] {
+    if constexpr (R <= 3)
+      return k_lncc_rh<FT, BMAX, R>;
+    else
+      return k_lncc<FT, BMAX, R>;
+  }();
   const size_t smem = smem_of<R>();
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
