@@ -35,9 +35,14 @@ UNIT = "Gvoxels/s"
 # Algorithmic bytes per voxel (inputs read once per sweep, du written once):
 # MI needs two sweeps because the histogram is a global dependency.
 ALGO_BYTES = {4: 2 * (4 + 12 + 4) + 12, 5: 2 * (2 + 12 + 2) + 12}
-# Dominant kernel's algorithmic bytes per voxel (the gradient sweep reads
-# F, u and M and writes du).
-SWEEP2_BYTES = {4: 4 + 12 + 4 + 12, 5: 2 + 12 + 2 + 12}
+# Single-pass lower bound: F, M and u read once, du written once.
+SINGLE_PASS_BYTES = {4: 4 + 4 + 12 + 12, 5: 2 + 2 + 12 + 12}
+# Algorithmic bytes per voxel of each kernel of the objective:
+#   k_sweep1  F + u + M read (+ J written when LNCC is on)
+#   k_lncc    F + J read, dL/dJ written
+#   k_sweep2  u + M + (F for MI | dL/dJ for LNCC) read, du written
+KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4, "k_lncc": 4 + 4 + 4, "k_sweep2": 4 + 12 + 4 + 12},
+                5: {"k_sweep1": 2 + 12 + 2, "k_sweep2": 2 + 12 + 2 + 12}}
 HBM_NOMINAL_GBS = 8000.0
 
 
@@ -199,6 +204,9 @@ def run_reference(args, ws, rank, local):
 
 
 def _traffic_per_launch(kernel, workload, N):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    record (bytes per voxel x N), or None when the kernel's sources changed
+    since the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -206,16 +214,17 @@ def _traffic_per_launch(kernel, workload, N):
         import hashlib
         with open(p) as f:
             d = json.load(f)
-        rec = d.get(kernel)
-        if not rec or rec.get("workload") != workload:
-            return None
-        src = "".join(open(os.path.join(ROOT, "voxel_grid_sampler_gb300", "csrc", s)).read()
-                      for s in sorted(rec["sources"]))
-        if hashlib.sha256(src.encode()).hexdigest()[:16] != rec["source_sha"]:
-            return None
-        return rec["bytes_per_voxel"] * N
+        for rec in d.get("records", []):
+            if rec.get("kernel") != kernel or rec.get("workload") != workload:
+                continue
+            src = "".join(open(os.path.join(ROOT, "voxel_grid_sampler_gb300", "csrc", s)).read()
+                          for s in sorted(rec["sources"]))
+            if hashlib.sha256(src.encode()).hexdigest()[:16] != rec["source_sha"]:
+                return None
+            return rec["bytes_per_voxel"] * N
     except Exception:
         return None
+    return None
 
 
 def run_gpu(args, ws, rank, local):
@@ -325,12 +334,16 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
     dom_name, (dom_n, dom_ms) = dom
     dom_avg = dom_ms / max(dom_n, 1)
     per_launch_voxels = N
-    algo = {"k_lncc": SWEEP2_BYTES, "k_sweep2": SWEEP2_BYTES}.get(dom_name, {4: 20, 5: 16})
-    achieved = algo[args.workload] * per_launch_voxels / (dom_avg * 1e-3) / 1e9
+    bpv = KERNEL_BYTES[args.workload].get(dom_name, 0)
+    achieved = bpv * per_launch_voxels / (dom_avg * 1e-3) / 1e9
     traffic = _traffic_per_launch(dom_name, wl.name, N)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,
-                "algorithmic_bytes_per_voxel": algo[args.workload], "peak_source": peak_kind}
+                "algorithmic_bytes_per_voxel": bpv, "peak_source": peak_kind,
+                "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": KERNEL_BYTES[args.workload].get(k, 0),
+                                "frac": KERNEL_BYTES[args.workload].get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3)
+                                        / 1e9 / peak}
+                            for k, v in kern.items() if k in KERNEL_BYTES[args.workload]}}
     step_gbs = ALGO_BYTES[args.workload] * N / (ms * 1e-3) / 1e9
     if rank != 0:
         return
@@ -346,7 +359,10 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
         "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs,
                              "of_8tbs": step_gbs / HBM_NOMINAL_GBS,
                              "of_measured": step_gbs / peak,
-                             "bytes_per_voxel": ALGO_BYTES[args.workload]},
+                             "bytes_per_voxel": ALGO_BYTES[args.workload],
+                             "single_pass_bytes_per_voxel": SINGLE_PASS_BYTES[args.workload],
+                             "single_pass_of_8tbs": SINGLE_PASS_BYTES[args.workload] * N / (ms * 1e-3) / 1e9
+                                                    / HBM_NOMINAL_GBS},
         "roofline": roofline,
         "kernels_ms_per_launch": {k: v[1] / max(v[0], 1) for k, v in kern.items()},
         "gpu_launches": int(launches),

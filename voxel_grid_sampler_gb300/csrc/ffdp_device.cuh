@@ -213,9 +213,35 @@ __device__ __forceinline__ float ldg_f<__half>(const __half* p) {
   return __half2float(__ldg(p));
 }
 
-// The 8 taps of cell b (m[z][y][x] order: 000,001,010,011,100,101,110,111),
-// zero outside M.  Split from the interpolation so callers can issue the
-// loads of several voxels before using any of them.
+// Raw tap registers: a float register holds either an fp32 tap or the 16
+// bits of an fp16 tap.  Half taps are converted only when they are
+// interpolated, so no conversion sits between the loads of a cell and the
+// eight loads stay in flight together.
+template <typename T>
+__device__ __forceinline__ float ldg_raw(const T* p);
+template <>
+__device__ __forceinline__ float ldg_raw<float>(const float* p) {
+  return __ldg(p);
+}
+template <>
+__device__ __forceinline__ float ldg_raw<__half>(const __half* p) {
+  return __uint_as_float((unsigned)__ldg(reinterpret_cast<const unsigned short*>(p)));
+}
+template <typename T>
+__device__ __forceinline__ float tap_value(float raw);
+template <>
+__device__ __forceinline__ float tap_value<float>(float raw) {
+  return raw;
+}
+template <>
+__device__ __forceinline__ float tap_value<__half>(float raw) {
+  return __half2float(__ushort_as_half((unsigned short)__float_as_uint(raw)));
+}
+
+// The 8 raw taps of cell b (m[z][y][x] order: 000,001,010,011,100,101,110,111),
+// zero outside M (the zero bit pattern is +0 in both types).  Split from the
+// interpolation so callers can issue the loads of several voxels before
+// using any of them.
 template <typename MT>
 __device__ __forceinline__ void gather8(const MT* __restrict__ M, const Geom& g, const int b[3], float m[8]) {
   const int bx = b[0], by = b[1], bz = b[2];
@@ -226,20 +252,20 @@ __device__ __forceinline__ void gather8(const MT* __restrict__ M, const Geom& g,
     const MT* q = M + (off + (unsigned)g.mW);
     const MT* p2 = M + (off + (unsigned)g.mHW);
     const MT* q2 = M + (off + (unsigned)g.mHW + (unsigned)g.mW);
-    m[0] = ldg_f(p);
-    m[1] = ldg_f(p + 1);
-    m[2] = ldg_f(q);
-    m[3] = ldg_f(q + 1);
-    m[4] = ldg_f(p2);
-    m[5] = ldg_f(p2 + 1);
-    m[6] = ldg_f(q2);
-    m[7] = ldg_f(q2 + 1);
+    m[0] = ldg_raw(p);
+    m[1] = ldg_raw(p + 1);
+    m[2] = ldg_raw(q);
+    m[3] = ldg_raw(q + 1);
+    m[4] = ldg_raw(p2);
+    m[5] = ldg_raw(p2 + 1);
+    m[6] = ldg_raw(q2);
+    m[7] = ldg_raw(q2 + 1);
   } else {
     const bool x0 = (unsigned)bx < (unsigned)g.mW, x1 = (unsigned)(bx + 1) < (unsigned)g.mW;
     const bool y0 = (unsigned)by < (unsigned)g.mH, y1 = (unsigned)(by + 1) < (unsigned)g.mH;
     const bool z0 = (unsigned)bz < (unsigned)g.mD, z1 = (unsigned)(bz + 1) < (unsigned)g.mD;
     auto at = [&](int dz, int dy, int dx, bool ok) -> float {
-      return ok ? ldg_f(M + ((long long)(bz + dz) * g.mH + (by + dy)) * g.mW + (bx + dx)) : 0.0f;
+      return ok ? ldg_raw(M + ((long long)(bz + dz) * g.mH + (by + dy)) * g.mW + (bx + dx)) : 0.0f;
     };
     m[0] = at(0, 0, 0, z0 && y0 && x0);
     m[1] = at(0, 0, 1, z0 && y0 && x1);
@@ -263,62 +289,6 @@ __device__ __forceinline__ float interp8(const float m[8], const float r[3], flo
   const float2 ca = fma2(rx2, dxa, a0), cb = fma2(rx2, dxb, b0);
   const float2 dy = sub2(cb, ca);
   const float2 c = fma2(ry2, dy, ca);
-  const float dz = c.y - c.x;
-  if (GRAD) {
-    gz = dz;
-    gy = fmaf(rz, dy.y - dy.x, dy.x);
-    const float2 e = fma2(ry2, sub2(dxb, dxa), dxa);
-    gx = fmaf(rz, e.y - e.x, e.x);
-  }
-  return fmaf(rz, dz, c.x);
-}
-
-// Trilinear sample of M at cell (b, r) with zero padding per tap; optionally
-// the slope dJ/dq from the same 8 taps (cell [b, b+1] on every axis).
-template <typename MT, bool GRAD>
-__device__ __forceinline__ float trilinear(const MT* __restrict__ M, const Geom& g, const int b[3],
-                                           const float r[3], float& gx, float& gy, float& gz) {
-  float m000, m001, m010, m011, m100, m101, m110, m111;  // m[z][y][x]
-  const int bx = b[0], by = b[1], bz = b[2];
-  if ((unsigned)bx < (unsigned)(g.mW - 1) && (unsigned)by < (unsigned)(g.mH - 1) &&
-      (unsigned)bz < (unsigned)(g.mD - 1)) {
-    const MT* p = M + ((long long)bz * g.mH + by) * g.mW + bx;
-    const MT* q = p + g.mW;
-    m000 = ldg_f(p);
-    m001 = ldg_f(p + 1);
-    m010 = ldg_f(q);
-    m011 = ldg_f(q + 1);
-    p += g.mHW;
-    q += g.mHW;
-    m100 = ldg_f(p);
-    m101 = ldg_f(p + 1);
-    m110 = ldg_f(q);
-    m111 = ldg_f(q + 1);
-  } else {
-    const bool x0 = (unsigned)bx < (unsigned)g.mW, x1 = (unsigned)(bx + 1) < (unsigned)g.mW;
-    const bool y0 = (unsigned)by < (unsigned)g.mH, y1 = (unsigned)(by + 1) < (unsigned)g.mH;
-    const bool z0 = (unsigned)bz < (unsigned)g.mD, z1 = (unsigned)(bz + 1) < (unsigned)g.mD;
-    auto at = [&](int dz, int dy, int dx, bool ok) -> float {
-      return ok ? ldg_f(M + ((long long)(bz + dz) * g.mH + (by + dy)) * g.mW + (bx + dx)) : 0.0f;
-    };
-    m000 = at(0, 0, 0, z0 && y0 && x0);
-    m001 = at(0, 0, 1, z0 && y0 && x1);
-    m010 = at(0, 1, 0, z0 && y1 && x0);
-    m011 = at(0, 1, 1, z0 && y1 && x1);
-    m100 = at(1, 0, 0, z1 && y0 && x0);
-    m101 = at(1, 0, 1, z1 && y0 && x1);
-    m110 = at(1, 1, 0, z1 && y1 && x0);
-    m111 = at(1, 1, 1, z1 && y1 && x1);
-  }
-  // the two z planes of the cell run as packed pairs (z0, z1)
-  const float rz = r[2];
-  const float2 rx2 = make_float2(r[0], r[0]), ry2 = make_float2(r[1], r[1]);
-  const float2 a0 = make_float2(m000, m100), a1 = make_float2(m001, m101);
-  const float2 b0 = make_float2(m010, m110), b1 = make_float2(m011, m111);
-  const float2 dxa = sub2(a1, a0), dxb = sub2(b1, b0);           // x differences at y0, y1
-  const float2 ca = fma2(rx2, dxa, a0), cb = fma2(rx2, dxb, b0);  // x-lerped at y0, y1
-  const float2 dy = sub2(cb, ca);
-  const float2 c = fma2(ry2, dy, ca);                             // (c0, c1)
   const float dz = c.y - c.x;
   if (GRAD) {
     gz = dz;

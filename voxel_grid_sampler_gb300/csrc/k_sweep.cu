@@ -539,14 +539,16 @@ struct S1Cfg {
   static constexpr size_t kSmem = kHistBytes + RG::kBytes;
 };
 
-template <int BMAX, bool HIST, bool WRITEJ>
+template <typename MT, int BMAX, bool HIST, bool WRITEJ>
 __device__ __forceinline__ void sweep1_half(const Half& H, unsigned* hist, const HistLane& hl, const Sweep1Args& a,
                                             bool sample) {
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     if (j < H.nv) {
-      float d0, d1, d2;
-      const float jv = sample ? interp8<false>(H.taps[j], H.rr[j], d0, d1, d2) : H.x[j];
+      float d0, d1, d2, m[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
+      const float jv = sample ? interp8<false>(m, H.rr[j], d0, d1, d2) : H.x[j];
       if (HIST) hist_add<BMAX>(hist, hl, a.bf, a.bj, H.f[j], jv);
       if (WRITEJ) a.Jout[H.lin + 32u * j] = jv;
     }
@@ -587,9 +589,9 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a)
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
     prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
-    sweep1_half<BMAX, HIST, WRITEJ>(A, hist_sm, hl, a, SAMPLE);
+    sweep1_half<MT, BMAX, HIST, WRITEJ>(A, hist_sm, hl, a, SAMPLE);
     prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
-    sweep1_half<BMAX, HIST, WRITEJ>(B, hist_sm, hl, a, SAMPLE);
+    sweep1_half<MT, BMAX, HIST, WRITEJ>(B, hist_sm, hl, a, SAMPLE);
     if (HIST && ++pending == flush_every<BMAX>()) {
       hist_flush<BMAX>(hist_sm, a.ghist, a.B);
       pending = 0;
@@ -703,7 +705,7 @@ struct S2Cfg {
   static constexpr size_t kSmem = kTableBytes + RG::kBytes;
 };
 
-template <int BMAX, bool MI, bool SAMPLE>
+template <typename MT, int BMAX, bool MI, bool SAMPLE>
 __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, const Sweep2Args& a, float acc[12]) {
   const Geom& g = a.g;
 #pragma unroll
@@ -714,8 +716,10 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
       a.dJ[lin] = mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], H.x[j]);
       continue;
     }
-    float gq0, gq1, gq2;
-    const float jv = interp8<true>(H.taps[j], H.rr[j], gq0, gq1, gq2);
+    float gq0, gq1, gq2, m[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
+    const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
     const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
     const float e0 = gv * gq0, e1 = gv * gq1, e2 = gv * gq2;
     if (a.du) {
@@ -791,9 +795,9 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a)
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
     prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
-    sweep2_half<BMAX, MI, SAMPLE>(A, tsm, a, acc);
+    sweep2_half<MT, BMAX, MI, SAMPLE>(A, tsm, a, acc);
     prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
-    sweep2_half<BMAX, MI, SAMPLE>(B, tsm, a, acc);
+    sweep2_half<MT, BMAX, MI, SAMPLE>(B, tsm, a, acc);
     if (BWD && ++pending == kFoldEvery) {
 #pragma unroll
       for (int q = 0; q < 12; ++q) {
