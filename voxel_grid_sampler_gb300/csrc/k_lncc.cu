@@ -739,45 +739,48 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
           }
           __syncthreads();
           if (pass1) {
-            // [D] y sums -> window sums at plane zc on the R-halo region; cc and g-terms
-            constexpr int YR = (E1H + 3) / 4;
+            // [D] y sums -> window sums at plane zc on the R-halo region; cc and
+            // g-terms.  Runs of 3 rows per item (one round of items for the
+            // CTA); rows are read as the window slides, keeping only the two
+            // rows that leave it.
+            constexpr int RUN = 3;
+            constexpr int YR = (E1H + RUN - 1) / RUN;
             const int zc = zi - R;
             const bool zin = zc >= 0 && zc < g.fD;
             const bool zown = zc >= z0 && zc < z1;
             for (int it = tid; it < E1W * YR; it += kThreads) {
-              const int x1 = it % E1W, r4 = it / E1W;
-              const int ys = 4 * r4;
-              float2 vP[4 + 2 * R], vQ[4 + 2 * R];
-              float vX[4 + 2 * R];
+              const int x1 = it % E1W, ys = RUN * (it / E1W);
+              auto rowP = [&](int row) { return row < L::E2H ? xP[row * E1S + x1] : make_float2(0.f, 0.f); };
+              auto rowQ = [&](int row) { return row < L::E2H ? xQ[row * E1S + x1] : make_float2(0.f, 0.f); };
+              auto rowX = [&](int row) { return row < L::E2H ? xX[row * E1S + x1] : 0.f; };
+              float2 oP[RUN - 1], oQ[RUN - 1];
+              float oX[RUN - 1];
 #pragma unroll
-              for (int k = 0; k < 4 + 2 * R; ++k) {
-                const int row = ys + k;
-                if (row < L::E2H) {
-                  vP[k] = xP[row * E1S + x1];
-                  vQ[k] = xQ[row * E1S + x1];
-                  vX[k] = xX[row * E1S + x1];
-                } else {
-                  vP[k] = vQ[k] = make_float2(0.f, 0.f);
-                  vX[k] = 0.f;
-                }
+              for (int k = 0; k < RUN - 1; ++k) {
+                oP[k] = rowP(ys + k);
+                oQ[k] = rowQ(ys + k);
+                oX[k] = rowX(ys + k);
               }
-              float2 aP = vP[0], aQ = vQ[0];
-              float aX = vX[0];
+              float2 aP = oP[0], aQ = oQ[0];
+              float aX = oX[0];
 #pragma unroll
               for (int k = 1; k <= 2 * R; ++k) {
-                aP = add2(aP, vP[k]);
-                aQ = add2(aQ, vQ[k]);
-                aX += vX[k];
+                const float2 p = k < RUN - 1 ? oP[k] : rowP(ys + k);
+                const float2 q = k < RUN - 1 ? oQ[k] : rowQ(ys + k);
+                const float x = k < RUN - 1 ? oX[k] : rowX(ys + k);
+                aP = add2(aP, p);
+                aQ = add2(aQ, q);
+                aX += x;
               }
               const int x = x0 - R + x1;
               const bool xin = (unsigned)x < (unsigned)g.fW;
               const bool xown = x1 >= R && x1 < R + kTX;
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int k = 0; k < RUN; ++k) {
                 if (k > 0) {
-                  aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
-                  aQ = sub2(add2(aQ, vQ[2 * R + k]), vQ[k - 1]);
-                  aX = (aX + vX[2 * R + k]) - vX[k - 1];
+                  aP = sub2(add2(aP, rowP(ys + 2 * R + k)), oP[k - 1]);
+                  aQ = sub2(add2(aQ, rowQ(ys + 2 * R + k)), oQ[k - 1]);
+                  aX = (aX + rowX(ys + 2 * R + k)) - oX[k - 1];
                 }
                 const int y1 = ys + k;
                 if (y1 < E1H) {
