@@ -217,7 +217,6 @@ ffdp_status make_geom(ffdp_dims f, ffdp_dims m, const ffdp_transform* T, Geom& g
     g.hM[r] = (float)hM[r];
     g.ctr[r] = (float)((nf[r] - 1.0) / 2.0);
   }
-  g.w4 = (f.w % 4) == 0 ? 1 : 0;
   g.a_diag = (g.Gq[1] == 0 && g.Gq[2] == 0 && g.Gq[3] == 0 && g.Gq[5] == 0 && g.Gq[6] == 0 && g.Gq[7] == 0) ? 1 : 0;
   g.k_diag = (T->S[1] == 0.f && T->S[2] == 0.f && T->S[3] == 0.f && T->S[5] == 0.f && T->S[6] == 0.f &&
               T->S[7] == 0.f)
@@ -243,7 +242,6 @@ void make_grid_only(ffdp_dims f, Geom& g) {
   g.fH = (int)f.h;
   g.fD = (int)f.d;
   g.N = (unsigned)nvox(f);
-  g.w4 = (f.w % 4) == 0 ? 1 : 0;
   fast_div_magic((uint32_t)f.w, g.divW_m, g.divW_s);
   fast_div_magic((uint32_t)(f.w * f.h), g.divHW_m, g.divHW_s);
 }

@@ -53,22 +53,7 @@ struct Geom {
   int divW_s, divHW_s;
   int k_diag;       // K is diagonal (S diagonal): u enters q component-wise
   int a_diag;       // G is diagonal (A diagonal)
-  int w4;           // fW % 4 == 0: a 4-voxel group never crosses a row
 };
-
-// Integer part k and fraction f in [0, 1) of the fixed-point anchor of voxel
-// (ix, iy, iz); |k| < 2^25 is guaranteed by the host-side range check.
-__device__ __forceinline__ void anchor_kf(const Geom& g, int ix, int iy, int iz, int k[3], float f[3]) {
-  const int idx[3] = {ix, iy, iz};
-#pragma unroll
-  for (int r = 0; r < 3; ++r) {
-    // a diagonal affine part (the common case) needs one product per axis
-    const long long P = g.a_diag ? g.g0q[r] + g.Gq[r * 4] * idx[r]
-                                 : g.g0q[r] + g.Gq[r * 3 + 0] * ix + g.Gq[r * 3 + 1] * iy + g.Gq[r * 3 + 2] * iz;
-    k[r] = (int)(P >> 32);
-    f[r] = __uint_as_float(0x3f800000u | ((unsigned)(P & 0xffffffffll) >> 9)) - 1.0f;
-  }
-}
 
 // Unsigned division by a runtime-invariant divisor (round-up method).
 __device__ __forceinline__ unsigned fast_div(unsigned n, unsigned m, int s) {
@@ -119,11 +104,12 @@ __device__ __forceinline__ void floor_split(float t, int& fi, float& fr) {
 #endif
 }
 
-// Cell of the moving image containing q = P + K u: integer corner b (clamped
-// to [-2, n] so that far-away points keep every tap outside) and fractions r.
+// Cell of the moving image containing q = P + K u: integer corner b and
+// fractions r.  The in-cell coordinate is clamped to +-2^20, so |b| < 2^26
+// (|k| < 2^25 by the host-side range check) and every consumer's unsigned
+// range test rejects far-away corners without overflow.
 __device__ __forceinline__ void cell_of(const Geom& g, const long long P[3], float u0, float u1,
                                         float u2, int b[3], float r[3]) {
-  const int nm[3] = {g.mW, g.mH, g.mD};
 #pragma unroll
   for (int c = 0; c < 3; ++c) {
     const int k = (int)(P[c] >> 32);
@@ -139,30 +125,7 @@ __device__ __forceinline__ void cell_of(const Geom& g, const long long P[3], flo
     int fi;
     float fr;
     floor_split(t, fi, fr);
-    b[c] = min(max(k + fi, -2), nm[c]);
-    r[c] = fr;
-  }
-}
-
-// Cell of voxel v (0..3) of a 4-voxel group in one row: q = k + f + v Gx + K u.
-// The small part f + v Gx + K u stays below ~2^21 in magnitude, so float
-// rounding there is ~1e-7 voxel while k carries the large part exactly.
-__device__ __forceinline__ void cell_v(const Geom& g, const int k[3], const float f[3], float v, float u0,
-                                       float u1, float u2, int b[3], float r[3]) {
-  const int nm[3] = {g.mW, g.mH, g.mD};
-#pragma unroll
-  for (int c = 0; c < 3; ++c) {
-    float t = fmaf(v, g.Gx[c], f[c]);
-    if (g.k_diag) {
-      t = fmaf(g.K[c * 4], c == 0 ? u0 : (c == 1 ? u1 : u2), t);
-    } else {
-      t = fmaf(g.K[c * 3 + 0], u0, fmaf(g.K[c * 3 + 1], u1, fmaf(g.K[c * 3 + 2], u2, t)));
-    }
-    t = fminf(fmaxf(t, -1048576.0f), 1048576.0f);
-    int fi;
-    float fr;
-    floor_split(t, fi, fr);
-    b[c] = min(max(k[c] + fi, -2), nm[c]);
+    b[c] = k + fi;
     r[c] = fr;
   }
 }
@@ -202,17 +165,6 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
 }
 
 // ------------------------------------------------------------- M access
-template <typename T>
-__device__ __forceinline__ float ldg_f(const T* p);
-template <>
-__device__ __forceinline__ float ldg_f<float>(const float* p) {
-  return __ldg(p);
-}
-template <>
-__device__ __forceinline__ float ldg_f<__half>(const __half* p) {
-  return __half2float(__ldg(p));
-}
-
 // Raw tap registers: a float register holds either an fp32 tap or the 16
 // bits of an fp16 tap.  Half taps are converted only when they are
 // interpolated, so no conversion sits between the loads of a cell and the
@@ -341,23 +293,7 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Loads of 4 consecutive fixed-image values as float.
-__device__ __forceinline__ void load4(const float* __restrict__ p, float v[4]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  v[0] = a.x;
-  v[1] = a.y;
-  v[2] = a.z;
-  v[3] = a.w;
-}
-__device__ __forceinline__ void load4(const __half* __restrict__ p, float v[4]) {
-  const uint2 a = __ldg(reinterpret_cast<const uint2*>(p));
-  const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&a.x));
-  const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&a.y));
-  v[0] = lo.x;
-  v[1] = lo.y;
-  v[2] = hi.x;
-  v[3] = hi.y;
-}
+// One fixed-image value as float.
 __device__ __forceinline__ float load1(const float* __restrict__ p) { return __ldg(p); }
 __device__ __forceinline__ float load1(const __half* __restrict__ p) { return __half2float(__ldg(p)); }
 
