@@ -533,11 +533,21 @@ struct LTR {
   static constexpr int NEXTRA = (NHALO + kThreads - 1) / kThreads;
   static constexpr int NSTG = NOUT + NEXTRA;
   static_assert(NOUT * kThreads == NCORE, "outputs per thread");
+  // Row stride of the z-sum buffer: the x pass reads 2-output items (16 bytes
+  // of (S_J, S_F) pairs, 8 bytes of S_FJ per lane), E1S/2 items per row; the
+  // stride makes a row continue the bank sequence of the previous one, so
+  // lanes that cross a row boundary inside a warp do not collide.
+  static constexpr int XG = L::E1S / 2;
+  static constexpr int zs_of(int s) { return (s % 2 == 0 && ((s / 2 - XG) % 16 + 16) % 16 == 0) ? s : zs_of(s + 1); }
+  static constexpr int ZS = zs_of(L::E2W);
+  static constexpr int ZB = L::E2H * ZS * 5;
   // shared memory: zbuf (z sums, later the g-terms) and xbuf (x sums, later
   // the x-summed g-terms); no plane ring
   static constexpr int OFF_Z = 0;
-  static constexpr int OFF_X = L::ZB + L::PAD;
+  static constexpr int OFF_X = ZB + L::PAD;
   static constexpr int TOTAL = OFF_X + L::XB + L::PAD;
+  static_assert(L::E1H * L::E1S * 3 <= ZB, "g-term plane must fit in the z buffer");
+  static_assert(OFF_X % 4 == 0, "16-byte alignment");
 };
 
 // Halo position h (outside the output core) of a tile: the top and bottom 2R
@@ -565,7 +575,7 @@ template <typename FT, int BMAX, int R>
 __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
   using L = LT<R>;
   using Q = LTR<R>;
-  constexpr int W = L::W, TY = L::TY, E2S = L::E2S;
+  constexpr int W = L::W, TY = L::TY, E2S = Q::ZS;
   constexpr int E1W = L::E1W, E1H = L::E1H, E1S = L::E1S, NIN = L::NIN;
   constexpr int NOUT = Q::NOUT, NSTG = Q::NSTG;
   constexpr bool MI = BMAX != 0;
