@@ -322,8 +322,12 @@ int persistent_grid(unsigned nIter, int per_sm) {
   return (int)(g < 1 ? 1 : g);
 }
 
-unsigned n_iter(uint64_t N) {
-  return (unsigned)((N + (uint64_t)(kSweepThreads * kVPT) - 1) / (kSweepThreads * kVPT));
+// CTA iterations of the histogram / forward sweep and of the gradient sweep
+unsigned n_iter1(uint64_t N) {
+  return (unsigned)((N + (uint64_t)(kSweep1Threads * kVPT) - 1) / (kSweep1Threads * kVPT));
+}
+unsigned n_iter2(uint64_t N) {
+  return (unsigned)((N + (uint64_t)(kSweep2Threads * kVPT) - 1) / (kSweep2Threads * kVPT));
 }
 
 #define FFDP_TRY(x)                    \
@@ -399,7 +403,7 @@ extern "C" ffdp_status ffdp_grid_sample_fwd(const void* M, ffdp_dtype mt, ffdp_d
   a.M = M;
   a.u = u;
   a.Jout = J_out;
-  a.nIter = n_iter(a.g.N);
+  a.nIter = n_iter1(a.g.N);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = persistent_grid(a.nIter, sweep1_ctas_per_sm(S1_WRITEJ, 0, mt, 32));
   FFDP_CUDA(launch_sweep1(S1_WRITEJ, 0, mt, 32, a, grid, s), "grid_sample_fwd launch");
@@ -426,7 +430,7 @@ extern "C" ffdp_status ffdp_grid_sample_bwd(const void* M, ffdp_dtype mt, ffdp_d
   a.gbuf = gJ;
   a.du = du;
   a.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
-  a.nIter = n_iter(a.g.N);
+  a.nIter = n_iter2(a.g.N);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = persistent_grid(a.nIter, sweep2_ctas_per_sm(S2_GBUF, 0, mt, 32));
   FFDP_CUDA(launch_sweep2(S2_GBUF, 0, mt, 32, a, grid, s), "grid_sample_bwd launch");
@@ -476,7 +480,7 @@ extern "C" ffdp_status ffdp_mi_fwd_bwd(const void* F, ffdp_dtype ft, const float
   a1.bf = bin_map(p->f_lo, p->f_hi, p->bins);
   a1.bj = bin_map(p->m_lo, p->m_hi, p->bins);
   a1.B = p->bins;
-  a1.nIter = n_iter(g.N);
+  a1.nIter = n_iter1(g.N);
   FFDP_CUDA(launch_sweep1(S1_HIST_JBUF, ft, 0, bmax,
                           a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(S1_HIST_JBUF, ft, 0, bmax)), s),
             "MI histogram launch");
@@ -498,7 +502,7 @@ extern "C" ffdp_status ffdp_mi_fwd_bwd(const void* F, ffdp_dtype ft, const float
     a2.bf = a1.bf;
     a2.bj = a1.bj;
     a2.B = p->bins;
-    a2.nIter = a1.nIter;
+    a2.nIter = n_iter2(g.N);
     FFDP_CUDA(launch_sweep2(S2_MI_JBUF, ft, 0, bmax, a2,
                             persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MI_JBUF, ft, 0, bmax)), s),
               "MI gradient launch");
@@ -602,7 +606,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   a1.bf = bf;
   a1.bj = bj;
   a1.B = mi ? p->mi.bins : 32;
-  a1.nIter = n_iter(N);
+  a1.nIter = n_iter1(N);
   const int m1 = mi ? (ln ? S1_HIST_WRITEJ : S1_HIST) : S1_WRITEJ;
   FFDP_CUDA(launch_sweep1(m1, ft, mt, bmax, a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(m1, ft, mt, bmax)), s),
             "sweep 1 launch");
@@ -647,7 +651,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a2.gbuf = Gbuf;
     a2.du = du;
     a2.partials = partials + (size_t)grid * kPartialStride;
-    a2.nIter = n_iter(N);
+    a2.nIter = n_iter2(N);
     const int grid2 = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_GBUF, 0, mt, 32));
     FFDP_CUDA(launch_sweep2(S2_GBUF, 0, mt, 32, a2, grid2, s), "sampler backward launch");
     nparts = grid + grid2;
@@ -663,7 +667,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a2.bf = bf;
     a2.bj = bj;
     a2.B = p->mi.bins;
-    a2.nIter = n_iter(N);
+    a2.nIter = n_iter2(N);
     const int grid = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MI, ft, mt, bmax));
     FFDP_CUDA(launch_sweep2(S2_MI, ft, mt, bmax, a2, grid, s), "sweep 2 launch");
     nparts = grid;

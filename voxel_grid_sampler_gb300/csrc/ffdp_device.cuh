@@ -14,10 +14,16 @@ namespace ffdp {
 
 // ---------------------------------------------------------------- constants
 constexpr int kThreads = 256;           // threads per CTA of the LNCC kernel
-#ifndef FFDP_SWEEP_THREADS
-#define FFDP_SWEEP_THREADS 512
+#ifndef FFDP_SWEEP1_THREADS
+#define FFDP_SWEEP1_THREADS 640
 #endif
-constexpr int kSweepThreads = FFDP_SWEEP_THREADS;  // threads per CTA of the voxel sweeps (one CTA per SM)
+#ifndef FFDP_SWEEP2_THREADS
+#define FFDP_SWEEP2_THREADS 512
+#endif
+// threads per CTA of the histogram / forward sweep and of the gradient sweep
+// (one CTA per SM each; the gradient sweep needs more registers per thread)
+constexpr int kSweep1Threads = FFDP_SWEEP1_THREADS;
+constexpr int kSweep2Threads = FFDP_SWEEP2_THREADS;
 constexpr int kVPT = 4;                 // voxels per sweep thread per iteration (32 apart)
 constexpr int kHistFrac = 20;           // fixed-point fraction bits of histogram weights
 constexpr float kHistOne = 1048576.0f;  // 2^kHistFrac

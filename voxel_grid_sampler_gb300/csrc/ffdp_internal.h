@@ -35,7 +35,7 @@ struct Sweep1Args {
   Geom g;
   BinMap bf, bj;
   int B;
-  unsigned nIter;             // CTA iterations of kSweepThreads*kVPT voxels
+  unsigned nIter;             // CTA iterations of (CTA threads)*kVPT voxels
 };
 
 // Gradient sweep: MI table lookups and/or a given dL/dJ, sampler backward.

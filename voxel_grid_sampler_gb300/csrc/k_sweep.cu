@@ -7,7 +7,7 @@
 // Parzen window -- histogram entries accumulate per voxel in shared memory and
 // the per-voxel partial gradient reads a small table, so no B x N block exists.
 //
-// Layout of the work: a CTA iteration covers kSweepThreads*kVPT consecutive
+// Layout of the work: a CTA iteration covers (CTA threads)*kVPT consecutive
 // voxels of the flattened [D][H][W] grid; each warp owns 32*kVPT of them and
 // each lane every 32nd (see the lane walk), taken two at a time through a
 // two-stage gather pipeline.  Grids are persistent (one CTA per SM striding
@@ -36,8 +36,6 @@ struct HistLayout {
   static constexpr int COL = PRIVATE ? 32 : 4 * R;  // word stride of b
   static constexpr int QROW = COL * BMAX;         // words per row (private) / per group of four rows
   static constexpr int WORDS = BMAX * BMAX * R;
-  // voxels reaching one word per CTA iteration: lanes sharing a copy
-  static constexpr int VOX_PER_ITER = kSweepThreads * kVPT / R;
   __host__ __device__ static constexpr int word(int a, int b) {
     return PRIVATE ? (a * BMAX + b) * 32 : (a >> 2) * QROW + COL * b + R * (a & 3);
   }
@@ -45,12 +43,14 @@ struct HistLayout {
 
 // u32 fixed-point counts (kHistFrac fraction bits): one voxel adds at most
 // (2/3)^2 to a word, so a CTA flushes its copies to the u64 global histogram
-// at least every flush_every<BMAX>() iterations.
-template <int BMAX>
+// at least every flush_every<BMAX, NT>() iterations.
+// A CTA of NT threads adds at most NT * kVPT / R voxels to one word per iteration.
+template <int BMAX, int NT>
 __host__ __device__ constexpr int flush_every() {
-  return (int)(4294967295.0 / (HistLayout<BMAX>::VOX_PER_ITER * (4.0 / 9.0) * kHistOne)) - 1;
+  return (int)(4294967295.0 / ((double)NT * kVPT / HistLayout<BMAX>::R * (4.0 / 9.0) * kHistOne)) - 1;
 }
-static_assert(flush_every<32>() >= 16 && flush_every<64>() >= 16, "histogram flush interval");
+static_assert(flush_every<32, kSweep1Threads>() >= 16 && flush_every<64, kSweep1Threads>() >= 16,
+              "histogram flush interval");
 
 // fp32 per-thread gradient partials are folded into fp64 every this many iterations.
 constexpr int kFoldEvery = 16;
@@ -65,13 +65,13 @@ __global__ void k_zero_u64(unsigned long long* p, int n) {
 // and takes its two 16-byte halves in lane-dependent order, so the 8 lanes of
 // each quarter-warp read 8 different bank quads (rows run to B rounded up to
 // a multiple of 4).
-template <int BMAX>
+template <int BMAX, int NT>
 __device__ __forceinline__ void hist_flush(unsigned* hist, unsigned long long* gh, int B) {
   using L = HistLayout<BMAX>;
   __syncthreads();
   if (L::PRIVATE) {
     const int lane = threadIdx.x & 31;
-    for (int i = threadIdx.x; i < B * B; i += kSweepThreads) {
+    for (int i = threadIdx.x; i < B * B; i += NT) {
       const int ra = i / B, rb = i - ra * B;
       unsigned* w = hist + L::word(ra, rb);
       unsigned long long s = 0ull;
@@ -87,7 +87,7 @@ __device__ __forceinline__ void hist_flush(unsigned* hist, unsigned long long* g
     static_assert(L::PRIVATE || L::R == 8, "flush reads two uint4 per bin");
     const int h = (threadIdx.x >> 2) & 1;
     const int n = ((B + 3) & ~3) * B;
-    for (int i = threadIdx.x; i < n; i += kSweepThreads) {
+    for (int i = threadIdx.x; i < n; i += NT) {
       const int rest = i >> 2, rb = rest % B, ra = ((rest / B) << 2) | (i & 3);
       if (ra >= B) continue;
       uint4* w = reinterpret_cast<uint4*>(hist + L::word(ra, rb));
@@ -214,7 +214,7 @@ __device__ __forceinline__ float mi_grad(const float* tsm, const BinMap& bf, con
 
 // ------------------------------------------------------------- lane walk
 // Lane l of warp w handles, in CTA iteration it, the voxels
-//   lin = it * kSweepThreads * kVPT + w * 32 * kVPT + l + 32 v,  v = 0..kVPT-1.
+//   lin = it * NT * kVPT + w * 32 * kVPT + l + 32 v,  v = 0..kVPT-1  (NT threads per CTA).
 // Every load, gather and store instruction of a warp covers 32 consecutive
 // voxels, so F, J, g and dJ move in whole 128-byte lines and the trilinear
 // taps of 32 neighbouring points share one or two lines per M row.
@@ -322,14 +322,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, unsigned
 
 // Ring geometry: per slot [u][F][X] for one chunk; NST slots per warp, then
 // one 8-byte mbarrier per slot after all warps' slots.
-template <typename FT, bool SU, bool SF, bool SX, int NST>
+template <typename FT, bool SU, bool SF, bool SX, int NST, int NT>
 struct Ring {
   static constexpr int kChunk = 32 * kVPT;
   static constexpr int kU = SU ? kChunk * 12 : 0;
   static constexpr int kF = SF ? kChunk * (int)sizeof(FT) : 0;
   static constexpr int kX = SX ? kChunk * 4 : 0;
   static constexpr int kSlot = kU + kF + kX;
-  static constexpr int kWarps = kSweepThreads / 32;
+  static constexpr int kWarps = NT / 32;
   static constexpr size_t kBytes = (size_t)kWarps * NST * (kSlot + 8);
   static_assert(kU % 16 == 0 && kF % 16 == 0 && kX % 16 == 0, "bulk copies move multiples of 16 bytes");
 };
@@ -337,6 +337,7 @@ struct Ring {
 // Per-warp view of the ring.
 template <class RG, int NST>
 struct WarpRing {
+  using RGT = RG;
   char* slots;    // this warp's NST slots
   uint32_t bars;  // shared address of this warp's first mbarrier
   unsigned tx;    // bytes per chunk (0: nothing streamed)
@@ -393,7 +394,7 @@ struct RingSched {
   unsigned nIter, nFull;  // CTA iterations; whole chunks in the grid
   int kfail;              // first iteration whose wait gave up (-1: none)
 
-  __device__ __forceinline__ unsigned chunk(unsigned it) const { return it * (kSweepThreads / 32) + (threadIdx.x >> 5); }
+  __device__ __forceinline__ unsigned chunk(unsigned it) const { return it * WR::RGT::kWarps + (threadIdx.x >> 5); }
   __device__ __forceinline__ bool streamed(unsigned it) const { return it < nIter && chunk(it) < nFull; }
 
   template <typename FT>
@@ -530,12 +531,12 @@ struct S1Cfg {
   static constexpr bool HIST = MODE != S1_WRITEJ;
   static constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
   static constexpr size_t kHistBytes = HIST ? (size_t)HistLayout<BMAX>::WORDS * sizeof(unsigned) : 0;
-  using RG1 = Ring<FT, SAMPLE, HIST, !SAMPLE, 1>;
+  using RG1 = Ring<FT, SAMPLE, HIST, !SAMPLE, 1, kSweep1Threads>;
   // as many ring slots (up to 4) as fit next to the histogram in 220 KiB
-  static constexpr int NST_FIT = (int)((220 * 1024 - kHistBytes) / ((kSweepThreads / 32) * (RG1::kSlot + 8)));
+  static constexpr int NST_FIT = (int)((220 * 1024 - kHistBytes) / ((kSweep1Threads / 32) * (RG1::kSlot + 8)));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
   static_assert(NST >= 2, "ring needs two slots");
-  using RG = Ring<FT, SAMPLE, HIST, !SAMPLE, NST>;
+  using RG = Ring<FT, SAMPLE, HIST, !SAMPLE, NST, kSweep1Threads>;
   static constexpr size_t kSmem = kHistBytes + RG::kBytes;
 };
 
@@ -556,7 +557,7 @@ __device__ __forceinline__ void sweep1_half(const Half& H, unsigned* hist, const
 }
 
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a) {
+__global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a) {
   using C = S1Cfg<FT, BMAX, MODE>;
   constexpr bool HIST = C::HIST;
   constexpr bool SAMPLE = C::SAMPLE;
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a)
   HistLane hl;
   if (HIST) {
     hist_lane_init<BMAX>(hl);
-    for (int i = threadIdx.x; i < L::WORDS / 4; i += kSweepThreads) smem4[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < L::WORDS / 4; i += kSweep1Threads) smem4[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
@@ -592,13 +593,13 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep1(const Sweep1Args a)
     sweep1_half<MT, BMAX, HIST, WRITEJ>(A, hist_sm, hl, a, SAMPLE);
     prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
     sweep1_half<MT, BMAX, HIST, WRITEJ>(B, hist_sm, hl, a, SAMPLE);
-    if (HIST && ++pending == flush_every<BMAX>()) {
-      hist_flush<BMAX>(hist_sm, a.ghist, a.B);
+    if (HIST && ++pending == flush_every<BMAX, kSweep1Threads>()) {
+      hist_flush<BMAX, kSweep1Threads>(hist_sm, a.ghist, a.B);
       pending = 0;
     }
   }
   rs.drain(wr);
-  if (HIST) hist_flush<BMAX>(hist_sm, a.ghist, a.B);
+  if (HIST) hist_flush<BMAX, kSweep1Threads>(hist_sm, a.ghist, a.B);
 }
 
 // ------------------------------------------------------------ MI finalize
@@ -695,13 +696,13 @@ struct S2Cfg {
   static constexpr bool MI = MODE != S2_GBUF;
   static constexpr bool SAMPLE = MODE != S2_MI_JBUF;
   static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
-  using RG1 = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, 1>;
+  using RG1 = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, 1, kSweep2Threads>;
   // as many ring slots (up to 4) as fit next to the table in 220 KiB
-  static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (kSweepThreads / 32) * 96) /
-                                       ((kSweepThreads / 32) * (RG1::kSlot + 8)));
+  static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (kSweep2Threads / 32) * 96) /
+                                       ((kSweep2Threads / 32) * (RG1::kSlot + 8)));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
   static_assert(NST >= 2, "ring needs two slots");
-  using RG = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, NST>;
+  using RG = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, NST, kSweep2Threads>;
   static constexpr size_t kSmem = kTableBytes + RG::kBytes;
 };
 
@@ -773,7 +774,7 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
 }
 
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a) {
+__global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a) {
   using C = S2Cfg<FT, BMAX, MODE>;
   constexpr bool MI = C::MI;
   constexpr bool SAMPLE = C::SAMPLE;
@@ -783,12 +784,12 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a)
   using WR = WarpRing<RG, NST>;
   extern __shared__ float4 tsm4[];
   float* tsm = reinterpret_cast<float*>(tsm4);
-  __shared__ double wsum[kSweepThreads / 32][12];
+  __shared__ double wsum[kSweep2Threads / 32][12];
   const Geom& g = a.g;
   if (MI) {
     constexpr int n4 = table_floats<BMAX>() / 4;
     const float4* src = reinterpret_cast<const float4*>(a.T);
-    for (int i = threadIdx.x; i < n4; i += kSweepThreads) tsm4[i] = __ldg(src + i);
+    for (int i = threadIdx.x; i < n4; i += kSweep2Threads) tsm4[i] = __ldg(src + i);
     __syncthreads();
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
@@ -837,7 +838,7 @@ __global__ void __launch_bounds__(kSweepThreads, 1) k_sweep2(const Sweep2Args a)
     if (threadIdx.x < kPartialStride) {
       double s = 0.0;
       if (threadIdx.x < 12)
-        for (int q = 0; q < kSweepThreads / 32; ++q) s += wsum[q][threadIdx.x];
+        for (int q = 0; q < kSweep2Threads / 32; ++q) s += wsum[q][threadIdx.x];
       a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = s;
     }
   }
@@ -900,9 +901,9 @@ static cudaError_t run_sweep1(const Sweep1Args& a, int grid, cudaStream_t s, int
   const size_t smem = S1Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweepThreads, smem);
+  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweep1Threads, smem);
   note_launch_begin("k_sweep1", s);
-  k<<<grid, kSweepThreads, smem, s>>>(a);
+  k<<<grid, kSweep1Threads, smem, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
@@ -952,9 +953,9 @@ static cudaError_t run_sweep2(const Sweep2Args& a, int grid, cudaStream_t s, int
   const size_t smem = S2Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweepThreads, smem);
+  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweep2Threads, smem);
   note_launch_begin("k_sweep2", s);
-  k<<<grid, kSweepThreads, smem, s>>>(a);
+  k<<<grid, kSweep2Threads, smem, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
