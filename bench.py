@@ -38,10 +38,10 @@ ALGO_BYTES = {4: 2 * (4 + 12 + 4) + 12, 5: 2 * (2 + 12 + 2) + 12}
 # Single-pass lower bound: F, M and u read once, du written once.
 SINGLE_PASS_BYTES = {4: 4 + 4 + 12 + 12, 5: 2 + 2 + 12 + 12}
 # Algorithmic bytes per voxel of each kernel of the objective:
-#   k_sweep1  F + u + M read (+ J written when LNCC is on)
+#   k_sweep1  F + u + M read (+ J and dJ/dq written when LNCC is on)
 #   k_lncc    F + J read, dL/dJ written
-#   k_sweep2  u + M + (F for MI | dL/dJ for LNCC) read, du written
-KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4, "k_lncc": 4 + 4 + 4, "k_sweep2": 4 + 12 + 4 + 12},
+#   k_sweep2  MI: F + u + M read, du written;  LNCC: dL/dJ + dJ/dq read, du written
+KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc": 4 + 4 + 4, "k_sweep2": 4 + 12 + 12},
                 5: {"k_sweep1": 2 + 12 + 2, "k_sweep2": 2 + 12 + 2 + 12}}
 HBM_NOMINAL_GBS = 8000.0
 

@@ -278,7 +278,7 @@ int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
 
 // Workspace layout (byte offsets, 256-aligned).
 struct Ws {
-  size_t hist, table, table2, scalars, partials, J, G, total;
+  size_t hist, table, table2, scalars, partials, J, G, DG, total;
 };
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -301,6 +301,8 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
   if (needJ) o = al(o + (size_t)N * sizeof(float));
   w.G = o;
   if (needJ) o = al(o + (size_t)N * sizeof(float));
+  w.DG = o;  // dJ/dq, [N][3]
+  if (needJ) o = al(o + (size_t)N * 3 * sizeof(float));
   w.total = o;
   return w;
 }
@@ -602,12 +604,15 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   a1.M = M;
   a1.u = u;
   a1.Jout = Jbuf;
+  a1.Gout = ln ? reinterpret_cast<float*>(wb + w.DG) : nullptr;
   a1.ghist = hist;
   a1.bf = bf;
   a1.bj = bj;
   a1.B = mi ? p->mi.bins : 32;
   a1.nIter = n_iter1(N);
-  const int m1 = mi ? (ln ? S1_HIST_WRITEJ : S1_HIST) : S1_WRITEJ;
+  // with LNCC, J and its slope dJ/dq are stored for the window kernel and the
+  // streaming sampler backward
+  const int m1 = mi ? (ln ? S1_HIST_WRITEJG : S1_HIST) : S1_WRITEJG;
   FFDP_CUDA(launch_sweep1(m1, ft, mt, bmax, a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(m1, ft, mt, bmax)), s),
             "sweep 1 launch");
   if (mi) {
@@ -643,17 +648,16 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     int grid = 1;
     lncc_tiling(fdims, a.R, a, lncc_ctas_per_sm(LN_DJ, ft, 0, bm, a.R), grid);
     FFDP_CUDA(launch_lncc(LN_DJ, ft, 0, bm, a, grid, s), "LNCC window launch");
-    // sampler backward of g: du, affine partials
+    // sampler backward of g from the stored slope: du, affine partials
     Sweep2Args a2{};
     a2.g = g;
-    a2.M = M;
-    a2.u = u;
     a2.gbuf = Gbuf;
+    a2.dJdq = reinterpret_cast<const float*>(wb + w.DG);
     a2.du = du;
     a2.partials = partials + (size_t)grid * kPartialStride;
     a2.nIter = n_iter2(N);
-    const int grid2 = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_GBUF, 0, mt, 32));
-    FFDP_CUDA(launch_sweep2(S2_GBUF, 0, mt, 32, a2, grid2, s), "sampler backward launch");
+    const int grid2 = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_GBUF_DJ, 0, 0, 32));
+    FFDP_CUDA(launch_sweep2(S2_GBUF_DJ, 0, 0, 32, a2, grid2, s), "sampler backward launch");
     nparts = grid + grid2;
   } else {
     Sweep2Args a2{};

@@ -460,7 +460,10 @@ struct Half {
 // J/g (from the ring slot of a streamed chunk, else from global memory),
 // walks the coordinates and issues the gathers.  Half 0 waits for the chunk's
 // slot; half 1 releases the slot for refilling.
-template <typename FT, typename MT, bool LF, bool LU, bool LX, class WR, int NST>
+// LU streams the 3-vector slot (u, or the stored dJ/dq when GATHER is off);
+// GATHER walks the fixed-point coordinates and gathers the taps; without it
+// the slot's vector is kept in H.rr and only the voxel indices are walked.
+template <typename FT, typename MT, bool LF, bool LU, bool LX, bool GATHER, class WR, int NST>
 __device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __restrict__ M, const FT* __restrict__ F,
                                         const float* u, const float* X, WR& wr, RingSched<WR, NST>& rs,
                                         LaneWalk& w, unsigned it, unsigned k, int h, unsigned long long pol) {
@@ -502,7 +505,7 @@ __device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __rest
     }
   }
   if (streamed && h == 1) rs.template refill<FT>(wr, k, it, u, F, X, pol);
-  if (LU) {
+  if (LU && GATHER) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int v = 2 * h + j;
@@ -520,15 +523,34 @@ __device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __rest
       if (v >= nvc) b[0] = -2;  // past the end: no loads
       gather8<MT>(M, g, b, H.taps[j]);
     }
+  } else if (LU) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int v = 2 * h + j;
+      if (v < nvc) {
+        if (v > 0 && w.x + 32 < g.fW)
+          w.x += 32;
+        else
+          lin_to_xyz(g, lin0 + 32u * v, w.x, w.y, w.z);
+      }
+      H.ix[j] = w.x;
+      H.iy[j] = w.y;
+      H.iz[j] = w.z;
+      H.rr[j][0] = uu[j][0];
+      H.rr[j][1] = uu[j][1];
+      H.rr[j][2] = uu[j][2];
+    }
   }
 }
 
 // ------------------------------------------------------------------ sweep 1
-// Sampling (or reading J) plus, per mode, the histogram and/or a J store.
+// Sampling (or reading J) plus, per mode, the histogram and/or a J store
+// (and, for the LNCC objective, a store of the slope dJ/dq, so that its
+// sampler backward streams instead of gathering M again).
 // Streams: u (sampling), F (histogram), J (histogram of a given J).
 template <typename FT, int BMAX, int MODE>
 struct S1Cfg {
-  static constexpr bool HIST = MODE != S1_WRITEJ;
+  static constexpr bool HIST = MODE != S1_WRITEJ && MODE != S1_WRITEJG;
   static constexpr bool SAMPLE = MODE != S1_HIST_JBUF;
   static constexpr size_t kHistBytes = HIST ? (size_t)HistLayout<BMAX>::WORDS * sizeof(unsigned) : 0;
   using RG1 = Ring<FT, SAMPLE, HIST, !SAMPLE, 1, kSweep1Threads>;
@@ -540,7 +562,7 @@ struct S1Cfg {
   static constexpr size_t kSmem = kHistBytes + RG::kBytes;
 };
 
-template <typename MT, int BMAX, bool HIST, bool WRITEJ>
+template <typename MT, int BMAX, bool HIST, bool WRITEJ, bool WRITEG>
 __device__ __forceinline__ void sweep1_half(const Half& H, unsigned* hist, const HistLane& hl, const Sweep1Args& a,
                                             bool sample) {
 #pragma unroll
@@ -549,9 +571,15 @@ __device__ __forceinline__ void sweep1_half(const Half& H, unsigned* hist, const
       float d0, d1, d2, m[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
-      const float jv = sample ? interp8<false>(m, H.rr[j], d0, d1, d2) : H.x[j];
+      const float jv = sample ? interp8<WRITEG>(m, H.rr[j], d0, d1, d2) : H.x[j];
       if (HIST) hist_add<BMAX>(hist, hl, a.bf, a.bj, H.f[j], jv);
       if (WRITEJ) a.Jout[H.lin + 32u * j] = jv;
+      if (WRITEG) {
+        float* gp = a.Gout + 3ull * (H.lin + 32u * j);
+        gp[0] = d0;
+        gp[1] = d1;
+        gp[2] = d2;
+      }
     }
   }
 }
@@ -561,7 +589,8 @@ __global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a
   using C = S1Cfg<FT, BMAX, MODE>;
   constexpr bool HIST = C::HIST;
   constexpr bool SAMPLE = C::SAMPLE;
-  constexpr bool WRITEJ = (MODE == S1_WRITEJ) || (MODE == S1_HIST_WRITEJ);
+  constexpr bool WRITEG = (MODE == S1_HIST_WRITEJG) || (MODE == S1_WRITEJG);
+  constexpr bool WRITEJ = (MODE == S1_WRITEJ) || (MODE == S1_HIST_WRITEJ) || WRITEG;
   constexpr int NST = C::NST;
   using L = HistLayout<BMAX>;
   using RG = typename C::RG;
@@ -586,13 +615,13 @@ __global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a
   LaneWalk w;
   Half A, B;
   unsigned k = 0;
-  prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
-    prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
-    sweep1_half<MT, BMAX, HIST, WRITEJ>(A, hist_sm, hl, a, SAMPLE);
-    prepare<FT, MT, HIST, SAMPLE, !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
-    sweep1_half<MT, BMAX, HIST, WRITEJ>(B, hist_sm, hl, a, SAMPLE);
+    prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
+    sweep1_half<MT, BMAX, HIST, WRITEJ, WRITEG>(A, hist_sm, hl, a, SAMPLE);
+    prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+    sweep1_half<MT, BMAX, HIST, WRITEJ, WRITEG>(B, hist_sm, hl, a, SAMPLE);
     if (HIST && ++pending == flush_every<BMAX, kSweep1Threads>()) {
       hist_flush<BMAX, kSweep1Threads>(hist_sm, a.ghist, a.B);
       pending = 0;
@@ -693,23 +722,26 @@ __global__ void __launch_bounds__(1024) k_mi_finalize(const FinalizeArgs a) {
 // g (given gradient) or J (MI on a given J).
 template <typename FT, int BMAX, int MODE>
 struct S2Cfg {
-  static constexpr bool MI = MODE != S2_GBUF;
-  static constexpr bool SAMPLE = MODE != S2_MI_JBUF;
+  static constexpr bool MI = MODE == S2_MI || MODE == S2_MI_JBUF;  // g from the MI table
+  static constexpr bool GATHER = MODE == S2_MI || MODE == S2_GBUF;  // resample J and dJ/dq
+  static constexpr bool VEC = GATHER || MODE == S2_GBUF_DJ;         // 3-vector stream: u or dJ/dq
+  static constexpr bool BWD = MODE != S2_MI_JBUF;                   // du and affine partials
+  static constexpr bool XS = MODE != S2_MI;                         // g (given) or J (given)
   static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
-  using RG1 = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, 1, kSweep2Threads>;
+  using RG1 = Ring<FT, VEC, MI, XS, 1, kSweep2Threads>;
   // as many ring slots (up to 4) as fit next to the table in 220 KiB
   static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (kSweep2Threads / 32) * 96) /
                                        ((kSweep2Threads / 32) * (RG1::kSlot + 8)));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
   static_assert(NST >= 2, "ring needs two slots");
-  using RG = Ring<FT, SAMPLE, MI, !MI || !SAMPLE, NST, kSweep2Threads>;
+  using RG = Ring<FT, VEC, MI, XS, NST, kSweep2Threads>;
   static constexpr size_t kSmem = kTableBytes + RG::kBytes;
 };
 
-template <typename MT, int BMAX, bool MI, bool SAMPLE>
+template <typename MT, int BMAX, bool MI, bool GATHER, bool BWD>
 __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, const Sweep2Args& a, float acc[12]) {
   const Geom& g = a.g;
-  if (!SAMPLE) {
+  if (!BWD) {
 #pragma unroll
     for (int j = 0; j < 2; ++j)
       if (j < H.nv) a.dJ[H.lin + 32u * j] = mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], H.x[j]);
@@ -720,11 +752,20 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
   for (int j = 0; j < 2; ++j) {
     e[j][0] = e[j][1] = e[j][2] = 0.0f;
     if (j >= H.nv) continue;
-    float gq0, gq1, gq2, m[8];
+    float gq0, gq1, gq2, gv;
+    if (GATHER) {
+      float m[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
-    const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
-    const float gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
+      for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
+      const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
+      gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
+    } else {
+      // the stored slope of J and the given g
+      gq0 = H.rr[j][0];
+      gq1 = H.rr[j][1];
+      gq2 = H.rr[j][2];
+      gv = H.x[j];
+    }
     e[j][0] = gv * gq0;
     e[j][1] = gv * gq1;
     e[j][2] = gv * gq2;
@@ -776,9 +817,7 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
 template <typename FT, typename MT, int BMAX, int MODE>
 __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a) {
   using C = S2Cfg<FT, BMAX, MODE>;
-  constexpr bool MI = C::MI;
-  constexpr bool SAMPLE = C::SAMPLE;
-  constexpr bool BWD = SAMPLE;
+  constexpr bool MI = C::MI, GATHER = C::GATHER, VEC = C::VEC, BWD = C::BWD, XS = C::XS;
   constexpr int NST = C::NST;
   using RG = typename C::RG;
   using WR = WarpRing<RG, NST>;
@@ -794,7 +833,8 @@ __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
   const MT* __restrict__ M = static_cast<const MT*>(a.M);
-  const float* X = SAMPLE ? a.gbuf : a.Jin;
+  const float* X = MODE == S2_MI_JBUF ? a.Jin : a.gbuf;
+  const float* U = GATHER ? a.u : a.dJdq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (BWD && lane == 0)
 #pragma unroll
@@ -803,20 +843,20 @@ __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a
 #pragma unroll
   for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
   WR wr;
-  wr.init(reinterpret_cast<char*>(tsm4) + C::kTableBytes, SAMPLE && a.u != nullptr);
+  wr.init(reinterpret_cast<char*>(tsm4) + C::kTableBytes, VEC && U != nullptr);
   RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
   const unsigned long long pol = policy_evict_first();
-  rs.template prologue<FT>(wr, a.u, F, X, pol);
+  rs.template prologue<FT>(wr, U, F, X, pol);
   LaneWalk w;
   Half A, B;
   unsigned k = 0;
-  prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
-    prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
-    sweep2_half<MT, BMAX, MI, SAMPLE>(A, tsm, a, acc);
-    prepare<FT, MT, MI, SAMPLE, !MI || !SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
-    sweep2_half<MT, BMAX, MI, SAMPLE>(B, tsm, a, acc);
+    prepare<FT, MT, MI, VEC, XS, GATHER>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
+    sweep2_half<MT, BMAX, MI, GATHER, BWD>(A, tsm, a, acc);
+    prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+    sweep2_half<MT, BMAX, MI, GATHER, BWD>(B, tsm, a, acc);
     if (BWD && ++pending == kFoldEvery) {
 #pragma unroll
       for (int q = 0; q < 12; ++q) {
@@ -918,6 +958,8 @@ static cudaError_t dispatch_sweep1(int mode, int ft, int mt, int bmax, const Swe
         case S1_HIST_WRITEJ: e = run_sweep1<FT, MT, 32, S1_HIST_WRITEJ>(a, grid, s, occ); break;
         case S1_WRITEJ: e = run_sweep1<float, MT, 32, S1_WRITEJ>(a, grid, s, occ); break;
         case S1_HIST_JBUF: e = run_sweep1<FT, float, 32, S1_HIST_JBUF>(a, grid, s, occ); break;
+        case S1_HIST_WRITEJG: e = run_sweep1<FT, MT, 32, S1_HIST_WRITEJG>(a, grid, s, occ); break;
+        case S1_WRITEJG: e = run_sweep1<float, MT, 32, S1_WRITEJG>(a, grid, s, occ); break;
       }
     } else {
       switch (mode) {
@@ -925,6 +967,8 @@ static cudaError_t dispatch_sweep1(int mode, int ft, int mt, int bmax, const Swe
         case S1_HIST_WRITEJ: e = run_sweep1<FT, MT, 64, S1_HIST_WRITEJ>(a, grid, s, occ); break;
         case S1_WRITEJ: e = run_sweep1<float, MT, 32, S1_WRITEJ>(a, grid, s, occ); break;
         case S1_HIST_JBUF: e = run_sweep1<FT, float, 64, S1_HIST_JBUF>(a, grid, s, occ); break;
+        case S1_HIST_WRITEJG: e = run_sweep1<FT, MT, 64, S1_HIST_WRITEJG>(a, grid, s, occ); break;
+        case S1_WRITEJG: e = run_sweep1<float, MT, 32, S1_WRITEJG>(a, grid, s, occ); break;
       }
     }
   }));
@@ -936,7 +980,7 @@ cudaError_t launch_sweep1(int mode, int ft, int mt, int bmax, const Sweep1Args& 
 }
 
 int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax) {
-  static int cache[4][2][2][2] = {};
+  static int cache[kSweep1Modes][2][2][2] = {};
   int& c = cache[mode][ft][mt][bmax == 64];
   if (c == 0) {
     int occ = 0;
@@ -969,12 +1013,14 @@ static cudaError_t dispatch_sweep2(int mode, int ft, int mt, int bmax, const Swe
         case S2_MI: e = run_sweep2<FT, MT, 32, S2_MI>(a, grid, s, occ); break;
         case S2_GBUF: e = run_sweep2<float, MT, 32, S2_GBUF>(a, grid, s, occ); break;
         case S2_MI_JBUF: e = run_sweep2<FT, float, 32, S2_MI_JBUF>(a, grid, s, occ); break;
+        case S2_GBUF_DJ: e = run_sweep2<float, float, 32, S2_GBUF_DJ>(a, grid, s, occ); break;
       }
     } else {
       switch (mode) {
         case S2_MI: e = run_sweep2<FT, MT, 64, S2_MI>(a, grid, s, occ); break;
         case S2_GBUF: e = run_sweep2<float, MT, 32, S2_GBUF>(a, grid, s, occ); break;
         case S2_MI_JBUF: e = run_sweep2<FT, float, 64, S2_MI_JBUF>(a, grid, s, occ); break;
+        case S2_GBUF_DJ: e = run_sweep2<float, float, 32, S2_GBUF_DJ>(a, grid, s, occ); break;
       }
     }
   }));
@@ -986,7 +1032,7 @@ cudaError_t launch_sweep2(int mode, int ft, int mt, int bmax, const Sweep2Args& 
 }
 
 int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax) {
-  static int cache[3][2][2][2] = {};
+  static int cache[kSweep2Modes][2][2][2] = {};
   int& c = cache[mode][ft][mt][bmax == 64];
   if (c == 0) {
     int occ = 0;
