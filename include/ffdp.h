@@ -198,6 +198,14 @@ size_t ffdp_static_scratch_bytes(void);
  * last call and 0 otherwise, and clears the word. */
 ffdp_status ffdp_device_error(int *flag);
 
+/* Test hook for the report above (not part of the method): when `on` is
+ * non-zero, the next objective call arms the first ring slot of every warp of
+ * its first sweep with 16 bytes more than the slot's copies deliver, so every
+ * wait on it runs out (about two seconds in all) and the call reports through
+ * ffdp_device_error and NaN losses.  Nothing faults and no copy is left in
+ * flight; the request applies to one call and then clears itself. */
+ffdp_status ffdp_test_ring_stall(int on);
+
 /* Human-readable name of a status. */
 const char *ffdp_status_string(ffdp_status s);
 

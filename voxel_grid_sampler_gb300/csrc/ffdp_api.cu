@@ -85,6 +85,17 @@ void ffdp::note_launch_end(cudaStream_t s) {
 
 extern "C" uint64_t ffdp_launch_count(void) { return g_launches.load(); }
 
+namespace {
+std::atomic<unsigned> g_test_stall{0};
+}
+
+unsigned ffdp::take_test_stall() { return g_test_stall.exchange(0u); }
+
+extern "C" ffdp_status ffdp_test_ring_stall(int on) {
+  g_test_stall.store(on ? 16u : 0u);
+  return FFDP_OK;
+}
+
 extern "C" ffdp_status ffdp_device_error(int* flag) {
   if (!flag) return fail(FFDP_ERR_INVALID_ARGUMENT, "flag is NULL");
   unsigned v = 0;
@@ -605,6 +616,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   a1.u = u;
   a1.Jout = Jbuf;
   a1.Gout = ln ? reinterpret_cast<float*>(wb + w.DG) : nullptr;
+  a1.stall_tx = take_test_stall();
   a1.ghist = hist;
   a1.bf = bf;
   a1.bj = bj;

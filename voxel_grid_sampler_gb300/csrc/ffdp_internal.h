@@ -38,6 +38,7 @@ struct Sweep1Args {
   const float* Jin;
   float* Jout;
   float* Gout;                // [N][3] dJ/dq (S1_*WRITEJG)
+  unsigned stall_tx;          // tests only: extra bytes armed on ring slot 0 (0 = none)
   unsigned long long* ghist;  // [B*B] fixed-point (kHistFrac) joint histogram
   Geom g;
   BinMap bf, bj;
@@ -118,6 +119,8 @@ cudaError_t launch_lncc(int mode, int ft, int mt, int bmax_or0, const LnccArgs& 
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s);
 
 // Occupancy-derived persistent grid sizes (CTAs per SM), cached.
+// Test hook: returns and clears the one-shot ring stall request.
+unsigned take_test_stall();
 // Reads the device error word of the current device (synchronous) and clears it.
 cudaError_t take_device_error(unsigned* v);
 int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax);

@@ -357,14 +357,15 @@ struct WarpRing {
     __syncwarp();
   }
 
-  // lane 0: copy chunk ch into slot s
+  // lane 0: copy chunk ch into slot s (the barrier expects `extra` bytes more
+  // than the copies deliver when a test arms a stall)
   template <typename FT>
   __device__ __forceinline__ void issue(int s, unsigned ch, const float* u, const FT* F, const float* X,
-                                        unsigned long long pol) const {
+                                        unsigned long long pol, unsigned extra = 0) const {
     const size_t v0 = (size_t)ch * RG::kChunk;
     char* slot = slots + s * RG::kSlot;
     const uint32_t bar = bars + 8 * s;
-    mbar_expect_tx(bar, tx);
+    mbar_expect_tx(bar, tx + extra);
     if (RG::kU && has_u) bulk_g2s(smem_u32(slot), u + 3 * v0, RG::kU, bar, pol);
     if (RG::kF) bulk_g2s(smem_u32(slot + RG::kU), F + v0, RG::kF, bar, pol);
     if (RG::kX) bulk_g2s(smem_u32(slot + RG::kU + RG::kF), X + v0, RG::kX, bar, pol);
@@ -397,14 +398,16 @@ struct RingSched {
   __device__ __forceinline__ unsigned chunk(unsigned it) const { return it * WR::RGT::kWarps + (threadIdx.x >> 5); }
   __device__ __forceinline__ bool streamed(unsigned it) const { return it < nIter && chunk(it) < nFull; }
 
+  // stall_tx != 0 (tests only): slot 0 expects that many bytes more than its
+  // copies deliver, so every wait on it runs out.
   template <typename FT>
   __device__ __forceinline__ void prologue(const WR& r, const float* u, const FT* F, const float* X,
-                                           unsigned long long pol) const {
+                                           unsigned long long pol, unsigned stall_tx = 0) const {
     if (r.tx != 0 && (threadIdx.x & 31) == 0) {
 #pragma unroll
       for (int s = 0; s < NST; ++s) {
         const unsigned it = blockIdx.x + s * gridDim.x;
-        if (streamed(it)) r.template issue<FT>(s, chunk(it), u, F, X, pol);
+        if (streamed(it)) r.template issue<FT>(s, chunk(it), u, F, X, pol, s == 0 ? stall_tx : 0u);
       }
     }
     __syncwarp();
@@ -611,7 +614,7 @@ __global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a
   wr.init(reinterpret_cast<char*>(smem4) + C::kHistBytes, SAMPLE && a.u != nullptr);
   RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
   const unsigned long long pol = policy_evict_first();
-  rs.template prologue<FT>(wr, a.u, F, X, pol);
+  rs.template prologue<FT>(wr, a.u, F, X, pol, a.stall_tx);
   LaneWalk w;
   Half A, B;
   unsigned k = 0;

@@ -96,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.ffdp_timing_read.restype = ctypes.c_int
         L.ffdp_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
         L.ffdp_device_error.restype = ctypes.c_int
+        L.ffdp_test_ring_stall.argtypes = [ctypes.c_int]
+        L.ffdp_test_ring_stall.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -283,6 +285,11 @@ def device_error() -> bool:
     return bool(flag.value)
 
 
+def test_ring_stall(on: bool = True) -> None:
+    """Arm (or disarm) the one-shot ring stall of the next objective call (tests)."""
+    _check(lib().ffdp_test_ring_stall(1 if on else 0))
+
+
 def timing_enable(capacity: int) -> None:
     _check(lib().ffdp_timing_enable(int(capacity)))
 
@@ -305,7 +312,7 @@ class Declared:
     names: tuple = ("ffdp_workspace_bytes", "ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd",
                     "ffdp_mi_fwd_bwd", "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_status_string",
                     "ffdp_last_error", "ffdp_launch_count", "ffdp_timing_enable", "ffdp_timing_read",
-                    "ffdp_device_error")
+                    "ffdp_device_error", "ffdp_test_ring_stall")
 
 
 def ffdp_objective_mi_static(F, M, u, T: ffdp_transform, params: ffdp_objective_params, loss, du, dA, dt,
