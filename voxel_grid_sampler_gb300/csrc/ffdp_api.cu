@@ -304,7 +304,7 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
   w.table2 = o;
   if (mi && needJ) o = al(o + (size_t)bmax * bmax * 2 * sizeof(float));
   w.scalars = o;
-  o = al(o + 16 * sizeof(double));
+  o = al(o + 64 * sizeof(double));  // MI part per histogram row
   // two partial-record sets: the LNCC kernel's and the gradient sweep's
   w.partials = o;
   o = al(o + 2 * max_parts * kPartialStride * sizeof(double));
@@ -522,6 +522,7 @@ extern "C" ffdp_status ffdp_mi_fwd_bwd(const void* F, ffdp_dtype ft, const float
   }
   FinishArgs f{};
   f.scalars = fa.scalars;
+  f.mi_rows = bmax;
   f.nparts = 0;
   f.partials = reinterpret_cast<double*>(wb + w.partials);
   f.loss = loss;
@@ -692,6 +693,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   f.partials = partials;
   f.nparts = nparts;
   f.scalars = scalars;
+  f.mi_rows = mi ? bmax : 0;
   f.dA = dA;
   f.dt = dt;
   f.loss = loss;

@@ -69,7 +69,7 @@ struct FinalizeArgs {
   const unsigned long long* ghist;
   float* T;        // gradient table of the linear sweep (polynomial cells for 32 bins)
   float* T2;       // optional: T rows packed as float2 pairs (LNCC-fused gradient)
-  double* scalars; // [0] = MI
+  double* scalars; // [0 .. BMAX) = MI part of histogram row a
   int B;
   double N;
   double tscale;   // multiplies T (w_mi * (B-5)/(m_hi-m_lo) / N)
@@ -99,7 +99,8 @@ struct LnccArgs {
 struct FinishArgs {
   const double* partials;
   int nparts;
-  const double* scalars;  // [0] = MI (if MI on)
+  const double* scalars;  // [0 .. mi_rows) = MI parts per histogram row (if MI on)
+  int mi_rows;
   float* dA;
   float* dt;
   float* loss;            // NULL or [nloss]

@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
   using L = LT<R>;
   using Q = LTR<R>;
   constexpr int W = L::W, TY = L::TY, E2S = Q::ZS;
-  constexpr int E1W = L::E1W, E1H = L::E1H, E1S = L::E1S, NIN = L::NIN;
+  constexpr int E1W = L::E1W, E1H = L::E1H, E1S = L::E1S;
   constexpr int NOUT = Q::NOUT, NSTG = Q::NSTG;
   constexpr bool MI = BMAX != 0;
 

@@ -635,41 +635,49 @@ __global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a
 }
 
 // ------------------------------------------------------------ MI finalize
-// One CTA: P = H / (N 2^kHistFrac); marginals as row / column sums of the
-// joint (equal to the separately defined marginals by partition of unity);
-// MI = sum_{P>0} P (ln P - ln P_F - ln P_J); the gradient table of the
-// scaled T = tscale (ln P - ln P_F - ln P_J) (0 where P = 0).
+// One CTA per histogram row a (BMAX CTAs; rows >= B are empty):
+// P = H / (N 2^kHistFrac); marginals as row / column sums of the joint (equal
+// to the separately defined marginals by partition of unity); the row's MI
+// part sum_{b, P>0} P (ln P - ln P_F - ln P_J), added over rows in a fixed
+// order by the finish kernel; and the row's entries of the gradient table of
+// the scaled T = tscale (ln P - ln P_F - ln P_J) (0 where P = 0).  Every CTA
+// recomputes the marginals (B^2 reads) so the logarithms, the costly part in
+// fp64, are spread over BMAX SMs.
 template <int BMAX>
-__global__ void __launch_bounds__(1024) k_mi_finalize(const FinalizeArgs a) {
+__global__ void __launch_bounds__(256) k_mi_finalize(const FinalizeArgs a) {
+  constexpr int TW = BMAX + 3;  // T columns -1 .. BMAX + 1
   __shared__ double P[BMAX * BMAX];
-  __shared__ double PF[BMAX], PJ[BMAX];
-  __shared__ double red[32];
-  const int B = a.B, nb = B * B, tid = threadIdx.x;
+  __shared__ double lPF[BMAX], lPJ[BMAX];
+  __shared__ double Ts[4][TW];  // unscaled T of rows a-1 .. a+2
+  __shared__ double red[8];
+  const int B = a.B, nb = B * B, tid = threadIdx.x, row = blockIdx.x;
   const double inv = 1.0 / (a.N * (double)kHistOne);
   for (int i = tid; i < nb; i += blockDim.x) P[i] = (double)a.ghist[i] * inv;
   __syncthreads();
   if (tid < B) {
     double s = 0.0;
-    for (int b = 0; b < B; ++b) s += P[tid * B + b];
-    PF[tid] = s;
-  } else if (tid >= 512 && tid - 512 < B) {
-    const int b = tid - 512;
+    for (int c = 0; c < B; ++c) s += P[tid * B + c];
+    lPF[tid] = s > 0.0 ? log(s) : 0.0;
+  } else if (tid >= 128 && tid - 128 < B) {
+    const int c = tid - 128;
     double s = 0.0;
-    for (int r = 0; r < B; ++r) s += P[r * B + b];
-    PJ[b] = s;
+    for (int r = 0; r < B; ++r) s += P[r * B + c];
+    lPJ[c] = s > 0.0 ? log(s) : 0.0;
   }
   __syncthreads();
-  double mi = 0.0;
-  for (int i = tid; i < nb; i += blockDim.x) {
-    const int ra = i / B, rb = i - ra * B;
-    const double p = P[i];
+  for (int i = tid; i < 4 * TW; i += blockDim.x) {
+    const int q = i / TW, c = i - q * TW - 1, ra = row - 1 + q;
     double t = 0.0;
-    if (p > 0.0) {
-      t = log(p) - log(PF[ra]) - log(PJ[rb]);
-      mi += p * t;
+    if (ra >= 0 && ra < B && c >= 0 && c < B) {
+      const double p = P[ra * B + c];
+      if (p > 0.0) t = log(p) - lPF[ra] - lPJ[c];
     }
-    P[i] = t * a.tscale;
+    Ts[q][c + 1] = t;
   }
+  __syncthreads();
+  // this row's MI part
+  double mi = 0.0;
+  if (row < B && tid < B) mi = P[row * B + tid] * Ts[1][tid + 1];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mi += __shfl_xor_sync(0xffffffffu, mi, o);
   if ((tid & 31) == 0) red[tid >> 5] = mi;
@@ -677,24 +685,25 @@ __global__ void __launch_bounds__(1024) k_mi_finalize(const FinalizeArgs a) {
   if (tid == 0) {
     double s = 0.0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-    a.scalars[0] = s;
+    a.scalars[row] = s;
   }
-  auto T = [&](int ra, int rb) -> double { return (ra >= 0 && ra < B && rb >= 0 && rb < B) ? P[ra * B + rb] : 0.0; };
-  if (BMAX == 32) {
-    // cell (fa, fb): C[p][r] = sum_{i,k} T(fa-1+i, fb-1+k) W[i][p] D[k][r]
-    const double W[4][4] = {{1.0 / 6, -0.5, 0.5, -1.0 / 6},
-                            {2.0 / 3, 0.0, -1.0, 0.5},
-                            {1.0 / 6, 0.5, 0.5, -0.5},
-                            {0.0, 0.0, 0.0, 1.0 / 6}};
-    // beta'(s) at s = (fb-1+k) - cJ as a polynomial in tJ:
-    //   d0 = (1-t)^2/2, d1 = 2t - 1.5t^2, d2 = -1/2 - t + 1.5t^2, d3 = -t^2/2
-    const double Dc[4][3] = {{0.5, -1.0, 0.5}, {0.0, 2.0, -1.5}, {-0.5, -1.0, 1.5}, {0.0, 0.0, -0.5}};
-    for (int i = tid; i < BMAX * BMAX; i += blockDim.x) {
-      const int fa = i / BMAX, fb = i - fa * BMAX;
+  const double ts = a.tscale;
+  auto T = [&](int q, int c) -> double { return Ts[q][c + 1] * ts; };  // row a-1+q, column c
+  if (tid < BMAX) {
+    const int fb = tid, i = row * BMAX + fb;
+    if constexpr (BMAX == 32) {
+      // cell (row, fb): C[p][r] = sum_{ii,kk} T(row-1+ii, fb-1+kk) W[ii][p] D[kk][r]
+      const double W[4][4] = {{1.0 / 6, -0.5, 0.5, -1.0 / 6},
+                              {2.0 / 3, 0.0, -1.0, 0.5},
+                              {1.0 / 6, 0.5, 0.5, -0.5},
+                              {0.0, 0.0, 0.0, 1.0 / 6}};
+      // beta'(s) at s = (fb-1+k) - cJ as a polynomial in tJ:
+      //   d0 = (1-t)^2/2, d1 = 2t - 1.5t^2, d2 = -1/2 - t + 1.5t^2, d3 = -t^2/2
+      const double Dc[4][3] = {{0.5, -1.0, 0.5}, {0.0, 2.0, -1.5}, {-0.5, -1.0, 1.5}, {0.0, 0.0, -0.5}};
       double C[4][3] = {};
       for (int ii = 0; ii < 4; ++ii)
         for (int kk = 0; kk < 4; ++kk) {
-          const double t = T(fa - 1 + ii, fb - 1 + kk);
+          const double t = T(ii, fb - 1 + kk);
           if (t == 0.0) continue;
           for (int p = 0; p < 4; ++p)
             for (int r = 0; r < 3; ++r) C[p][r] += t * W[ii][p] * Dc[kk][r];
@@ -703,19 +712,12 @@ __global__ void __launch_bounds__(1024) k_mi_finalize(const FinalizeArgs a) {
       out[0] = make_float4((float)C[0][0], (float)C[0][1], (float)C[0][2], (float)C[1][0]);
       out[1] = make_float4((float)C[1][1], (float)C[1][2], (float)C[2][0], (float)C[2][1]);
       out[2] = make_float4((float)C[2][2], (float)C[3][0], (float)C[3][1], (float)C[3][2]);
+    } else {
+      reinterpret_cast<float2*>(a.T)[i] = make_float2((float)T(1, fb), (float)T(1, fb + 1));
     }
-  } else {
-    for (int i = tid; i < BMAX * BMAX; i += blockDim.x) {
-      const int ra = i / BMAX, rb = i - ra * BMAX;
-      reinterpret_cast<float2*>(a.T)[i] = make_float2((float)T(ra, rb), (float)T(ra, rb + 1));
-    }
+    // LNCC fusion reads the plain packed table for any bin count
+    if (a.T2) reinterpret_cast<float2*>(a.T2)[i] = make_float2((float)T(1, fb), (float)T(1, fb + 1));
   }
-  // LNCC fusion reads the plain packed table for any bin count
-  if (a.T2)
-    for (int i = tid; i < BMAX * BMAX; i += blockDim.x) {
-      const int ra = i / BMAX, rb = i - ra * BMAX;
-      reinterpret_cast<float2*>(a.T2)[i] = make_float2((float)T(ra, rb), (float)T(ra, rb + 1));
-    }
 }
 
 // ------------------------------------------------------------------ sweep 2
@@ -917,7 +919,9 @@ __global__ void __launch_bounds__(256) k_finish(const FinishArgs a) {
     if (a.loss && g_ffdp_device_error) {
       for (int i = 0; i < a.nloss; ++i) a.loss[i] = __int_as_float(0x7fc00000);  // a ring wait gave up: NaN
     } else if (a.loss) {
-      const double mi = a.has_mi ? a.scalars[0] : 0.0;
+      double mi = 0.0;
+      if (a.has_mi)
+        for (int r = 0; r < a.mi_rows; ++r) mi += a.scalars[r];  // fixed order
       const double lncc = a.has_lncc ? sm[kPCC][16] / a.N : 0.0;
       if (a.nloss == 3) {
         a.loss[0] = (float)(a.w_mi * (-mi) + a.w_lncc * (-lncc));
@@ -1049,9 +1053,9 @@ int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax) {
 cudaError_t launch_finalize(int bmax, const FinalizeArgs& a, cudaStream_t s) {
   note_launch_begin("k_mi_finalize", s);
   if (bmax == 32)
-    k_mi_finalize<32><<<1, 1024, 0, s>>>(a);
+    k_mi_finalize<32><<<32, 256, 0, s>>>(a);
   else
-    k_mi_finalize<64><<<1, 1024, 0, s>>>(a);
+    k_mi_finalize<64><<<64, 256, 0, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
