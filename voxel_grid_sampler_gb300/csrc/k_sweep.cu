@@ -746,7 +746,7 @@ struct S2Cfg {
 template <typename MT, int BMAX, bool MI, bool GATHER, bool BWD>
 __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, const Sweep2Args& a, float acc[12]) {
   const Geom& g = a.g;
-  if (!BWD) {
+  if constexpr (!BWD) {
 #pragma unroll
     for (int j = 0; j < 2; ++j)
       if (j < H.nv) a.dJ[H.lin + 32u * j] = mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], H.x[j]);
