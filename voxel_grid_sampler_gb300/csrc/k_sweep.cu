@@ -750,71 +750,71 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
 #pragma unroll
     for (int j = 0; j < 2; ++j)
       if (j < H.nv) a.dJ[H.lin + 32u * j] = mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], H.x[j]);
-    return;
-  }
-  float e[2][3];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    e[j][0] = e[j][1] = e[j][2] = 0.0f;
-    if (j >= H.nv) continue;
-    float gq0, gq1, gq2, gv;
-    if (GATHER) {
-      float m[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
-      const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
-      gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
-    } else {
-      // the stored slope of J and the given g
-      gq0 = H.rr[j][0];
-      gq1 = H.rr[j][1];
-      gq2 = H.rr[j][2];
-      gv = H.x[j];
-    }
-    e[j][0] = gv * gq0;
-    e[j][1] = gv * gq1;
-    e[j][2] = gv * gq2;
-    if (a.du) {
-      float o0, o1, o2;
-      if (g.k_diag) {
-        o0 = g.K[0] * e[j][0];
-        o1 = g.K[4] * e[j][1];
-        o2 = g.K[8] * e[j][2];
-      } else {
-        o0 = fmaf(g.K[0], e[j][0], fmaf(g.K[3], e[j][1], g.K[6] * e[j][2]));
-        o1 = fmaf(g.K[1], e[j][0], fmaf(g.K[4], e[j][1], g.K[7] * e[j][2]));
-        o2 = fmaf(g.K[2], e[j][0], fmaf(g.K[5], e[j][1], g.K[8] * e[j][2]));
-      }
-      float* dp = a.du + 3ull * (H.lin + 32u * j);
-      dp[0] = o0;
-      dp[1] = o1;
-      dp[2] = o2;
-    }
-    const float cx = (float)H.ix[j] - g.ctr[0];
-#pragma unroll
-    for (int r = 0; r < 3; ++r) acc[kPM + 3 * r] = fmaf(e[j][r], cx, acc[kPM + 3 * r]);
-  }
-  // the two voxels of a half share (y, z) unless a row ends between them:
-  // their y and z moments then take one product per half
-  const float s[3] = {e[0][0] + e[1][0], e[0][1] + e[1][1], e[0][2] + e[1][2]};
-#pragma unroll
-  for (int r = 0; r < 3; ++r) acc[kPS + r] += s[r];
-  if (H.nv == 2 && (H.iy[0] != H.iy[1] || H.iz[0] != H.iz[1])) {
+  } else {
+    float e[2][3];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float cy = (float)H.iy[j] - g.ctr[1], cz = (float)H.iz[j] - g.ctr[2];
+      e[j][0] = e[j][1] = e[j][2] = 0.0f;
+      if (j >= H.nv) continue;
+      float gq0, gq1, gq2, gv;
+      if (GATHER) {
+        float m[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
+        const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
+        gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
+      } else {
+        // the stored slope of J and the given g
+        gq0 = H.rr[j][0];
+        gq1 = H.rr[j][1];
+        gq2 = H.rr[j][2];
+        gv = H.x[j];
+      }
+      e[j][0] = gv * gq0;
+      e[j][1] = gv * gq1;
+      e[j][2] = gv * gq2;
+      if (a.du) {
+        float o0, o1, o2;
+        if (g.k_diag) {
+          o0 = g.K[0] * e[j][0];
+          o1 = g.K[4] * e[j][1];
+          o2 = g.K[8] * e[j][2];
+        } else {
+          o0 = fmaf(g.K[0], e[j][0], fmaf(g.K[3], e[j][1], g.K[6] * e[j][2]));
+          o1 = fmaf(g.K[1], e[j][0], fmaf(g.K[4], e[j][1], g.K[7] * e[j][2]));
+          o2 = fmaf(g.K[2], e[j][0], fmaf(g.K[5], e[j][1], g.K[8] * e[j][2]));
+        }
+        float* dp = a.du + 3ull * (H.lin + 32u * j);
+        dp[0] = o0;
+        dp[1] = o1;
+        dp[2] = o2;
+      }
+      const float cx = (float)H.ix[j] - g.ctr[0];
+#pragma unroll
+      for (int r = 0; r < 3; ++r) acc[kPM + 3 * r] = fmaf(e[j][r], cx, acc[kPM + 3 * r]);
+    }
+    // the two voxels of a half share (y, z) unless a row ends between them:
+    // their y and z moments then take one product per half
+    const float s[3] = {e[0][0] + e[1][0], e[0][1] + e[1][1], e[0][2] + e[1][2]};
+#pragma unroll
+    for (int r = 0; r < 3; ++r) acc[kPS + r] += s[r];
+    if (H.nv == 2 && (H.iy[0] != H.iy[1] || H.iz[0] != H.iz[1])) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float cy = (float)H.iy[j] - g.ctr[1], cz = (float)H.iz[j] - g.ctr[2];
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+          acc[kPM + 3 * r + 1] = fmaf(e[j][r], cy, acc[kPM + 3 * r + 1]);
+          acc[kPM + 3 * r + 2] = fmaf(e[j][r], cz, acc[kPM + 3 * r + 2]);
+        }
+      }
+    } else {
+      const float cy = (float)H.iy[0] - g.ctr[1], cz = (float)H.iz[0] - g.ctr[2];
 #pragma unroll
       for (int r = 0; r < 3; ++r) {
-        acc[kPM + 3 * r + 1] = fmaf(e[j][r], cy, acc[kPM + 3 * r + 1]);
-        acc[kPM + 3 * r + 2] = fmaf(e[j][r], cz, acc[kPM + 3 * r + 2]);
+        acc[kPM + 3 * r + 1] = fmaf(s[r], cy, acc[kPM + 3 * r + 1]);
+        acc[kPM + 3 * r + 2] = fmaf(s[r], cz, acc[kPM + 3 * r + 2]);
       }
-    }
-  } else {
-    const float cy = (float)H.iy[0] - g.ctr[1], cz = (float)H.iz[0] - g.ctr[2];
-#pragma unroll
-    for (int r = 0; r < 3; ++r) {
-      acc[kPM + 3 * r + 1] = fmaf(s[r], cy, acc[kPM + 3 * r + 1]);
-      acc[kPM + 3 * r + 2] = fmaf(s[r], cz, acc[kPM + 3 * r + 2]);
     }
   }
 }
