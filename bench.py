@@ -41,8 +41,17 @@ SINGLE_PASS_BYTES = {4: 4 + 4 + 12 + 12, 5: 2 + 2 + 12 + 12}
 #   k_sweep1  F + u + M read (+ J and dJ/dq written when LNCC is on)
 #   k_lncc    F + J read, dL/dJ written
 #   k_sweep2  MI: F + u + M read, du written;  LNCC: dL/dJ + dJ/dq read, du written
+#   (MI-only with stored J and slope: k_sweep1 also writes J + dJ/dq; k_sweep2
+#   reads F + J + dJ/dq and writes du)
 KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc": 4 + 4 + 4, "k_sweep2": 4 + 12 + 12},
                 5: {"k_sweep1": 2 + 12 + 2, "k_sweep2": 2 + 12 + 2 + 12}}
+KERNEL_BYTES_STORED = {5: {"k_sweep1": 2 + 12 + 2 + 4 + 12, "k_sweep2": 2 + 4 + 12 + 12}}
+
+
+def _kernel_bytes(args, wl):
+    if wl.w_lncc == 0.0 and args.store_slope and args.workload in KERNEL_BYTES_STORED:
+        return KERNEL_BYTES_STORED[args.workload]
+    return KERNEL_BYTES[args.workload]
 HBM_NOMINAL_GBS = 8000.0
 
 
@@ -238,7 +247,8 @@ def run_gpu(args, ws, rank, local):
     F, M, u = pair.F, pair.M, pair.u
     N = F.numel()
     T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
-    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
+                              store_slope=bool(args.store_slope))
     wsbuf = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P, dev)
     loss = torch.empty(3, device=dev)
     du = torch.empty(tuple(F.shape) + (3,), device=dev)
@@ -277,12 +287,35 @@ def run_gpu(args, ws, rank, local):
     ms = _max_over_ranks(ms, ws, dev)
     value = N * ws / (ms * 1e-3) / 1e9
 
+    # the other MI mode of an MI-only objective, timed the same way for reference
+    alt = None
+    if wl.w_lncc == 0.0:
+        P2 = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
+                                   store_slope=not args.store_slope)
+        ws2 = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P2, dev)
+        for _ in range(3):
+            ffdp.ffdp_objective(F, M, u, T, P2, loss, du, dA, dt, ws2, stream)
+        torch.cuda.synchronize(dev)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        n_alt = max(3, min(args.steps, 10))
+        a0.record(stream)
+        for _ in range(n_alt):
+            ffdp.ffdp_objective(F, M, u, T, P2, loss, du, dA, dt, ws2, stream)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        alt = {"mi_mode": _mi_mode(not args.store_slope), "ms_per_step": a0.elapsed_time(a1) / n_alt}
+        del ws2
+        torch.cuda.empty_cache()
+        step()  # leave the outputs of the timed mode in place
+        torch.cuda.synchronize(dev)
+
     # ---- end to end through the public API with host buffers
     if args.no_e2e:
         ms_e2e, h2d, d2h = float("nan"), 0, 0
     else:
         ms_e2e, h2d, d2h = _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws)
-    _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h)
+    _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h, alt)
 
 
 def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
@@ -355,7 +388,12 @@ def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
     return ms_e2e, h2d, d2h
 
 
-def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h):
+def _mi_mode(store):
+    return ("stored J and dJ/dp (16 B/voxel workspace), streaming gradient pass" if store
+            else "implicit (no per-voxel workspace), gradient pass gathers M again")
+
+
+def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h, alt=None):
     value = N * ws / (ms * 1e-3) / 1e9
     # ---- roofline of the dominant kernel (algorithmic bytes / its own time)
     peak, peak_kind = _peaks()
@@ -363,16 +401,16 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
     dom_name, (dom_n, dom_ms) = dom
     dom_avg = dom_ms / max(dom_n, 1)
     per_launch_voxels = N
-    bpv = KERNEL_BYTES[args.workload].get(dom_name, 0)
+    kb = _kernel_bytes(args, wl)
+    bpv = kb.get(dom_name, 0)
     achieved = bpv * per_launch_voxels / (dom_avg * 1e-3) / 1e9
     traffic = _traffic_per_launch(dom_name, wl.name, N)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,
                 "algorithmic_bytes_per_voxel": bpv, "peak_source": peak_kind,
-                "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": KERNEL_BYTES[args.workload].get(k, 0),
-                                "frac": KERNEL_BYTES[args.workload].get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3)
-                                        / 1e9 / peak}
-                            for k, v in kern.items() if k in KERNEL_BYTES[args.workload]}}
+                "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": kb.get(k, 0),
+                                "frac": kb.get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3) / 1e9 / peak}
+                            for k, v in kern.items() if k in kb}}
     step_gbs = ALGO_BYTES[args.workload] * N / (ms * 1e-3) / 1e9
     if rank != 0:
         return
@@ -384,7 +422,10 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
         "config": {"workload": wl.name, "shape": list(F.shape), "voxels": N,
                    "l2": "inputs larger than L2 (%.2f GB algorithmic bytes per step)"
                          % (ALGO_BYTES[args.workload] * N / 1e9),
-                   "parallelism": "independent pair per rank" if ws > 1 else "single GPU"},
+                   "parallelism": "independent pair per rank" if ws > 1 else "single GPU",
+                   "mi_mode": (_mi_mode(bool(args.store_slope)) if wl.w_lncc == 0.0
+                               else "LNCC on: J, dJ/dp and dL/dJ stored (20 B/voxel workspace)")},
+        "other_mode": alt,
         "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs,
                              "of_8tbs": step_gbs / HBM_NOMINAL_GBS,
                              "of_measured": step_gbs / peak,
@@ -422,6 +463,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--shape", type=int, default=0, help="cube edge overriding the workload size (profiling)")
+    ap.add_argument("--store-slope", type=int, default=1, choices=[0, 1],
+                    help="MI-only objectives: store J and dJ/dp (1) or stay implicit (0)")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if ws > 1:

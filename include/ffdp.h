@@ -92,11 +92,18 @@ typedef struct {
 } ffdp_lncc_params;
 
 /* Objective L = w_mi * (-MI) + w_lncc * (-LNCC).  A weight of 0 disables (does
- * not evaluate) that term; at least one weight must be non-zero. */
+ * not evaluate) that term; at least one weight must be non-zero.
+ * store_slope (MI-only objectives): 0 = fully implicit, the workspace does not
+ * grow with the volume and the gradient pass samples M again; 1 = the first
+ * pass also stores J and its slope dJ/dp in the workspace (16 bytes per
+ * voxel) and the gradient pass streams them instead of gathering M (faster
+ * where the memory is available).  Objectives with LNCC always store them.
+ * The results are the same in both modes up to rounding. */
 typedef struct {
   float w_mi, w_lncc;
   ffdp_mi_params mi;
   ffdp_lncc_params lncc;
+  int store_slope;
 } ffdp_objective_params;
 
 /* Operation codes for ffdp_workspace_bytes. */
@@ -113,8 +120,9 @@ enum {
  * the warped image J, its slope dJ/dp and the per-voxel dL/dJ (20 bytes per
  * voxel): the window sums read their halo instead of re-sampling it and the
  * sampler backward streams the slope instead of gathering M again; the
- * paper's fused LNCC keeps five such intermediates.  Queries the current
- * device's SM count. */
+ * paper's fused LNCC keeps five such intermediates.  An MI-only objective
+ * with store_slope = 1 holds J and dJ/dp (16 bytes per voxel).  Queries the
+ * current device's SM count. */
 size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void *params);
 
 /* Design 1, forward: J[i] = M(A x_i + t + S u_i) for every fixed voxel i.
@@ -169,9 +177,10 @@ ffdp_status ffdp_objective(const void *F, ffdp_dtype ft, ffdp_dims fdims, const 
  * the library image instead: ffdp_static_scratch_bytes() bytes (512 KiB) that
  * every GPU loading the library holds until the process exits.  It never
  * calls an allocator.
- *   - MI only: p->w_lncc must be 0 (LNCC keeps a per-voxel image that does not
- *     fit); a call whose scratch need (ffdp_workspace_bytes of the MI-only
- *     objective) exceeds the static scratch returns FFDP_ERR_UNSUPPORTED.
+ *   - MI only and implicit: p->w_lncc and p->store_slope must be 0 (per-voxel
+ *     images do not fit); a call whose scratch need (ffdp_workspace_bytes of
+ *     the MI-only objective) exceeds the static scratch returns
+ *     FFDP_ERR_UNSUPPORTED.
  *   - The first call on a device looks up the scratch's device address (a
  *     one-time set-up per device); make that first call before any stream
  *     capture.

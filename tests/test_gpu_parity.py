@@ -142,8 +142,9 @@ OBJ_CASES = [
 ]
 
 
+@pytest.mark.parametrize("store", [False, True])
 @pytest.mark.parametrize("fs,ms,dt_,wmi,wln,B,w", OBJ_CASES)
-def test_objective(ffdp, fs, ms, dt_, wmi, wln, B, w):
+def test_objective(ffdp, fs, ms, dt_, wmi, wln, B, w, store):
     rng = np.random.default_rng(sum(fs) + B + w)
     F = _vol(fs, 21, 0.0, 1.0, dt_)
     M = _vol(ms, 22, 0.0, 1.0, dt_)
@@ -152,7 +153,7 @@ def test_objective(ffdp, fs, ms, dt_, wmi, wln, B, w):
     fr = (float(F.min()), float(F.max()))
     mr = (float(M.min()), float(M.max()))
     T = ffdp.transform(A, t, S, xmin, xmax)
-    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5)
+    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5, store_slope=store)
     loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P)
     ref = oracle.objective(F, M, u, oracle_T(A, t, S, xmin, xmax),
                            oracle.ObjectiveParams(wmi, wln, B, fr, mr, w, 1e-5))
@@ -172,14 +173,16 @@ def test_objective(ffdp, fs, ms, dt_, wmi, wln, B, w):
 # MI is of order 1 instead of the near-zero MI of two independent volumes,
 # whose relative error is ill-conditioned.
 LARGE_CASES = [
-    # shape, dtype, w_mi, w_lncc, bins, window
-    ((41, 199, 257), np.float32, 1.0, 1.0, 64, 5),
-    ((41, 199, 257), np.float16, 1.0, 0.0, 32, 5),
+    # shape, dtype, w_mi, w_lncc, bins, window, store_slope
+    ((41, 199, 257), np.float32, 1.0, 1.0, 64, 5, False),
+    ((41, 199, 257), np.float16, 1.0, 0.0, 32, 5, False),
+    ((41, 199, 257), np.float16, 1.0, 0.0, 32, 5, True),
+    ((41, 199, 257), np.float32, 1.0, 0.0, 64, 5, True),
 ]
 
 
-@pytest.mark.parametrize("fs,dt_,wmi,wln,B,w", LARGE_CASES)
-def test_objective_large(ffdp, fs, dt_, wmi, wln, B, w):
+@pytest.mark.parametrize("fs,dt_,wmi,wln,B,w,store", LARGE_CASES)
+def test_objective_large(ffdp, fs, dt_, wmi, wln, B, w, store):
     rng = np.random.default_rng(sum(fs) + B)
     base = _vol(fs, 23, sigma=2.0)
     F = base.astype(dt_)
@@ -190,7 +193,7 @@ def test_objective_large(ffdp, fs, dt_, wmi, wln, B, w):
     fr = (float(F.min()), float(F.max()))
     mr = (float(M.min()), float(M.max()))
     T = ffdp.transform(A, t, S, xmin, xmax)
-    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5)
+    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5, store_slope=store)
     loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P)
     ref = oracle.objective(F, M, u, oracle_T(A, t, S, xmin, xmax),
                            oracle.ObjectiveParams(wmi, wln, B, fr, mr, w, 1e-5))
@@ -222,6 +225,10 @@ def test_workspace_is_independent_of_volume_size_for_mi(ffdp):
     a = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (64, 64, 64), p)
     b = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), p)
     assert a == b and a < (1 << 20)
+    # stored J and slope: 16 bytes per voxel on top
+    q = ffdp.objective_params(1.0, 0.0, 64, (0, 1), (0, 1), 5, store_slope=True)
+    c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), q)
+    assert 16 * 512 ** 3 <= c - a <= 16 * 512 ** 3 + 4096
 
 
 def test_no_device_error_after_runs(ffdp):

@@ -294,7 +294,9 @@ struct Ws {
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
 
-Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
+// ln: LNCC on (J, dJ/dq and dL/dJ per voxel); store: J and dJ/dq per voxel.
+Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N) {
+  const bool needJ = ln || store;
   Ws w;
   size_t o = 0;
   w.hist = o;
@@ -302,7 +304,7 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
   w.table = o;
   if (mi) o = al(o + mi_table_bytes(bmax));
   w.table2 = o;
-  if (mi && needJ) o = al(o + (size_t)bmax * bmax * 2 * sizeof(float));
+  if (mi && ln) o = al(o + (size_t)bmax * bmax * 2 * sizeof(float));
   w.scalars = o;
   o = al(o + 64 * sizeof(double));  // MI part per histogram row
   // two partial-record sets: the LNCC kernel's and the gradient sweep's
@@ -311,7 +313,7 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool needJ, uint64_t N) {
   w.J = o;
   if (needJ) o = al(o + (size_t)N * sizeof(float));
   w.G = o;
-  if (needJ) o = al(o + (size_t)N * sizeof(float));
+  if (ln) o = al(o + (size_t)N * sizeof(float));
   w.DG = o;  // dJ/dq, [N][3]
   if (needJ) o = al(o + (size_t)N * 3 * sizeof(float));
   w.total = o;
@@ -379,16 +381,16 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
   const uint64_t N = nvox(fixed);
   switch (op) {
     case FFDP_OP_GRID_SAMPLE_BWD:
-      return ws_layout(false, 32, max_parts(), false, N).total;
+      return ws_layout(false, 32, max_parts(), false, false, N).total;
     case FFDP_OP_MI: {
       const ffdp_mi_params* p = static_cast<const ffdp_mi_params*>(params);
       if (check_mi(p) != FFDP_OK) return 0;
-      return ws_layout(true, bmax_of(p->bins), max_parts(), false, N).total;
+      return ws_layout(true, bmax_of(p->bins), max_parts(), false, false, N).total;
     }
     case FFDP_OP_LNCC: {
       const ffdp_lncc_params* p = static_cast<const ffdp_lncc_params*>(params);
       if (check_lncc(p) != FFDP_OK) return 0;
-      return ws_layout(false, 32, max_parts(), false, N).total;
+      return ws_layout(false, 32, max_parts(), false, false, N).total;
     }
     case FFDP_OP_OBJECTIVE: {
       const ffdp_objective_params* p = static_cast<const ffdp_objective_params*>(params);
@@ -396,7 +398,7 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
       const bool mi = p->w_mi != 0.0f, ln = p->w_lncc != 0.0f;
       if (mi && check_mi(&p->mi) != FFDP_OK) return 0;
       if (ln && check_lncc(&p->lncc) != FFDP_OK) return 0;
-      return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln, N).total;
+      return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln, mi && p->store_slope != 0, N).total;
     }
   }
   return 0;
@@ -434,7 +436,7 @@ extern "C" ffdp_status ffdp_grid_sample_bwd(const void* M, ffdp_dtype mt, ffdp_d
   FFDP_TRY(check_dims(out_dims, "output"));
   if ((u && !aligned16(u)) || !aligned16(gJ) || (du && !aligned16(du)))
     return fail(FFDP_ERR_INVALID_ARGUMENT, "u, gJ and du must be 16-byte aligned");
-  const Ws w = ws_layout(false, 32, max_parts(), false, nvox(out_dims));
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(out_dims));
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   Sweep2Args a{};
   FFDP_TRY(make_geom(out_dims, mdims, T, a.g));
@@ -477,7 +479,7 @@ extern "C" ffdp_status ffdp_mi_fwd_bwd(const void* F, ffdp_dtype ft, const float
   if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
   const int bmax = bmax_of(p->bins);
-  const Ws w = ws_layout(true, bmax, max_parts(), false, nvox(dims));
+  const Ws w = ws_layout(true, bmax, max_parts(), false, false, nvox(dims));
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -543,7 +545,7 @@ extern "C" ffdp_status ffdp_lncc_fwd_bwd(const void* F, ffdp_dtype ft, const flo
   FFDP_TRY(check_lncc(p));
   if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
-  const Ws w = ws_layout(false, 32, max_parts(), false, nvox(dims));
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims));
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -593,7 +595,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, u and du must be 16-byte aligned");
   const int bmax = mi ? bmax_of(p->mi.bins) : 32;
   const uint64_t N = nvox(fdims);
-  const Ws w = ws_layout(mi, bmax, max_parts(), ln, N);
+  const bool store = ln || (mi && p->store_slope != 0);
+  const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N);
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -604,7 +607,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   float* table2 = (mi && ln) ? reinterpret_cast<float*>(wb + w.table2) : nullptr;
   double* scalars = reinterpret_cast<double*>(wb + w.scalars);
   double* partials = reinterpret_cast<double*>(wb + w.partials);
-  float* Jbuf = ln ? reinterpret_cast<float*>(wb + w.J) : nullptr;
+  float* Jbuf = store ? reinterpret_cast<float*>(wb + w.J) : nullptr;
+  float* DGbuf = store ? reinterpret_cast<float*>(wb + w.DG) : nullptr;
   const BinMap bf = mi ? bin_map(p->mi.f_lo, p->mi.f_hi, p->mi.bins) : BinMap{0, 1, 1, 0};
   const BinMap bj = mi ? bin_map(p->mi.m_lo, p->mi.m_hi, p->mi.bins) : BinMap{0, 1, 1, 0};
 
@@ -616,16 +620,16 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   a1.M = M;
   a1.u = u;
   a1.Jout = Jbuf;
-  a1.Gout = ln ? reinterpret_cast<float*>(wb + w.DG) : nullptr;
+  a1.Gout = DGbuf;
   a1.stall_tx = take_test_stall();
   a1.ghist = hist;
   a1.bf = bf;
   a1.bj = bj;
   a1.B = mi ? p->mi.bins : 32;
   a1.nIter = n_iter1(N);
-  // with LNCC, J and its slope dJ/dq are stored for the window kernel and the
-  // streaming sampler backward
-  const int m1 = mi ? (ln ? S1_HIST_WRITEJG : S1_HIST) : S1_WRITEJG;
+  // with LNCC (or store_slope), J and its slope dJ/dq are stored for the
+  // window kernel and the streaming gradient pass
+  const int m1 = mi ? (store ? S1_HIST_WRITEJG : S1_HIST) : S1_WRITEJG;
   FFDP_CUDA(launch_sweep1(m1, ft, mt, bmax, a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(m1, ft, mt, bmax)), s),
             "sweep 1 launch");
   if (mi) {
@@ -665,7 +669,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     Sweep2Args a2{};
     a2.g = g;
     a2.gbuf = Gbuf;
-    a2.dJdq = reinterpret_cast<const float*>(wb + w.DG);
+    a2.dJdq = DGbuf;
     a2.du = du;
     a2.partials = partials + (size_t)grid * kPartialStride;
     a2.nIter = n_iter2(N);
@@ -673,11 +677,15 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     FFDP_CUDA(launch_sweep2(S2_GBUF_DJ, 0, 0, 32, a2, grid2, s), "sampler backward launch");
     nparts = grid + grid2;
   } else {
+    // MI gradient and sampler backward: gathers M again, or streams the stored J and slope
+    const int m2 = store ? S2_MI_DJ : S2_MI;
     Sweep2Args a2{};
     a2.g = g;
     a2.F = F;
     a2.M = M;
     a2.u = u;
+    a2.Jin = Jbuf;
+    a2.dJdq = DGbuf;
     a2.du = du;
     a2.T = table;
     a2.partials = partials;
@@ -685,8 +693,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a2.bj = bj;
     a2.B = p->mi.bins;
     a2.nIter = n_iter2(N);
-    const int grid = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MI, ft, mt, bmax));
-    FFDP_CUDA(launch_sweep2(S2_MI, ft, mt, bmax, a2, grid, s), "sweep 2 launch");
+    const int grid = persistent_grid(a2.nIter, sweep2_ctas_per_sm(m2, ft, mt, bmax));
+    FFDP_CUDA(launch_sweep2(m2, ft, mt, bmax, a2, grid, s), "sweep 2 launch");
     nparts = grid;
   }
   FinishArgs f{};
@@ -761,6 +769,11 @@ extern "C" ffdp_status ffdp_objective_mi_static(const void* F, ffdp_dtype ft, ff
     return fail(FFDP_ERR_UNSUPPORTED,
                 "the workspace-free objective evaluates MI only (w_lncc must be 0): LNCC keeps a "
                 "per-voxel image that does not fit the %zu-byte static scratch",
+                kStaticScratchBytes);
+  if (p->store_slope != 0)
+    return fail(FFDP_ERR_UNSUPPORTED,
+                "the workspace-free objective is implicit (store_slope must be 0): stored J and "
+                "dJ/dp do not fit the %zu-byte static scratch",
                 kStaticScratchBytes);
   const size_t need = ffdp_workspace_bytes(FFDP_OP_OBJECTIVE, fdims, p);
   if (need == 0) {

@@ -25,9 +25,10 @@ namespace ffdp {
 enum Sweep1Mode { S1_HIST = 0, S1_HIST_WRITEJ = 1, S1_WRITEJ = 2, S1_HIST_JBUF = 3, S1_HIST_WRITEJG = 4, S1_WRITEJG = 5 };
 constexpr int kSweep1Modes = 6;
 // Sweep 2: MI gradient + sampler backward; sampler backward of a given g;
-// MI gradient of a given J; backward of a given g with the stored dJ/dq (no gathers).
-enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2, S2_GBUF_DJ = 3 };
-constexpr int kSweep2Modes = 4;
+// MI gradient of a given J; backward of a given g with the stored dJ/dq (no
+// gathers); MI gradient + backward from the stored J and dJ/dq (no gathers).
+enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2, S2_GBUF_DJ = 3, S2_MI_DJ = 4 };
+constexpr int kSweep2Modes = 5;
 enum LnccMode { LN_DJ = 0, LN_BWD = 1 };
 
 // Histogram sweep / forward sampler.
@@ -51,9 +52,9 @@ struct Sweep2Args {
   const void* F;
   const void* M;
   const float* u;
-  const float* Jin;   // S2_MI_JBUF
+  const float* Jin;   // S2_MI_JBUF, S2_MI_DJ
   const float* gbuf;  // S2_GBUF, S2_GBUF_DJ
-  const float* dJdq;  // S2_GBUF_DJ: [N][3] stored slope of J
+  const float* dJdq;  // S2_GBUF_DJ, S2_MI_DJ: [N][3] stored slope of J
   float* du;
   float* dJ;          // S2_MI_JBUF
   const float* T;     // packed MI table (scaled by w_mi * c' / N)

@@ -727,11 +727,11 @@ __global__ void __launch_bounds__(256) k_mi_finalize(const FinalizeArgs a) {
 // g (given gradient) or J (MI on a given J).
 template <typename FT, int BMAX, int MODE>
 struct S2Cfg {
-  static constexpr bool MI = MODE == S2_MI || MODE == S2_MI_JBUF;  // g from the MI table
-  static constexpr bool GATHER = MODE == S2_MI || MODE == S2_GBUF;  // resample J and dJ/dq
-  static constexpr bool VEC = GATHER || MODE == S2_GBUF_DJ;         // 3-vector stream: u or dJ/dq
-  static constexpr bool BWD = MODE != S2_MI_JBUF;                   // du and affine partials
-  static constexpr bool XS = MODE != S2_MI;                         // g (given) or J (given)
+  static constexpr bool MI = MODE == S2_MI || MODE == S2_MI_JBUF || MODE == S2_MI_DJ;  // g from the MI table
+  static constexpr bool GATHER = MODE == S2_MI || MODE == S2_GBUF;                     // resample J and dJ/dq
+  static constexpr bool VEC = GATHER || MODE == S2_GBUF_DJ || MODE == S2_MI_DJ;        // u or the stored dJ/dq
+  static constexpr bool BWD = MODE != S2_MI_JBUF;                                      // du and affine partials
+  static constexpr bool XS = MODE != S2_MI;                                            // g or J (given / stored)
   static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
   using RG1 = Ring<FT, VEC, MI, XS, 1, kSweep2Threads>;
   // as many ring slots (up to 4) as fit next to the table in 220 KiB
@@ -764,11 +764,11 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
         const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
         gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
       } else {
-        // the stored slope of J and the given g
+        // the stored slope of J, and g given or from the MI table at the stored J
         gq0 = H.rr[j][0];
         gq1 = H.rr[j][1];
         gq2 = H.rr[j][2];
-        gv = H.x[j];
+        gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], H.x[j]) : H.x[j];
       }
       e[j][0] = gv * gq0;
       e[j][1] = gv * gq1;
@@ -838,7 +838,7 @@ __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
   const MT* __restrict__ M = static_cast<const MT*>(a.M);
-  const float* X = MODE == S2_MI_JBUF ? a.Jin : a.gbuf;
+  const float* X = (MODE == S2_MI_JBUF || MODE == S2_MI_DJ) ? a.Jin : a.gbuf;
   const float* U = GATHER ? a.u : a.dJdq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (BWD && lane == 0)
@@ -1021,6 +1021,7 @@ static cudaError_t dispatch_sweep2(int mode, int ft, int mt, int bmax, const Swe
         case S2_GBUF: e = run_sweep2<float, MT, 32, S2_GBUF>(a, grid, s, occ); break;
         case S2_MI_JBUF: e = run_sweep2<FT, float, 32, S2_MI_JBUF>(a, grid, s, occ); break;
         case S2_GBUF_DJ: e = run_sweep2<float, float, 32, S2_GBUF_DJ>(a, grid, s, occ); break;
+        case S2_MI_DJ: e = run_sweep2<FT, float, 32, S2_MI_DJ>(a, grid, s, occ); break;
       }
     } else {
       switch (mode) {
@@ -1028,6 +1029,7 @@ static cudaError_t dispatch_sweep2(int mode, int ft, int mt, int bmax, const Swe
         case S2_GBUF: e = run_sweep2<float, MT, 32, S2_GBUF>(a, grid, s, occ); break;
         case S2_MI_JBUF: e = run_sweep2<FT, float, 64, S2_MI_JBUF>(a, grid, s, occ); break;
         case S2_GBUF_DJ: e = run_sweep2<float, float, 32, S2_GBUF_DJ>(a, grid, s, occ); break;
+        case S2_MI_DJ: e = run_sweep2<FT, float, 64, S2_MI_DJ>(a, grid, s, occ); break;
       }
     }
   }));

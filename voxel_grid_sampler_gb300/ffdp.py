@@ -51,7 +51,7 @@ class ffdp_lncc_params(ctypes.Structure):
 
 class ffdp_objective_params(ctypes.Structure):
     _fields_ = [("w_mi", ctypes.c_float), ("w_lncc", ctypes.c_float), ("mi", ffdp_mi_params),
-                ("lncc", ffdp_lncc_params)]
+                ("lncc", ffdp_lncc_params), ("store_slope", ctypes.c_int)]
 
 
 _lib = None
@@ -133,9 +133,10 @@ def lncc_params(window, eps=1e-5) -> ffdp_lncc_params:
     return ffdp_lncc_params(int(window), float(eps))
 
 
-def objective_params(w_mi, w_lncc, bins, f_range, m_range, window, eps=1e-5) -> ffdp_objective_params:
+def objective_params(w_mi, w_lncc, bins, f_range, m_range, window, eps=1e-5,
+                     store_slope=False) -> ffdp_objective_params:
     return ffdp_objective_params(float(w_mi), float(w_lncc), mi_params(bins, f_range, m_range),
-                                 lncc_params(window, eps))
+                                 lncc_params(window, eps), 1 if store_slope else 0)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
