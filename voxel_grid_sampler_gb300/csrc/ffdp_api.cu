@@ -359,7 +359,7 @@ unsigned n_iter2(uint64_t N) {
 
 // LNCC tiling for a fixed grid: persistent CTAs over (32 x TY) columns x z-chunks.
 void lncc_tiling(ffdp_dims f, int R, LnccArgs& a, int per_sm, int& grid) {
-  const int TY = R <= 2 ? 16 : 8;
+  const int TY = lncc_ty(R);
   a.tilesX = (int)((f.w + kLnccTX - 1) / kLnccTX);
   a.tilesY = (int)((f.h + TY - 1) / TY);
   const long long cols = (long long)a.tilesX * a.tilesY;

@@ -137,5 +137,23 @@ void note_launch_end(cudaStream_t s);
 
 constexpr int kMaxCtasPerSm = 8;
 constexpr int kLnccTX = 32;
+// LNCC tile height (rows of output voxels per CTA) for window radius <= 2, 3
+// and 4, the thread count of the register-history kernel (radius <= 3) and
+// the resident CTAs per SM it requests.
+#ifndef FFDP_LNCC_TY_SMALL
+#define FFDP_LNCC_TY_SMALL 16
+#endif
+#ifndef FFDP_LNCC_MINB
+#define FFDP_LNCC_MINB 2
+#endif
+#ifndef FFDP_LNCC_THREADS
+#define FFDP_LNCC_THREADS 256
+#endif
+#ifndef FFDP_LNCC_TY_MID
+#define FFDP_LNCC_TY_MID 8
+#endif
+constexpr int kLnccTYSmall = FFDP_LNCC_TY_SMALL;
+constexpr int kLnccRHThreads = FFDP_LNCC_THREADS;  // threads per CTA of the register-history LNCC kernel
+__host__ __device__ constexpr int lncc_ty(int R) { return R <= 2 ? kLnccTYSmall : (R == 3 ? FFDP_LNCC_TY_MID : 8); }
 
 }  // namespace ffdp

@@ -38,7 +38,7 @@ constexpr int kTX = kLnccTX;
 template <int R>
 struct LT {
   static constexpr int W = 2 * R + 1;
-  static constexpr int TY = R <= 2 ? 16 : 8;
+  static constexpr int TY = lncc_ty(R);
   static constexpr int E2W = kTX + 4 * R;  // multiple of 4
   static constexpr int E2H = TY + 4 * R;
   static constexpr int E1W = kTX + 2 * R;
@@ -527,12 +527,12 @@ template <int R>
 struct LTR {
   using L = LT<R>;
   static constexpr int W = L::W, TY = L::TY, E2W = L::E2W, E2H = L::E2H;
-  static constexpr int NOUT = TY * kTX / kThreads;       // outputs per thread
+  static constexpr int NOUT = TY * kTX / kLnccRHThreads;       // outputs per thread
   static constexpr int NCORE = TY * kTX;
   static constexpr int NHALO = E2H * E2W - NCORE;        // halo positions outside the outputs
-  static constexpr int NEXTRA = (NHALO + kThreads - 1) / kThreads;
+  static constexpr int NEXTRA = (NHALO + kLnccRHThreads - 1) / kLnccRHThreads;
   static constexpr int NSTG = NOUT + NEXTRA;
-  static_assert(NOUT * kThreads == NCORE, "outputs per thread");
+  static_assert(NOUT * kLnccRHThreads == NCORE, "outputs per thread");
   // Row stride of the z-sum buffer: the x pass reads 2-output items (16 bytes
   // of (S_J, S_F) pairs, 8 bytes of S_FJ per lane), E1S/2 items per row; the
   // stride makes a row continue the bank sequence of the previous one, so
@@ -572,7 +572,7 @@ __device__ __forceinline__ void halo_pos(int h, int& row, int& col) {
 }
 
 template <typename FT, int BMAX, int R>
-__global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
+__global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(const LnccArgs a) {
   using L = LT<R>;
   using Q = LTR<R>;
   constexpr int W = L::W, TY = L::TY, E2S = Q::ZS;
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
 
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
-  __shared__ double wsum[kThreads / 32][13];
+  __shared__ double wsum[kLnccRHThreads / 32][13];
   float2* zP = reinterpret_cast<float2*>(sm + Q::OFF_Z);
   float2* zQ = zP + L::E2H * E2S;
   float* zX = sm + Q::OFF_Z + 4 * L::E2H * E2S;
@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
       row = oy0 + i + 2 * R;
       col = ox + 2 * R;
     } else {
-      const int h = tid + (i - NOUT) * kThreads;
+      const int h = tid + (i - NOUT) * kLnccRHThreads;
       if (h < Q::NHALO) {
         halo_pos<R>(h, row, col);
       } else {
@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
             // neighbouring 16-byte vectors (no bank conflicts)
             constexpr int XG = E1S / 2;
             constexpr int NI = 2 + 2 * R;  // inputs of a 2-output run
-            for (int it = tid; it < L::E2H * XG; it += kThreads) {
+            for (int it = tid; it < L::E2H * XG; it += kLnccRHThreads) {
               const int row = it / XG, g2 = it - row * XG;
               float2 vP[NI], vQ[NI];
               float vX[NI];
@@ -758,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
             const int zc = zi - R;
             const bool zin = zc >= 0 && zc < g.fD;
             const bool zown = zc >= z0 && zc < z1;
-            for (int it = tid; it < E1W * YR; it += kThreads) {
+            for (int it = tid; it < E1W * YR; it += kLnccRHThreads) {
               const int x1 = it % E1W, ys = RUN * (it / E1W);
               auto rowP = [&](int row) { return row < L::E2H ? xP[row * E1S + x1] : make_float2(0.f, 0.f); };
               auto rowQ = [&](int row) { return row < L::E2H ? xQ[row * E1S + x1] : make_float2(0.f, 0.f); };
@@ -823,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
             // [E] x sums of the g-terms onto the 32 output columns, 2 per item
             constexpr int XG2 = kTX / 2;
             constexpr int NI = 2 + 2 * R;
-            for (int it = tid; it < E1H * XG2; it += kThreads) {
+            for (int it = tid; it < E1H * XG2; it += kLnccRHThreads) {
               const int row = it / XG2, g2 = it - row * XG2;
               float2 vP[NI];
               float vX[NI];
@@ -924,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_lncc_rh(const LnccArgs a) {
   if (tid < kPartialStride) {
     double s = 0.0;
     if (tid == kPCC)
-      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][kPCC];
+      for (int k = 0; k < kLnccRHThreads / 32; ++k) s += wsum[k][kPCC];
     a.partials[(size_t)blockIdx.x * kPartialStride + tid] = s;
   }
 }
@@ -950,9 +950,10 @@ static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* oc
   const size_t smem = smem_of<R>();
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kThreads, smem);
+  constexpr int nt = R <= 3 ? kLnccRHThreads : kThreads;
+  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, nt, smem);
   note_launch_begin("k_lncc", s);
-  k<<<grid, kThreads, smem, s>>>(a);
+  k<<<grid, nt, smem, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
