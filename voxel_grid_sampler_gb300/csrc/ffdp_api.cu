@@ -304,7 +304,8 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t 
   w.table = o;
   if (mi) o = al(o + mi_table_bytes(bmax));
   w.table2 = o;
-  if (mi && ln) o = al(o + (size_t)bmax * bmax * 2 * sizeof(float));
+  // the LNCC epilogue reads polynomial cells: the main table for 32 bins, this one for 64
+  if (mi && ln && bmax == 64) o = al(o + (size_t)bmax * bmax * 12 * sizeof(float));
   w.scalars = o;
   o = al(o + 64 * sizeof(double));  // MI part per histogram row
   // two partial-record sets: the LNCC kernel's and the gradient sweep's
@@ -604,7 +605,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   FFDP_TRY(make_geom(fdims, mdims, T, g));
   unsigned long long* hist = reinterpret_cast<unsigned long long*>(wb + w.hist);
   float* table = reinterpret_cast<float*>(wb + w.table);
-  float* table2 = (mi && ln) ? reinterpret_cast<float*>(wb + w.table2) : nullptr;
+  float* table2 = (mi && ln && bmax == 64) ? reinterpret_cast<float*>(wb + w.table2) : nullptr;
   double* scalars = reinterpret_cast<double*>(wb + w.scalars);
   double* partials = reinterpret_cast<double*>(wb + w.partials);
   float* Jbuf = store ? reinterpret_cast<float*>(wb + w.J) : nullptr;
@@ -652,7 +653,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a.F = F;
     a.J = Jbuf;
     a.dJ = Gbuf;
-    a.T = table2;
+    a.T = bmax == 64 ? table2 : table;  // polynomial cells
     a.partials = partials;
     a.bf = bf;
     a.bj = bj;

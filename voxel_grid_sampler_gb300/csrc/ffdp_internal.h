@@ -69,7 +69,7 @@ struct Sweep2Args {
 struct FinalizeArgs {
   const unsigned long long* ghist;
   float* T;        // gradient table of the linear sweep (polynomial cells for 32 bins)
-  float* T2;       // optional: T rows packed as float2 pairs (LNCC-fused gradient)
+  float* T2;       // optional: polynomial cells for 64 bins (LNCC-fused gradient)
   double* scalars; // [0 .. BMAX) = MI part of histogram row a
   int B;
   double N;

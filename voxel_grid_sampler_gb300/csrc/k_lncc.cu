@@ -77,7 +77,9 @@ size_t lncc_smem_bytes(int R, int /*bmax*/) {
   }
 }
 
-// MI partial gradient from T rows packed as float2 pairs (global, read through L1).
+// MI partial gradient from the polynomial cells of the MI table (global,
+// read through L1): per cell (floor cF, floor cJ) the 12 coefficients of the
+// bicubic-in-tF, biquadratic-in-tJ polynomial sum_{a,b} T beta beta'.
 template <int BMAX>
 __device__ __forceinline__ float mi_grad_ln(const float* __restrict__ T, const BinMap& bf, const BinMap& bj,
                                             float f, float j) {
@@ -85,16 +87,15 @@ __device__ __forceinline__ float mi_grad_ln(const float* __restrict__ T, const B
   float tf, tj;
   floor_split(bin_coord(bf, f), af, tf);
   floor_split(bin_coord(bj, j), aj, tj);
-  float wf[4], d[4];
-  bspline4(tf, 1.0f, wf);
-  bspline4_deriv(tj, d);
-  float s = 0.0f;
-  const float2* t2 = reinterpret_cast<const float2*>(T) + (af - 1) * BMAX + (aj - 1);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 p = __ldg(t2 + i * BMAX), q = __ldg(t2 + i * BMAX + 2);
-    s = fmaf(wf[i], fmaf(p.x, d[0], fmaf(p.y, d[1], fmaf(q.x, d[2], q.y * d[3]))), s);
-  }
+  const float4* c = reinterpret_cast<const float4*>(T) + 3 * (af * BMAX + aj);
+  const float4 c0 = __ldg(c), c1 = __ldg(c + 1), c2 = __ldg(c + 2);
+  // coefficients C[p][r] of tF^p tJ^r: c0 = (C00, C01, C02, C10), c1 = (C11, C12, C20, C21),
+  // c2 = (C22, C30, C31, C32)
+  const float p0 = fmaf(fmaf(c0.z, tj, c0.y), tj, c0.x);
+  const float p1 = fmaf(fmaf(c1.y, tj, c1.x), tj, c0.w);
+  const float p2 = fmaf(fmaf(c2.x, tj, c1.w), tj, c1.z);
+  const float p3 = fmaf(fmaf(c2.w, tj, c2.z), tj, c2.y);
+  const float s = fmaf(fmaf(fmaf(p3, tf, p2), tf, p1), tf, p0);
   return (j >= bj.lo && j <= bj.hi) ? s : 0.0f;
 }
 

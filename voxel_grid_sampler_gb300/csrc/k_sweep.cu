@@ -689,34 +689,37 @@ __global__ void __launch_bounds__(256) k_mi_finalize(const FinalizeArgs a) {
   }
   const double ts = a.tscale;
   auto T = [&](int q, int c) -> double { return Ts[q][c + 1] * ts; };  // row a-1+q, column c
+  // polynomial cell (row, fb): C[p][r] = sum_{ii,kk} T(row-1+ii, fb-1+kk) W[ii][p] D[kk][r]
+  auto poly_cell = [&](int fb, float4* out) {
+    const double W[4][4] = {{1.0 / 6, -0.5, 0.5, -1.0 / 6},
+                            {2.0 / 3, 0.0, -1.0, 0.5},
+                            {1.0 / 6, 0.5, 0.5, -0.5},
+                            {0.0, 0.0, 0.0, 1.0 / 6}};
+    // beta'(s) at s = (fb-1+k) - cJ as a polynomial in tJ:
+    //   d0 = (1-t)^2/2, d1 = 2t - 1.5t^2, d2 = -1/2 - t + 1.5t^2, d3 = -t^2/2
+    const double Dc[4][3] = {{0.5, -1.0, 0.5}, {0.0, 2.0, -1.5}, {-0.5, -1.0, 1.5}, {0.0, 0.0, -0.5}};
+    double C[4][3] = {};
+    for (int ii = 0; ii < 4; ++ii)
+      for (int kk = 0; kk < 4; ++kk) {
+        const double t = T(ii, fb - 1 + kk);
+        if (t == 0.0) continue;
+        for (int p = 0; p < 4; ++p)
+          for (int r = 0; r < 3; ++r) C[p][r] += t * W[ii][p] * Dc[kk][r];
+      }
+    out[0] = make_float4((float)C[0][0], (float)C[0][1], (float)C[0][2], (float)C[1][0]);
+    out[1] = make_float4((float)C[1][1], (float)C[1][2], (float)C[2][0], (float)C[2][1]);
+    out[2] = make_float4((float)C[2][2], (float)C[3][0], (float)C[3][1], (float)C[3][2]);
+  };
   if (tid < BMAX) {
     const int fb = tid, i = row * BMAX + fb;
     if constexpr (BMAX == 32) {
-      // cell (row, fb): C[p][r] = sum_{ii,kk} T(row-1+ii, fb-1+kk) W[ii][p] D[kk][r]
-      const double W[4][4] = {{1.0 / 6, -0.5, 0.5, -1.0 / 6},
-                              {2.0 / 3, 0.0, -1.0, 0.5},
-                              {1.0 / 6, 0.5, 0.5, -0.5},
-                              {0.0, 0.0, 0.0, 1.0 / 6}};
-      // beta'(s) at s = (fb-1+k) - cJ as a polynomial in tJ:
-      //   d0 = (1-t)^2/2, d1 = 2t - 1.5t^2, d2 = -1/2 - t + 1.5t^2, d3 = -t^2/2
-      const double Dc[4][3] = {{0.5, -1.0, 0.5}, {0.0, 2.0, -1.5}, {-0.5, -1.0, 1.5}, {0.0, 0.0, -0.5}};
-      double C[4][3] = {};
-      for (int ii = 0; ii < 4; ++ii)
-        for (int kk = 0; kk < 4; ++kk) {
-          const double t = T(ii, fb - 1 + kk);
-          if (t == 0.0) continue;
-          for (int p = 0; p < 4; ++p)
-            for (int r = 0; r < 3; ++r) C[p][r] += t * W[ii][p] * Dc[kk][r];
-        }
-      float4* out = reinterpret_cast<float4*>(a.T) + 3 * i;
-      out[0] = make_float4((float)C[0][0], (float)C[0][1], (float)C[0][2], (float)C[1][0]);
-      out[1] = make_float4((float)C[1][1], (float)C[1][2], (float)C[2][0], (float)C[2][1]);
-      out[2] = make_float4((float)C[2][2], (float)C[3][0], (float)C[3][1], (float)C[3][2]);
+      poly_cell(fb, reinterpret_cast<float4*>(a.T) + 3 * i);
     } else {
+      // rows of T packed as float2 pairs for the sweeps; polynomial cells for
+      // the LNCC epilogue when requested
       reinterpret_cast<float2*>(a.T)[i] = make_float2((float)T(1, fb), (float)T(1, fb + 1));
+      if (a.T2) poly_cell(fb, reinterpret_cast<float4*>(a.T2) + 3 * i);
     }
-    // LNCC fusion reads the plain packed table for any bin count
-    if (a.T2) reinterpret_cast<float2*>(a.T2)[i] = make_float2((float)T(1, fb), (float)T(1, fb + 1));
   }
 }
 
