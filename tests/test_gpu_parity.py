@@ -139,6 +139,9 @@ OBJ_CASES = [
     ((18, 21, 35), (18, 21, 35), np.float32, 0.7, 0.0, 64, 5),
     ((18, 21, 35), (18, 21, 35), np.float32, 0.0, 1.3, 32, 7),
     ((17, 19, 37), (17, 19, 37), np.float16, 1.0, 0.5, 48, 3),
+    # window 9 (the shared-memory plane-ring kernel) with the MI term fused, both table sizes
+    ((16, 18, 40), (16, 18, 40), np.float32, 1.0, 1.0, 64, 9),
+    ((15, 17, 33), (15, 17, 33), np.float16, 1.0, 0.5, 32, 9),
 ]
 
 
