@@ -546,6 +546,65 @@ __device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __rest
   }
 }
 
+// Non-gathering passes (streamed J / g and slope): a whole chunk per step,
+// one wait, one refill and one coordinate seek for the lane's four voxels.
+template <typename FT, bool LF, bool LU, bool LX, class WR, int NST>
+__device__ __forceinline__ void prepare_chunk(Half& A, Half& B, const Geom& g, const FT* __restrict__ F,
+                                              const float* u, const float* X, WR& wr, RingSched<WR, NST>& rs,
+                                              unsigned it, unsigned k, unsigned long long pol) {
+  const int lane = threadIdx.x & 31;
+  const unsigned ch = rs.chunk(it);
+  const unsigned lin0 = ch * (32 * kVPT) + lane;
+  const int nvc = it < rs.nIter ? lane_count(lin0, g.N) : 0;
+  A.lin = lin0;
+  B.lin = lin0 + 64u;
+  A.nv = min(nvc, 2);
+  B.nv = min(max(nvc - 2, 0), 2);
+  const bool streamed = wr.tx && it < rs.nIter && ch < rs.nFull;
+  bool ok = true;
+  if (streamed) ok = rs.wait(wr, k);
+  const int s = k % NST;
+  int x = 0, y = 0, z = 0;
+  if (nvc > 0) lin_to_xyz(g, lin0, x, y, z);
+#pragma unroll
+  for (int v = 0; v < kVPT; ++v) {
+    Half& H = v < 2 ? A : B;
+    const int j = v & 1;
+    const unsigned lin = lin0 + 32u * v;
+    H.f[j] = H.x[j] = H.rr[j][0] = H.rr[j][1] = H.rr[j][2] = 0.0f;
+    if (streamed) {
+      if (ok) {
+        const int e = lane + 32 * v;
+        if (LF) H.f[j] = to_f(wr.template f_of<FT>(s)[e]);
+        if (LU && wr.has_u) {
+          H.rr[j][0] = wr.u_of(s)[3 * e + 0];
+          H.rr[j][1] = wr.u_of(s)[3 * e + 1];
+          H.rr[j][2] = wr.u_of(s)[3 * e + 2];
+        }
+        if (LX) H.x[j] = wr.x_of(s)[e];
+      }
+    } else if (v < nvc) {
+      if (LF) H.f[j] = load1(F + lin);
+      if (LU && u) {
+        H.rr[j][0] = __ldg(u + 3ull * lin + 0);
+        H.rr[j][1] = __ldg(u + 3ull * lin + 1);
+        H.rr[j][2] = __ldg(u + 3ull * lin + 2);
+      }
+      if (LX) H.x[j] = __ldg(X + lin);
+    }
+    if (v > 0 && v < nvc) {
+      if (x + 32 < g.fW)
+        x += 32;
+      else
+        lin_to_xyz(g, lin, x, y, z);
+    }
+    H.ix[j] = x;
+    H.iy[j] = y;
+    H.iz[j] = z;
+  }
+  if (streamed) rs.template refill<FT>(wr, k, it, u, F, X, pol);
+}
+
 // ------------------------------------------------------------------ sweep 1
 // Sampling (or reading J) plus, per mode, the histogram and/or a J store
 // (and, for the LNCC objective, a store of the slope dJ/dq, so that its
@@ -858,13 +917,20 @@ __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a
   LaneWalk w;
   Half A, B;
   unsigned k = 0;
-  prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  if constexpr (GATHER) prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
-    prepare<FT, MT, MI, VEC, XS, GATHER>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
-    sweep2_half<MT, BMAX, MI, GATHER, BWD>(A, tsm, a, acc);
-    prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
-    sweep2_half<MT, BMAX, MI, GATHER, BWD>(B, tsm, a, acc);
+    if constexpr (GATHER) {
+      // gathers of the next half are in flight while the current one computes
+      prepare<FT, MT, MI, VEC, XS, GATHER>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
+      sweep2_half<MT, BMAX, MI, GATHER, BWD>(A, tsm, a, acc);
+      prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+      sweep2_half<MT, BMAX, MI, GATHER, BWD>(B, tsm, a, acc);
+    } else {
+      prepare_chunk<FT, MI, VEC, XS>(A, B, g, F, U, X, wr, rs, it, k, pol);
+      sweep2_half<MT, BMAX, MI, GATHER, BWD>(A, tsm, a, acc);
+      sweep2_half<MT, BMAX, MI, GATHER, BWD>(B, tsm, a, acc);
+    }
     if (BWD && ++pending == kFoldEvery) {
 #pragma unroll
       for (int q = 0; q < 12; ++q) {
