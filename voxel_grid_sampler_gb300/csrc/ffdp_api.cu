@@ -358,20 +358,20 @@ unsigned n_iter2(uint64_t N) {
     if (_e != cudaSuccess) return cuda_fail(_e, where); \
   } while (0)
 
-// LNCC tiling for a fixed grid: persistent CTAs over (32 x TY) columns x z-chunks.
+// LNCC tiling for a fixed grid: one resident CTA per slot, each taking an
+// equal run of the (column, plane) sequence over (32 x TY) columns, at least
+// 32 planes per CTA.
 void lncc_tiling(ffdp_dims f, int R, LnccArgs& a, int per_sm, int& grid) {
   const int TY = lncc_ty(R);
   a.tilesX = (int)((f.w + kLnccTX - 1) / kLnccTX);
   a.tilesY = (int)((f.h + TY - 1) / TY);
-  const long long cols = (long long)a.tilesX * a.tilesY;
+  const long long total = (long long)a.tilesX * a.tilesY * (long long)f.d;
   const long long slots = (long long)sm_count() * per_sm;
-  // z chunks: enough tiles to fill every resident CTA twice, >= 32 planes each
-  int tz = (int)f.d;
-  while (cols * ((f.d + tz - 1) / tz) < 2 * slots && tz > 32) tz = (tz + 1) / 2;
-  a.tz = tz;
-  const long long ntiles = cols * ((f.d + tz - 1) / tz);
-  grid = (int)(ntiles < slots ? ntiles : slots);
-  if (grid < 1) grid = 1;
+  long long n = (total + 31) / 32;
+  if (n > slots) n = slots;
+  if (n < 1) n = 1;
+  a.per = (total + n - 1) / n;
+  grid = (int)((total + a.per - 1) / a.per);
 }
 
 }  // namespace

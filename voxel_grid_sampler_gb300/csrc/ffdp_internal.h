@@ -93,7 +93,8 @@ struct LnccArgs {
   float eps;
   float inv_n;     // 1 / window^3
   float gscale;    // -w_lncc / N
-  int tilesX, tilesY, tz;  // tile grid and z planes per CTA
+  int tilesX, tilesY;  // tile grid (32 x TY columns)
+  long long per;       // (column, plane) pairs per CTA
 };
 
 // Reduction of per-CTA partials into dA, dt and the loss values.

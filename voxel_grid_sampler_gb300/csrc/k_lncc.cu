@@ -99,6 +99,30 @@ __device__ __forceinline__ float mi_grad_ln(const float* __restrict__ T, const B
   return (j >= bj.lo && j <= bj.hi) ? s : 0.0f;
 }
 
+// Work of one CTA: an equal share (a.per planes) of the sequence of (column,
+// plane) pairs, columns outermost, cut at column boundaries into z segments.
+// Every segment costs 4R extra planes of window halo, against a round-robin
+// of fixed z chunks whose last round leaves most CTAs idle.
+struct LnccSegs {
+  long long u, end;
+  int D, tilesX;
+  __device__ explicit LnccSegs(const LnccArgs& a) : D(a.g.fD), tilesX(a.tilesX) {
+    const long long total = (long long)a.tilesX * a.tilesY * a.g.fD;
+    u = (long long)blockIdx.x * a.per;
+    end = min(total, u + a.per);
+  }
+  __device__ bool next(int& tx, int& ty, int& z0, int& z1) {
+    if (u >= end) return false;
+    const long long col = u / D;
+    z0 = (int)(u - col * D);
+    z1 = (int)min((long long)D, z0 + (end - u));
+    tx = (int)(col % tilesX);
+    ty = (int)(col / tilesX);
+    u += z1 - z0;
+    return true;
+  }
+};
+
 __device__ __forceinline__ float rcp_approx(float x) {
   float r;
   asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -167,16 +191,10 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
     }
   };
 
-  const int chunksZ = (g.fD + a.tz - 1) / a.tz;
-  const int ntiles = a.tilesX * a.tilesY * chunksZ;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    int t = tile;
-    const int tx = t % a.tilesX;
-    t /= a.tilesX;
-    const int ty = t % a.tilesY;
-    const int tzc = t / a.tilesY;
-    const int x0 = tx * kTX, y0 = ty * TY, z0 = tzc * a.tz;
-    const int z1 = min(z0 + a.tz, g.fD);
+  LnccSegs seg(a);
+  int tx, ty, z0, z1;
+  while (seg.next(tx, ty, z0, z1)) {
+    const int x0 = tx * kTX, y0 = ty * TY;
     const int nsteps = (z1 - z0) + 4 * R;
 
     // output positions of this thread
@@ -646,16 +664,10 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
     }
   };
 
-  const int chunksZ = (g.fD + a.tz - 1) / a.tz;
-  const int ntiles = a.tilesX * a.tilesY * chunksZ;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    int t = tile;
-    const int tx = t % a.tilesX;
-    t /= a.tilesX;
-    const int ty = t % a.tilesY;
-    const int tzc = t / a.tilesY;
-    const int x0 = tx * kTX, y0 = ty * TY, z0 = tzc * a.tz;
-    const int z1 = min(z0 + a.tz, g.fD);
+  LnccSegs seg(a);
+  int tx, ty, z0, z1;
+  while (seg.next(tx, ty, z0, z1)) {
+    const int x0 = tx * kTX, y0 = ty * TY;
     const int nsteps = (z1 - z0) + 4 * R;
 #pragma unroll
     for (int i = 0; i < NSTG; ++i) {
