@@ -39,11 +39,12 @@ ALGO_BYTES = {4: 2 * (4 + 12 + 4) + 12, 5: 2 * (2 + 12 + 2) + 12}
 SINGLE_PASS_BYTES = {4: 4 + 4 + 12 + 12, 5: 2 + 2 + 12 + 12}
 # Algorithmic bytes per voxel of each kernel of the objective:
 #   k_sweep1  F + u + M read (+ J and dJ/dq written when LNCC is on)
-#   k_lncc    F + J read, dL/dJ written
-#   k_sweep2  MI: F + u + M read, du written;  LNCC: dL/dJ + dJ/dq read, du written
+#   k_lncc    F + J + dJ/dq read, du written (window sums, dL/dJ and the
+#             sampler backward in one kernel)
+#   k_sweep2  MI: F + u + M read, du written
 #   (MI-only with stored J and slope: k_sweep1 also writes J + dJ/dq; k_sweep2
 #   reads F + J + dJ/dq and writes du)
-KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc": 4 + 4 + 4, "k_sweep2": 4 + 12 + 12},
+KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc": 4 + 4 + 12 + 12},
                 5: {"k_sweep1": 2 + 12 + 2, "k_sweep2": 2 + 12 + 2 + 12}}
 KERNEL_BYTES_STORED = {5: {"k_sweep1": 2 + 12 + 2 + 4 + 12, "k_sweep2": 2 + 4 + 12 + 12}}
 
@@ -430,7 +431,7 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
                          % (ALGO_BYTES[args.workload] * N / 1e9),
                    "parallelism": "independent pair per rank" if ws > 1 else "single GPU",
                    "mi_mode": (_mi_mode(bool(args.store_slope)) if wl.w_lncc == 0.0
-                               else "LNCC on: J, dJ/dp and dL/dJ stored (20 B/voxel workspace)")},
+                               else "LNCC on: J and dJ/dp stored (16 B/voxel workspace)")},
         "other_mode": alt,
         "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs,
                              "of_8tbs": step_gbs / HBM_NOMINAL_GBS,

@@ -117,11 +117,11 @@ enum {
 /* Bytes of device workspace a call of `op` on fixed grid `fixed` needs (0 for
  * an invalid request).  MI and the sampler need O(bins^2 + #SMs) bytes,
  * independent of the volume size.  An objective with LNCC enabled also holds
- * the warped image J, its slope dJ/dp and the per-voxel dL/dJ (20 bytes per
- * voxel): the window sums read their halo instead of re-sampling it and the
- * sampler backward streams the slope instead of gathering M again; the
- * paper's fused LNCC keeps five such intermediates.  An MI-only objective
- * with store_slope = 1 holds J and dJ/dp (16 bytes per voxel).  Queries the
+ * the warped image J and its slope dJ/dp (16 bytes per voxel): the window
+ * sums read their halo instead of re-sampling it and the sampler backward,
+ * done in the window kernel's epilogue, reads the slope instead of gathering
+ * M again; the paper's fused LNCC keeps five such intermediates.  An MI-only
+ * objective with store_slope = 1 holds the same two buffers.  Queries the
  * current device's SM count. */
 size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void *params);
 

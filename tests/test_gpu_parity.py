@@ -232,6 +232,11 @@ def test_workspace_is_independent_of_volume_size_for_mi(ffdp):
     q = ffdp.objective_params(1.0, 0.0, 64, (0, 1), (0, 1), 5, store_slope=True)
     c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), q)
     assert 16 * 512 ** 3 <= c - a <= 16 * 512 ** 3 + 4096
+    # LNCC on: the same two per-voxel buffers (the sampler backward runs in the
+    # window kernel's epilogue), plus the 64-bin polynomial cells
+    r = ffdp.objective_params(0.5, 0.5, 64, (0, 1), (0, 1), 5)
+    d = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), r)
+    assert 16 * 512 ** 3 <= d - a <= 16 * 512 ** 3 + 64 * 64 * 12 * 4 + 4096
 
 
 def test_no_device_error_after_runs(ffdp):

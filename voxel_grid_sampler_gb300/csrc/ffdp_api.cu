@@ -289,12 +289,12 @@ int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
 
 // Workspace layout (byte offsets, 256-aligned).
 struct Ws {
-  size_t hist, table, table2, scalars, partials, J, G, DG, total;
+  size_t hist, table, table2, scalars, partials, J, DG, total;
 };
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// ln: LNCC on (J, dJ/dq and dL/dJ per voxel); store: J and dJ/dq per voxel.
+// ln: LNCC on; ln or store: J and dJ/dq per voxel.
 Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N) {
   const bool needJ = ln || store;
   Ws w;
@@ -308,13 +308,10 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t 
   if (mi && ln && bmax == 64) o = al(o + (size_t)bmax * bmax * 12 * sizeof(float));
   w.scalars = o;
   o = al(o + 64 * sizeof(double));  // MI part per histogram row
-  // two partial-record sets: the LNCC kernel's and the gradient sweep's
-  w.partials = o;
-  o = al(o + 2 * max_parts * kPartialStride * sizeof(double));
+  w.partials = o;  // one record per CTA of the last kernel of the path
+  o = al(o + max_parts * kPartialStride * sizeof(double));
   w.J = o;
   if (needJ) o = al(o + (size_t)N * sizeof(float));
-  w.G = o;
-  if (ln) o = al(o + (size_t)N * sizeof(float));
   w.DG = o;  // dJ/dq, [N][3]
   if (needJ) o = al(o + (size_t)N * 3 * sizeof(float));
   w.total = o;
@@ -646,13 +643,14 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   }
   int nparts = 0;
   if (ln) {
-    // LNCC window kernel: g = dL/dJ (LNCC term + MI term from on-chip J, F)
-    float* Gbuf = reinterpret_cast<float*>(wb + w.G);
+    // LNCC window kernel: g = dL/dJ (LNCC term + MI term from on-chip J, F),
+    // then the sampler backward from the stored slope (du, affine partials)
     LnccArgs a{};
     a.g = g;
     a.F = F;
     a.J = Jbuf;
-    a.dJ = Gbuf;
+    a.dJdq = DGbuf;
+    a.du = du;
     a.T = bmax == 64 ? table2 : table;  // polynomial cells
     a.partials = partials;
     a.bf = bf;
@@ -664,19 +662,9 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a.gscale = (float)(-(double)p->w_lncc / (double)N);
     const int bm = mi ? bmax : 0;
     int grid = 1;
-    lncc_tiling(fdims, a.R, a, lncc_ctas_per_sm(LN_DJ, ft, 0, bm, a.R), grid);
-    FFDP_CUDA(launch_lncc(LN_DJ, ft, 0, bm, a, grid, s), "LNCC window launch");
-    // sampler backward of g from the stored slope: du, affine partials
-    Sweep2Args a2{};
-    a2.g = g;
-    a2.gbuf = Gbuf;
-    a2.dJdq = DGbuf;
-    a2.du = du;
-    a2.partials = partials + (size_t)grid * kPartialStride;
-    a2.nIter = n_iter2(N);
-    const int grid2 = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_GBUF_DJ, 0, 0, 32));
-    FFDP_CUDA(launch_sweep2(S2_GBUF_DJ, 0, 0, 32, a2, grid2, s), "sampler backward launch");
-    nparts = grid + grid2;
+    lncc_tiling(fdims, a.R, a, lncc_ctas_per_sm(LN_DU, ft, 0, bm, a.R), grid);
+    FFDP_CUDA(launch_lncc(LN_DU, ft, 0, bm, a, grid, s), "LNCC window launch");
+    nparts = grid;
   } else {
     // MI gradient and sampler backward: gathers M again, or streams the stored J and slope
     const int m2 = store ? S2_MI_DJ : S2_MI;

@@ -29,7 +29,7 @@ constexpr int kSweep1Modes = 6;
 // gathers); MI gradient + backward from the stored J and dJ/dq (no gathers).
 enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2, S2_GBUF_DJ = 3, S2_MI_DJ = 4 };
 constexpr int kSweep2Modes = 5;
-enum LnccMode { LN_DJ = 0, LN_BWD = 1 };
+enum LnccMode { LN_DJ = 0, LN_DU = 1 };  // write dL/dJ; or du and affine partials from the stored slope
 
 // Histogram sweep / forward sampler.
 struct Sweep1Args {
@@ -80,13 +80,12 @@ struct FinalizeArgs {
 struct LnccArgs {
   const void* F;
   const float* J;
-  const void* M;
-  const float* u;
-  float* du;
-  float* dJ;
+  const float* dJdq;  // LN_DU: [N][3] stored slope of J
+  float* du;          // LN_DU: [N][3] or NULL (affine partials only)
+  float* dJ;          // LN_DJ: [N] dL/dJ or NULL
   const float* T;
   double* partials;
-  Geom g;          // fixed-grid extents always valid; sampler fields for LN_BWD
+  Geom g;          // fixed-grid extents always valid; K and ctr for LN_DU
   BinMap bf, bj;
   int B;
   int R;           // window radius
@@ -128,7 +127,6 @@ unsigned take_test_stall();
 cudaError_t take_device_error(unsigned* v);
 int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax);
 int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax);
-size_t lncc_smem_bytes(int R, int bmax_or0);
 size_t mi_table_bytes(int bmax);
 int lncc_ctas_per_sm(int mode, int ft, int mt, int bmax_or0, int R);
 

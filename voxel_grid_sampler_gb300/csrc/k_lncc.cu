@@ -65,17 +65,69 @@ struct LT {
 template <int R>
 struct LTR;
 
-template <int R>
-static size_t smem_of();
+// LN_DU: the stored slope dJ/dq of a later step's output plane (TY x 32
+// voxels, 3 floats each), staged in shared memory by asynchronous copies so
+// that the epilogue does not wait on DRAM.  Three slots: the copy for step
+// s + 1 is issued at the start of step s, waited for (by its issuing thread)
+// before the first barrier of step s + 1 and read after it; its slot was
+// last read in step s - 2, before the first barrier of step s - 1.
+template <int TY>
+struct SlopeStage {
+  static constexpr int ROW = 3 * kTX;       // floats per staged row
+  static constexpr int SLOT = TY * ROW;     // floats per slot
+  static constexpr int FLOATS = 3 * SLOT;   // three slots
+};
 
-size_t lncc_smem_bytes(int R, int /*bmax*/) {
-  switch (R) {
-    case 1: return smem_of<1>();
-    case 2: return smem_of<2>();
-    case 3: return smem_of<3>();
-    default: return smem_of<4>();
-  }
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+
+// Issue the copies of one output plane (none if src is null) of the tile into
+// slot, then commit one group (possibly empty).  src: the slope of the tile's
+// first voxel in that plane; rs: floats per grid row.  Full tiles of a grid
+// whose rows are a multiple of 4 voxels (every tile row then starts 16-byte
+// aligned) take 16-byte copies, 24 per row; edge tiles and other widths take
+// 4-byte copies.
+template <int TY, int NT>
+__device__ __forceinline__ void stage_slope(float* slot, const float* src, const Geom& g, int x0, int y0, bool full,
+                                            int tid) {
+  constexpr int ROW = SlopeStage<TY>::ROW;
+  const size_t rs = 3 * (size_t)g.fW;
+  if (src) {
+    if (full) {
+      constexpr int CPR = ROW / 4;
+#pragma unroll
+      for (int c0 = 0; c0 < TY * CPR; c0 += NT) {
+        const int c = c0 + tid;
+        if (c < TY * CPR) {
+          const int r = c / CPR, k = c - r * CPR;
+          cp_async16(slot + r * ROW + 4 * k, src + r * rs + 4 * k);
+        }
+      }
+    } else {
+      const int ncol = min(kTX, g.fW - x0), nrow = min(TY, g.fH - y0);
+      const int cpr = 3 * ncol;
+      for (int c = tid; c < nrow * cpr; c += NT) {
+        const int r = c / cpr, k = c - r * cpr;
+        cp_async4(slot + r * ROW + k, src + r * rs + k);
+      }
+    }
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// all but the most recent group of this thread's copies have landed
+__device__ __forceinline__ void slope_wait_prev() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+template <int R, bool DU>
+static size_t smem_of();
 
 // MI partial gradient from the polynomial cells of the MI table (global,
 // read through L1): per cell (floor cF, floor cJ) the 12 coefficients of the
@@ -129,7 +181,73 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return r;
 }
 
-template <typename FT, int BMAX, int R>
+// Sampler backward in the window kernel's epilogue (LN_DU), from the slope
+// dJ/dq that the sampling sweep stored: per voxel e = g dJ/dq with g = dL/dJ,
+// du = K^T e, and the affine moments sum e_r and sum e_r (i_c - ctr_c).  A
+// thread's outputs keep their column and rows over a z segment, so its x and
+// y moments follow from per-row sums at fold time; only the z moment is
+// accumulated per voxel.  Folded into the CTA's fp64 records every 32 planes
+// and at the end of each segment.
+template <int NOUT>
+struct DuAcc {
+  float S[NOUT][3];  // sum of e_r per output row
+  float Zm[3];       // sum of e_r (iz - ctr_z)
+  __device__ __forceinline__ void clear() {
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) S[k][r] = 0.0f;
+      Zm[r] = 0.0f;
+    }
+  }
+  // q: the voxel's staged slope (shared memory)
+  __device__ __forceinline__ void add(const LnccArgs& a, int k, size_t lin, const float* q, float cz, float gv) {
+    const float e0 = gv * q[0], e1 = gv * q[1], e2 = gv * q[2];
+    if (a.du) {
+      const float* K = a.g.K;
+      float* d = a.du + 3 * lin;
+      if (a.g.k_diag) {
+        d[0] = K[0] * e0;
+        d[1] = K[4] * e1;
+        d[2] = K[8] * e2;
+      } else {
+        d[0] = fmaf(K[0], e0, fmaf(K[3], e1, K[6] * e2));
+        d[1] = fmaf(K[1], e0, fmaf(K[4], e1, K[7] * e2));
+        d[2] = fmaf(K[2], e0, fmaf(K[5], e1, K[8] * e2));
+      }
+    }
+    S[k][0] += e0;
+    S[k][1] += e1;
+    S[k][2] += e2;
+    Zm[0] = fmaf(e0, cz, Zm[0]);
+    Zm[1] = fmaf(e1, cz, Zm[1]);
+    Zm[2] = fmaf(e2, cz, Zm[2]);
+  }
+  // warp-uniform; ws = this warp's fp64 record, cx / cy = centred column / rows
+  __device__ __forceinline__ void fold(double* ws, int lane, float cx, const float cy[NOUT]) {
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      float s = S[0][r], ym = S[0][r] * cy[0];
+#pragma unroll
+      for (int k = 1; k < NOUT; ++k) {
+        s += S[k][r];
+        ym = fmaf(S[k][r], cy[k], ym);
+      }
+      const float v0 = warp_sum(s), v1 = warp_sum(s * cx), v2 = warp_sum(ym), v3 = warp_sum(Zm[r]);
+      if (lane == 0) {
+        ws[kPS + r] += (double)v0;
+        ws[kPM + 3 * r] += (double)v1;
+        ws[kPM + 3 * r + 1] += (double)v2;
+        ws[kPM + 3 * r + 2] += (double)v3;
+      }
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) S[k][r] = 0.0f;
+      Zm[r] = 0.0f;
+    }
+  }
+};
+
+template <typename FT, int BMAX, int R, bool DU>
 __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArgs a) {
   using L = LT<R>;
   constexpr int W = L::W, TY = L::TY, E2H = L::E2H, E2W = L::E2W, E2S = L::E2S;
@@ -155,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   float* gxX = sm + L::OFF_X + 2 * E1H * kTX;
   float2* grP = reinterpret_cast<float2*>(sm + L::OFF_G);
   float* grX = sm + L::OFF_G + W * TY * kTX * 2;
+  float* slope = sm + L::TOTAL;  // LN_DU only
 
   const Geom& g = a.g;
   const int tid = threadIdx.x;
@@ -163,7 +282,10 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   const float2 ninv2 = make_float2(-inv_n, -inv_n);
   const size_t plane = (size_t)g.fW * g.fH;
   float cc_acc = 0.0f;
-  if ((tid & 31) == 0) wsum[tid >> 5][12] = 0.0;
+  if ((tid & 31) == 0)
+    for (int q = 0; q < 13; ++q) wsum[tid >> 5][q] = 0.0;
+  DuAcc<NOUT> dacc;
+  dacc.clear();
 
   // this thread's staged elements of a halo plane: in-plane offset, or -1
   // where the element lies outside the grid (read as zero)
@@ -196,8 +318,14 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   while (seg.next(tx, ty, z0, z1)) {
     const int x0 = tx * kTX, y0 = ty * TY;
     const int nsteps = (z1 - z0) + 4 * R;
+    // LN_DU: the tile's slope (plane stride slope_plane) and its staging slots;
+    // slot_rd is the slot of the current step's output plane (s mod 3)
+    const bool full = x0 + kTX <= g.fW && y0 + TY <= g.fH && (g.fW & 3) == 0;
+    const size_t slope_plane = 3 * (size_t)g.fW * g.fH;
+    const float* slope_tile = DU ? a.dJdq + 3 * ((size_t)y0 * g.fW + x0) : nullptr;
+    int slot_rd = 2;
 
-    // output positions of this thread
+    // output positions of this thread (one column: kThreads is a multiple of kTX)
     int oX[NOUT], oY[NOUT];
 #pragma unroll
     for (int k = 0; k < NOUT; ++k) {
@@ -205,6 +333,12 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
       oY[k] = y0 + e / kTX;
       oX[k] = x0 + (e % kTX);
     }
+    auto fold_du = [&] {
+      float cy[NOUT];
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) cy[k] = (float)oY[k] - g.ctr[1];
+      dacc.fold(wsum[tid >> 5], tid & 31, (float)oX[0] - g.ctr[0], cy);
+    };
 #pragma unroll
     for (int i = 0; i < NSTG; ++i) {
       const int e = tid + i * kThreads;
@@ -223,6 +357,13 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
       const int zi = z0 - 2 * R + s;
       const bool pass1 = s >= 2 * R;
       const bool pass2 = s >= 4 * R;
+      if constexpr (DU) {
+        slot_rd = slot_rd == 2 ? 0 : slot_rd + 1;
+        const int sn = s + 1;  // the output plane of the next step
+        const float* src = (sn >= 4 * R && sn < nsteps) ? slope_tile + (size_t)(zi + 1 - 2 * R) * slope_plane : nullptr;
+        stage_slope<TY, kThreads>(slope + (slot_rd == 2 ? 0 : slot_rd + 1) * SlopeStage<TY>::SLOT, src,
+                                  g, x0, y0, full, tid);
+      }
       // (J, F) at this thread's outputs of plane zo = zi - 2R: the ring slot
       // about to be overwritten.
       float2 jfo[NOUT];
@@ -269,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
           *reinterpret_cast<float4*>(zX + row * E2S + 4 * c4) = make_float4(sX[0], sX[1], sX[2], sX[3]);
         }
       }
+      if constexpr (DU) slope_wait_prev();
       __syncthreads();
       // the oldest ring slot is free: write the staged plane, fetch the next
       if (s + 1 < nsteps) {
@@ -506,17 +648,24 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
           if (X < g.fW && Y < g.fH) {
             float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
             if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
-            if (a.dJ) a.dJ[((size_t)zo * g.fH + Y) * g.fW + X] = gv;
+            const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
+            if constexpr (DU)
+              dacc.add(a, k, lin, slope + slot_rd * SlopeStage<TY>::SLOT + 3 * e, (float)zo - g.ctr[2], gv);
+            else if (a.dJ)
+              a.dJ[lin] = gv;
           }
         }
       }
-      // fold the fp32 cc partial into fp64 every 32 planes (uniform across the CTA)
+      // fold the fp32 cc (and affine) partials into fp64 every 32 planes
+      // (uniform across the CTA)
       if ((s & 31) == 31) {
         const float v = warp_sum(cc_acc);
         if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
         cc_acc = 0.0f;
+        if constexpr (DU) fold_du();
       }
     }
+    if constexpr (DU) fold_du();  // the next segment has other columns and rows
   }
   {
     const float v = warp_sum(cc_acc);
@@ -525,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArg
   __syncthreads();
   if (tid < kPartialStride) {
     double s = 0.0;
-    if (tid == kPCC)
-      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][kPCC];
+    if (tid == kPCC || (DU && tid < 12))
+      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][tid];
     a.partials[(size_t)blockIdx.x * kPartialStride + tid] = s;
   }
 }
@@ -590,7 +739,7 @@ __device__ __forceinline__ void halo_pos(int h, int& row, int& col) {
   }
 }
 
-template <typename FT, int BMAX, int R>
+template <typename FT, int BMAX, int R, bool DU>
 __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(const LnccArgs a) {
   using L = LT<R>;
   using Q = LTR<R>;
@@ -612,6 +761,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   float* gX = sm + Q::OFF_Z + 2 * E1H * E1S;
   float2* gxP = reinterpret_cast<float2*>(sm + Q::OFF_X);
   float* gxX = sm + Q::OFF_X + 2 * E1H * kTX;
+  float* slope = sm + Q::TOTAL;  // LN_DU only
 
   const Geom& g = a.g;
   const int tid = threadIdx.x;
@@ -620,7 +770,10 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   const float2 ninv2 = make_float2(-inv_n, -inv_n);
   const size_t plane = (size_t)g.fW * g.fH;
   float cc_acc = 0.0f;
-  if ((tid & 31) == 0) wsum[tid >> 5][12] = 0.0;
+  if ((tid & 31) == 0)
+    for (int q = 0; q < 13; ++q) wsum[tid >> 5][q] = 0.0;
+  DuAcc<NOUT> dacc;
+  dacc.clear();
 
   // staged positions: shared-memory index in the halo plane and in-plane
   // global offset (-1: outside the grid, read as zero; -2: no position)
@@ -669,6 +822,18 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   while (seg.next(tx, ty, z0, z1)) {
     const int x0 = tx * kTX, y0 = ty * TY;
     const int nsteps = (z1 - z0) + 4 * R;
+    // LN_DU: the tile's slope (plane stride slope_plane) and its staging slots;
+    // slot_rd is the slot of the current step's output plane (s mod 3)
+    const bool full = x0 + kTX <= g.fW && y0 + TY <= g.fH && (g.fW & 3) == 0;
+    const size_t slope_plane = 3 * (size_t)g.fW * g.fH;
+    const float* slope_tile = DU ? a.dJdq + 3 * ((size_t)y0 * g.fW + x0) : nullptr;
+    int slot_rd = 2;
+    auto fold_du = [&] {
+      float cy[NOUT];
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) cy[k] = (float)(y0 + oy0 + k) - g.ctr[1];
+      dacc.fold(wsum[tid >> 5], tid & 31, (float)(x0 + ox) - g.ctr[0], cy);
+    };
 #pragma unroll
     for (int i = 0; i < NSTG; ++i) {
       soff[i] = -2;
@@ -700,6 +865,14 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
 #pragma unroll
           for (int i = 0; i < NSTG; ++i) hist[j][i] = nxt[i];
           if (s + 1 < nsteps) load_plane(zi + 1);
+          if constexpr (DU) {
+            slot_rd = slot_rd == 2 ? 0 : slot_rd + 1;
+            const int sn = s + 1;  // the output plane of the next step
+            const float* src =
+                (sn >= 4 * R && sn < nsteps) ? slope_tile + (size_t)(zi + 1 - 2 * R) * slope_plane : nullptr;
+            stage_slope<TY, kLnccRHThreads>(slope + (slot_rd == 2 ? 0 : slot_rd + 1) * SlopeStage<TY>::SLOT, src,
+                                            g, x0, y0, full, tid);
+          }
           if (pass1) {
             // [B] z sums over the register history -> zbuf
 #pragma unroll
@@ -720,6 +893,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
               }
             }
           }
+          if constexpr (DU) slope_wait_prev();
           __syncthreads();
           if (pass1) {
             // [C] x sums, 2 outputs per item: neighbouring lanes read
@@ -915,19 +1089,27 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
               if (X < g.fW && Y < g.fH) {
                 float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
                 if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
-                if (a.dJ) a.dJ[((size_t)zo * g.fH + Y) * g.fW + X] = gv;
+                const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
+                if constexpr (DU)
+                  dacc.add(a, k, lin, slope + slot_rd * SlopeStage<TY>::SLOT + (oy0 + k) * SlopeStage<TY>::ROW + 3 * ox,
+                           (float)zo - g.ctr[2], gv);
+                else if (a.dJ)
+                  a.dJ[lin] = gv;
               }
             }
           }
-          // fold the fp32 cc partial into fp64 every 32 planes (uniform across the CTA)
+          // fold the fp32 cc (and affine) partials into fp64 every 32 planes
+          // (uniform across the CTA)
           if ((s & 31) == 31) {
             const float v = warp_sum(cc_acc);
             if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
             cc_acc = 0.0f;
+            if constexpr (DU) fold_du();
           }
         }
       }
     }
+    if constexpr (DU) fold_du();  // the next segment has other columns and rows
   }
   {
     const float v = warp_sum(cc_acc);
@@ -936,31 +1118,32 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   __syncthreads();
   if (tid < kPartialStride) {
     double s = 0.0;
-    if (tid == kPCC)
-      for (int k = 0; k < kLnccRHThreads / 32; ++k) s += wsum[k][kPCC];
+    if (tid == kPCC || (DU && tid < 12))
+      for (int k = 0; k < kLnccRHThreads / 32; ++k) s += wsum[k][tid];
     a.partials[(size_t)blockIdx.x * kPartialStride + tid] = s;
   }
 }
 
-template <int R>
+template <int R, bool DU>
 static size_t smem_of() {
+  const size_t stage = DU ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0;
   if constexpr (R <= 3)
-    return (size_t)LTR<R>::TOTAL * sizeof(float);
+    return ((size_t)LTR<R>::TOTAL + stage) * sizeof(float);
   else
-    return (size_t)LT<R>::TOTAL * sizeof(float);
+    return ((size_t)LT<R>::TOTAL + stage) * sizeof(float);
 }
 
 // occ != nullptr: report resident CTAs per SM instead of launching.
-template <typename FT, int BMAX, int R>
+template <typename FT, int BMAX, int R, bool DU>
 static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
   // radius <= 3: register-history kernel; radius 4: shared-memory plane ring
   auto k = [] {
     if constexpr (R <= 3)
-      return k_lncc_rh<FT, BMAX, R>;
+      return k_lncc_rh<FT, BMAX, R, DU>;
     else
-      return k_lncc<FT, BMAX, R>;
+      return k_lncc<FT, BMAX, R, DU>;
   }();
-  const size_t smem = smem_of<R>();
+  const size_t smem = smem_of<R, DU>();
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   constexpr int nt = R <= 3 ? kLnccRHThreads : kThreads;
@@ -973,15 +1156,19 @@ static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* oc
 
 template <int R>
 static cudaError_t dispatch_r(int mode, int ft, int bmax, const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
+  // LN_DJ (the stand-alone LNCC gradient) carries no MI term; LN_DU (the
+  // objective) any bin count
   cudaError_t e = cudaErrorInvalidValue;
-  if (mode != LN_DJ) return e;
+  if (mode == LN_DJ && bmax != 0) return e;
   FFDP_DT_SWITCH(ft, FT, {
-    if (bmax == 0)
-      e = run_lncc<FT, 0, R>(a, grid, s, occ);
+    if (mode == LN_DJ)
+      e = run_lncc<FT, 0, R, false>(a, grid, s, occ);
+    else if (bmax == 0)
+      e = run_lncc<FT, 0, R, true>(a, grid, s, occ);
     else if (bmax == 32)
-      e = run_lncc<FT, 32, R>(a, grid, s, occ);
+      e = run_lncc<FT, 32, R, true>(a, grid, s, occ);
     else
-      e = run_lncc<FT, 64, R>(a, grid, s, occ);
+      e = run_lncc<FT, 64, R, true>(a, grid, s, occ);
   });
   return e;
 }
