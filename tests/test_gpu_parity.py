@@ -142,6 +142,11 @@ OBJ_CASES = [
     # window 9 (the shared-memory plane-ring kernel) with the MI term fused, both table sizes
     ((16, 18, 40), (16, 18, 40), np.float32, 1.0, 1.0, 64, 9),
     ((15, 17, 33), (15, 17, 33), np.float16, 1.0, 0.5, 32, 9),
+    # rows a multiple of 4 voxels: full tiles stage the stored slope by 16-byte
+    # copies, the ragged last tile in x and y by 4-byte copies
+    ((19, 37, 100), (19, 37, 100), np.float32, 1.0, 1.0, 64, 5),
+    ((12, 16, 64), (12, 16, 64), np.float32, 0.5, 1.0, 32, 9),
+    ((10, 48, 96), (10, 48, 96), np.float16, 0.0, 1.0, 32, 3),
 ]
 
 
