@@ -339,8 +339,9 @@ int persistent_grid(unsigned nIter, int per_sm) {
 unsigned n_iter1(uint64_t N) {
   return (unsigned)((N + (uint64_t)(kSweep1Threads * kVPT) - 1) / (kSweep1Threads * kVPT));
 }
-unsigned n_iter2(uint64_t N) {
-  return (unsigned)((N + (uint64_t)(kSweep2Threads * kVPT) - 1) / (kSweep2Threads * kVPT));
+unsigned n_iter2(uint64_t N, int mode) {
+  const uint64_t per = (uint64_t)sweep2_threads(mode) * kVPT;
+  return (unsigned)((N + per - 1) / per);
 }
 
 #define FFDP_TRY(x)                    \
@@ -443,7 +444,7 @@ extern "C" ffdp_status ffdp_grid_sample_bwd(const void* M, ffdp_dtype mt, ffdp_d
   a.gbuf = gJ;
   a.du = du;
   a.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
-  a.nIter = n_iter2(a.g.N);
+  a.nIter = n_iter2(a.g.N, S2_GBUF);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = persistent_grid(a.nIter, sweep2_ctas_per_sm(S2_GBUF, 0, mt, 32));
   FFDP_CUDA(launch_sweep2(S2_GBUF, 0, mt, 32, a, grid, s), "grid_sample_bwd launch");
@@ -515,7 +516,7 @@ extern "C" ffdp_status ffdp_mi_fwd_bwd(const void* F, ffdp_dtype ft, const float
     a2.bf = a1.bf;
     a2.bj = a1.bj;
     a2.B = p->bins;
-    a2.nIter = n_iter2(g.N);
+    a2.nIter = n_iter2(g.N, S2_MI_JBUF);
     FFDP_CUDA(launch_sweep2(S2_MI_JBUF, ft, 0, bmax, a2,
                             persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MI_JBUF, ft, 0, bmax)), s),
               "MI gradient launch");
@@ -681,7 +682,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a2.bf = bf;
     a2.bj = bj;
     a2.B = p->mi.bins;
-    a2.nIter = n_iter2(N);
+    a2.nIter = n_iter2(N, m2);
     const int grid = persistent_grid(a2.nIter, sweep2_ctas_per_sm(m2, ft, mt, bmax));
     FFDP_CUDA(launch_sweep2(m2, ft, mt, bmax, a2, grid, s), "sweep 2 launch");
     nparts = grid;

@@ -20,10 +20,16 @@ constexpr int kThreads = 256;           // threads per CTA of the LNCC kernel
 #ifndef FFDP_SWEEP2_THREADS
 #define FFDP_SWEEP2_THREADS 512
 #endif
-// threads per CTA of the histogram / forward sweep and of the gradient sweep
-// (one CTA per SM each; the gradient sweep needs more registers per thread)
+#ifndef FFDP_SWEEP2_STREAM_THREADS
+#define FFDP_SWEEP2_STREAM_THREADS 768
+#endif
+// threads per CTA (one CTA per SM) of the histogram / forward sweep, of the
+// gradient sweep that gathers M again (more registers per thread), and of the
+// gradient sweeps that only stream stored per-voxel inputs (more warps keep
+// more bulk copies and stores in flight)
 constexpr int kSweep1Threads = FFDP_SWEEP1_THREADS;
 constexpr int kSweep2Threads = FFDP_SWEEP2_THREADS;
+constexpr int kSweep2StreamThreads = FFDP_SWEEP2_STREAM_THREADS;
 constexpr int kVPT = 4;                 // voxels per sweep thread per iteration (32 apart)
 constexpr int kHistFrac = 20;           // fixed-point fraction bits of histogram weights
 constexpr float kHistOne = 1048576.0f;  // 2^kHistFrac

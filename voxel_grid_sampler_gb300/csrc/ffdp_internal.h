@@ -28,6 +28,11 @@ constexpr int kSweep1Modes = 6;
 // MI gradient of a given J; backward of a given g with the stored dJ/dq (no
 // gathers); MI gradient + backward from the stored J and dJ/dq (no gathers).
 enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2, S2_GBUF_DJ = 3, S2_MI_DJ = 4 };
+// threads per CTA of a gradient-sweep mode: the gathering modes at
+// kSweep2Threads, the streaming ones at kSweep2StreamThreads
+__host__ __device__ constexpr int sweep2_threads(int mode) {
+  return (mode == S2_MI || mode == S2_GBUF) ? kSweep2Threads : kSweep2StreamThreads;
+}
 constexpr int kSweep2Modes = 5;
 enum LnccMode { LN_DJ = 0, LN_DU = 1 };  // write dL/dJ; or du and affine partials from the stored slope
 

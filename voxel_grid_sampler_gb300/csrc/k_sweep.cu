@@ -795,13 +795,13 @@ struct S2Cfg {
   static constexpr bool BWD = MODE != S2_MI_JBUF;                                      // du and affine partials
   static constexpr bool XS = MODE != S2_MI;                                            // g or J (given / stored)
   static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
-  using RG1 = Ring<FT, VEC, MI, XS, 1, kSweep2Threads>;
+  static constexpr int NT = sweep2_threads(MODE);
+  using RG1 = Ring<FT, VEC, MI, XS, 1, NT>;
   // as many ring slots (up to 4) as fit next to the table in 220 KiB
-  static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (kSweep2Threads / 32) * 96) /
-                                       ((kSweep2Threads / 32) * (RG1::kSlot + 8)));
+  static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (NT / 32) * 96) / ((NT / 32) * (RG1::kSlot + 8)));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
   static_assert(NST >= 2, "ring needs two slots");
-  using RG = Ring<FT, VEC, MI, XS, NST, kSweep2Threads>;
+  using RG = Ring<FT, VEC, MI, XS, NST, NT>;
   static constexpr size_t kSmem = kTableBytes + RG::kBytes;
 };
 
@@ -882,7 +882,7 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
 }
 
 template <typename FT, typename MT, int BMAX, int MODE>
-__global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a) {
+__global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2Args a) {
   using C = S2Cfg<FT, BMAX, MODE>;
   constexpr bool MI = C::MI, GATHER = C::GATHER, VEC = C::VEC, BWD = C::BWD, XS = C::XS;
   constexpr int NST = C::NST;
@@ -890,12 +890,13 @@ __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a
   using WR = WarpRing<RG, NST>;
   extern __shared__ float4 tsm4[];
   float* tsm = reinterpret_cast<float*>(tsm4);
-  __shared__ double wsum[kSweep2Threads / 32][12];
+  constexpr int NT = C::NT;
+  __shared__ double wsum[NT / 32][12];
   const Geom& g = a.g;
   if (MI) {
     constexpr int n4 = table_floats<BMAX>() / 4;
     const float4* src = reinterpret_cast<const float4*>(a.T);
-    for (int i = threadIdx.x; i < n4; i += kSweep2Threads) tsm4[i] = __ldg(src + i);
+    for (int i = threadIdx.x; i < n4; i += NT) tsm4[i] = __ldg(src + i);
     __syncthreads();
   }
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
@@ -952,7 +953,7 @@ __global__ void __launch_bounds__(kSweep2Threads, 1) k_sweep2(const Sweep2Args a
     if (threadIdx.x < kPartialStride) {
       double s = 0.0;
       if (threadIdx.x < 12)
-        for (int q = 0; q < kSweep2Threads / 32; ++q) s += wsum[q][threadIdx.x];
+        for (int q = 0; q < NT / 32; ++q) s += wsum[q][threadIdx.x];
       a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = s;
     }
   }
@@ -1073,9 +1074,10 @@ static cudaError_t run_sweep2(const Sweep2Args& a, int grid, cudaStream_t s, int
   const size_t smem = S2Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, kSweep2Threads, smem);
+  constexpr int nt = S2Cfg<FT, BMAX, MODE>::NT;
+  if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, nt, smem);
   note_launch_begin("k_sweep2", s);
-  k<<<grid, kSweep2Threads, smem, s>>>(a);
+  k<<<grid, nt, smem, s>>>(a);
   note_launch_end(s);
   return cudaGetLastError();
 }
