@@ -84,6 +84,12 @@ def lib():
         L.oracle_mi.restype = ctypes.c_double
         L.oracle_lncc.argtypes = [_fp, _dp, _ip, ctypes.c_int, ctypes.c_double, _dp, _dp]
         L.oracle_lncc.restype = ctypes.c_double
+        L.oracle_sample_channels.argtypes = [_fp, ctypes.c_int, _ip, _ip, _fp, _dp, ctypes.c_int,
+                                             ctypes.c_int64, ctypes.c_int64, _dp]
+        L.oracle_sample_channels_bwd.argtypes = [_fp, ctypes.c_int, _ip, _ip, _fp, _dp, ctypes.c_int,
+                                                 ctypes.c_int64, ctypes.c_int64, _dp, _dp, _dp, _dp, _dp]
+        L.oracle_mse.argtypes = [_fp, _dp, ctypes.c_int64, _dp]
+        L.oracle_mse.restype = ctypes.c_double
         _lib = L
     return _lib
 
@@ -174,6 +180,64 @@ def grid_sample_bwd(M, fixed_shape, u, T: Transform, gJ, z0: int = 0, z1: int | 
                                  _dims(fixed_shape).ctypes.data_as(_ip), _pf(u32),
                                  _pd(T.packed()), z0, z1, _pd(g), _pd(du), _pd(dA), _pd(dt))
     return du, dA, dt
+
+
+# ------------------------------------------------- C-channel sampler / compose
+def sample_channels(V, fixed_shape, u, T: Transform, compose: bool = False, z0: int = 0,
+                    z1: int | None = None):
+    """out[z0:z1] = V(A x + t + S u(x)) (+ S u(x) when compose) for a channel-last
+    volume V of shape (Dv, Hv, Wv, C); returns (z1-z0, H, W, C) float64."""
+    V = _f32(V)
+    C = V.shape[3]
+    D, H, W = fixed_shape
+    z1 = D if z1 is None else z1
+    u32 = None if u is None else _f32(u)
+    out = np.empty((z1 - z0, H, W, C), np.float64)
+    lib().oracle_sample_channels(_pf(V), C, _dims(V.shape[:3]).ctypes.data_as(_ip),
+                                 _dims(fixed_shape).ctypes.data_as(_ip), _pf(u32), _pd(T.packed()),
+                                 int(bool(compose)), z0, z1, _pd(out))
+    return out
+
+
+def sample_channels_bwd(V, fixed_shape, u, T: Transform, gout, compose: bool = False,
+                        want_du: bool = True, want_dV: bool = True):
+    """Backward of sample_channels over the whole fixed grid: (du, dA, dt, dV)."""
+    V = _f32(V)
+    C = V.shape[3]
+    D, H, W = fixed_shape
+    u32 = None if u is None else _f32(u)
+    g = _f64(gout)
+    du = np.empty((D, H, W, 3), np.float64) if want_du else None
+    dA = np.zeros(9, np.float64)
+    dt = np.zeros(3, np.float64)
+    dV = np.zeros(V.shape, np.float64) if want_dV else None
+    lib().oracle_sample_channels_bwd(_pf(V), C, _dims(V.shape[:3]).ctypes.data_as(_ip),
+                                     _dims(fixed_shape).ctypes.data_as(_ip), _pf(u32), _pd(T.packed()),
+                                     int(bool(compose)), 0, D, _pd(g), _pd(du), _pd(dA), _pd(dt), _pd(dV))
+    return du, dA.reshape(3, 3), dt, dV
+
+
+# ------------------------------------------------------------------------ MSE
+def mse(F, J, want_grad: bool = True):
+    """Returns dict(mse, dJ) for same-size F and J."""
+    F32 = _f32(F).reshape(-1)
+    J64 = _f64(J).reshape(-1)
+    dJ = np.empty(F32.size, np.float64) if want_grad else None
+    v = lib().oracle_mse(_pf(F32), _pd(J64), F32.size, _pd(dJ))
+    return dict(mse=float(v), dJ=None if dJ is None else dJ.reshape(np.shape(J)))
+
+
+def objective_mse(F, M, u, T: Transform, w_mse: float = 1.0, want_du: bool = True):
+    """MSE objective L = w_mse * MSE(F, M o phi) and its sampler backward.
+
+    Returns dict(loss=[w_mse * MSE, MSE], J, gJ, du, dA, dt)."""
+    F32 = _f32(F)
+    shape = F32.shape
+    J = grid_sample(M, shape, u, T)
+    r = mse(F32, J)
+    gJ = w_mse * r["dJ"]
+    du, dA, dt = grid_sample_bwd(M, shape, u, T, gJ, want_du=want_du)
+    return dict(loss=np.array([w_mse * r["mse"], r["mse"]]), J=J, gJ=gJ, du=du, dA=dA.reshape(3, 3), dt=dt)
 
 
 # ------------------------------------------------------------------------- MI

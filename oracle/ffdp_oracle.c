@@ -481,3 +481,169 @@ double oracle_lncc(const float *F, const double *J, const int64_t *dims, int w, 
   }
   return tot / (double)N;
 }
+
+/* ------------------------------------------------------------------ */
+/* warp composition: the design-1 sampler on a C-channel volume         */
+/* ------------------------------------------------------------------ */
+
+/* The "Background" section names deformation interpolation and warp
+ * composition as the first of the three memory bottlenecks; design 1's
+ * sampler I(Ax + t + Su(x)) applies unchanged when I has several channels.
+ * A channel-last volume V is [Dv][Hv][Wv][C] (channel fastest).  Composing a
+ * displacement field V (C = 3, normalised units of its own domain) after
+ * phi(x) = Ax + t + Su(x) gives
+ *   V o phi composed:  phi_V(phi(x)) = phi(x) + V(phi(x)) = Ax + t + d(x),
+ *   d(x) = S u(x) + V(phi(x)),
+ * i.e. the composite warp in the same form with S = I and displacement d.
+ * Readings: the same conventions as the scalar sampler (align_corners grid,
+ * zero padding per tap, floor cell for the slope); `compose` adds S u(x). */
+
+/* Value of channel ch of V at integer voxel (x, y, z); 0 outside. */
+static double v_at(const float *V, int C, const int64_t *vd, int64_t x, int64_t y, int64_t z, int ch) {
+  if (x < 0 || y < 0 || z < 0 || x >= vd[2] || y >= vd[1] || z >= vd[0]) return 0.0;
+  return (double)V[((z * vd[1] + y) * vd[2] + x) * C + ch];
+}
+
+/* Cell of normalised point p in a volume of extents vd: corner b, fractions
+ * r; returns 0 when every tap is outside (q < -1 or q >= n on some axis). */
+static int cell_of_point(const int64_t *vd, const double p[3], int64_t b[3], double r[3]) {
+  const int64_t n[3] = {vd[2], vd[1], vd[0]};
+  for (int c = 0; c < 3; ++c) {
+    const double q = (p[c] + 1.0) * 0.5 * (double)(n[c] - 1);
+    if (!(q >= -1.0 && q < (double)n[c])) return 0;
+    const double fl = floor(q);
+    b[c] = (int64_t)fl;
+    r[c] = q - fl;
+  }
+  return 1;
+}
+
+/* Trilinear weight of corner (cx, cy, cz) of a cell with fractions r. */
+static double corner_weight(const double r[3], int cx, int cy, int cz) {
+  return (cx ? r[0] : 1.0 - r[0]) * (cy ? r[1] : 1.0 - r[1]) * (cz ? r[2] : 1.0 - r[2]);
+}
+
+/* Sampled channels val[C] at p and their slopes dvdp[C][3] w.r.t. p. */
+static void sample_channels_point(const float *V, int C, const int64_t *vd, const double p[3], double *val,
+                                  double *dvdp) {
+  const int64_t n[3] = {vd[2], vd[1], vd[0]};
+  int64_t b[3];
+  double r[3];
+  for (int ch = 0; ch < C; ++ch) {
+    val[ch] = 0.0;
+    if (dvdp) dvdp[ch * 3 + 0] = dvdp[ch * 3 + 1] = dvdp[ch * 3 + 2] = 0.0;
+  }
+  if (!cell_of_point(vd, p, b, r)) return;
+  for (int cz = 0; cz < 2; ++cz)
+    for (int cy = 0; cy < 2; ++cy)
+      for (int cx = 0; cx < 2; ++cx) {
+        const double wx = cx ? r[0] : 1.0 - r[0];
+        const double wy = cy ? r[1] : 1.0 - r[1];
+        const double wz = cz ? r[2] : 1.0 - r[2];
+        for (int ch = 0; ch < C; ++ch) {
+          const double m = v_at(V, C, vd, b[0] + cx, b[1] + cy, b[2] + cz, ch);
+          val[ch] += wx * wy * wz * m;
+          if (dvdp) {
+            dvdp[ch * 3 + 0] += (cx ? 1.0 : -1.0) * wy * wz * m * 0.5 * (double)(n[0] - 1);
+            dvdp[ch * 3 + 1] += (cy ? 1.0 : -1.0) * wx * wz * m * 0.5 * (double)(n[1] - 1);
+            dvdp[ch * 3 + 2] += (cz ? 1.0 : -1.0) * wx * wy * m * 0.5 * (double)(n[2] - 1);
+          }
+        }
+      }
+}
+
+/* out[i][c] = V_c(A x_i + t + S u_i) (+ (S u_i)_c when compose, C = 3) for
+ * fixed planes z0 <= z < z1; out is [z1-z0][H][W][C], indexed from z0. */
+void oracle_sample_channels(const float *V, int C, const int64_t *vd, const int64_t *fd, const float *u,
+                            const double *T, int compose, int64_t z0, int64_t z1, double *out) {
+  const int64_t H = fd[1], W = fd[2];
+  const double *S = T + 12;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t z = z0; z < z1; ++z)
+    for (int64_t y = 0; y < H; ++y)
+      for (int64_t x = 0; x < W; ++x) {
+        const int64_t lin = (z * H + y) * W + x;
+        const int64_t loc = ((z - z0) * H + y) * W + x;
+        double xc[3], uv[3], p[3], val[4];
+        fixed_coord(T, fd, x, y, z, xc);
+        load_u(u, lin, uv);
+        warp_point(T, xc, uv, p);
+        sample_channels_point(V, C, vd, p, val, NULL);
+        for (int ch = 0; ch < C; ++ch) {
+          double v = val[ch];
+          if (compose) v += S[ch * 3 + 0] * uv[0] + S[ch * 3 + 1] * uv[1] + S[ch * 3 + 2] * uv[2];
+          out[loc * C + ch] = v;
+        }
+      }
+}
+
+/* Backward of oracle_sample_channels for planes z0 <= z < z1 given
+ * gout = dL/dout ([z1-z0][H][W][C]):
+ *   e_i      = sum_c gout_ic dV_c/dp (p_i)
+ *   du_i     = S^T e_i  (+ S^T gout_i when compose)
+ *   dA[r][c] += sum_i e_ir x_ic,   dt[r] += sum_i e_ir
+ *   dV[v][c] += sum_i gout_ic w_v(p_i)   (w_v: trilinear weight of corner v)
+ * du (indexed from z0) and dV may be NULL; dA, dt and dV are ACCUMULATED.
+ * Runs serially (the scatter into dV has no fixed owner per voxel). */
+void oracle_sample_channels_bwd(const float *V, int C, const int64_t *vd, const int64_t *fd, const float *u,
+                                const double *T, int compose, int64_t z0, int64_t z1, const double *gout,
+                                double *du, double *dA, double *dt, double *dV) {
+  const int64_t H = fd[1], W = fd[2];
+  const double *S = T + 12;
+  for (int64_t z = z0; z < z1; ++z)
+    for (int64_t y = 0; y < H; ++y)
+      for (int64_t x = 0; x < W; ++x) {
+        const int64_t lin = (z * H + y) * W + x;
+        const int64_t loc = ((z - z0) * H + y) * W + x;
+        double xc[3], uv[3], p[3], val[4], dv[12], e[3] = {0.0, 0.0, 0.0};
+        fixed_coord(T, fd, x, y, z, xc);
+        load_u(u, lin, uv);
+        warp_point(T, xc, uv, p);
+        sample_channels_point(V, C, vd, p, val, dv);
+        const double *g = gout + loc * C;
+        for (int ch = 0; ch < C; ++ch)
+          for (int r = 0; r < 3; ++r) e[r] += g[ch] * dv[ch * 3 + r];
+        if (du)
+          for (int c = 0; c < 3; ++c) {
+            double s = S[0 * 3 + c] * e[0] + S[1 * 3 + c] * e[1] + S[2 * 3 + c] * e[2];
+            if (compose) s += S[0 * 3 + c] * g[0] + S[1 * 3 + c] * g[1] + S[2 * 3 + c] * g[2];
+            du[loc * 3 + c] = s;
+          }
+        for (int r = 0; r < 3; ++r) {
+          for (int c = 0; c < 3; ++c) dA[r * 3 + c] += e[r] * xc[c];
+          dt[r] += e[r];
+        }
+        if (dV) {
+          int64_t b[3];
+          double rr[3];
+          if (!cell_of_point(vd, p, b, rr)) continue;
+          for (int cz = 0; cz < 2; ++cz)
+            for (int cy = 0; cy < 2; ++cy)
+              for (int cx = 0; cx < 2; ++cx) {
+                const int64_t vx = b[0] + cx, vy = b[1] + cy, vz = b[2] + cz;
+                if (vx < 0 || vy < 0 || vz < 0 || vx >= vd[2] || vy >= vd[1] || vz >= vd[0]) continue;
+                const double w = corner_weight(rr, cx, cy, cz);
+                const int64_t v = (vz * vd[1] + vy) * vd[2] + vx;
+                for (int ch = 0; ch < C; ++ch) dV[v * C + ch] += g[ch] * w;
+              }
+        }
+      }
+}
+
+/* ------------------------------------------------------------------ */
+/* MSE similarity                                                       */
+/* ------------------------------------------------------------------ */
+
+/* "Background": C(F, M o phi) may be the mean squared error; design 5 calls
+ * it a per-voxel loss.  MSE = (1/n) sum_k (J_k - F_k)^2 and
+ * dMSE/dJ_k = 2 (J_k - F_k) / n (dJ may be NULL).  Plain sum in index
+ * order. */
+double oracle_mse(const float *F, const double *J, int64_t n, double *dJ) {
+  double s = 0.0;
+  for (int64_t k = 0; k < n; ++k) {
+    const double d = J[k] - (double)F[k];
+    s += d * d;
+    if (dJ) dJ[k] = 2.0 * d / (double)n;
+  }
+  return s / (double)n;
+}
