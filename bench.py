@@ -6,6 +6,8 @@ path -- implicit sampler, histogram sweep, MI table, LNCC window sums, MI and
 LNCC gradients, sampler backward, affine reductions.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4|5] [--impl reference]
+    python bench.py --path mse|compose     (the MSE objective / warp composition on the
+                                            512^3 pair; one JSON line each, same keys)
 
 Under torch.distributed.run each rank evaluates its own independent pair
 (weak scaling, no collective on the data path); the step time is the maximum
@@ -458,6 +460,174 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------- other paths
+# The fused MSE objective (one pass: F + u + M read, du written) and warp
+# composition (forward: u + V read, out written; backward: u + gout + V read,
+# du and dV written) on the 512^3 workload-4 pair; V is the pair's own
+# displacement field (the warp composed with itself), gout a seeded normal
+# field.
+PATH_METRIC = {"mse": "Gvoxels/s fused warp+MSE fwd+bwd on 1 GB300; % of HBM roofline",
+               "compose": "Gvoxels/s warp composition fwd+bwd (du, dA, dt, dV) on 1 GB300; % of HBM roofline"}
+PATH_KERNEL_BYTES = {"mse": {"k_sweep2": 4 + 12 + 4 + 12},
+                     "compose": {"k_chan_fwd": 12 + 12 + 12, "k_chan_bwd": 12 + 12 + 12 + 12 + 12,
+                                 "k_zero_f32": 12}}
+PATH_ALGO_BYTES = {"mse": 32, "compose": 36 + 60}
+
+
+def _path_setup(args, pair, dev):
+    from voxel_grid_sampler_gb300 import ffdp
+    F, M, u = pair.F, pair.M, pair.u
+    T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
+    shape = tuple(F.shape)
+    if args.path == "mse":
+        o = dict(loss=torch.empty(2, device=dev), du=torch.empty(shape + (3,), device=dev),
+                 dA=torch.empty(9, device=dev), dt=torch.empty(3, device=dev),
+                 ws=ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE_MSE, shape, None, dev))
+
+        def call(F_, M_, u_, o_, stream):
+            ffdp.ffdp_objective_mse(F_, M_, u_, T, 1.0, o_["loss"], o_["du"], o_["dA"], o_["dt"], o_["ws"], stream)
+        ins = dict(F=F, M=M, u=u)
+        outs = ("loss", "du", "dA", "dt")
+    else:
+        g = torch.Generator(device=dev).manual_seed(2024)
+        gout = torch.randn(shape + (3,), device=dev, generator=g)
+        o = dict(out=torch.empty(shape + (3,), device=dev), du=torch.empty(shape + (3,), device=dev),
+                 dA=torch.empty(9, device=dev), dt=torch.empty(3, device=dev), dV=torch.empty_like(u),
+                 ws=ffdp.workspace(ffdp.FFDP_OP_SAMPLE_CHANNELS_BWD, shape, None, dev))
+
+        def call(V_, g_, u_, o_, stream):
+            ffdp.ffdp_sample_channels_fwd(V_, shape, u_, T, True, o_["out"], stream)
+            ffdp.ffdp_sample_channels_bwd(V_, u_, T, g_, True, o_["du"], o_["dA"], o_["dt"], o_["dV"], o_["ws"],
+                                          stream)
+        ins = dict(V=u, g=gout, u=u)
+        outs = ("out", "du", "dA", "dt", "dV")
+    return call, ins, o, outs
+
+
+def _path_oracle_sample(args, pair, ds):
+    """The oracle on the first ds fixed planes of the path (one fwd+bwd)."""
+    import oracle
+    F = pair.F[:ds].float().cpu().numpy()
+    u = pair.u[:ds].cpu().numpy()
+    xmax = _crop_transform(pair, ds)
+    T = oracle.Transform(pair.A.astype(np.float64), pair.t.astype(np.float64), pair.S.astype(np.float64),
+                         pair.xmin.astype(np.float64), xmax.astype(np.float32).astype(np.float64))
+    t0 = time.perf_counter()
+    if args.path == "mse":
+        oracle.objective_mse(F, pair.M.float().cpu().numpy(), u, T, 1.0)
+    else:
+        V = pair.u.cpu().numpy()
+        g = np.random.default_rng(0).normal(size=u.shape)
+        oracle.sample_channels(V, F.shape, u, T, True)
+        oracle.sample_channels_bwd(V, F.shape, u, T, g, True)
+    return F.size, time.perf_counter() - t0, oracle.max_threads()
+
+
+def run_gpu_path(args, ws, rank, local):
+    from voxel_grid_sampler_gb300 import build, ffdp, synth
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    shape = None if not args.shape else (args.shape,) * 3
+    pair = synth.make_pair(4, device=dev, shape=shape, seed=1004 + 100 * rank)
+    N = pair.F.numel()
+    call, ins, o, outs = _path_setup(args, pair, dev)
+    stream = torch.cuda.current_stream(dev)
+    a, b, c = (ins[k] for k in ins)
+
+    def step():
+        call(a, b, c, o, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    ffdp.timing_enable(args.steps * 8)
+    n0 = ffdp.launch_count()
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.15)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    clk = clocks.stop()
+    launches = ffdp.launch_count() - n0
+    kern = ffdp.timing_read()
+    ffdp.timing_enable(0)
+    ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
+    value = _aggregate_gvox(N, ws, ms)
+
+    # end to end: pinned host inputs copied in and every output copied out, each step
+    e2e = None
+    if not args.no_e2e:
+        hin = [ins[k].cpu().pin_memory() for k in ins]
+        din = [torch.empty_like(ins[k]) for k in ins]
+        hout = [torch.empty(o[k].shape, dtype=o[k].dtype).pin_memory() for k in outs]
+        n_e2e = max(4, min(args.steps, 10))
+
+        def e2e_step():
+            for d, h in zip(din, hin):
+                d.copy_(h, non_blocking=True)
+            call(din[0], din[1], din[2], o, stream)
+            for h, k in zip(hout, outs):
+                h.copy_(o[k], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        _barrier(ws)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = _max_over_ranks(e0.elapsed_time(e1) / n_e2e, ws, dev)
+        e2e = {"value": N * ws / (ms_e2e * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hin)),
+               "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hout))}
+        del hin, din, hout
+    if rank != 0:
+        return
+    peak, peak_kind = _peaks()
+    kb = PATH_KERNEL_BYTES[args.path]
+    dom_name, (dom_n, dom_ms) = max(kern.items(), key=lambda kv: kv[1][1])
+    dom_avg = dom_ms / max(dom_n, 1)
+    achieved = kb.get(dom_name, 0) * N / (dom_avg * 1e-3) / 1e9
+    step_gbs = PATH_ALGO_BYTES[args.path] * N / (ms * 1e-3) / 1e9
+    out = {
+        "metric": PATH_METRIC[args.path], "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s on the %s pair" % (args.path, pair.workload.name), "shape": list(pair.F.shape),
+                   "voxels": N, "l2": "inputs larger than L2 (%.2f GB algorithmic bytes per step)"
+                                     % (PATH_ALGO_BYTES[args.path] * N / 1e9),
+                   "parallelism": "independent pair per rank" if ws > 1 else "single GPU"},
+        "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs, "of_8tbs": step_gbs / HBM_NOMINAL_GBS,
+                             "of_measured": step_gbs / peak, "bytes_per_voxel": PATH_ALGO_BYTES[args.path]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": _traffic_per_launch(dom_name, "%s 512^3" % args.path, N), "kernel": dom_name,
+                     "algorithmic_bytes_per_voxel": kb.get(dom_name, 0), "peak_source": peak_kind,
+                     "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": kb.get(k, 0),
+                                     "frac": kb.get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3) / 1e9 / peak}
+                                 for k, v in kern.items()}},
+        "kernels_ms_per_launch": {k: v[1] / max(v[0], 1) for k, v in kern.items()},
+        "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        n1, t1, _ = _path_oracle_sample(args, pair, 2)
+        ds = int(max(2, min(pair.F.shape[0], args.cpu_budget_s / max(t1 / 2.0, 1e-3))))
+        n, t, cores = _path_oracle_sample(args, pair, ds)
+        out["cpu_baseline"] = {"value": n / t / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": "oracle %s fwd+bwd on fixed planes z<%d of the %s pair (%d voxels, %.1f s)"
+                                         % (args.path, ds, "x".join(map(str, pair.F.shape)), n, t)}
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,6 +642,9 @@ def main():
     ap.add_argument("--shape", type=int, default=0, help="cube edge overriding the workload size (profiling)")
     ap.add_argument("--store-slope", type=int, default=1, choices=[0, 1],
                     help="MI-only objectives: store J and dJ/dp (1) or stay implicit (0)")
+    ap.add_argument("--path", default="objective", choices=["objective", "mse", "compose"],
+                    help="objective (default, --workload 4|5), or the MSE objective / warp composition "
+                         "on the 512^3 pair")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if ws > 1:
@@ -480,6 +653,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ws, rank, local)
+        elif args.path != "objective":
+            run_gpu_path(args, ws, rank, local)
         else:
             run_gpu(args, ws, rank, local)
     finally:

@@ -111,7 +111,10 @@ enum {
   FFDP_OP_GRID_SAMPLE_BWD = 1, /* params: NULL */
   FFDP_OP_MI = 2,              /* params: const ffdp_mi_params* */
   FFDP_OP_LNCC = 3,            /* params: const ffdp_lncc_params* */
-  FFDP_OP_OBJECTIVE = 4        /* params: const ffdp_objective_params* */
+  FFDP_OP_OBJECTIVE = 4,       /* params: const ffdp_objective_params* */
+  FFDP_OP_SAMPLE_CHANNELS_BWD = 5, /* params: NULL */
+  FFDP_OP_MSE = 6,             /* params: NULL */
+  FFDP_OP_OBJECTIVE_MSE = 7    /* params: NULL */
 };
 
 /* Bytes of device workspace a call of `op` on fixed grid `fixed` needs (0 for
@@ -166,6 +169,60 @@ ffdp_status ffdp_objective(const void *F, ffdp_dtype ft, ffdp_dims fdims, const 
                            const ffdp_transform *T, const ffdp_objective_params *p, float *loss,
                            float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
                            void *stream);
+
+/* ---- warp composition, image gradient, MSE -----------------------------
+ * "Background" of the paper: the similarity C may be MSE, LNCC or MI, and
+ * deformation interpolation / warp composition is one of the three memory
+ * bottlenecks it profiles; design 1's sampler applies to a volume with
+ * several channels unchanged, and its backward pass gives (as PyTorch's
+ * grid_sample does) the gradient with respect to the sampled volume too.
+ *
+ * A channel-last volume V is [vdims][C] float32 (C in [1, 4], channel
+ * fastest), e.g. a displacement field [D][H][W][3] like u, or the moving image
+ * itself with C = 1.  p = A x + t + S u as everywhere; zero padding per tap. */
+
+/* out[i][c] = V_c(p_i), plus (S u_i)_c when compose != 0.  compose (C = 3)
+ * is warp composition: with phi(x) = A x + t + S u(x) and a second warp
+ * y -> y + V(y) on V's normalised domain, V o phi composed is
+ * A x + t + d(x) with d = S u + V(phi(x)) (a composite warp with S = I), and
+ * out = d.  u may be NULL (u = 0); out is [out_dims][C] float32.  No
+ * workspace. */
+ffdp_status ffdp_sample_channels_fwd(const float *V, int C, ffdp_dims vdims, ffdp_dims out_dims,
+                                     const float *u, const ffdp_transform *T, int compose, float *out,
+                                     void *stream);
+
+/* Backward of ffdp_sample_channels_fwd given gout = dL/dout ([out_dims][C]):
+ *   e_i = sum_c gout_ic dV_c/dp (p_i),   du_i = S^T e_i (+ S^T gout_i if compose),
+ *   dA = sum_i e_i x_i^T,  dt = sum_i e_i,
+ *   dV[v][c] = sum_i gout_ic w_v(p_i)  (w_v: trilinear weight of tap v; the
+ *   gradient with respect to the sampled volume -- with C = 1 and V = M, dM).
+ * du ([out_dims][3]), dA (9), dt (3) and dV ([vdims][C]) may each be NULL.
+ * dV is overwritten: the call zeroes it, then adds every tap's share with
+ * float atomics, so its summation order (and last bits) vary between runs.
+ * Workspace: ffdp_workspace_bytes(FFDP_OP_SAMPLE_CHANNELS_BWD, out_dims, NULL). */
+ffdp_status ffdp_sample_channels_bwd(const float *V, int C, ffdp_dims vdims, ffdp_dims out_dims,
+                                     const float *u, const ffdp_transform *T, int compose,
+                                     const float *gout, float *du, float *dA, float *dt, float *dV,
+                                     void *ws, size_t ws_bytes, void *stream);
+
+/* MSE on a materialised J (design 5 calls MSE a per-voxel loss):
+ * loss[0] = (1/N) sum_k (J_k - F_k)^2;  dJ = 2 (J - F) / N ([dims] float32,
+ * may be NULL).  F has dtype ft; J is float32.
+ * Workspace: ffdp_workspace_bytes(FFDP_OP_MSE, dims, NULL). */
+ffdp_status ffdp_mse_fwd_bwd(const void *F, ffdp_dtype ft, const float *J, ffdp_dims dims, float *loss,
+                             float *dJ, void *ws, size_t ws_bytes, void *stream);
+
+/* The fused MSE objective L = w_mse * MSE(F, M o phi) in one pass over the
+ * fixed grid: J = M(Ax + t + Su) and its slope are sampled in registers, the
+ * per-voxel gradient 2 w_mse (J - F) / N goes straight into the sampler
+ * backward; nothing per-voxel is stored.
+ *   loss[2] (device float32) = { w_mse * MSE, MSE };  du [fdims][3], dA[9],
+ *   dt[3] as in ffdp_grid_sample_bwd (each may be NULL).  w_mse != 0.
+ * Workspace: ffdp_workspace_bytes(FFDP_OP_OBJECTIVE_MSE, fdims, NULL). */
+ffdp_status ffdp_objective_mse(const void *F, ffdp_dtype ft, ffdp_dims fdims, const void *M, ffdp_dtype mt,
+                               ffdp_dims mdims, const float *u, const ffdp_transform *T, float w_mse,
+                               float *loss, float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
+                               void *stream);
 
 /* Workspace-free variant of ffdp_objective for the MI term (the paper has no
  * counterpart; it exists for callers that cannot allocate device memory).

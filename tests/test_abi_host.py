@@ -110,3 +110,42 @@ def test_workspace_is_o1_for_mi_and_sampler(lib):
     c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (64, 64, 64), q)
     assert c >= 4 * 64 ** 3
     assert ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (1, 64, 64), q) == 0
+
+
+@nogpu
+def test_channel_sampler_and_mse_reject_invalid_arguments(lib):
+    from voxel_grid_sampler_gb300 import ffdp
+    n0 = lib.ffdp_launch_count()
+    T = ffdp.transform()
+    good = ffdp.dims_of((8, 8, 8))
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1004)
+    ws = ctypes.c_void_p(0x2000)
+    # channels outside [1, 4]; compose with C != 3; misaligned V; null gout
+    for C in (0, 5):
+        assert lib.ffdp_sample_channels_fwd(fake, C, good, good, None, ctypes.byref(T), 0, fake, None) == 1
+    assert lib.ffdp_sample_channels_fwd(fake, 2, good, good, None, ctypes.byref(T), 1, fake, None) == 1
+    assert lib.ffdp_sample_channels_fwd(odd, 3, good, good, None, ctypes.byref(T), 0, fake, None) == 1
+    assert lib.ffdp_sample_channels_bwd(fake, 3, good, good, None, ctypes.byref(T), 1, None, fake, fake, fake,
+                                        fake, ws, 1 << 30, None) == 1
+    assert lib.ffdp_sample_channels_bwd(fake, 3, good, good, None, ctypes.byref(T), 1, fake, fake, fake, fake,
+                                        odd, ws, 1 << 30, None) == 1
+    assert lib.ffdp_sample_channels_bwd(fake, 3, good, good, None, ctypes.byref(T), 1, fake, fake, fake, fake,
+                                        fake, ws, 16, None) == 3
+    # MSE: misaligned J, tiny dims, zero or non-finite weight, missing workspace
+    assert lib.ffdp_mse_fwd_bwd(fake, 0, odd, good, fake, fake, ws, 1 << 30, None) == 1
+    assert lib.ffdp_mse_fwd_bwd(fake, 0, fake, ffdp.dims_of((8, 1, 8)), fake, fake, ws, 1 << 30, None) == 1
+    for w in (0.0, float("inf")):
+        assert lib.ffdp_objective_mse(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), w, fake, fake, fake,
+                                      fake, ws, 1 << 30, None) == 1
+    assert lib.ffdp_objective_mse(fake, 0, good, fake, 0, good, fake, ctypes.byref(T), 1.0, fake, fake, fake,
+                                  fake, None, 0, None) == 3
+    assert lib.ffdp_launch_count() == n0
+
+
+def test_channel_and_mse_workspaces_are_o1(lib):
+    from voxel_grid_sampler_gb300 import ffdp
+    for op in (ffdp.FFDP_OP_SAMPLE_CHANNELS_BWD, ffdp.FFDP_OP_MSE, ffdp.FFDP_OP_OBJECTIVE_MSE):
+        a = ffdp.ffdp_workspace_bytes(op, (16, 16, 16))
+        b = ffdp.ffdp_workspace_bytes(op, (1024, 1024, 1024))
+        assert a == b > 0

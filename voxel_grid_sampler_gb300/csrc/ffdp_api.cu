@@ -399,6 +399,10 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
       if (ln && check_lncc(&p->lncc) != FFDP_OK) return 0;
       return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln, mi && p->store_slope != 0, N).total;
     }
+    case FFDP_OP_SAMPLE_CHANNELS_BWD:
+    case FFDP_OP_MSE:
+    case FFDP_OP_OBJECTIVE_MSE:
+      return ws_layout(false, 32, max_parts(), false, false, N).total;
   }
   return 0;
 }
@@ -709,6 +713,170 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     f.dx[c] = ((double)T->xmax[c] - (double)T->xmin[c]) / (nf - 1.0);
     f.xc[c] = (double)T->xmin[c] + f.dx[c] * (nf - 1.0) / 2.0;
   }
+  FFDP_CUDA(launch_finish(f, s), "finish launch");
+  return FFDP_OK;
+}
+
+// ------------------------------------------- C-channel sampler (composition)
+namespace {
+
+ffdp_status check_channels(const float* V, int C, ffdp_dims vdims, ffdp_dims out_dims, int compose) {
+  if (!V) return fail(FFDP_ERR_INVALID_ARGUMENT, "null V");
+  if (C < 1 || C > 4) return fail(FFDP_ERR_INVALID_ARGUMENT, "channels must be in [1, 4] (got %d)", C);
+  if (compose && C != 3) return fail(FFDP_ERR_INVALID_ARGUMENT, "compose needs a 3-channel displacement field V");
+  FFDP_TRY(check_dims(vdims, "V"));
+  FFDP_TRY(check_dims(out_dims, "output"));
+  if (!aligned16(V)) return fail(FFDP_ERR_INVALID_ARGUMENT, "V must be 16-byte aligned");
+  return FFDP_OK;
+}
+
+void fill_finish_affine(FinishArgs& f, ffdp_dims fdims, ffdp_dims mdims, const ffdp_transform* T) {
+  for (int c = 0; c < 3; ++c) {
+    const double nf = c == 0 ? (double)fdims.w : (c == 1 ? (double)fdims.h : (double)fdims.d);
+    const double nmv = c == 0 ? (double)mdims.w : (c == 1 ? (double)mdims.h : (double)mdims.d);
+    f.hM[c] = (nmv - 1.0) / 2.0;
+    f.dx[c] = ((double)T->xmax[c] - (double)T->xmin[c]) / (nf - 1.0);
+    f.xc[c] = (double)T->xmin[c] + f.dx[c] * (nf - 1.0) / 2.0;
+  }
+}
+
+int chan_grid(uint64_t N, int C, int compose, int bwd) {
+  const uint64_t ctas = (N + kChanThreads - 1) / kChanThreads;
+  const uint64_t slots = (uint64_t)(sm_count() > 0 ? sm_count() : 1) * chan_ctas_per_sm(C, compose, bwd);
+  return (int)(ctas < slots ? (ctas < 1 ? 1 : ctas) : slots);
+}
+
+}  // namespace
+
+extern "C" ffdp_status ffdp_sample_channels_fwd(const float* V, int C, ffdp_dims vdims, ffdp_dims out_dims,
+                                                const float* u, const ffdp_transform* T, int compose, float* out,
+                                                void* stream) {
+  g_err[0] = '\0';
+  if (!T || !out) return fail(FFDP_ERR_INVALID_ARGUMENT, "null T or out");
+  FFDP_TRY(check_channels(V, C, vdims, out_dims, compose));
+  if (!aligned16(out) || (u && !aligned16(u))) return fail(FFDP_ERR_INVALID_ARGUMENT, "out and u must be 16-byte aligned");
+  ChanArgs a{};
+  FFDP_TRY(make_geom(out_dims, vdims, T, a.g));
+  a.V = V;
+  a.u = u;
+  a.out = out;
+  for (int k = 0; k < 9; ++k) a.S[k] = T->S[k];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FFDP_CUDA(launch_chan_fwd(C, compose, a, chan_grid(a.g.N, C, compose, 0), s), "channel sampler launch");
+  return FFDP_OK;
+}
+
+extern "C" ffdp_status ffdp_sample_channels_bwd(const float* V, int C, ffdp_dims vdims, ffdp_dims out_dims,
+                                                const float* u, const ffdp_transform* T, int compose,
+                                                const float* gout, float* du, float* dA, float* dt, float* dV,
+                                                void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!T || !gout) return fail(FFDP_ERR_INVALID_ARGUMENT, "null T or gout");
+  FFDP_TRY(check_channels(V, C, vdims, out_dims, compose));
+  if ((u && !aligned16(u)) || !aligned16(gout) || (du && !aligned16(du)) || (dV && !aligned16(dV)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "u, gout, du and dV must be 16-byte aligned");
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(out_dims));
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  ChanArgs a{};
+  FFDP_TRY(make_geom(out_dims, vdims, T, a.g));
+  a.V = V;
+  a.u = u;
+  a.gout = gout;
+  a.du = du;
+  a.dV = dV;
+  a.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
+  a.nV = (long long)nvox(vdims) * C;
+  for (int k = 0; k < 9; ++k) a.S[k] = T->S[k];
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dV) FFDP_CUDA(launch_zero_f32(dV, a.nV, s), "dV zero launch");
+  const int grid = chan_grid(a.g.N, C, compose, 1);
+  FFDP_CUDA(launch_chan_bwd(C, compose, a, grid, s), "channel sampler backward launch");
+  if (dA || dt) {
+    FinishArgs f{};
+    f.partials = a.partials;
+    f.nparts = grid;
+    f.dA = dA;
+    f.dt = dt;
+    f.has_affine = 1;
+    fill_finish_affine(f, out_dims, vdims, T);
+    FFDP_CUDA(launch_finish(f, s), "finish launch");
+  }
+  return FFDP_OK;
+}
+
+// ------------------------------------------------------------------- MSE
+extern "C" ffdp_status ffdp_mse_fwd_bwd(const void* F, ffdp_dtype ft, const float* J, ffdp_dims dims, float* loss,
+                                        float* dJ, void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!F || !J || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null F, J or loss");
+  FFDP_TRY(check_dtype(ft, "F"));
+  FFDP_TRY(check_dims(dims, "image"));
+  if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims));
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MseArgs a{};
+  a.F = F;
+  a.J = J;
+  a.dJ = dJ;
+  a.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
+  a.N = (unsigned)nvox(dims);
+  a.c = (float)(2.0 / (double)a.N);
+  const int grid = chan_grid((a.N + 3) / 4, 0, 0, 0);
+  FFDP_CUDA(launch_mse(ft, a, grid, s), "MSE launch");
+  FinishArgs f{};
+  f.partials = a.partials;
+  f.nparts = grid;
+  f.loss = loss;
+  f.nloss = 1;
+  f.has_mse = 1;
+  f.w_mse = 1.0;
+  f.N = (double)a.N;
+  FFDP_CUDA(launch_finish(f, s), "finish launch");
+  return FFDP_OK;
+}
+
+extern "C" ffdp_status ffdp_objective_mse(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M,
+                                          ffdp_dtype mt, ffdp_dims mdims, const float* u, const ffdp_transform* T,
+                                          float w_mse, float* loss, float* du, float* dA, float* dt, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!F || !M || !T || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null F, M, T or loss");
+  FFDP_TRY(check_dtype(ft, "F"));
+  FFDP_TRY(check_dtype(mt, "M"));
+  FFDP_TRY(check_dims(fdims, "fixed"));
+  FFDP_TRY(check_dims(mdims, "moving"));
+  if (!std::isfinite(w_mse) || w_mse == 0.0f) return fail(FFDP_ERR_INVALID_ARGUMENT, "w_mse must be finite and non-zero");
+  if (!aligned16(F) || (u && !aligned16(u)) || (du && !aligned16(du)))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "F, u and du must be 16-byte aligned");
+  const uint64_t N = nvox(fdims);
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, N);
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Sweep2Args a2{};
+  FFDP_TRY(make_geom(fdims, mdims, T, a2.g));
+  a2.F = F;
+  a2.M = M;
+  a2.u = u;
+  a2.du = du;
+  a2.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
+  a2.mse_c = (float)(2.0 * (double)w_mse / (double)N);
+  a2.nIter = n_iter2(N, S2_MSE);
+  const int grid = persistent_grid(a2.nIter, sweep2_ctas_per_sm(S2_MSE, ft, mt, 32));
+  FFDP_CUDA(launch_sweep2(S2_MSE, ft, mt, 32, a2, grid, s), "MSE sweep launch");
+  FinishArgs f{};
+  f.partials = a2.partials;
+  f.nparts = grid;
+  f.dA = dA;
+  f.dt = dt;
+  f.loss = loss;
+  f.nloss = 2;
+  f.N = (double)N;
+  f.w_mse = w_mse;
+  f.has_mse = 1;
+  f.has_affine = 1;
+  fill_finish_affine(f, fdims, mdims, T);
   FFDP_CUDA(launch_finish(f, s), "finish launch");
   return FFDP_OK;
 }

@@ -41,7 +41,8 @@ constexpr int kPartialStride = 16;      // doubles per CTA partial record
 //   [0..2]  s_r   = sum g dJ/dq_r
 //   [3..11] m_rc  = sum g dJ/dq_r (i_c - c_c)   (c_c: grid centre index)
 //   [12]    sum cc (LNCC)
-enum { kPS = 0, kPM = 3, kPCC = 12 };
+//   [13]    sum (J - F)^2 (MSE)
+enum { kPS = 0, kPM = 3, kPCC = 12, kPSE = 13 };
 
 // ------------------------------------------------------------ geometry
 // Fixed-grid index i = (ix, iy, iz) maps to moving-image voxel coordinates

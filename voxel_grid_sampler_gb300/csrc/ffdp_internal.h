@@ -26,14 +26,15 @@ enum Sweep1Mode { S1_HIST = 0, S1_HIST_WRITEJ = 1, S1_WRITEJ = 2, S1_HIST_JBUF =
 constexpr int kSweep1Modes = 6;
 // Sweep 2: MI gradient + sampler backward; sampler backward of a given g;
 // MI gradient of a given J; backward of a given g with the stored dJ/dq (no
-// gathers); MI gradient + backward from the stored J and dJ/dq (no gathers).
-enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2, S2_GBUF_DJ = 3, S2_MI_DJ = 4 };
+// gathers); MI gradient + backward from the stored J and dJ/dq (no gathers);
+// MSE gradient 2 w (J - F) / N + backward, one pass (gathers).
+enum Sweep2Mode { S2_MI = 0, S2_GBUF = 1, S2_MI_JBUF = 2, S2_GBUF_DJ = 3, S2_MI_DJ = 4, S2_MSE = 5 };
 // threads per CTA of a gradient-sweep mode: the gathering modes at
 // kSweep2Threads, the streaming ones at kSweep2StreamThreads
 __host__ __device__ constexpr int sweep2_threads(int mode) {
-  return (mode == S2_MI || mode == S2_GBUF) ? kSweep2Threads : kSweep2StreamThreads;
+  return (mode == S2_MI || mode == S2_GBUF || mode == S2_MSE) ? kSweep2Threads : kSweep2StreamThreads;
 }
-constexpr int kSweep2Modes = 5;
+constexpr int kSweep2Modes = 6;
 enum LnccMode { LN_DJ = 0, LN_DU = 1 };  // write dL/dJ; or du and affine partials from the stored slope
 
 // Histogram sweep / forward sampler.
@@ -68,6 +69,7 @@ struct Sweep2Args {
   BinMap bf, bj;
   int B;
   unsigned nIter;
+  float mse_c;        // S2_MSE: g = mse_c (J - F), mse_c = 2 w_mse / N
 };
 
 // MI table: normalise the histogram, MI value, packed T = ln P - ln P_F - ln P_J.
@@ -110,11 +112,36 @@ struct FinishArgs {
   float* dA;
   float* dt;
   float* loss;            // NULL or [nloss]
-  int nloss;              // 1 (single-term ops) or 3 (objective)
+  int nloss;              // 1 (single-term ops), 2 (MSE objective) or 3 (objective)
   double hM[3], xc[3], dx[3];
   double N;
-  double w_mi, w_lncc;
-  int has_mi, has_lncc, has_affine;
+  double w_mi, w_lncc, w_mse;
+  int has_mi, has_lncc, has_mse, has_affine;
+};
+
+// C-channel sampler (warp composition / image gradient): V is channel-last
+// [Dv][Hv][Wv][C] float32; the geometry's moving extents are V's.
+struct ChanArgs {
+  const float* V;
+  const float* u;     // [N][3] or NULL (u = 0)
+  const float* gout;  // backward: [N][C]
+  float* out;         // forward: [N][C]
+  float* du;          // backward: [N][3] or NULL
+  float* dV;          // backward: [Dv Hv Wv][C] or NULL (zeroed by the call, then scattered into)
+  double* partials;   // backward: [gridDim.x][kPartialStride]
+  Geom g;
+  float S[9];         // compose: the out / du terms S u and S^T gout
+  long long nV;       // Dv Hv Wv C
+};
+
+// MSE of a materialised J: per-CTA partial sum (J - F)^2, dJ = c (J - F).
+struct MseArgs {
+  const void* F;
+  const float* J;
+  float* dJ;          // or NULL
+  double* partials;
+  unsigned N;
+  float c;            // 2 / N
 };
 
 // Launchers (return cudaGetLastError() after the launch).
@@ -124,6 +151,12 @@ cudaError_t launch_sweep2(int mode, int ft, int mt, int bmax, const Sweep2Args& 
 cudaError_t launch_finalize(int bmax, const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_lncc(int mode, int ft, int mt, int bmax_or0, const LnccArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s);
+cudaError_t launch_chan_fwd(int C, int compose, const ChanArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_chan_bwd(int C, int compose, const ChanArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_zero_f32(float* p, long long n, cudaStream_t s);
+cudaError_t launch_mse(int ft, const MseArgs& a, int grid, cudaStream_t s);
+int chan_ctas_per_sm(int C, int compose, int bwd);
+constexpr int kChanThreads = 256;  // threads per CTA of the channel sampler and the MSE kernel
 
 // Occupancy-derived persistent grid sizes (CTAs per SM), cached.
 // Test hook: returns and clears the one-shot ring stall request.

@@ -790,23 +790,27 @@ __global__ void __launch_bounds__(256) k_mi_finalize(const FinalizeArgs a) {
 template <typename FT, int BMAX, int MODE>
 struct S2Cfg {
   static constexpr bool MI = MODE == S2_MI || MODE == S2_MI_JBUF || MODE == S2_MI_DJ;  // g from the MI table
-  static constexpr bool GATHER = MODE == S2_MI || MODE == S2_GBUF;                     // resample J and dJ/dq
+  static constexpr bool MSE = MODE == S2_MSE;                                          // g = c (J - F)
+  static constexpr bool GATHER = MODE == S2_MI || MODE == S2_GBUF || MSE;              // resample J and dJ/dq
   static constexpr bool VEC = GATHER || MODE == S2_GBUF_DJ || MODE == S2_MI_DJ;        // u or the stored dJ/dq
   static constexpr bool BWD = MODE != S2_MI_JBUF;                                      // du and affine partials
-  static constexpr bool XS = MODE != S2_MI;                                            // g or J (given / stored)
+  static constexpr bool XS = MODE != S2_MI && !MSE;                                    // g or J (given / stored)
+  static constexpr bool LF = MI || MSE;                                                // F streamed
+  static constexpr int NACC = MSE ? 13 : 12;                                           // + sum (J - F)^2
   static constexpr size_t kTableBytes = MI ? (size_t)table_floats<BMAX>() * sizeof(float) : 0;
   static constexpr int NT = sweep2_threads(MODE);
-  using RG1 = Ring<FT, VEC, MI, XS, 1, NT>;
+  using RG1 = Ring<FT, VEC, LF, XS, 1, NT>;
   // as many ring slots (up to 4) as fit next to the table in 220 KiB
   static constexpr int NST_FIT = (int)((220 * 1024 - kTableBytes - (NT / 32) * 96) / ((NT / 32) * (RG1::kSlot + 8)));
   static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
   static_assert(NST >= 2, "ring needs two slots");
-  using RG = Ring<FT, VEC, MI, XS, NST, NT>;
+  using RG = Ring<FT, VEC, LF, XS, NST, NT>;
   static constexpr size_t kSmem = kTableBytes + RG::kBytes;
 };
 
-template <typename MT, int BMAX, bool MI, bool GATHER, bool BWD>
-__device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, const Sweep2Args& a, float acc[12]) {
+template <typename MT, int BMAX, bool MI, bool GATHER, bool BWD, bool MSE = false>
+__device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, const Sweep2Args& a,
+                                            float acc[MSE ? 13 : 12]) {
   const Geom& g = a.g;
   if constexpr (!BWD) {
 #pragma unroll
@@ -824,7 +828,13 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
 #pragma unroll
         for (int q = 0; q < 8; ++q) m[q] = tap_value<MT>(H.taps[j][q]);
         const float jv = interp8<true>(m, H.rr[j], gq0, gq1, gq2);
-        gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
+        if constexpr (MSE) {
+          const float d = jv - H.f[j];
+          gv = a.mse_c * d;
+          acc[12] = fmaf(d, d, acc[12]);  // this thread's sum (J - F)^2
+        } else {
+          gv = MI ? mi_grad<BMAX>(tsm, a.bf, a.bj, H.f[j], jv) : H.x[j];
+        }
       } else {
         // the stored slope of J, and g given or from the MI table at the stored J
         gq0 = H.rr[j][0];
@@ -884,14 +894,15 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
 template <typename FT, typename MT, int BMAX, int MODE>
 __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2Args a) {
   using C = S2Cfg<FT, BMAX, MODE>;
-  constexpr bool MI = C::MI, GATHER = C::GATHER, VEC = C::VEC, BWD = C::BWD, XS = C::XS;
-  constexpr int NST = C::NST;
+  constexpr bool MI = C::MI, GATHER = C::GATHER, VEC = C::VEC, BWD = C::BWD, XS = C::XS, MSE = C::MSE;
+  constexpr bool LF = C::LF;
+  constexpr int NST = C::NST, NACC = C::NACC;
   using RG = typename C::RG;
   using WR = WarpRing<RG, NST>;
   extern __shared__ float4 tsm4[];
   float* tsm = reinterpret_cast<float*>(tsm4);
   constexpr int NT = C::NT;
-  __shared__ double wsum[NT / 32][12];
+  __shared__ double wsum[NT / 32][NACC];
   const Geom& g = a.g;
   if (MI) {
     constexpr int n4 = table_floats<BMAX>() / 4;
@@ -906,10 +917,10 @@ __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (BWD && lane == 0)
 #pragma unroll
-    for (int q = 0; q < 12; ++q) wsum[warp][q] = 0.0;
-  float acc[12];
+    for (int q = 0; q < NACC; ++q) wsum[warp][q] = 0.0;
+  float acc[NACC];
 #pragma unroll
-  for (int q = 0; q < 12; ++q) acc[q] = 0.0f;
+  for (int q = 0; q < NACC; ++q) acc[q] = 0.0f;
   WR wr;
   wr.init(reinterpret_cast<char*>(tsm4) + C::kTableBytes, VEC && U != nullptr);
   RingSched<WR, NST> rs{a.nIter, g.N / RG::kChunk, -1};
@@ -918,15 +929,15 @@ __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2
   LaneWalk w;
   Half A, B;
   unsigned k = 0;
-  if constexpr (GATHER) prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  if constexpr (GATHER) prepare<FT, MT, LF, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
     if constexpr (GATHER) {
       // gathers of the next half are in flight while the current one computes
-      prepare<FT, MT, MI, VEC, XS, GATHER>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
-      sweep2_half<MT, BMAX, MI, GATHER, BWD>(A, tsm, a, acc);
-      prepare<FT, MT, MI, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
-      sweep2_half<MT, BMAX, MI, GATHER, BWD>(B, tsm, a, acc);
+      prepare<FT, MT, LF, VEC, XS, GATHER>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
+      sweep2_half<MT, BMAX, MI, GATHER, BWD, MSE>(A, tsm, a, acc);
+      prepare<FT, MT, LF, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+      sweep2_half<MT, BMAX, MI, GATHER, BWD, MSE>(B, tsm, a, acc);
     } else {
       prepare_chunk<FT, MI, VEC, XS>(A, B, g, F, U, X, wr, rs, it, k, pol);
       sweep2_half<MT, BMAX, MI, GATHER, BWD>(A, tsm, a, acc);
@@ -934,7 +945,7 @@ __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2
     }
     if (BWD && ++pending == kFoldEvery) {
 #pragma unroll
-      for (int q = 0; q < 12; ++q) {
+      for (int q = 0; q < NACC; ++q) {
         const float s = warp_sum(acc[q]);
         if (lane == 0) wsum[warp][q] += (double)s;
         acc[q] = 0.0f;
@@ -945,15 +956,17 @@ __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2
   rs.drain(wr);
   if (BWD) {
 #pragma unroll
-    for (int q = 0; q < 12; ++q) {
+    for (int q = 0; q < NACC; ++q) {
       const float s = warp_sum(acc[q]);
       if (lane == 0) wsum[warp][q] += (double)s;
     }
     __syncthreads();
     if (threadIdx.x < kPartialStride) {
+      // acc[12] (MSE) goes to record slot kPSE; slot kPCC stays 0
+      const int q = threadIdx.x < 12 ? (int)threadIdx.x : (MSE && threadIdx.x == kPSE ? 12 : -1);
       double s = 0.0;
-      if (threadIdx.x < 12)
-        for (int q = 0; q < NT / 32; ++q) s += wsum[q][threadIdx.x];
+      if (q >= 0)
+        for (int w2 = 0; w2 < NT / 32; ++w2) s += wsum[w2][q];
       a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = s;
     }
   }
@@ -993,7 +1006,15 @@ __global__ void __launch_bounds__(256) k_finish(const FinishArgs a) {
       if (a.has_mi)
         for (int r = 0; r < a.mi_rows; ++r) mi += a.scalars[r];  // fixed order
       const double lncc = a.has_lncc ? sm[kPCC][16] / a.N : 0.0;
-      if (a.nloss == 3) {
+      const double mse = a.has_mse ? sm[kPSE][16] / a.N : 0.0;
+      if (a.has_mse) {
+        if (a.nloss == 2) {
+          a.loss[0] = (float)(a.w_mse * mse);
+          a.loss[1] = (float)mse;
+        } else {
+          a.loss[0] = (float)mse;
+        }
+      } else if (a.nloss == 3) {
         a.loss[0] = (float)(a.w_mi * (-mi) + a.w_lncc * (-lncc));
         a.loss[1] = (float)(-mi);
         a.loss[2] = (float)(-lncc);
@@ -1093,6 +1114,7 @@ static cudaError_t dispatch_sweep2(int mode, int ft, int mt, int bmax, const Swe
         case S2_MI_JBUF: e = run_sweep2<FT, float, 32, S2_MI_JBUF>(a, grid, s, occ); break;
         case S2_GBUF_DJ: e = run_sweep2<float, float, 32, S2_GBUF_DJ>(a, grid, s, occ); break;
         case S2_MI_DJ: e = run_sweep2<FT, float, 32, S2_MI_DJ>(a, grid, s, occ); break;
+        case S2_MSE: e = run_sweep2<FT, MT, 32, S2_MSE>(a, grid, s, occ); break;
       }
     } else {
       switch (mode) {
@@ -1101,6 +1123,7 @@ static cudaError_t dispatch_sweep2(int mode, int ft, int mt, int bmax, const Swe
         case S2_MI_JBUF: e = run_sweep2<FT, float, 64, S2_MI_JBUF>(a, grid, s, occ); break;
         case S2_GBUF_DJ: e = run_sweep2<float, float, 32, S2_GBUF_DJ>(a, grid, s, occ); break;
         case S2_MI_DJ: e = run_sweep2<FT, float, 64, S2_MI_DJ>(a, grid, s, occ); break;
+        case S2_MSE: e = run_sweep2<FT, MT, 32, S2_MSE>(a, grid, s, occ); break;
       }
     }
   }));

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libffdp.so")
 
 FFDP_F32, FFDP_F16 = 0, 1
 FFDP_OP_GRID_SAMPLE_BWD, FFDP_OP_MI, FFDP_OP_LNCC, FFDP_OP_OBJECTIVE = 1, 2, 3, 4
+FFDP_OP_SAMPLE_CHANNELS_BWD, FFDP_OP_MSE, FFDP_OP_OBJECTIVE_MSE = 5, 6, 7
 STATUS = {0: "FFDP_OK", 1: "FFDP_ERR_INVALID_ARGUMENT", 2: "FFDP_ERR_UNSUPPORTED",
           3: "FFDP_ERR_WORKSPACE", 4: "FFDP_ERR_CUDA", 5: "FFDP_ERR_INTERNAL"}
 
@@ -82,8 +83,18 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(ffdp_transform),
                                      ctypes.POINTER(ffdp_objective_params), _vp, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp]
+        L.ffdp_sample_channels_fwd.argtypes = [_vp, ctypes.c_int, ffdp_dims, ffdp_dims, _vp,
+                                               ctypes.POINTER(ffdp_transform), ctypes.c_int, _vp, _vp]
+        L.ffdp_sample_channels_bwd.argtypes = [_vp, ctypes.c_int, ffdp_dims, ffdp_dims, _vp,
+                                               ctypes.POINTER(ffdp_transform), ctypes.c_int, _vp, _vp, _vp,
+                                               _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.ffdp_mse_fwd_bwd.argtypes = [_vp, ctypes.c_int, _vp, ffdp_dims, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.ffdp_objective_mse.argtypes = [_vp, ctypes.c_int, ffdp_dims, _vp, ctypes.c_int, ffdp_dims, _vp,
+                                         ctypes.POINTER(ffdp_transform), ctypes.c_float, _vp, _vp, _vp, _vp,
+                                         _vp, ctypes.c_size_t, _vp]
         for f in ("ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd", "ffdp_mi_fwd_bwd",
-                  "ffdp_lncc_fwd_bwd", "ffdp_objective"):
+                  "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_sample_channels_fwd",
+                  "ffdp_sample_channels_bwd", "ffdp_mse_fwd_bwd", "ffdp_objective_mse"):
             getattr(L, f).restype = ctypes.c_int
         L.ffdp_status_string.restype = ctypes.c_char_p
         L.ffdp_status_string.argtypes = [ctypes.c_int]
@@ -274,6 +285,82 @@ def ffdp_objective(F, M, u, T: ffdp_transform, params: ffdp_objective_params, lo
 
 
 # ------------------------------------------------------------ instrumentation
+def ffdp_sample_channels_fwd(V, out_shape, u, T: ffdp_transform, compose=False, out=None, stream=None):
+    """out = V(A x + t + S u) (+ S u when compose) for a channel-last float32 volume V
+    of shape (Dv, Hv, Wv, C); returns (D, H, W, C)."""
+    _dev(V, "V", torch.float32, 4)
+    _dev(u, "u", torch.float32, 4)
+    C = int(V.shape[3])
+    if out is None:
+        out = torch.empty(tuple(out_shape) + (C,), dtype=torch.float32, device=V.device)
+    _dev(out, "out", torch.float32, 4)
+    _check(lib().ffdp_sample_channels_fwd(_ptr(V), C, dims_of(V.shape[:3]), dims_of(out_shape), _ptr(u),
+                                          ctypes.byref(T), int(bool(compose)), _ptr(out), _stream(stream)))
+    return out
+
+
+def ffdp_sample_channels_bwd(V, u, T: ffdp_transform, gout, compose=False, du=None, dA=None, dt=None,
+                             dV=None, ws=None, stream=None, want_du=True, want_dV=True):
+    """Backward of ffdp_sample_channels_fwd: returns (du, dA, dt, dV)."""
+    _dev(V, "V", torch.float32, 4)
+    _dev(u, "u", torch.float32, 4)
+    _dev(gout, "gout", torch.float32, 4)
+    C = int(V.shape[3])
+    shape = tuple(gout.shape[:3])
+    dev = V.device
+    if du is None and want_du:
+        du = torch.empty(shape + (3,), dtype=torch.float32, device=dev)
+    if dV is None and want_dV:
+        dV = torch.empty_like(V)
+    if dA is None:
+        dA = torch.empty(9, dtype=torch.float32, device=dev)
+    if dt is None:
+        dt = torch.empty(3, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(FFDP_OP_SAMPLE_CHANNELS_BWD, shape, None, dev)
+    _check(lib().ffdp_sample_channels_bwd(_ptr(V), C, dims_of(V.shape[:3]), dims_of(shape), _ptr(u),
+                                          ctypes.byref(T), int(bool(compose)), _ptr(gout), _ptr(du), _ptr(dA),
+                                          _ptr(dt), _ptr(dV), _ptr(ws), ws.numel(), _stream(stream)))
+    return du, dA, dt, dV
+
+
+def ffdp_mse_fwd_bwd(F, J, loss=None, dJ=None, ws=None, stream=None, want_grad=True):
+    _dev(F, "F", ndim=3)
+    _dev(J, "J", torch.float32, 3)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=F.device)
+    if dJ is None and want_grad:
+        dJ = torch.empty_like(J)
+    if ws is None:
+        ws = workspace(FFDP_OP_MSE, F.shape, None, F.device)
+    _check(lib().ffdp_mse_fwd_bwd(_ptr(F), _dtype_code(F), _ptr(J), dims_of(F.shape), _ptr(loss), _ptr(dJ),
+                                  _ptr(ws), ws.numel(), _stream(stream)))
+    return loss, dJ
+
+
+def ffdp_objective_mse(F, M, u, T: ffdp_transform, w_mse=1.0, loss=None, du=None, dA=None, dt=None,
+                       ws=None, stream=None, want_du=True):
+    """Fused L = w_mse * MSE(F, M o phi): returns (loss[2] = {w_mse MSE, MSE}, du, dA, dt)."""
+    _dev(F, "F", ndim=3)
+    _dev(M, "M", ndim=3)
+    _dev(u, "u", torch.float32, 4)
+    dev = F.device
+    if loss is None:
+        loss = torch.empty(2, dtype=torch.float32, device=dev)
+    if du is None and want_du:
+        du = torch.empty(tuple(F.shape) + (3,), dtype=torch.float32, device=dev)
+    if dA is None:
+        dA = torch.empty(9, dtype=torch.float32, device=dev)
+    if dt is None:
+        dt = torch.empty(3, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(FFDP_OP_OBJECTIVE_MSE, F.shape, None, dev)
+    _check(lib().ffdp_objective_mse(_ptr(F), _dtype_code(F), dims_of(F.shape), _ptr(M), _dtype_code(M),
+                                    dims_of(M.shape), _ptr(u), ctypes.byref(T), float(w_mse), _ptr(loss),
+                                    _ptr(du), _ptr(dA), _ptr(dt), _ptr(ws), ws.numel(), _stream(stream)))
+    return loss, du, dA, dt
+
+
 def launch_count() -> int:
     return int(lib().ffdp_launch_count())
 
