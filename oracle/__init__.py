@@ -15,6 +15,9 @@ objective:
     dL/dJ  = w_mi * d(-MI)/dJ + w_lncc * d(-LNCC)/dJ
     du, dA, dt = sampler backward of dL/dJ         (design 1)
 
+and, for the next rows of the path, the sampler on a C-channel volume (warp
+composition, the gradient dV of the sampled volume) and the MSE objective.
+
 Inputs are numpy arrays holding exactly the values the GPU path receives:
 fp16 volumes are widened to float32 (exact), transforms are the float32 values
 widened to float64 (exact).

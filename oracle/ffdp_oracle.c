@@ -23,7 +23,11 @@
  *                (P = sum_h (N_h/N) P^(h)), which lets callers accumulate
  *                histograms slab by slab with oracle_mi_accumulate.
  *   "Background" -- the objective L = C(F, M o phi) + R(phi) with
- *                phi(x) = Ax + t + u(x).
+ *                phi(x) = Ax + t + u(x), C one of MSE, LNCC or MI, and warp
+ *                composition among the memory bottlenecks: the sampler on a
+ *                C-channel volume (oracle_sample_channels[_bwd], including
+ *                the gradient with respect to the sampled volume) and the
+ *                MSE similarity (oracle_mse).
  *
  * Readings where the page is silent (each also stated at its use):
  *   - coordinates follow the PyTorch grid_sample convention: normalised

@@ -16,9 +16,9 @@
 // loads and out / du stores cover contiguous spans and the trilinear taps of
 // 32 neighbouring points share cache lines of V.  V is channel-last, so the C
 // channels of one tap are adjacent (one 16-byte load for C = 4, 8 bytes for
-// C = 2).  The image gradient dV is a scatter: every tap adds gout * weight
-// with a global reduction (vector reductions for C = 2 and 4), which L2
-// resolves; the affine partial sums are kept per thread in fp32 and folded
+// C = 2).  The image gradient dV is a scatter: every cell row adds gout *
+// weight for its two x taps with 16-byte vector reductions (red_pair), which
+// L2 resolves; the affine partial sums are kept per thread in fp32 and folded
 // into per-warp fp64 sums every kChanFold voxel groups, then per CTA.
 #include "ffdp_internal.h"
 
@@ -50,6 +50,20 @@ __device__ __forceinline__ void load_tap(const float* __restrict__ V, long long 
 // nothing).
 __device__ __forceinline__ void corner_index(const Geom& g, const int b[3], long long idx[8]) {
   const int bx = b[0], by = b[1], bz = b[2];
+  if ((unsigned)bx < (unsigned)(g.mW - 1) && (unsigned)by < (unsigned)(g.mH - 1) &&
+      (unsigned)bz < (unsigned)(g.mD - 1)) {
+    // interior cell: one base index, fixed corner offsets
+    const long long o = ((long long)bz * g.mH + by) * g.mW + bx;
+    idx[0] = o;
+    idx[1] = o + 1;
+    idx[2] = o + g.mW;
+    idx[3] = o + g.mW + 1;
+    idx[4] = o + g.mHW;
+    idx[5] = o + g.mHW + 1;
+    idx[6] = o + g.mHW + g.mW;
+    idx[7] = o + g.mHW + g.mW + 1;
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int x = bx + (k & 1), y = by + ((k >> 1) & 1), z = bz + (k >> 2);
@@ -72,6 +86,47 @@ __device__ __forceinline__ void gather_c(const float* __restrict__ V, const long
     }
 #pragma unroll
     for (int c = 0; c < C; ++c) m[c][k] = v[c];
+  }
+}
+
+// Adds vals[0 .. 2C) to dV[f0 .. f0 + 2C) (the two x taps of one cell row,
+// adjacent in a channel-last volume; a tap outside V has zero vals) with
+// 16-byte vector reductions over the aligned 4-float chunks covering the
+// span, padded with zeros (adding 0 leaves a value unchanged).  A chunk that
+// would reach outside dV[0 .. nV) is sent as scalar reductions of the span's
+// own elements instead.  The chunk offset off = f0 mod 4 selects, for every
+// chunk element, which val (or 0) it carries, by compile-time unrolled
+// selects (no dynamically indexed register array).
+template <int C>
+__device__ __forceinline__ void red_pair(float* __restrict__ dV, long long nV, long long f0, const float vals[2 * C]) {
+  constexpr int N = 2 * C;
+  constexpr int NCH = (3 + N + 3) / 4;  // chunks for the worst offset
+  const long long a = f0 & ~3ll;
+  const int off = (int)(f0 - a);
+  const int nch = (off + N + 3) >> 2;
+#pragma unroll
+  for (int k = 0; k < NCH; ++k) {
+    if (k >= nch) break;
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * k + j;  // element of the chunk run; source val index e - off
+      const float c0 = (e < N) ? vals[e] : 0.0f;
+      const float c1 = (e - 1 >= 0 && e - 1 < N) ? vals[e - 1] : 0.0f;
+      const float c2 = (e - 2 >= 0 && e - 2 < N) ? vals[e - 2] : 0.0f;
+      const float c3 = (e - 3 >= 0 && e - 3 < N) ? vals[e - 3] : 0.0f;
+      v[j] = off == 0 ? c0 : (off == 1 ? c1 : (off == 2 ? c2 : c3));
+    }
+    const long long base = a + 4 * k;
+    if (base >= 0 && base + 4 <= nV) {
+      atomicAdd(reinterpret_cast<float4*>(dV + base), make_float4(v[0], v[1], v[2], v[3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int src = 4 * k + j - off;
+        if (src >= 0 && src < N && base + j >= 0 && base + j < nV) atomicAdd(dV + base + j, v[j]);
+      }
+    }
   }
 }
 
@@ -179,20 +234,23 @@ __global__ void __launch_bounds__(kChanThreads) k_chan_bwd(const ChanArgs a) {
         for (int c = 0; c < 3; ++c) acc[kPM + 3 * rr + c] = fmaf(e[rr], cc[c], acc[kPM + 3 * rr + c]);
       }
       if (a.dV) {
+        // per row of the cell, both x taps at once (their 2C floats are adjacent)
         const float wx[2] = {1.0f - r[0], r[0]}, wy[2] = {1.0f - r[1], r[1]}, wz[2] = {1.0f - r[2], r[2]};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (idx[k] < 0) continue;
-          const float w = wx[k & 1] * wy[(k >> 1) & 1] * wz[k >> 2];
-          float* p = a.dV + idx[k] * C;
-          if constexpr (C == 4) {
-            atomicAdd(reinterpret_cast<float4*>(p), make_float4(go[0] * w, go[1] * w, go[2] * w, go[3] * w));
-          } else if constexpr (C == 2) {
-            atomicAdd(reinterpret_cast<float2*>(p), make_float2(go[0] * w, go[1] * w));
-          } else {
+        for (int row = 0; row < 4; ++row) {
+          const int y = b[1] + (row & 1), z = b[2] + (row >> 1);
+          if ((unsigned)y >= (unsigned)g.mH || (unsigned)z >= (unsigned)g.mD) continue;
+          const float wyz = wy[row & 1] * wz[row >> 1];
+          const bool in0 = idx[2 * row] >= 0, in1 = idx[2 * row + 1] >= 0;
+          if (!in0 && !in1) continue;
+          float vals[2 * C];
 #pragma unroll
-            for (int c = 0; c < C; ++c) atomicAdd(p + c, go[c] * w);
+          for (int c = 0; c < C; ++c) {
+            vals[c] = in0 ? go[c] * (wx[0] * wyz) : 0.0f;
+            vals[C + c] = in1 ? go[c] * (wx[1] * wyz) : 0.0f;
           }
+          const long long f0 = (((long long)z * g.mH + y) * g.mW + b[0]) * C;
+          red_pair<C>(a.dV, a.nV, f0, vals);
         }
       }
     }
