@@ -33,6 +33,11 @@ constexpr int kSweep2StreamThreads = FFDP_SWEEP2_STREAM_THREADS;
 constexpr int kVPT = 4;                 // voxels per sweep thread per iteration (32 apart)
 constexpr int kHistFrac = 20;           // fixed-point fraction bits of histogram weights
 constexpr float kHistOne = 1048576.0f;  // 2^kHistFrac
+// histogram weight scales whose product is 2^(kHistFrac - 149): a product of
+// two weights is then the subnormal float holding the fixed-point count
+constexpr float kHistScaleF = 2.7105054312137611e-20f;  // 2^-65
+constexpr float kHistScaleJ = 5.4210108624275222e-20f;  // 2^-64
+static_assert(kHistFrac == 20, "kHistScaleF * kHistScaleJ = 2^(kHistFrac - 149)");
 constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23: x + kMagic holds round(x) in its low bits
 constexpr unsigned kMagicBits = 0x4B400000u;
 constexpr int kPartialStride = 16;      // doubles per CTA partial record

@@ -128,7 +128,12 @@ __device__ __forceinline__ void rotate4(const float w[4], int s, float r[4]) {
 }
 
 // Parzen contribution of one voxel: beta(a - cF) beta(b - cJ) on the 4x4 bins
-// around (cF, cJ), rounded to fixed point with the 1.5*2^23 trick.
+// around (cF, cJ), rounded to fixed point by the multiply itself: the F
+// weights carry 2^-65 and the J weights 2^-64 (both stay normal floats), so
+// their product beta beta' 2^-129 = (beta beta' 2^kHistFrac) 2^-149 is a
+// subnormal float whose bit pattern is that count rounded to nearest even --
+// one multiply per bin, no conversion (device code keeps subnormals: no
+// flush-to-zero).
 template <int BMAX>
 __device__ __forceinline__ void hist_add(unsigned* hist, const HistLane& h, const BinMap& bf, const BinMap& bj,
                                          float f, float j) {
@@ -138,15 +143,15 @@ __device__ __forceinline__ void hist_add(unsigned* hist, const HistLane& h, cons
   floor_split(bin_coord(bf, f), af, tf);
   floor_split(bin_coord(bj, j), aj, tj);
   float wf[4], wj[4];
-  bspline4(tf, kHistOne, wf);
-  bspline4(tj, 1.0f, wj);
+  bspline4(tf, kHistScaleF, wf);
+  bspline4(tj, kHistScaleJ, wj);
   if (L::PRIVATE) {
     unsigned* base = hist + L::word(af - 1, aj - 1) + h.rowoff[0];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        atomicAdd(base + i * L::QROW + k * L::COL, __float_as_uint(fmaf(wf[i], wj[k], kMagic)) - kMagicBits);
+        atomicAdd(base + i * L::QROW + k * L::COL, __float_as_uint(__fmul_rn(wf[i], wj[k])));
   } else {
     // step i takes kernel row a_i = af - 1 + ((i + s) mod 4), s = ga - af + 1,
     // so that a_i = i + ga (mod 4)
@@ -160,7 +165,7 @@ __device__ __forceinline__ void hist_add(unsigned* hist, const HistLane& h, cons
       unsigned* row = col + (ai >> 2) * L::QROW + h.rowoff[i];
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        atomicAdd(row + k * L::COL, __float_as_uint(fmaf(wr[i], wj[k], kMagic)) - kMagicBits);
+        atomicAdd(row + k * L::COL, __float_as_uint(__fmul_rn(wr[i], wj[k])));
     }
   }
 }
