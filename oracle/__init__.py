@@ -203,20 +203,24 @@ def sample_channels(V, fixed_shape, u, T: Transform, compose: bool = False, z0: 
 
 
 def sample_channels_bwd(V, fixed_shape, u, T: Transform, gout, compose: bool = False,
-                        want_du: bool = True, want_dV: bool = True):
-    """Backward of sample_channels over the whole fixed grid: (du, dA, dt, dV)."""
+                        want_du: bool = True, want_dV: bool = True, z0: int = 0, z1: int | None = None,
+                        dA=None, dt=None):
+    """Backward of sample_channels for planes [z0, z1) (gout indexed from z0):
+    (du, dA, dt, dV).  dA / dt are accumulated into the given arrays (fresh
+    zeros if None); dV covers the whole volume V."""
     V = _f32(V)
     C = V.shape[3]
     D, H, W = fixed_shape
+    z1 = D if z1 is None else z1
     u32 = None if u is None else _f32(u)
     g = _f64(gout)
-    du = np.empty((D, H, W, 3), np.float64) if want_du else None
-    dA = np.zeros(9, np.float64)
-    dt = np.zeros(3, np.float64)
+    du = np.empty((z1 - z0, H, W, 3), np.float64) if want_du else None
+    dA = np.zeros(9, np.float64) if dA is None else dA
+    dt = np.zeros(3, np.float64) if dt is None else dt
     dV = np.zeros(V.shape, np.float64) if want_dV else None
     lib().oracle_sample_channels_bwd(_pf(V), C, _dims(V.shape[:3]).ctypes.data_as(_ip),
                                      _dims(fixed_shape).ctypes.data_as(_ip), _pf(u32), _pd(T.packed()),
-                                     int(bool(compose)), 0, D, _pd(g), _pd(du), _pd(dA), _pd(dt), _pd(dV))
+                                     int(bool(compose)), z0, z1, _pd(g), _pd(du), _pd(dA), _pd(dt), _pd(dV))
     return du, dA.reshape(3, 3), dt, dV
 
 

@@ -587,51 +587,72 @@ void oracle_sample_channels(const float *V, int C, const int64_t *vd, const int6
  *   du_i     = S^T e_i  (+ S^T gout_i when compose)
  *   dA[r][c] += sum_i e_ir x_ic,   dt[r] += sum_i e_ir
  *   dV[v][c] += sum_i gout_ic w_v(p_i)   (w_v: trilinear weight of corner v)
- * du (indexed from z0) and dV may be NULL; dA, dt and dV are ACCUMULATED.
- * Runs serially (the scatter into dV has no fixed owner per voxel). */
+ * du (indexed from z0) and dV may be NULL; dA, dt and dV are ACCUMULATED
+ * (per-plane partials of dA, dt added in plane order).  With dV the planes
+ * run serially (the scatter has no fixed owner per voxel); without it,
+ * OpenMP over planes. */
+static void channels_bwd_plane(const float *V, int C, const int64_t *vd, const int64_t *fd, const float *u,
+                               const double *T, int compose, int64_t z0, int64_t z, const double *gout,
+                               double *du, double *pp, double *dV) {
+  const int64_t H = fd[1], W = fd[2];
+  const double *S = T + 12;
+  for (int64_t y = 0; y < H; ++y)
+    for (int64_t x = 0; x < W; ++x) {
+      const int64_t lin = (z * H + y) * W + x;
+      const int64_t loc = ((z - z0) * H + y) * W + x;
+      double xc[3], uv[3], p[3], val[4], dv[12], e[3] = {0.0, 0.0, 0.0};
+      fixed_coord(T, fd, x, y, z, xc);
+      load_u(u, lin, uv);
+      warp_point(T, xc, uv, p);
+      sample_channels_point(V, C, vd, p, val, dv);
+      const double *g = gout + loc * C;
+      for (int ch = 0; ch < C; ++ch)
+        for (int r = 0; r < 3; ++r) e[r] += g[ch] * dv[ch * 3 + r];
+      if (du)
+        for (int c = 0; c < 3; ++c) {
+          double s = S[0 * 3 + c] * e[0] + S[1 * 3 + c] * e[1] + S[2 * 3 + c] * e[2];
+          if (compose) s += S[0 * 3 + c] * g[0] + S[1 * 3 + c] * g[1] + S[2 * 3 + c] * g[2];
+          du[loc * 3 + c] = s;
+        }
+      for (int r = 0; r < 3; ++r) {
+        for (int c = 0; c < 3; ++c) pp[r * 3 + c] += e[r] * xc[c];
+        pp[9 + r] += e[r];
+      }
+      if (dV) {
+        int64_t b[3];
+        double rr[3];
+        if (!cell_of_point(vd, p, b, rr)) continue;
+        for (int cz = 0; cz < 2; ++cz)
+          for (int cy = 0; cy < 2; ++cy)
+            for (int cx = 0; cx < 2; ++cx) {
+              const int64_t vx = b[0] + cx, vy = b[1] + cy, vz = b[2] + cz;
+              if (vx < 0 || vy < 0 || vz < 0 || vx >= vd[2] || vy >= vd[1] || vz >= vd[0]) continue;
+              const double w = corner_weight(rr, cx, cy, cz);
+              const int64_t v = (vz * vd[1] + vy) * vd[2] + vx;
+              for (int ch = 0; ch < C; ++ch) dV[v * C + ch] += g[ch] * w;
+            }
+      }
+    }
+}
+
 void oracle_sample_channels_bwd(const float *V, int C, const int64_t *vd, const int64_t *fd, const float *u,
                                 const double *T, int compose, int64_t z0, int64_t z1, const double *gout,
                                 double *du, double *dA, double *dt, double *dV) {
-  const int64_t H = fd[1], W = fd[2];
-  const double *S = T + 12;
-  for (int64_t z = z0; z < z1; ++z)
-    for (int64_t y = 0; y < H; ++y)
-      for (int64_t x = 0; x < W; ++x) {
-        const int64_t lin = (z * H + y) * W + x;
-        const int64_t loc = ((z - z0) * H + y) * W + x;
-        double xc[3], uv[3], p[3], val[4], dv[12], e[3] = {0.0, 0.0, 0.0};
-        fixed_coord(T, fd, x, y, z, xc);
-        load_u(u, lin, uv);
-        warp_point(T, xc, uv, p);
-        sample_channels_point(V, C, vd, p, val, dv);
-        const double *g = gout + loc * C;
-        for (int ch = 0; ch < C; ++ch)
-          for (int r = 0; r < 3; ++r) e[r] += g[ch] * dv[ch * 3 + r];
-        if (du)
-          for (int c = 0; c < 3; ++c) {
-            double s = S[0 * 3 + c] * e[0] + S[1 * 3 + c] * e[1] + S[2 * 3 + c] * e[2];
-            if (compose) s += S[0 * 3 + c] * g[0] + S[1 * 3 + c] * g[1] + S[2 * 3 + c] * g[2];
-            du[loc * 3 + c] = s;
-          }
-        for (int r = 0; r < 3; ++r) {
-          for (int c = 0; c < 3; ++c) dA[r * 3 + c] += e[r] * xc[c];
-          dt[r] += e[r];
-        }
-        if (dV) {
-          int64_t b[3];
-          double rr[3];
-          if (!cell_of_point(vd, p, b, rr)) continue;
-          for (int cz = 0; cz < 2; ++cz)
-            for (int cy = 0; cy < 2; ++cy)
-              for (int cx = 0; cx < 2; ++cx) {
-                const int64_t vx = b[0] + cx, vy = b[1] + cy, vz = b[2] + cz;
-                if (vx < 0 || vy < 0 || vz < 0 || vx >= vd[2] || vy >= vd[1] || vz >= vd[0]) continue;
-                const double w = corner_weight(rr, cx, cy, cz);
-                const int64_t v = (vz * vd[1] + vy) * vd[2] + vx;
-                for (int ch = 0; ch < C; ++ch) dV[v * C + ch] += g[ch] * w;
-              }
-        }
-      }
+  const int64_t nz = z1 - z0;
+  double *part = (double *)calloc((size_t)(nz > 0 ? nz : 1) * 12, sizeof(double));
+  if (dV) {
+    for (int64_t z = z0; z < z1; ++z)
+      channels_bwd_plane(V, C, vd, fd, u, T, compose, z0, z, gout, du, part + (z - z0) * 12, dV);
+  } else {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t z = z0; z < z1; ++z)
+      channels_bwd_plane(V, C, vd, fd, u, T, compose, z0, z, gout, du, part + (z - z0) * 12, NULL);
+  }
+  for (int64_t z = 0; z < nz; ++z) {
+    for (int k = 0; k < 9; ++k) dA[k] += part[z * 12 + k];
+    for (int k = 0; k < 3; ++k) dt[k] += part[z * 12 + 9 + k];
+  }
+  free(part);
 }
 
 /* ------------------------------------------------------------------ */

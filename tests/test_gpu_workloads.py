@@ -91,3 +91,65 @@ def test_workload5_gigavoxel_streamed(ffdp):
     _check_losses(l, ref["loss"])
     assert rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
     assert rel_l2(du_s, ref["du_samples"]) <= TOL_GRAD
+
+
+# ------------------------------------------- next rows at the bench's full size
+def _pair_T(ffdp, pair):
+    return ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
+
+
+def test_mse_objective_512_full_arrays(ffdp):
+    # bench.py --path mse: the one-pass MSE objective on the 512^3 pair
+    from voxel_grid_sampler_gb300 import synth
+    pair = synth.make_pair(4, device="cuda")
+    loss, du, dA, dt = ffdp.ffdp_objective_mse(pair.F, pair.M, pair.u, _pair_T(ffdp, pair), 1.0)
+    torch.cuda.synchronize()
+    l, du, dA, dt = loss.cpu().numpy(), du.cpu().numpy(), dA.cpu().numpy(), dt.cpu().numpy()
+    F = pair.F.cpu().float().numpy()
+    M = pair.M.cpu().float().numpy()
+    u = pair.u.cpu().numpy()
+    del pair.F, pair.M, pair.u
+    torch.cuda.empty_cache()
+    ref = oracle.objective_mse(F, M, u, oracle_T_of(pair), 1.0)
+    report("mse 512^3", loss=rel_err(l[1], ref["loss"][1]), du=rel_l2(du, ref["du"]),
+           dAdt=rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]))
+    assert rel_err(l[0], ref["loss"][0]) <= TOL_LOSS and rel_err(l[1], ref["loss"][1]) <= TOL_LOSS
+    assert rel_l2(du, ref["du"]) <= TOL_GRAD
+    assert rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
+
+
+def test_compose_512_sampled_planes_and_adjoint(ffdp):
+    # bench.py --path compose: the pair's field composed with itself on 512^3.
+    # out and du on sampled planes and dA, dt in full against the oracle; dV
+    # (the whole 512^3 x 3 volume) through the adjoint identity
+    # <dV, W> = <gout, sample(W)> for a random W, both sides on the GPU.
+    from voxel_grid_sampler_gb300 import synth
+    pair = synth.make_pair(4, device="cuda")
+    T = _pair_T(ffdp, pair)
+    V, u = pair.u, pair.u
+    shape = tuple(pair.F.shape)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    gout = torch.randn(shape + (3,), device="cuda", generator=g)
+    out = ffdp.ffdp_sample_channels_fwd(V, shape, u, T, True)
+    du, dA, dt, dV = ffdp.ffdp_sample_channels_bwd(V, u, T, gout, True)
+    W = torch.randn(V.shape, device="cuda", generator=g)
+    outW = ffdp.ffdp_sample_channels_fwd(W, shape, u, T, False)
+    lhs = float((dV.double() * W.double()).sum())
+    rhs = float((gout.double() * outW.double()).sum())
+    del W, outW
+    To = oracle_T_of(pair)
+    Vh, uh = V.cpu().numpy(), u.cpu().numpy()
+    planes = [0, 1, 255, 511]
+    for z in planes:
+        o = oracle.sample_channels(Vh, shape, uh, To, True, z, z + 1)
+        assert np.max(np.abs(out[z].cpu().numpy() - o[0])) <= TOL_J
+    gh = gout.cpu().numpy()
+    dA_o = np.zeros(9)
+    dt_o = np.zeros(3)
+    du_o, _, _, _ = oracle.sample_channels_bwd(Vh, shape, uh, To, gh, True, want_dV=False, dA=dA_o, dt=dt_o)
+    du = du.cpu().numpy()
+    report("compose 512^3", adjoint=abs(lhs - rhs) / abs(rhs), du=rel_l2(du, du_o),
+           dAdt=rel_l2(np.r_[dA.cpu().numpy(), dt.cpu().numpy()], np.r_[dA_o, dt_o]))
+    assert abs(lhs - rhs) <= 1e-4 * abs(rhs)
+    assert rel_l2(du, du_o) <= TOL_GRAD
+    assert rel_l2(np.r_[dA.cpu().numpy(), dt.cpu().numpy()], np.r_[dA_o, dt_o]) <= TOL_GRAD
