@@ -463,9 +463,9 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
 # ---------------------------------------------------------------- other paths
 # The fused MSE objective (one pass: F + u + M read, du written) and warp
 # composition (forward: u + V read, out written; backward: u + gout + V read,
-# du and dV written) on the 512^3 workload-4 pair; V is the pair's own
-# displacement field (the warp composed with itself), gout a seeded normal
-# field.
+# du and dV written) on the 512^3 workload-4 pair; V is a second smooth
+# displacement field (the pair's own field mirrored in z), gout a seeded
+# normal field.
 PATH_METRIC = {"mse": "Gvoxels/s fused warp+MSE fwd+bwd on 1 GB300; % of HBM roofline",
                "compose": "Gvoxels/s warp composition fwd+bwd (du, dA, dt, dV) on 1 GB300; % of HBM roofline"}
 PATH_KERNEL_BYTES = {"mse": {"k_sweep2": 4 + 12 + 4 + 12},
@@ -499,7 +499,7 @@ def _path_setup(args, pair, dev):
             ffdp.ffdp_sample_channels_fwd(V_, shape, u_, T, True, o_["out"], stream)
             ffdp.ffdp_sample_channels_bwd(V_, u_, T, g_, True, o_["du"], o_["dA"], o_["dt"], o_["dV"], o_["ws"],
                                           stream)
-        ins = dict(V=u, g=gout, u=u)
+        ins = dict(V=u.flip(0).contiguous(), g=gout, u=u)
         outs = ("out", "du", "dA", "dt", "dV")
     return call, ins, o, outs
 
@@ -516,7 +516,7 @@ def _path_oracle_sample(args, pair, ds):
     if args.path == "mse":
         oracle.objective_mse(F, pair.M.float().cpu().numpy(), u, T, 1.0)
     else:
-        V = pair.u.cpu().numpy()
+        V = np.ascontiguousarray(pair.u.cpu().numpy()[::-1])
         g = np.random.default_rng(0).normal(size=u.shape)
         oracle.sample_channels(V, F.shape, u, T, True)
         oracle.sample_channels_bwd(V, F.shape, u, T, g, True)

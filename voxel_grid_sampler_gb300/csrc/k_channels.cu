@@ -91,39 +91,51 @@ __device__ __forceinline__ void gather_c(const float* __restrict__ V, const long
 
 // Adds vals[0 .. 2C) to dV[f0 .. f0 + 2C) (the two x taps of one cell row,
 // adjacent in a channel-last volume; a tap outside V has zero vals) with
-// 16-byte vector reductions over the aligned 4-float chunks covering the
-// span, padded with zeros (adding 0 leaves a value unchanged).  A chunk that
-// would reach outside dV[0 .. nV) is sent as scalar reductions of the span's
-// own elements instead.  The chunk offset off = f0 mod 4 selects, for every
-// chunk element, which val (or 0) it carries, by compile-time unrolled
-// selects (no dynamically indexed register array).
+// vector reductions of kDvChunk floats (8 or 16 bytes) over the aligned
+// chunks covering the span, padded with zeros (adding 0 leaves a value
+// unchanged).  A chunk that would reach outside dV[0 .. nV) is sent as scalar
+// reductions of the span's own elements instead.  The chunk offset
+// off = f0 mod kDvChunk selects, for every chunk element, which val (or 0) it
+// carries, by compile-time unrolled selects (no dynamically indexed register
+// array).
+#ifndef FFDP_DV_CHUNK
+#define FFDP_DV_CHUNK 4
+#endif
+constexpr int kDvChunk = FFDP_DV_CHUNK;  // floats per vector reduction of the dV scatter
+static_assert(kDvChunk == 2 || kDvChunk == 4, "8- or 16-byte vector reductions");
+
 template <int C>
 __device__ __forceinline__ void red_pair(float* __restrict__ dV, long long nV, long long f0, const float vals[2 * C]) {
-  constexpr int N = 2 * C;
-  constexpr int NCH = (3 + N + 3) / 4;  // chunks for the worst offset
-  const long long a = f0 & ~3ll;
+  constexpr int N = 2 * C, Q = kDvChunk;
+  constexpr int NCH = (Q - 1 + N + Q - 1) / Q;  // chunks for the worst offset
+  const long long a = f0 & ~(long long)(Q - 1);
   const int off = (int)(f0 - a);
-  const int nch = (off + N + 3) >> 2;
+  const int nch = (off + N + Q - 1) / Q;
 #pragma unroll
   for (int k = 0; k < NCH; ++k) {
     if (k >= nch) break;
-    float v[4];
+    float v[Q];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = 4 * k + j;  // element of the chunk run; source val index e - off
-      const float c0 = (e < N) ? vals[e] : 0.0f;
-      const float c1 = (e - 1 >= 0 && e - 1 < N) ? vals[e - 1] : 0.0f;
-      const float c2 = (e - 2 >= 0 && e - 2 < N) ? vals[e - 2] : 0.0f;
-      const float c3 = (e - 3 >= 0 && e - 3 < N) ? vals[e - 3] : 0.0f;
-      v[j] = off == 0 ? c0 : (off == 1 ? c1 : (off == 2 ? c2 : c3));
+    for (int j = 0; j < Q; ++j) {
+      const int e = Q * k + j;  // element of the chunk run; source val index e - off
+      float x = (e < N) ? vals[e] : 0.0f;
+#pragma unroll
+      for (int o = 1; o < Q; ++o) {
+        const float c = (e - o >= 0 && e - o < N) ? vals[e - o] : 0.0f;
+        x = off == o ? c : x;
+      }
+      v[j] = x;
     }
-    const long long base = a + 4 * k;
-    if (base >= 0 && base + 4 <= nV) {
-      atomicAdd(reinterpret_cast<float4*>(dV + base), make_float4(v[0], v[1], v[2], v[3]));
+    const long long base = a + Q * k;
+    if (base >= 0 && base + Q <= nV) {
+      if constexpr (Q == 4)
+        atomicAdd(reinterpret_cast<float4*>(dV + base), make_float4(v[0], v[1], v[2], v[3]));
+      else
+        atomicAdd(reinterpret_cast<float2*>(dV + base), make_float2(v[0], v[1]));
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int src = 4 * k + j - off;
+      for (int j = 0; j < Q; ++j) {
+        const int src = Q * k + j - off;
         if (src >= 0 && src < N && base + j >= 0 && base + j < nV) atomicAdd(dV + base + j, v[j]);
       }
     }
