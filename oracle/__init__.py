@@ -93,6 +93,10 @@ def lib():
                                                  ctypes.c_int64, ctypes.c_int64, _dp, _dp, _dp, _dp, _dp]
         L.oracle_mse.argtypes = [_fp, _dp, ctypes.c_int64, _dp]
         L.oracle_mse.restype = ctypes.c_double
+        L.oracle_sobolev.argtypes = [_fp, _ip, ctypes.c_double, _dp]
+        L.oracle_sobolev.restype = ctypes.c_double
+        L.oracle_adam.argtypes = [_dp, _dp, _dp, _dp, ctypes.c_int64, ctypes.c_double, ctypes.c_double,
+                                  ctypes.c_double, ctypes.c_double, ctypes.c_int]
         _lib = L
     return _lib
 
@@ -245,6 +249,36 @@ def objective_mse(F, M, u, T: Transform, w_mse: float = 1.0, want_du: bool = Tru
     gJ = w_mse * r["dJ"]
     du, dA, dt = grid_sample_bwd(M, shape, u, T, gJ, want_du=want_du)
     return dict(loss=np.array([w_mse * r["mse"], r["mse"]]), J=J, gJ=gJ, du=du, dA=dA.reshape(3, 3), dt=dt)
+
+
+# ------------------------------------------------- Sobolev regulariser, Adam
+def sobolev(u, lam: float, want_grad: bool = True):
+    """Returns dict(R, dR) for a displacement field u of shape (D, H, W, 3)."""
+    u32 = _f32(u)
+    dR = np.empty(u32.shape, np.float64) if want_grad else None
+    v = lib().oracle_sobolev(_pf(u32), _dims(u32.shape[:3]).ctypes.data_as(_ip), float(lam), _pd(dR))
+    return dict(R=float(v), dR=dR)
+
+
+def adam(x, g, m1, m2, lr, b1, b2, eps, t):
+    """One Adam step: returns updated float64 copies (x, m1, m2)."""
+    x = _f64(x).copy()
+    m1 = _f64(m1).copy()
+    m2 = _f64(m2).copy()
+    gg = _f64(g)
+    lib().oracle_adam(_pd(x), _pd(gg), _pd(m1), _pd(m2), x.size, float(lr), float(b1), float(b2), float(eps),
+                      int(t))
+    return x, m1, m2
+
+
+def sobolev_adam_step(u, g, m1, m2, lam, lr, b1, b2, eps, t):
+    """One regularised iteration on u: G = g + dR/du, Adam step on u.
+
+    Returns dict(R, u, m1, m2, G)."""
+    r = sobolev(u, lam)
+    G = _f64(g) + r["dR"]
+    x, n1, n2 = adam(_f32(u).astype(np.float64), G, m1, m2, lr, b1, b2, eps, t)
+    return dict(R=r["R"], u=x, m1=n1, m2=n2, G=G)
 
 
 # ------------------------------------------------------------------------- MI

@@ -672,3 +672,63 @@ double oracle_mse(const float *F, const double *J, int64_t n, double *dJ) {
   }
   return s / (double)n;
 }
+
+/* ------------------------------------------------------------------ */
+/* Sobolev regulariser and the Adam update of the displacement field    */
+/* ------------------------------------------------------------------ */
+
+/* "Background": L(phi) = C(F, M o phi) + R(phi) with R a Sobolev norm; the
+ * overview updates the warp shards by gradient descent with optimiser state
+ * [m1], [m2] held per voxel beside u.  Readings (the page gives no formula):
+ *   R(u) = (lambda / N) sum_c sum_a sum_{i : i + e_a inside} (u_c(i + e_a) - u_c(i))^2,
+ * the first-order Sobolev (H^1) seminorm of u with forward differences in
+ * voxel units and no term across the boundary; its gradient is
+ *   dR/du_c(i) = (2 lambda / N) sum_{j neighbour of i inside} (u_c(i) - u_c(j)).
+ * u is [D][H][W][3].  dR may be NULL. */
+double oracle_sobolev(const float *u, const int64_t *fd, double lambda, double *dR) {
+  const int64_t D = fd[0], H = fd[1], W = fd[2];
+  const double N = (double)(D * H * W);
+  double *plane = (double *)calloc((size_t)D, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t z = 0; z < D; ++z) {
+    double s = 0.0;
+    for (int64_t y = 0; y < H; ++y)
+      for (int64_t x = 0; x < W; ++x) {
+        const int64_t i = (z * H + y) * W + x;
+        const int64_t nb[6][3] = {{x + 1, y, z}, {x, y + 1, z}, {x, y, z + 1},
+                                  {x - 1, y, z}, {x, y - 1, z}, {x, y, z - 1}};
+        double g[3] = {0.0, 0.0, 0.0};
+        for (int k = 0; k < 6; ++k) {
+          const int64_t xx = nb[k][0], yy = nb[k][1], zz = nb[k][2];
+          if (xx < 0 || yy < 0 || zz < 0 || xx >= W || yy >= H || zz >= D) continue;
+          const int64_t j = (zz * H + yy) * W + xx;
+          for (int c = 0; c < 3; ++c) {
+            const double d = (double)u[3 * j + c] - (double)u[3 * i + c];
+            if (k < 3) s += d * d;  /* forward edges: each edge once */
+            g[c] -= d;              /* u_i - u_j summed over neighbours */
+          }
+        }
+        if (dR)
+          for (int c = 0; c < 3; ++c) dR[3 * i + c] = 2.0 * lambda / N * g[c];
+      }
+    plane[z] = s;
+  }
+  double tot = 0.0;
+  for (int64_t z = 0; z < D; ++z) tot += plane[z];
+  free(plane);
+  return lambda / N * tot;
+}
+
+/* One Adam step (Kingma & Ba, with bias correction) on n values, step t >= 1:
+ *   m1 = b1 m1 + (1 - b1) g,   m2 = b2 m2 + (1 - b2) g^2,
+ *   x -= lr (m1 / (1 - b1^t)) / (sqrt(m2 / (1 - b2^t)) + eps).
+ * x, m1, m2 are updated in place. */
+void oracle_adam(double *x, const double *g, double *m1, double *m2, int64_t n, double lr, double b1, double b2,
+                 double eps, int t) {
+  const double c1 = 1.0 - pow(b1, (double)t), c2 = 1.0 - pow(b2, (double)t);
+  for (int64_t k = 0; k < n; ++k) {
+    m1[k] = b1 * m1[k] + (1.0 - b1) * g[k];
+    m2[k] = b2 * m2[k] + (1.0 - b2) * g[k] * g[k];
+    x[k] -= lr * (m1[k] / c1) / (sqrt(m2[k] / c2) + eps);
+  }
+}
