@@ -6,8 +6,9 @@ path -- implicit sampler, histogram sweep, MI table, LNCC window sums, MI and
 LNCC gradients, sampler backward, affine reductions.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 4|5] [--impl reference]
-    python bench.py --path mse|compose     (the MSE objective / warp composition on the
-                                            512^3 pair; one JSON line each, same keys)
+    python bench.py --path mse|compose|adam (the MSE objective / warp composition / the
+                                            regularised Adam step of u on the 512^3
+                                            pair; one JSON line each, same keys)
 
 Under torch.distributed.run each rank evaluates its own independent pair
 (weak scaling, no collective on the data path); the step time is the maximum
@@ -467,11 +468,13 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
 # displacement field (the pair's own field mirrored in z), gout a seeded
 # normal field.
 PATH_METRIC = {"mse": "Gvoxels/s fused warp+MSE fwd+bwd on 1 GB300; % of HBM roofline",
+               "adam": "Gvoxels/s Sobolev-regularised Adam step of u on 1 GB300; % of HBM roofline",
                "compose": "Gvoxels/s warp composition fwd+bwd (du, dA, dt, dV) on 1 GB300; % of HBM roofline"}
 PATH_KERNEL_BYTES = {"mse": {"k_sweep2": 4 + 12 + 4 + 12},
+                     "adam": {"k_reg_adam": 12 * 7},
                      "compose": {"k_chan_fwd": 12 + 12 + 12, "k_chan_bwd": 12 + 12 + 12 + 12 + 12,
                                  "k_zero_f32": 12}}
-PATH_ALGO_BYTES = {"mse": 32, "compose": 36 + 60}
+PATH_ALGO_BYTES = {"mse": 32, "compose": 36 + 60, "adam": 84}
 
 
 def _path_setup(args, pair, dev):
@@ -488,6 +491,19 @@ def _path_setup(args, pair, dev):
             ffdp.ffdp_objective_mse(F_, M_, u_, T, 1.0, o_["loss"], o_["du"], o_["dA"], o_["dt"], o_["ws"], stream)
         ins = dict(F=F, M=M, u=u)
         outs = ("loss", "du", "dA", "dt")
+    elif args.path == "adam":
+        # u, the objective gradient g (a seeded field of du's scale) and the moments in;
+        # u_out, the moments and R(u) out (u is not advanced between steps)
+        g = torch.Generator(device=dev).manual_seed(2025)
+        gr = torch.randn(shape + (3,), device=dev, generator=g) * 1e-6
+        o = dict(u_out=torch.empty_like(u), loss=torch.empty(1, device=dev),
+                 ws=ffdp.workspace(ffdp.FFDP_OP_SOBOLEV, shape, None, dev))
+        P = ffdp.sobolev_adam_params(0.1, 1e-3, 0.9, 0.999, 1e-8, 1)
+
+        def call(u_, g_, m1_, m2_, o_, stream):
+            ffdp.ffdp_sobolev_adam_step(u_, g_, m1_, m2_, P, o_["u_out"], o_["loss"], o_["ws"], stream)
+        ins = dict(u=u, g=gr, m1=torch.zeros_like(u), m2=torch.zeros_like(u))
+        outs = ("u_out", "loss")
     else:
         g = torch.Generator(device=dev).manual_seed(2024)
         gout = torch.randn(shape + (3,), device=dev, generator=g)
@@ -515,6 +531,9 @@ def _path_oracle_sample(args, pair, ds):
     t0 = time.perf_counter()
     if args.path == "mse":
         oracle.objective_mse(F, pair.M.float().cpu().numpy(), u, T, 1.0)
+    elif args.path == "adam":
+        g = np.random.default_rng(0).normal(size=u.shape) * 1e-6
+        oracle.sobolev_adam_step(u, g, np.zeros(u.shape), np.zeros(u.shape), 0.1, 1e-3, 0.9, 0.999, 1e-8, 1)
     else:
         V = np.ascontiguousarray(pair.u.cpu().numpy()[::-1])
         g = np.random.default_rng(0).normal(size=u.shape)
@@ -533,10 +552,10 @@ def run_gpu_path(args, ws, rank, local):
     N = pair.F.numel()
     call, ins, o, outs = _path_setup(args, pair, dev)
     stream = torch.cuda.current_stream(dev)
-    a, b, c = (ins[k] for k in ins)
+    args_in = [ins[k] for k in ins]
 
     def step():
-        call(a, b, c, o, stream)
+        call(*args_in, o, stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -574,7 +593,7 @@ def run_gpu_path(args, ws, rank, local):
         def e2e_step():
             for d, h in zip(din, hin):
                 d.copy_(h, non_blocking=True)
-            call(din[0], din[1], din[2], o, stream)
+            call(*din, o, stream)
             for h, k in zip(hout, outs):
                 h.copy_(o[k], non_blocking=True)
 
@@ -642,7 +661,7 @@ def main():
     ap.add_argument("--shape", type=int, default=0, help="cube edge overriding the workload size (profiling)")
     ap.add_argument("--store-slope", type=int, default=1, choices=[0, 1],
                     help="MI-only objectives: store J and dJ/dp (1) or stay implicit (0)")
-    ap.add_argument("--path", default="objective", choices=["objective", "mse", "compose"],
+    ap.add_argument("--path", default="objective", choices=["objective", "mse", "compose", "adam"],
                     help="objective (default, --workload 4|5), or the MSE objective / warp composition "
                          "on the 512^3 pair")
     args = ap.parse_args()

@@ -114,7 +114,8 @@ enum {
   FFDP_OP_OBJECTIVE = 4,       /* params: const ffdp_objective_params* */
   FFDP_OP_SAMPLE_CHANNELS_BWD = 5, /* params: NULL */
   FFDP_OP_MSE = 6,             /* params: NULL */
-  FFDP_OP_OBJECTIVE_MSE = 7    /* params: NULL */
+  FFDP_OP_OBJECTIVE_MSE = 7,   /* params: NULL */
+  FFDP_OP_SOBOLEV = 8          /* params: NULL (regulariser and Adam step) */
 };
 
 /* Bytes of device workspace a call of `op` on fixed grid `fixed` needs (0 for
@@ -223,6 +224,40 @@ ffdp_status ffdp_objective_mse(const void *F, ffdp_dtype ft, ffdp_dims fdims, co
                                ffdp_dims mdims, const float *u, const ffdp_transform *T, float w_mse,
                                float *loss, float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
                                void *stream);
+
+/* ---- regulariser and optimiser step -----------------------------------
+ * "Background": L(phi) = C(F, M o phi) + R(phi) with R a Sobolev norm; the
+ * method updates the warp by gradient descent with optimiser state [m1],
+ * [m2] held per voxel beside u.  The page gives no formula; these calls use
+ *   R(u) = (lambda / N) sum_c sum_a sum_{i: i + e_a inside} (u_c(i + e_a) - u_c(i))^2
+ * (the first-order Sobolev seminorm of u, forward differences in voxel
+ * units, nothing across the boundary) and Adam with bias correction. */
+
+/* Host struct.  step: the 1-based Adam step count t. */
+typedef struct {
+  float lambda;
+  float lr, beta1, beta2, eps;
+  int step;
+} ffdp_sobolev_adam_params;
+
+/* loss[0] = R(u); dR = dR/du = (2 lambda / N) sum_{neighbours j} (u_i - u_j)
+ * ([dims][3] float32, may be NULL; must not overlap u).  u: [dims][3].
+ * Workspace: ffdp_workspace_bytes(FFDP_OP_SOBOLEV, dims, NULL). */
+ffdp_status ffdp_sobolev_fwd_bwd(const float *u, ffdp_dims dims, float lambda, float *loss, float *dR,
+                                 void *ws, size_t ws_bytes, void *stream);
+
+/* One regularised optimiser step of the displacement field in one pass:
+ *   G = g + dR/du (g: the objective's du, e.g. from ffdp_objective),
+ *   m1 = b1 m1 + (1 - b1) G,  m2 = b2 m2 + (1 - b2) G^2  (in place),
+ *   u_out = u - lr (m1 / (1 - b1^t)) / (sqrt(m2 / (1 - b2^t)) + eps),
+ * and loss[0] = R(u).  u, u_out, g, m1, m2 are [dims][3] float32; u_out must
+ * not overlap u (the stencil reads u's neighbours: ping-pong two buffers);
+ * m1 and m2 start at zero for t = 1.  The affine part (A, t: 12 numbers) is
+ * left to the caller.  Workspace: ffdp_workspace_bytes(FFDP_OP_SOBOLEV, dims,
+ * NULL). */
+ffdp_status ffdp_sobolev_adam_step(const float *u, float *u_out, const float *g, float *m1, float *m2,
+                                   ffdp_dims dims, const ffdp_sobolev_adam_params *p, float *loss, void *ws,
+                                   size_t ws_bytes, void *stream);
 
 /* Workspace-free variant of ffdp_objective for the MI term (the paper has no
  * counterpart; it exists for callers that cannot allocate device memory).

@@ -149,3 +149,23 @@ def test_channel_and_mse_workspaces_are_o1(lib):
         a = ffdp.ffdp_workspace_bytes(op, (16, 16, 16))
         b = ffdp.ffdp_workspace_bytes(op, (1024, 1024, 1024))
         assert a == b > 0
+
+
+@nogpu
+def test_regulariser_and_step_reject_invalid_arguments(lib):
+    from voxel_grid_sampler_gb300 import ffdp
+    n0 = lib.ffdp_launch_count()
+    good = ffdp.dims_of((8, 8, 8))
+    a, b, c, d, e = (ctypes.c_void_p(0x100000 * k) for k in range(1, 6))
+    ws = ctypes.c_void_p(0x2000)
+    p = ffdp.sobolev_adam_params(0.1, 0.01)
+    assert lib.ffdp_sobolev_fwd_bwd(a, good, -1.0, b, c, ws, 1 << 30, None) == 1
+    assert lib.ffdp_sobolev_fwd_bwd(a, good, 1.0, b, a, ws, 1 << 30, None) == 1       # dR overlaps u
+    assert lib.ffdp_sobolev_fwd_bwd(a, good, 1.0, b, c, None, 0, None) == 3
+    assert lib.ffdp_sobolev_adam_step(a, a, b, c, d, good, ctypes.byref(p), e, ws, 1 << 30, None) == 1  # u_out = u
+    assert lib.ffdp_sobolev_adam_step(a, b, c, d, d, good, ctypes.byref(p), e, ws, 1 << 30, None) == 1  # m1 = m2
+    for bad in (ffdp.sobolev_adam_params(0.1, 0.01, beta1=1.0), ffdp.sobolev_adam_params(0.1, 0.01, step=0),
+                ffdp.sobolev_adam_params(0.1, 0.01, eps=-1.0), ffdp.sobolev_adam_params(float("nan"), 0.01)):
+        assert lib.ffdp_sobolev_adam_step(a, b, c, d, e, good, ctypes.byref(bad), ctypes.c_void_p(0x600000), ws,
+                                          1 << 30, None) == 1
+    assert lib.ffdp_launch_count() == n0

@@ -17,6 +17,7 @@
 
 #include "../../include/ffdp.h"
 #include "ffdp_internal.h"
+#include "ffdp_reg.h"
 
 using namespace ffdp;
 
@@ -402,6 +403,7 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
     case FFDP_OP_SAMPLE_CHANNELS_BWD:
     case FFDP_OP_MSE:
     case FFDP_OP_OBJECTIVE_MSE:
+    case FFDP_OP_SOBOLEV:
       return ws_layout(false, 32, max_parts(), false, false, N).total;
   }
   return 0;
@@ -879,6 +881,90 @@ extern "C" ffdp_status ffdp_objective_mse(const void* F, ffdp_dtype ft, ffdp_dim
   fill_finish_affine(f, fdims, mdims, T);
   FFDP_CUDA(launch_finish(f, s), "finish launch");
   return FFDP_OK;
+}
+
+// -------------------------------------- Sobolev regulariser, Adam step of u
+namespace {
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+ffdp_status reg_launch(int step, RegArgs& a, ffdp_dims dims, float* loss, void* ws, size_t ws_bytes, void* stream) {
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims));
+  FFDP_TRY(check_ws(ws, ws_bytes, w.total));
+  make_grid_only(dims, a.g3);
+  a.partials = reinterpret_cast<double*>(static_cast<char*>(ws) + w.partials);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint64_t N = nvox(dims);
+  const uint64_t groups = (N + 31) / 32;
+  const uint64_t ctas = (groups + kRegThreads / 32 - 1) / (kRegThreads / 32);
+  const uint64_t slots = (uint64_t)(sm_count() > 0 ? sm_count() : 1) * reg_ctas_per_sm(step);
+  const int grid = (int)(ctas < slots ? (ctas < 1 ? 1 : ctas) : slots);
+  FFDP_CUDA(launch_reg(step, a, grid, s), "regulariser launch");
+  FinishArgs f{};
+  f.partials = a.partials;
+  f.nparts = grid;
+  f.loss = loss;
+  f.nloss = 1;
+  f.has_mse = 1;  // the per-CTA slot holds lambda * sum of squares: loss = that / N
+  f.w_mse = 1.0;
+  f.N = (double)N;
+  FFDP_CUDA(launch_finish(f, s), "finish launch");
+  return FFDP_OK;
+}
+
+}  // namespace
+
+extern "C" ffdp_status ffdp_sobolev_fwd_bwd(const float* u, ffdp_dims dims, float lambda, float* loss, float* dR,
+                                            void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!u || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null u or loss");
+  FFDP_TRY(check_dims(dims, "u"));
+  if (!std::isfinite(lambda) || lambda < 0.0f) return fail(FFDP_ERR_INVALID_ARGUMENT, "lambda must be finite and >= 0");
+  if (!aligned16(u) || (dR && !aligned16(dR))) return fail(FFDP_ERR_INVALID_ARGUMENT, "u and dR must be 16-byte aligned");
+  const size_t bytes = (size_t)nvox(dims) * 12;
+  if (dR && overlaps(u, bytes, dR, bytes)) return fail(FFDP_ERR_INVALID_ARGUMENT, "dR must not overlap u");
+  RegArgs a{};
+  a.u = u;
+  a.dR = dR;
+  a.lambda = lambda;
+  a.coef = (float)(2.0 * (double)lambda / (double)nvox(dims));
+  return reg_launch(0, a, dims, loss, ws, ws_bytes, stream);
+}
+
+extern "C" ffdp_status ffdp_sobolev_adam_step(const float* u, float* u_out, const float* g, float* m1, float* m2,
+                                              ffdp_dims dims, const ffdp_sobolev_adam_params* p, float* loss,
+                                              void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = '\0';
+  if (!u || !u_out || !g || !m1 || !m2 || !p || !loss)
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "null u, u_out, g, m1, m2, params or loss");
+  FFDP_TRY(check_dims(dims, "u"));
+  if (!aligned16(u) || !aligned16(u_out) || !aligned16(g) || !aligned16(m1) || !aligned16(m2))
+    return fail(FFDP_ERR_INVALID_ARGUMENT, "u, u_out, g, m1 and m2 must be 16-byte aligned");
+  const size_t bytes = (size_t)nvox(dims) * 12;
+  if (overlaps(u, bytes, u_out, bytes)) return fail(FFDP_ERR_INVALID_ARGUMENT, "u_out must not overlap u");
+  if (overlaps(m1, bytes, m2, bytes)) return fail(FFDP_ERR_INVALID_ARGUMENT, "m1 and m2 must not overlap");
+  if (!std::isfinite(p->lambda) || p->lambda < 0.0f || !std::isfinite(p->lr) || !(p->beta1 >= 0.0f && p->beta1 < 1.0f) ||
+      !(p->beta2 >= 0.0f && p->beta2 < 1.0f) || !std::isfinite(p->eps) || p->eps < 0.0f || p->step < 1)
+    return fail(FFDP_ERR_INVALID_ARGUMENT,
+                "need finite lambda >= 0, finite lr, beta1 and beta2 in [0, 1), eps >= 0 and step >= 1");
+  RegArgs a{};
+  a.u = u;
+  a.g = g;
+  a.u_out = u_out;
+  a.m1 = m1;
+  a.m2 = m2;
+  a.lambda = p->lambda;
+  a.coef = (float)(2.0 * (double)p->lambda / (double)nvox(dims));
+  a.lr = p->lr;
+  a.b1 = p->beta1;
+  a.b2 = p->beta2;
+  a.eps = p->eps;
+  a.ic1 = (float)(1.0 / (1.0 - std::pow((double)p->beta1, (double)p->step)));
+  a.ic2 = (float)(1.0 / (1.0 - std::pow((double)p->beta2, (double)p->step)));
+  return reg_launch(1, a, dims, loss, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------ workspace-free MI objective

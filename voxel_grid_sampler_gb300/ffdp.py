@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libffdp.so")
 
 FFDP_F32, FFDP_F16 = 0, 1
 FFDP_OP_GRID_SAMPLE_BWD, FFDP_OP_MI, FFDP_OP_LNCC, FFDP_OP_OBJECTIVE = 1, 2, 3, 4
-FFDP_OP_SAMPLE_CHANNELS_BWD, FFDP_OP_MSE, FFDP_OP_OBJECTIVE_MSE = 5, 6, 7
+FFDP_OP_SAMPLE_CHANNELS_BWD, FFDP_OP_MSE, FFDP_OP_OBJECTIVE_MSE, FFDP_OP_SOBOLEV = 5, 6, 7, 8
 STATUS = {0: "FFDP_OK", 1: "FFDP_ERR_INVALID_ARGUMENT", 2: "FFDP_ERR_UNSUPPORTED",
           3: "FFDP_ERR_WORKSPACE", 4: "FFDP_ERR_CUDA", 5: "FFDP_ERR_INTERNAL"}
 
@@ -48,6 +48,11 @@ class ffdp_mi_params(ctypes.Structure):
 
 class ffdp_lncc_params(ctypes.Structure):
     _fields_ = [("window", ctypes.c_int), ("eps", ctypes.c_float)]
+
+
+class ffdp_sobolev_adam_params(ctypes.Structure):
+    _fields_ = [("lambda_", ctypes.c_float), ("lr", ctypes.c_float), ("beta1", ctypes.c_float),
+                ("beta2", ctypes.c_float), ("eps", ctypes.c_float), ("step", ctypes.c_int)]
 
 
 class ffdp_objective_params(ctypes.Structure):
@@ -92,9 +97,14 @@ def lib() -> ctypes.CDLL:
         L.ffdp_objective_mse.argtypes = [_vp, ctypes.c_int, ffdp_dims, _vp, ctypes.c_int, ffdp_dims, _vp,
                                          ctypes.POINTER(ffdp_transform), ctypes.c_float, _vp, _vp, _vp, _vp,
                                          _vp, ctypes.c_size_t, _vp]
+        L.ffdp_sobolev_fwd_bwd.argtypes = [_vp, ffdp_dims, ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        L.ffdp_sobolev_adam_step.argtypes = [_vp, _vp, _vp, _vp, _vp, ffdp_dims,
+                                             ctypes.POINTER(ffdp_sobolev_adam_params), _vp, _vp, ctypes.c_size_t,
+                                             _vp]
         for f in ("ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd", "ffdp_mi_fwd_bwd",
                   "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_sample_channels_fwd",
-                  "ffdp_sample_channels_bwd", "ffdp_mse_fwd_bwd", "ffdp_objective_mse"):
+                  "ffdp_sample_channels_bwd", "ffdp_mse_fwd_bwd", "ffdp_objective_mse",
+                  "ffdp_sobolev_fwd_bwd", "ffdp_sobolev_adam_step"):
             getattr(L, f).restype = ctypes.c_int
         L.ffdp_status_string.restype = ctypes.c_char_p
         L.ffdp_status_string.argtypes = [ctypes.c_int]
@@ -359,6 +369,42 @@ def ffdp_objective_mse(F, M, u, T: ffdp_transform, w_mse=1.0, loss=None, du=None
                                     dims_of(M.shape), _ptr(u), ctypes.byref(T), float(w_mse), _ptr(loss),
                                     _ptr(du), _ptr(dA), _ptr(dt), _ptr(ws), ws.numel(), _stream(stream)))
     return loss, du, dA, dt
+
+
+def sobolev_adam_params(lam, lr, beta1=0.9, beta2=0.999, eps=1e-8, step=1) -> ffdp_sobolev_adam_params:
+    return ffdp_sobolev_adam_params(float(lam), float(lr), float(beta1), float(beta2), float(eps), int(step))
+
+
+def ffdp_sobolev_fwd_bwd(u, lam, loss=None, dR=None, ws=None, stream=None, want_grad=True):
+    """R(u) (first-order Sobolev seminorm) and dR/du for u of shape (D, H, W, 3)."""
+    _dev(u, "u", torch.float32, 4)
+    shape = tuple(u.shape[:3])
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=u.device)
+    if dR is None and want_grad:
+        dR = torch.empty_like(u)
+    if ws is None:
+        ws = workspace(FFDP_OP_SOBOLEV, shape, None, u.device)
+    _check(lib().ffdp_sobolev_fwd_bwd(_ptr(u), dims_of(shape), float(lam), _ptr(loss), _ptr(dR), _ptr(ws),
+                                      ws.numel(), _stream(stream)))
+    return loss, dR
+
+
+def ffdp_sobolev_adam_step(u, g, m1, m2, params: ffdp_sobolev_adam_params, u_out=None, loss=None, ws=None,
+                           stream=None):
+    """One regularised Adam step: returns (u_out, loss[1] = R(u)); m1, m2 are updated in place."""
+    for t, n in ((u, "u"), (g, "g"), (m1, "m1"), (m2, "m2")):
+        _dev(t, n, torch.float32, 4)
+    shape = tuple(u.shape[:3])
+    if u_out is None:
+        u_out = torch.empty_like(u)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=u.device)
+    if ws is None:
+        ws = workspace(FFDP_OP_SOBOLEV, shape, None, u.device)
+    _check(lib().ffdp_sobolev_adam_step(_ptr(u), _ptr(u_out), _ptr(g), _ptr(m1), _ptr(m2), dims_of(shape),
+                                        ctypes.byref(params), _ptr(loss), _ptr(ws), ws.numel(), _stream(stream)))
+    return u_out, loss
 
 
 def launch_count() -> int:
