@@ -642,8 +642,10 @@ def run_gpu_path(args, ws, rank, local):
         ds = int(max(2, min(pair.F.shape[0], args.cpu_budget_s / max(t1 / 2.0, 1e-3))))
         n, t, cores = _path_oracle_sample(args, pair, ds)
         out["cpu_baseline"] = {"value": n / t / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
-                               "sample": "oracle %s fwd+bwd on fixed planes z<%d of the %s pair (%d voxels, %.1f s)"
-                                         % (args.path, ds, "x".join(map(str, pair.F.shape)), n, t)}
+                               "sample": "oracle %s on fixed planes z<%d of the %s pair (%d voxels, %.1f s)"
+                                         % ({"mse": "MSE objective fwd+bwd", "compose": "composition fwd+bwd",
+                                             "adam": "regularised Adam step"}[args.path], ds,
+                                            "x".join(map(str, pair.F.shape)), n, t)}
     print(json.dumps(out), flush=True)
 
 

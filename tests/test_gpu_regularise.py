@@ -33,7 +33,8 @@ def _field(shape, seed, scale=0.01):
     return (v * scale / v.abs().max()).numpy().astype(np.float32)
 
 
-SHAPES = [(2, 2, 2), (5, 7, 33), (9, 31, 17), (17, 19, 45), (16, 32, 64)]
+# W and N multiples of 4 take the 16-byte vector form, the others the per-voxel form
+SHAPES = [(2, 2, 2), (5, 7, 33), (9, 31, 17), (17, 19, 45), (16, 32, 64), (5, 7, 32), (3, 3, 4), (7, 9, 20)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
