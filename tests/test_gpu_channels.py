@@ -46,6 +46,9 @@ CHAN_CASES = [
     ((33, 41, 71), (30, 44, 64), 3, True, 0.03, 0.1),
     ((16, 16, 16), (16, 16, 16), 3, True, 0.4, 0.3),   # many samples leave V
     ((16, 16, 16), (16, 16, 16), 1, False, 0.4, 0.3),
+    ((2, 2, 2), (2, 2, 2), 3, True, 0.1, 0.1),            # smallest grids
+    ((3, 2, 257), (2, 5, 300), 1, False, 0.05, 0.1),      # elongated, two-voxel axes
+    ((2, 3, 130), (4, 2, 129), 4, False, 0.05, 0.1),
 ]
 
 
