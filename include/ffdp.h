@@ -20,12 +20,14 @@
  *   voxel i along axis c is x_min[c] + (x_max[c] - x_min[c]) * i_c / (n_c - 1).
  *   A displacement u is [D][H][W][3] float32 in normalised units of M.
  *
- *   Memory: every pointer named F, M, J, u, gJ, du, dJ, dA, dt, loss, ws is a
- *   DEVICE pointer owned by the caller; the library never allocates or frees
- *   device memory.  ffdp_transform and the *_params structs are HOST structs
- *   read during the call.  Float and half volumes and u/du/J/dJ must be 16-byte
- *   aligned (FFDP_ERR_INVALID_ARGUMENT otherwise).  Outputs are overwritten,
- *   never accumulated into.
+ *   Memory: every pointer named F, M, J, u, gJ, du, dJ, dA, dt, loss, ws (and
+ *   V, out, gout, dV, dR, g, m1, m2, u_out) is a DEVICE pointer owned by the
+ *   caller; the library never allocates or frees device memory.
+ *   ffdp_transform and the *_params structs are HOST structs read during the
+ *   call.  Float and half volumes and the per-voxel vector arrays must be
+ *   16-byte aligned (FFDP_ERR_INVALID_ARGUMENT otherwise).  Outputs are
+ *   overwritten, never accumulated into (m1 and m2 of the optimiser step are
+ *   state: read, then overwritten).
  *
  *   Streams: every call only enqueues work on `stream` (a cudaStream_t passed
  *   as void*, NULL = legacy default stream) and returns; results are ready
@@ -39,7 +41,8 @@
  *   on the device.
  *
  *   Limits: each dimension in [2, 2^20]; D*H*W < 2^32 voxels; bins in [8, 64];
- *   LNCC window odd in [3, 9].
+ *   LNCC window odd in [3, 9]; channels of a sampled volume in [1, 4]; a
+ *   moving or sampled volume below 2^31 voxels.
  */
 #ifndef FFDP_H
 #define FFDP_H
