@@ -67,3 +67,27 @@ def test_sobolev_adam_steps(ffdp, shape):
         assert rel_l2(host(m2d), ref["m2"]) <= 1e-5
         m1, m2 = ref["m1"], ref["m2"]          # continue both sides from their own state
         ud, uo = uo, ud                        # ping-pong
+
+
+def test_step_and_mse_objective_are_bitwise_reproducible(ffdp):
+    # fixed-order reductions, no float atomics on these paths
+    rng = np.random.default_rng(9)
+    shape = (12, 20, 36)
+    u = _cuda(_field(shape, 31))
+    g = _cuda((rng.normal(size=shape + (3,)) * 1e-4).astype(np.float32))
+    P = ffdp.sobolev_adam_params(0.3, 1e-3, 0.9, 0.999, 1e-8, 2)
+    outs = []
+    for _ in range(2):
+        m1 = torch.full_like(u, 1e-5)
+        m2 = torch.full_like(u, 1e-9)
+        uo, loss = ffdp.ffdp_sobolev_adam_step(u, g, m1, m2, P)
+        outs.append([host(x) for x in (uo, loss, m1, m2)])
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    F = _cuda(rng.uniform(0, 1, shape).astype(np.float32))
+    M = _cuda(rng.uniform(0, 1, shape).astype(np.float32))
+    T = ffdp.transform()
+    r1 = [host(x) for x in ffdp.ffdp_objective_mse(F, M, u, T, 1.0)]
+    r2 = [host(x) for x in ffdp.ffdp_objective_mse(F, M, u, T, 1.0)]
+    for a, b in zip(r1, r2):
+        assert np.array_equal(a, b)

@@ -153,3 +153,28 @@ def test_compose_512_sampled_planes_and_adjoint(ffdp):
     assert abs(lhs - rhs) <= 1e-4 * abs(rhs)
     assert rel_l2(du, du_o) <= TOL_GRAD
     assert rel_l2(np.r_[dA.cpu().numpy(), dt.cpu().numpy()], np.r_[dA_o, dt_o]) <= TOL_GRAD
+
+
+def test_adam_step_512_full_arrays(ffdp):
+    # bench.py --path adam: the regularised Adam step on the 512^3 pair's field (vector form)
+    from voxel_grid_sampler_gb300 import synth
+    pair = synth.make_pair(4, device="cuda")
+    u = pair.u
+    del pair.F, pair.M
+    torch.cuda.empty_cache()
+    g = torch.Generator(device="cuda").manual_seed(2025)
+    gr = torch.randn(u.shape, device="cuda", generator=g) * 1e-6
+    m1 = torch.randn(u.shape, device="cuda", generator=g) * 1e-7
+    m2 = torch.rand(u.shape, device="cuda", generator=g) * 1e-12
+    lam, lr, b1, b2, eps = (float(np.float32(v)) for v in (0.1, 1e-3, 0.9, 0.999, 1e-8))
+    uh, gh, m1h, m2h = (x.cpu().numpy() for x in (u, gr, m1, m2))
+    uo, loss = ffdp.ffdp_sobolev_adam_step(u, gr, m1, m2, ffdp.sobolev_adam_params(lam, lr, b1, b2, eps, 7))
+    torch.cuda.synchronize()
+    ref = oracle.sobolev_adam_step(uh, gh, m1h, m2h, lam, lr, b1, b2, eps, 7)
+    upd = uo.cpu().numpy().astype(np.float64) - uh
+    report("adam 512^3", R=rel_err(loss.item(), ref["R"]), update=rel_l2(upd, ref["u"] - uh),
+           m1=rel_l2(m1.cpu().numpy(), ref["m1"]), m2=rel_l2(m2.cpu().numpy(), ref["m2"]))
+    assert rel_err(loss.item(), ref["R"]) <= TOL_LOSS
+    assert rel_l2(upd, ref["u"] - uh) <= 1e-4
+    assert rel_l2(m1.cpu().numpy(), ref["m1"]) <= 1e-5
+    assert rel_l2(m2.cpu().numpy(), ref["m2"]) <= 1e-5
