@@ -12,10 +12,12 @@
 //   m1 = b1 m1 + (1 - b1) G,  m2 = b2 m2 + (1 - b2) G^2,
 //   u_out = u - lr (m1 / (1 - b1^t)) / (sqrt(m2 / (1 - b2^t)) + eps).
 //
-// Work layout: a persistent grid of kRegThreads-thread CTAs strides over
-// warp-uniform groups of 32 consecutive voxels.  A lane's x neighbours are
-// its neighbouring lanes' own u (shuffles; the group's two end lanes load
-// theirs), the y and z neighbours come from L1 / L2 (the rows and planes
+// Work layout: a persistent grid of kRegThreads-thread CTAs.  Two forms with
+// the same arithmetic: where W and N are multiples of 4, k_reg_v moves the
+// flat [N][3] arrays as one 16-byte vector per lane (below); otherwise k_reg
+// strides over warp-uniform groups of 32 consecutive voxels.  In both, x
+// neighbours come from the neighbouring lanes (shuffles; the end lanes
+// load theirs) and the y and z neighbours from L1 / L2 (the rows and planes
 // around the sweeping front stay resident), so u is read from HBM once; g,
 // m1, m2 stream once and u_out, m1, m2 are written once: 84 bytes per voxel
 // in the step mode.  The energy is summed per thread in fp32, folded into
