@@ -249,3 +249,44 @@ def test_mse_objective_finite_differences_through_the_sampler():
         Am = T.A.copy(); Am[rr, 1] -= e
         fd = (L(A=Ap) - L(A=Am)) / (2 * e)
         assert abs(fd - r["dA"][rr, 1]) <= 1e-5 * max(1.0, abs(fd))
+
+
+def _golden(name):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.txt")
+    for line in open(path):
+        line = line.strip()
+        if line and not line.startswith("#") and line.split("|")[0].strip() == name:
+            _, inp, exp = [s.strip() for s in line.split("|")]
+            kv = lambda s: dict(tok.split("=") for tok in s.split())
+            num = lambda s: np.array([float(v) for v in s.split(",")])
+            return {k: num(v) for k, v in kv(inp).items()}, {k: num(v) for k, v in kv(exp).items()}
+    raise KeyError(name)
+
+
+def test_golden_composition_and_image_gradient():
+    inp, exp = _golden("compose_linear2")
+    V = np.zeros((2, 2, 2, 3), np.float32)
+    for z in range(2):
+        for y in range(2):
+            for x in range(2):
+                for c in range(3):
+                    V[z, y, x, c] = (c + 1) * (x + 2 * y + 4 * z)
+    u = np.zeros((2, 2, 2, 3), np.float32)
+    u[0, 0, 0] = inp["u"]
+    # A = 0: the first fixed voxel lands on t + u = p
+    T = Transform(np.zeros((3, 3)), inp["p"] - u[0, 0, 0].astype(np.float64), np.eye(3), -np.ones(3), np.ones(3))
+    out = oracle.sample_channels(V, (2, 2, 2), u, T, compose=True)
+    assert np.allclose(out[0, 0, 0], exp["d"], atol=1e-6)  # u enters as float32
+    g = np.zeros((2, 2, 2, 3))
+    g[0, 0, 0, 0] = 1.0
+    _, _, _, dV = oracle.sample_channels_bwd(V, (2, 2, 2), u, T, g, compose=True)
+    assert np.allclose(dV[..., 0].ravel(), exp["dV0"], atol=1e-6)
+    assert np.all(dV[..., 1:] == 0.0)
+
+
+def test_golden_mse():
+    inp, exp = _golden("mse_four")
+    r = oracle.mse(inp["F"].astype(np.float32), inp["J"])
+    assert abs(r["mse"] - exp["MSE"][0]) <= 1e-15
+    assert np.allclose(r["dJ"], exp["dJ"], atol=1e-15)

@@ -122,3 +122,18 @@ def test_regularised_step_adds_the_regulariser_gradient():
     dR = oracle.sobolev(u, 0.5)["dR"]
     x, n1, n2 = oracle.adam(u.astype(np.float64), g + dR, m1, m2, 0.01, 0.9, 0.999, 1e-8, 3)
     assert np.array_equal(r["u"], x) and np.array_equal(r["m1"], n1) and np.array_equal(r["m2"], n2)
+
+
+def test_golden_sobolev_ramp():
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.txt")
+    row = [l for l in open(path) if l.startswith("sobolev_ramp2")][0]
+    _, inp, exp = [s.strip() for s in row.split("|")]
+    kv = dict(tok.split("=") for tok in (inp + " " + exp).split())
+    u = np.zeros((2, 2, 2, 3), np.float32)
+    u[..., 0] = np.arange(2)[None, None, :]
+    r = oracle.sobolev(u, float(kv["lambda"]))
+    assert abs(r["R"] - float(kv["R"])) <= 1e-15
+    lo, hi = (float(v) for v in kv["dRx"].split(","))
+    assert np.allclose(r["dR"][..., 0, 0], lo, atol=1e-15) and np.allclose(r["dR"][..., 1, 0], hi, atol=1e-15)
+    assert np.all(r["dR"][..., 1:] == 0.0)
