@@ -246,6 +246,59 @@ def _traffic_per_launch(kernel, workload, N):
     return None
 
 
+def _time_steps(step, n, stream, dev, ws, clocks=None):
+    """Device time of n back-to-back steps (CUDA events on the launching stream,
+    synchronised and barriered on both sides), max over ranks.  Returns the ms
+    per step and the library launches inside the timed region."""
+    from voxel_grid_sampler_gb300 import ffdp
+    n0 = ffdp.launch_count()
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.15)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    clk = clocks.stop() if clocks is not None else None
+    launches = ffdp.launch_count() - n0
+    ms = _max_over_ranks(e0.elapsed_time(e1) / n, ws, dev)
+    return ms, launches, clk
+
+
+def _kernel_times(step, n, dev):
+    """Per-kernel device times from a separate, instrumented pass of n steps
+    (CUDA events around every launch); the headline loop runs without them."""
+    from voxel_grid_sampler_gb300 import ffdp
+    ffdp.timing_enable(n * 8)
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize(dev)
+    kern = ffdp.timing_read()
+    ffdp.timing_enable(0)
+    return kern
+
+
+def _roofline(kern, kb, N, peak, peak_kind, traffic_of):
+    """Roofline of the dominant kernel: its algorithmic bytes per launch over
+    its average launch time, against the copy-bandwidth peak."""
+    dom_name, (dom_n, dom_ms) = max(kern.items(), key=lambda kv: kv[1][1])
+    dom_avg = dom_ms / max(dom_n, 1)
+    bpv = kb.get(dom_name, 0)
+    achieved = bpv * N / (dom_avg * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "traffic": traffic_of(dom_name), "kernel": dom_name,
+            "algorithmic_bytes_per_voxel": bpv, "peak_source": peak_kind,
+            "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": kb.get(k, 0),
+                            "frac": kb.get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3) / 1e9 / peak}
+                        for k, v in kern.items() if k in kb}}
+
+
 def run_gpu(args, ws, rank, local):
     from voxel_grid_sampler_gb300 import build, ffdp, synth
     torch.cuda.set_device(local)
@@ -273,29 +326,12 @@ def run_gpu(args, ws, rank, local):
         step()
     torch.cuda.synchronize(dev)
 
-    # ---- device-resident timed region (per-kernel events recorded live)
+    # ---- device-resident timed region: plain calls, no per-launch events
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
-    ffdp.timing_enable(args.steps * 8)
-    n0 = ffdp.launch_count()
-    _barrier(ws)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.15)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    _barrier(ws)
-    clk = clocks.stop()
-    launches = ffdp.launch_count() - n0
-    kern = ffdp.timing_read()
-    ffdp.timing_enable(0)
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = _max_over_ranks(ms, ws, dev)
+    ms, launches, clk = _time_steps(step, args.steps, stream, dev, ws, clocks)
     value = _aggregate_gvox(N, ws, ms)
+    # per-kernel times from a separate instrumented pass
+    kern = _kernel_times(step, max(3, min(args.steps, 10)), dev)
 
     # the other MI mode of an MI-only objective, timed the same way for reference
     alt = None
@@ -303,18 +339,14 @@ def run_gpu(args, ws, rank, local):
         P2 = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
                                    store_slope=not args.store_slope)
         ws2 = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P2, dev)
+
+        def step2():
+            ffdp.ffdp_objective(F, M, u, T, P2, loss, du, dA, dt, ws2, stream)
         for _ in range(3):
-            ffdp.ffdp_objective(F, M, u, T, P2, loss, du, dA, dt, ws2, stream)
+            step2()
         torch.cuda.synchronize(dev)
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        n_alt = max(3, min(args.steps, 10))
-        a0.record(stream)
-        for _ in range(n_alt):
-            ffdp.ffdp_objective(F, M, u, T, P2, loss, du, dA, dt, ws2, stream)
-        a1.record(stream)
-        torch.cuda.synchronize(dev)
-        alt = {"mi_mode": _mi_mode(not args.store_slope), "ms_per_step": a0.elapsed_time(a1) / n_alt}
+        ms2, _, _ = _time_steps(step2, max(3, min(args.steps, 10)), stream, dev, ws)
+        alt = {"mi_mode": _mi_mode(not args.store_slope), "ms_per_step": ms2}
         del ws2
         torch.cuda.empty_cache()
         step()  # leave the outputs of the timed mode in place
@@ -325,7 +357,63 @@ def run_gpu(args, ws, rank, local):
         ms_e2e, h2d, d2h = float("nan"), 0, 0
     else:
         ms_e2e, h2d, d2h = _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws)
-    _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h, alt)
+    out = _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h, alt)
+    # ---- the gigavoxel workload, timed the same way, on the same line
+    if out is not None and args.workload == 4 and not args.shape and not args.no_workload5 and ws == 1:
+        del pair, F, M, u, wsbuf, du, step
+        torch.cuda.empty_cache()
+        out["workload5"] = _workload5(args, dev, stream)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+def _workload5(args, dev, stream):
+    """The 1024^3 fp16 MI-32 objective (stored J and slope, the default mode),
+    timed like the headline: plain calls between CUDA events, per-kernel times
+    from a separate instrumented pass."""
+    from voxel_grid_sampler_gb300 import ffdp, synth
+    free, _ = torch.cuda.mem_get_info(dev)
+    if free < 64 * 2 ** 30:
+        return {"skipped": "needs 64 GiB of free device memory, %.1f GiB free" % (free / 2 ** 30)}
+    t0 = time.perf_counter()
+    pair = synth.make_pair(5, device=dev)
+    gen_s = time.perf_counter() - t0
+    wl = pair.workload
+    F, M, u = pair.F, pair.M, pair.u
+    N = F.numel()
+    T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
+                              store_slope=True)
+    wsbuf = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P, dev)
+    loss = torch.empty(3, device=dev)
+    du = torch.empty(tuple(F.shape) + (3,), device=dev)
+    dA = torch.empty(9, device=dev)
+    dt = torch.empty(3, device=dev)
+
+    def step():
+        ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, wsbuf, stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(torch.cuda.current_device())
+    n = max(3, min(args.steps, 10))
+    ms, launches, clk = _time_steps(step, n, stream, dev, 1, clocks)
+    kern = _kernel_times(step, 3, dev)
+    peak, peak_kind = _peaks()
+    kb = KERNEL_BYTES_STORED[5]
+    step_gbs = ALGO_BYTES[5] * N / (ms * 1e-3) / 1e9
+    res = {"workload": wl.name, "shape": list(F.shape), "voxels": N, "steps": n, "warmup": 3,
+           "ms_per_step": ms, "value": N / (ms * 1e-3) / 1e9, "unit": UNIT, "gpu_launches": int(launches),
+           "mi_mode": _mi_mode(True), "dtype": "f32 (f16 storage)", "generate_s": gen_s,
+           "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs, "of_8tbs": step_gbs / HBM_NOMINAL_GBS,
+                                "of_measured": step_gbs / peak, "bytes_per_voxel": ALGO_BYTES[5]},
+           "roofline": _roofline(kern, kb, N, peak, peak_kind, lambda k: _traffic_per_launch(k, wl.name, N)),
+           "kernels_ms_per_launch": {k: v[1] / max(v[0], 1) for k, v in kern.items()},
+           "clocks": clk, "loss": [float(x) for x in loss.tolist()]}
+    del pair, F, M, u, wsbuf, du
+    torch.cuda.empty_cache()
+    return res
 
 
 def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
@@ -407,23 +495,11 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
     value = _aggregate_gvox(N, ws, ms)
     # ---- roofline of the dominant kernel (algorithmic bytes / its own time)
     peak, peak_kind = _peaks()
-    dom = max(kern.items(), key=lambda kv: kv[1][1]) if kern else ("?", (1, ms))
-    dom_name, (dom_n, dom_ms) = dom
-    dom_avg = dom_ms / max(dom_n, 1)
-    per_launch_voxels = N
-    kb = _kernel_bytes(args, wl)
-    bpv = kb.get(dom_name, 0)
-    achieved = bpv * per_launch_voxels / (dom_avg * 1e-3) / 1e9
-    traffic = _traffic_per_launch(dom_name, wl.name, N)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic, "kernel": dom_name,
-                "algorithmic_bytes_per_voxel": bpv, "peak_source": peak_kind,
-                "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": kb.get(k, 0),
-                                "frac": kb.get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3) / 1e9 / peak}
-                            for k, v in kern.items() if k in kb}}
+    roofline = _roofline(kern, _kernel_bytes(args, wl), N, peak, peak_kind,
+                         lambda k: _traffic_per_launch(k, wl.name, N))
     step_gbs = ALGO_BYTES[args.workload] * N / (ms * 1e-3) / 1e9
     if rank != 0:
-        return
+        return None
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -458,7 +534,7 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
         out["cpu_baseline"] = {"value": n / t / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": "oracle objective on fixed planes z<%d of the %s pair "
                                          "(%d voxels, %.1f s)" % (ds, "x".join(map(str, F.shape)), n, t)}
-    print(json.dumps(out), flush=True)
+    return out
 
 
 # ---------------------------------------------------------------- other paths
@@ -561,26 +637,11 @@ def run_gpu_path(args, ws, rank, local):
         step()
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
-    ffdp.timing_enable(args.steps * 8)
-    n0 = ffdp.launch_count()
-    _barrier(ws)
-    torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.15)
+    ms, launches, clk = _time_steps(step, args.steps, stream, dev, ws, clocks)
+    kern = _kernel_times(step, max(3, min(args.steps, 10)), dev)
+    value = _aggregate_gvox(N, ws, ms)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    _barrier(ws)
-    clk = clocks.stop()
-    launches = ffdp.launch_count() - n0
-    kern = ffdp.timing_read()
-    ffdp.timing_enable(0)
-    ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
-    value = _aggregate_gvox(N, ws, ms)
 
     # end to end: pinned host inputs copied in and every output copied out, each step
     e2e = None
@@ -614,10 +675,11 @@ def run_gpu_path(args, ws, rank, local):
         return
     peak, peak_kind = _peaks()
     kb = PATH_KERNEL_BYTES[args.path]
-    dom_name, (dom_n, dom_ms) = max(kern.items(), key=lambda kv: kv[1][1])
-    dom_avg = dom_ms / max(dom_n, 1)
-    achieved = kb.get(dom_name, 0) * N / (dom_avg * 1e-3) / 1e9
     step_gbs = PATH_ALGO_BYTES[args.path] * N / (ms * 1e-3) / 1e9
+    roof = _roofline(kern, kb, N, peak, peak_kind, lambda k: _traffic_per_launch(k, "%s 512^3" % args.path, N))
+    roof["kernels"] = {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": kb.get(k, 0),
+                           "frac": kb.get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3) / 1e9 / peak}
+                       for k, v in kern.items()}
     out = {
         "metric": PATH_METRIC[args.path], "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -628,12 +690,7 @@ def run_gpu_path(args, ws, rank, local):
                    "parallelism": "independent pair per rank" if ws > 1 else "single GPU"},
         "pct_hbm_roofline": {"step_algorithmic_gbs": step_gbs, "of_8tbs": step_gbs / HBM_NOMINAL_GBS,
                              "of_measured": step_gbs / peak, "bytes_per_voxel": PATH_ALGO_BYTES[args.path]},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": _traffic_per_launch(dom_name, "%s 512^3" % args.path, N), "kernel": dom_name,
-                     "algorithmic_bytes_per_voxel": kb.get(dom_name, 0), "peak_source": peak_kind,
-                     "kernels": {k: {"ms": v[1] / max(v[0], 1), "bytes_per_voxel": kb.get(k, 0),
-                                     "frac": kb.get(k, 0) * N / (v[1] / max(v[0], 1) * 1e-3) / 1e9 / peak}
-                                 for k, v in kern.items()}},
+        "roofline": roof,
         "kernels_ms_per_launch": {k: v[1] / max(v[0], 1) for k, v in kern.items()},
         "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
     }
@@ -660,6 +717,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=6.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-workload5", action="store_true",
+                    help="skip the 1024^3 leg that the default workload-4 line carries")
     ap.add_argument("--shape", type=int, default=0, help="cube edge overriding the workload size (profiling)")
     ap.add_argument("--store-slope", type=int, default=1, choices=[0, 1],
                     help="MI-only objectives: store J and dJ/dp (1) or stay implicit (0)")

@@ -276,9 +276,12 @@ ffdp_status ffdp_sobolev_adam_step(const float *u, float *u_out, const float *g,
  *     images do not fit); a call whose scratch need (ffdp_workspace_bytes of
  *     the MI-only objective) exceeds the static scratch returns
  *     FFDP_ERR_UNSUPPORTED.
- *   - The first call on a device looks up the scratch's device address (a
- *     one-time set-up per device); make that first call before any stream
- *     capture.
+ *   - Each call looks up the scratch's device address on the current device
+ *     (cudaGetSymbolAddress).  The first call on a device also loads the
+ *     library's device code there, so make it before any stream capture;
+ *     later lookups are host-side table reads.  Because nothing is cached,
+ *     a cudaDeviceReset in the process needs no special handling: the next
+ *     call finds the array in the new context.
  *   - All calls on a device share the one scratch area, which keeps the last
  *     call's contents; each call re-initialises what must start at zero.
  *     Calls that overlap on the GPU (e.g. on two streams at once) race on it:

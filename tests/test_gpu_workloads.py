@@ -4,7 +4,10 @@ configuration bench.py times (one ffdp_objective call on the whole volume).
 Workloads 1-4 are compared element by element against the oracle on whole
 arrays (du in full, dA, dt, all three loss values, and the sampled image J);
 workload 5 (1024^3, ~1.07e9 voxels) streams the oracle slab by slab and
-compares the losses, dA and dt in full and du / J at 4096 sampled voxels.
+compares the losses, dA and dt in full, du on whole sampled z-planes (the
+first, two inner and the last) plus 4096 scattered voxels, and J at those
+voxels -- in both MI modes: stored J and slope (the mode bench.py times) and
+implicit.
 """
 import numpy as np
 import pytest
@@ -23,10 +26,11 @@ def ffdp():
     return f
 
 
-def _run_gpu(ffdp, pair):
+def _run_gpu(ffdp, pair, store_slope=False):
     wl = pair.workload
     T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
-    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
+                              store_slope=store_slope)
     loss, du, dA, dt = ffdp.ffdp_objective(pair.F, pair.M, pair.u, T, P)
     J = ffdp.ffdp_grid_sample_fwd(pair.M, pair.F.shape, pair.u, T)
     torch.cuda.synchronize()
@@ -69,28 +73,41 @@ def test_workload_full_arrays(ffdp, k):
     assert rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
 
 
-def test_workload5_gigavoxel_streamed(ffdp):
+@pytest.mark.parametrize("store_slope", [True, False], ids=["stored", "implicit"])
+def test_workload5_gigavoxel_streamed(ffdp, store_slope):
     from voxel_grid_sampler_gb300 import synth
     pair = synth.make_pair(5, device="cuda")
-    l, du, dA, dt, J = _run_gpu(ffdp, pair)
+    l, du, dA, dt, J = _run_gpu(ffdp, pair, store_slope=store_slope)
+    D, H, W = pair.F.shape
     N = pair.F.numel()
-    idx = np.sort(np.random.default_rng(5).choice(N, 4096, replace=False))
+    plane = H * W
+    planes = [0, 417, 730, D - 1]
+    idx = np.unique(np.concatenate([np.random.default_rng(5).choice(N, 4096, replace=False)] +
+                                   [np.arange(z * plane, (z + 1) * plane) for z in planes]))
     it = torch.from_numpy(idx).cuda()
     du_s = du.view(-1, 3)[it].cpu().numpy()
     J_s = J.view(-1)[it].cpu().numpy()
-    del du, J
+    del du, J, it
     F = pair.F.cpu().float().numpy()
     M = pair.M.cpu().float().numpy()
     u = pair.u.cpu().numpy()
     del pair.F, pair.M, pair.u
     torch.cuda.empty_cache()
     ref = oracle.objective_mi_slabs(F, M, u, oracle_T_of(pair), _oparams(pair), slab=16, du_index=idx)
-    report("workload 5", J=np.max(np.abs(J_s - ref["J_samples"])), loss=rel_err(l[0], ref["loss"][0]),
-           du=rel_l2(du_s, ref["du_samples"]), dAdt=rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]))
+    per_plane = []
+    for z in planes:
+        sel = (idx >= z * plane) & (idx < (z + 1) * plane)
+        assert sel.sum() == plane
+        per_plane.append(rel_l2(du_s[sel], ref["du_samples"][sel]))
+    report("workload 5 (%s)" % ("stored" if store_slope else "implicit"),
+           J=np.max(np.abs(J_s - ref["J_samples"])), loss=rel_err(l[0], ref["loss"][0]),
+           du=rel_l2(du_s, ref["du_samples"]), du_planes=max(per_plane),
+           dAdt=rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]))
     assert np.max(np.abs(J_s - ref["J_samples"])) <= TOL_J
     _check_losses(l, ref["loss"])
     assert rel_l2(np.r_[dA, dt], np.r_[ref["dA"].ravel(), ref["dt"]]) <= TOL_GRAD
     assert rel_l2(du_s, ref["du_samples"]) <= TOL_GRAD
+    assert max(per_plane) <= TOL_GRAD, per_plane
 
 
 # ------------------------------------------- next rows at the bench's full size

@@ -975,28 +975,22 @@ extern "C" ffdp_status ffdp_sobolev_adam_step(const float* u, float* u_out, cons
 // them the MI-only objective can run on scratch memory reserved inside the
 // library image: this file-scope array is created on every GPU that loads the
 // library and is held until the process exits.  Host code must not use the
-// array's name as a device address (in host code it is only a stand-in);
-// the device address is looked up once per device and passed to the kernels.
+// array's name as a device address (in host code it is only a stand-in): the
+// device address is looked up with cudaGetSymbolAddress, with the caller's
+// device current, and passed to the kernels.  The lookup is repeated on every
+// call (after the first call on a device, which loads the module, it is a
+// table lookup in the runtime), so an address never outlives the context it
+// belongs to: after a cudaDeviceReset the next call finds the array again in
+// the new context.
 static constexpr size_t kStaticScratchBytes = 512u * 1024u;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[64] = {};  // device address of g_static_scratch, per device ordinal
-
 ffdp_status static_scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= 64) return fail(FFDP_ERR_UNSUPPORTED, "device ordinal %d above 63", dev);
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+  *out = p;
   return FFDP_OK;
 }
 }  // namespace

@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "ffdp_device.cuh"
 
 // Instantiate a body for the float (code 0) or half (code 1) element type.
@@ -158,7 +160,31 @@ cudaError_t launch_mse(int ft, const MseArgs& a, int grid, cudaStream_t s);
 int chan_ctas_per_sm(int C, int compose, int bwd);
 constexpr int kChanThreads = 256;  // threads per CTA of the channel sampler and the MSE kernel
 
-// Occupancy-derived persistent grid sizes (CTAs per SM), cached.
+// Occupancy-derived persistent grid sizes (CTAs per SM), cached per device
+// ordinal and kernel variant.  The cache is a table of atomics (zero = not yet
+// queried), so host threads may launch concurrently, and each device keeps
+// its own counts (GPUs of different kinds in one process).
+constexpr int kMaxDevices = 64;
+constexpr int kMaxCtasPerSm = 8;
+template <int NKEYS>
+struct OccCache {
+  std::atomic<int> v[kMaxDevices * NKEYS];
+  // query() returns resident CTAs per SM (any value; clamped to 1..kMaxCtasPerSm)
+  template <class Fn>
+  int get(int key, Fn&& query) {
+    auto clampv = [](int x) { return x < 1 ? 1 : (x > kMaxCtasPerSm ? kMaxCtasPerSm : x); };
+    int dev = 0;
+    if (key < 0 || key >= NKEYS || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+      return clampv(query());
+    std::atomic<int>& c = v[dev * NKEYS + key];
+    int x = c.load(std::memory_order_relaxed);
+    if (x == 0) {
+      x = clampv(query());
+      c.store(x, std::memory_order_relaxed);
+    }
+    return x;
+  }
+};
 // Test hook: returns and clears the one-shot ring stall request.
 unsigned take_test_stall();
 // Reads the device error word of the current device (synchronous) and clears it.
@@ -172,7 +198,6 @@ int lncc_ctas_per_sm(int mode, int ft, int mt, int bmax_or0, int R);
 void note_launch_begin(const char* name, cudaStream_t s);
 void note_launch_end(cudaStream_t s);
 
-constexpr int kMaxCtasPerSm = 8;
 constexpr int kLnccTX = 32;
 // LNCC tile height (rows of output voxels per CTA) for window radius <= 2, 3
 // and 4, the thread count of the register-history kernel (radius <= 3) and

@@ -433,9 +433,8 @@ cudaError_t launch_mse(int ft, const MseArgs& a, int grid, cudaStream_t s) {
 
 // Resident CTAs per SM of the channel kernels (bwd: backward; C = 0: k_mse).
 int chan_ctas_per_sm(int C, int compose, int bwd) {
-  static int cache[2][5][2] = {};
-  int& c = cache[bwd ? 1 : 0][C][compose ? 1 : 0];
-  if (c == 0) {
+  static OccCache<2 * 5 * 2> cache;
+  return cache.get(((bwd ? 1 : 0) * 5 + C) * 2 + (compose ? 1 : 0), [&] {
     int occ = 0;
     cudaError_t e = cudaErrorInvalidValue;
     if (C == 0) {
@@ -445,10 +444,8 @@ int chan_ctas_per_sm(int C, int compose, int bwd) {
     } else {
       FFDP_CHAN_SWITCH(C, compose, e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_chan_fwd<kC, kComp>, kChanThreads, 0));
     }
-    if (e != cudaSuccess || occ < 1) occ = 1;
-    c = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
-  }
-  return c;
+    return e == cudaSuccess ? occ : 1;
+  });
 }
 
 }  // namespace ffdp

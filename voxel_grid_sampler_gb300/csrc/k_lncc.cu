@@ -1189,10 +1189,13 @@ cudaError_t launch_lncc(int mode, int ft, int mt, int bmax, const LnccArgs& a, i
 }
 
 int lncc_ctas_per_sm(int mode, int ft, int mt, int bmax, int R) {
-  int occ = 0;
-  LnccArgs dummy{};
-  if (dispatch_lncc(mode, ft, mt, bmax, dummy, 0, 0, R, &occ) != cudaSuccess || occ < 1) occ = 1;
-  return occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
+  static OccCache<2 * 2 * 3 * 5> cache;
+  const int bidx = bmax == 0 ? 0 : (bmax == 32 ? 1 : 2);
+  return cache.get(((mode * 2 + ft) * 3 + bidx) * 5 + (R >= 0 && R <= 4 ? R : 0), [&] {
+    int occ = 0;
+    LnccArgs dummy{};
+    return dispatch_lncc(mode, ft, mt, bmax, dummy, 0, 0, R, &occ) == cudaSuccess ? occ : 1;
+  });
 }
 
 }  // namespace ffdp

@@ -298,20 +298,16 @@ cudaError_t launch_reg(int step, const RegArgs& a, int grid, cudaStream_t s) {
 }
 
 int reg_ctas_per_sm(int step) {
-  static int cache[2] = {0, 0};
-  int& c = cache[step ? 1 : 0];
-  if (c == 0) {
+  static OccCache<2> cache;
+  return cache.get(step ? 1 : 0, [&] {
     // both forms are bounded to 64 registers (four 256-thread CTAs per SM); take the smaller occupancy
     int o1 = 0, o2 = 0;
     const cudaError_t e1 = step ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, k_reg<1>, kRegThreads, 0)
                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, k_reg<0>, kRegThreads, 0);
     const cudaError_t e2 = step ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, k_reg_v<1>, kRegThreads, 0)
                                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, k_reg_v<0>, kRegThreads, 0);
-    int occ = (e1 == cudaSuccess && e2 == cudaSuccess) ? (o1 < o2 ? o1 : o2) : 1;
-    if (occ < 1) occ = 1;
-    c = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
-  }
-  return c;
+    return (e1 == cudaSuccess && e2 == cudaSuccess) ? (o1 < o2 ? o1 : o2) : 1;
+  });
 }
 
 }  // namespace ffdp

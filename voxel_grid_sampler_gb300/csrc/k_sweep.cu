@@ -1083,15 +1083,12 @@ cudaError_t launch_sweep1(int mode, int ft, int mt, int bmax, const Sweep1Args& 
 }
 
 int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax) {
-  static int cache[kSweep1Modes][2][2][2] = {};
-  int& c = cache[mode][ft][mt][bmax == 64];
-  if (c == 0) {
+  static OccCache<kSweep1Modes * 8> cache;
+  return cache.get(((mode * 2 + ft) * 2 + mt) * 2 + (bmax == 64), [&] {
     int occ = 0;
     Sweep1Args dummy{};
-    if (dispatch_sweep1(mode, ft, mt, bmax, dummy, 0, 0, &occ) != cudaSuccess || occ < 1) occ = 1;
-    c = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
-  }
-  return c;
+    return dispatch_sweep1(mode, ft, mt, bmax, dummy, 0, 0, &occ) == cudaSuccess ? occ : 1;
+  });
 }
 
 template <typename FT, typename MT, int BMAX, int MODE>
@@ -1140,15 +1137,12 @@ cudaError_t launch_sweep2(int mode, int ft, int mt, int bmax, const Sweep2Args& 
 }
 
 int sweep2_ctas_per_sm(int mode, int ft, int mt, int bmax) {
-  static int cache[kSweep2Modes][2][2][2] = {};
-  int& c = cache[mode][ft][mt][bmax == 64];
-  if (c == 0) {
+  static OccCache<kSweep2Modes * 8> cache;
+  return cache.get(((mode * 2 + ft) * 2 + mt) * 2 + (bmax == 64), [&] {
     int occ = 0;
     Sweep2Args dummy{};
-    if (dispatch_sweep2(mode, ft, mt, bmax, dummy, 0, 0, &occ) != cudaSuccess || occ < 1) occ = 1;
-    c = occ > kMaxCtasPerSm ? kMaxCtasPerSm : occ;
-  }
-  return c;
+    return dispatch_sweep2(mode, ft, mt, bmax, dummy, 0, 0, &occ) == cudaSuccess ? occ : 1;
+  });
 }
 
 cudaError_t launch_finalize(int bmax, const FinalizeArgs& a, cudaStream_t s) {
