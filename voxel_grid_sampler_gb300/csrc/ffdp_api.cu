@@ -295,9 +295,13 @@ struct Ws {
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// ln: LNCC on; ln or store: J and dJ/dq per voxel.
+// True when the LNCC objective samples J on chip instead of storing it (the
+// halo-recompute build, window radius <= 3).
+bool lncc_recompute(int window) { return kLnccRecompute && window <= 7; }
+
+// ln: LNCC on; store: J and dJ/dq per voxel.
 Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N) {
-  const bool needJ = ln || store;
+  const bool needJ = store;
   Ws w;
   size_t o = 0;
   w.hist = o;
@@ -398,7 +402,8 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
       const bool mi = p->w_mi != 0.0f, ln = p->w_lncc != 0.0f;
       if (mi && check_mi(&p->mi) != FFDP_OK) return 0;
       if (ln && check_lncc(&p->lncc) != FFDP_OK) return 0;
-      return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln, mi && p->store_slope != 0, N).total;
+      return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln,
+                       (ln && !lncc_recompute(p->lncc.window)) || (mi && !ln && p->store_slope != 0), N).total;
     }
     case FFDP_OP_SAMPLE_CHANNELS_BWD:
     case FFDP_OP_MSE:
@@ -600,7 +605,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, u and du must be 16-byte aligned");
   const int bmax = mi ? bmax_of(p->mi.bins) : 32;
   const uint64_t N = nvox(fdims);
-  const bool store = ln || (mi && p->store_slope != 0);
+  const bool rc = ln && lncc_recompute(p->lncc.window);  // LNCC samples J on chip
+  const bool store = (ln && !rc) || (mi && !ln && p->store_slope != 0);
   const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N);
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
@@ -617,7 +623,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   const BinMap bf = mi ? bin_map(p->mi.f_lo, p->mi.f_hi, p->mi.bins) : BinMap{0, 1, 1, 0};
   const BinMap bj = mi ? bin_map(p->mi.m_lo, p->mi.m_hi, p->mi.bins) : BinMap{0, 1, 1, 0};
 
-  // sweep 1: histogram (MI) and/or the materialised J (LNCC)
+  // sweep 1: histogram (MI) and/or the materialised J (LNCC); none for an
+  // LNCC-only objective that samples J on chip
   if (mi) FFDP_CUDA(launch_zero_u64(hist, bmax * bmax, s), "zero launch");
   Sweep1Args a1{};
   a1.g = g;
@@ -635,8 +642,9 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   // with LNCC (or store_slope), J and its slope dJ/dq are stored for the
   // window kernel and the streaming gradient pass
   const int m1 = mi ? (store ? S1_HIST_WRITEJG : S1_HIST) : S1_WRITEJG;
-  FFDP_CUDA(launch_sweep1(m1, ft, mt, bmax, a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(m1, ft, mt, bmax)), s),
-            "sweep 1 launch");
+  if (mi || !rc)
+    FFDP_CUDA(launch_sweep1(m1, ft, mt, bmax, a1, persistent_grid(a1.nIter, sweep1_ctas_per_sm(m1, ft, mt, bmax)), s),
+              "sweep 1 launch");
   if (mi) {
     FinalizeArgs fa{};
     fa.ghist = hist;
@@ -657,6 +665,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     a.F = F;
     a.J = Jbuf;
     a.dJdq = DGbuf;
+    a.M = M;
+    a.u = u;
     a.du = du;
     a.T = bmax == 64 ? table2 : table;  // polynomial cells
     a.partials = partials;

@@ -39,6 +39,17 @@ __host__ __device__ constexpr int sweep2_threads(int mode) {
 constexpr int kSweep2Modes = 6;
 enum LnccMode { LN_DJ = 0, LN_DU = 1 };  // write dL/dJ; or du and affine partials from the stored slope
 
+// Compile-time variant of the LNCC objective path (FFDP_LNCC_RECOMPUTE): the
+// window kernel samples J (and, at its output voxels, the slope dJ/dq) from M
+// and u on chip instead of reading the J and slope that the histogram sweep
+// stores, so the workspace holds nothing per voxel (O(#SMs + B^2)).  The
+// default build stores J and the slope (16 B/voxel of workspace).
+#ifdef FFDP_LNCC_RECOMPUTE
+constexpr bool kLnccRecompute = true;
+#else
+constexpr bool kLnccRecompute = false;
+#endif
+
 // Histogram sweep / forward sampler.
 struct Sweep1Args {
   const void* F;
@@ -90,6 +101,8 @@ struct LnccArgs {
   const void* F;
   const float* J;
   const float* dJdq;  // LN_DU: [N][3] stored slope of J
+  const void* M;      // halo-recompute build (LN_DU): the moving image, sampled on chip
+  const float* u;     //                                and the displacement (NULL: 0)
   float* du;          // LN_DU: [N][3] or NULL (affine partials only)
   float* dJ;          // LN_DJ: [N] dL/dJ or NULL
   const float* T;

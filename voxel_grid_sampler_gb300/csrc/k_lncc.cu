@@ -29,6 +29,8 @@
 // first window pass uses direct fp32 sums in z (no sliding add/subtract) to
 // keep rounding low in flat regions.  CTAs are persistent over tiles, so the
 // per-CTA partial records stay O(#SMs).
+#include <type_traits>
+
 #include "ffdp_internal.h"
 
 namespace ffdp {
@@ -802,6 +804,35 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   float grX[W][NOUT];
   float2 nxt[NSTG];      // next plane, fetched one step ahead
   int soff[NSTG];
+  constexpr bool RC = DU && kLnccRecompute;  // J and its slope sampled here, nothing stored
+  const FT* __restrict__ Mp = static_cast<const FT*>(a.M);
+  // J at fixed-grid voxel (x, y, z) (and its slope dJ/dq when GRAD), sampled
+  // from M and u like the sweeps do
+  auto sample = [&](int x, int y, int z, size_t lin, float* dq, auto grad) -> float {
+    constexpr bool GRAD = decltype(grad)::value;
+    long long P[3];
+    anchor(g, x, y, z, P);
+    float u0 = 0.0f, u1 = 0.0f, u2 = 0.0f;
+    if (a.u) {
+      u0 = __ldg(a.u + 3 * lin);
+      u1 = __ldg(a.u + 3 * lin + 1);
+      u2 = __ldg(a.u + 3 * lin + 2);
+    }
+    int b[3];
+    float r[3], m[8];
+    cell_of(g, P, u0, u1, u2, b, r);
+    gather8<FT>(Mp, g, b, m);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m[q] = tap_value<FT>(m[q]);
+    float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f;
+    const float jv = interp8<GRAD>(m, r, d0, d1, d2);
+    if (GRAD) {
+      dq[0] = d0;
+      dq[1] = d1;
+      dq[2] = d2;
+    }
+    return jv;
+  };
 
   auto load_plane = [&](int zp) {
     const bool zin = zp >= 0 && zp < g.fD;
@@ -810,7 +841,12 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
     for (int i = 0; i < NSTG; ++i) {
       float2 v = make_float2(0.0f, 0.0f);
       if (zin && soff[i] >= 0) {
-        v.x = __ldg(a.J + base + soff[i]);
+        if constexpr (RC) {
+          const int y = (int)fast_div((unsigned)soff[i], g.divW_m, g.divW_s);
+          v.x = sample(soff[i] - y * g.fW, y, zp, base + soff[i], nullptr, std::false_type{});
+        } else {
+          v.x = __ldg(a.J + base + soff[i]);
+        }
         v.y = load1(F + base + soff[i]);
       }
       nxt[i] = v;
@@ -865,7 +901,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
 #pragma unroll
           for (int i = 0; i < NSTG; ++i) hist[j][i] = nxt[i];
           if (s + 1 < nsteps) load_plane(zi + 1);
-          if constexpr (DU) {
+          if constexpr (DU && !RC) {
             slot_rd = slot_rd == 2 ? 0 : slot_rd + 1;
             const int sn = s + 1;  // the output plane of the next step
             const float* src =
@@ -893,7 +929,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
               }
             }
           }
-          if constexpr (DU) slope_wait_prev();
+          if constexpr (DU && !RC) slope_wait_prev();
           __syncthreads();
           if (pass1) {
             // [C] x sums, 2 outputs per item: neighbouring lanes read
@@ -1090,7 +1126,11 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
                 float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
                 if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
                 const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
-                if constexpr (DU)
+                if constexpr (RC) {
+                  float q[3];
+                  sample(X, Y, zo, lin, q, std::true_type{});
+                  dacc.add(a, k, lin, q, (float)zo - g.ctr[2], gv);
+                } else if constexpr (DU)
                   dacc.add(a, k, lin, slope + slot_rd * SlopeStage<TY>::SLOT + (oy0 + k) * SlopeStage<TY>::ROW + 3 * ox,
                            (float)zo - g.ctr[2], gv);
                 else if (a.dJ)
@@ -1126,7 +1166,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
 
 template <int R, bool DU>
 static size_t smem_of() {
-  const size_t stage = DU ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0;
+  const size_t stage = (DU && !(kLnccRecompute && R <= 3)) ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0;
   if constexpr (R <= 3)
     return ((size_t)LTR<R>::TOTAL + stage) * sizeof(float);
   else
