@@ -234,6 +234,12 @@ ffdp_status make_geom(ffdp_dims f, ffdp_dims m, const ffdp_transform* T, Geom& g
               T->S[7] == 0.f)
                  ? 1
                  : 0;
+  const long long one = 1ll << 32;
+  g.ia = (g.a_diag && g.Gq[0] == one && g.Gq[4] == one && g.Gq[8] == one && (g.g0q[0] & (one - 1)) == 0 &&
+          (g.g0q[1] & (one - 1)) == 0 && (g.g0q[2] & (one - 1)) == 0)
+             ? 1
+             : 0;
+  for (int c = 0; c < 3; ++c) g.io[c] = g.ia ? (int)(g.g0q[c] >> 32) : 0;
   g.fW = (int)f.w;
   g.fH = (int)f.h;
   g.fD = (int)f.d;

@@ -71,6 +71,8 @@ struct Geom {
   int divW_s, divHW_s;
   int k_diag;       // K is diagonal (S diagonal): u enters q component-wise
   int a_diag;       // G is diagonal (A diagonal)
+  int ia;           // G = I and g0 integer: every anchor is the integer i + io
+  int io[3];        // g0 when ia
 };
 
 // Unsigned division by a runtime-invariant divisor (round-up method).
@@ -144,6 +146,31 @@ __device__ __forceinline__ void cell_of(const Geom& g, const long long P[3], flo
     float fr;
     floor_split(t, fi, fr);
     b[c] = k + fi;
+    r[c] = fr;
+  }
+}
+
+// The same cell when every anchor is an integer (G = I, g0 = io integer: a
+// grid sampled at its own voxel positions up to an integer shift, as for
+// A = I, t = 0 and equal fixed and moving extents): the fraction of the
+// anchor is 0, so q = (i + io) + K u with no fixed-point arithmetic.  Gives
+// the same b and r as cell_of on such anchors.
+__device__ __forceinline__ void cell_of_int(const Geom& g, int ix, int iy, int iz, float u0, float u1, float u2,
+                                            int b[3], float r[3]) {
+  const int idx[3] = {ix, iy, iz};
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    float t;
+    if (g.k_diag) {
+      t = g.K[c * 4] * (c == 0 ? u0 : (c == 1 ? u1 : u2));
+    } else {
+      t = fmaf(g.K[c * 3 + 0], u0, fmaf(g.K[c * 3 + 1], u1, g.K[c * 3 + 2] * u2));
+    }
+    t = fminf(fmaxf(t, -1048576.0f), 1048576.0f);
+    int fi;
+    float fr;
+    floor_split(t, fi, fr);
+    b[c] = idx[c] + g.io[c] + fi;
     r[c] = fr;
   }
 }

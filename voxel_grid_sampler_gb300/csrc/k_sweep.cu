@@ -471,7 +471,9 @@ struct Half {
 // LU streams the 3-vector slot (u, or the stored dJ/dq when GATHER is off);
 // GATHER walks the fixed-point coordinates and gathers the taps; without it
 // the slot's vector is kept in H.rr and only the voxel indices are walked.
-template <typename FT, typename MT, bool LF, bool LU, bool LX, bool GATHER, class WR, int NST>
+// IA: every anchor is an integer (Geom::ia), so the walk keeps voxel indices
+// only and the cell comes from cell_of_int (the same cells and fractions).
+template <typename FT, typename MT, bool LF, bool LU, bool LX, bool GATHER, bool IA, class WR, int NST>
 __device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __restrict__ M, const FT* __restrict__ F,
                                         const float* u, const float* X, WR& wr, RingSched<WR, NST>& rs,
                                         LaneWalk& w, unsigned it, unsigned k, int h, unsigned long long pol) {
@@ -518,13 +520,24 @@ __device__ __forceinline__ void prepare(Half& H, const Geom& g, const MT* __rest
     for (int j = 0; j < 2; ++j) {
       const int v = 2 * h + j;
       int b[3];
-      if (v < nvc) {
-        if (v == 0)
-          lw_seek(g, lin0, w);
-        else
-          lw_step(g, lin0 + 32u * v, w);
+      if constexpr (IA) {
+        // integer anchors: the walk needs only the voxel indices
+        if (v < nvc) {
+          if (v > 0 && w.x + 32 < g.fW)
+            w.x += 32;
+          else
+            lin_to_xyz(g, lin0 + 32u * v, w.x, w.y, w.z);
+        }
+        cell_of_int(g, w.x, w.y, w.z, uu[j][0], uu[j][1], uu[j][2], b, H.rr[j]);
+      } else {
+        if (v < nvc) {
+          if (v == 0)
+            lw_seek(g, lin0, w);
+          else
+            lw_step(g, lin0 + 32u * v, w);
+        }
+        cell_of(g, w.P, uu[j][0], uu[j][1], uu[j][2], b, H.rr[j]);
       }
-      cell_of(g, w.P, uu[j][0], uu[j][1], uu[j][2], b, H.rr[j]);
       H.ix[j] = w.x;
       H.iy[j] = w.y;
       H.iz[j] = w.z;
@@ -651,7 +664,7 @@ __device__ __forceinline__ void sweep1_half(const Half& H, unsigned* hist, const
   }
 }
 
-template <typename FT, typename MT, int BMAX, int MODE>
+template <typename FT, typename MT, int BMAX, int MODE, bool IA>
 __global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a) {
   using C = S1Cfg<FT, BMAX, MODE>;
   constexpr bool HIST = C::HIST;
@@ -682,12 +695,12 @@ __global__ void __launch_bounds__(kSweep1Threads, 1) k_sweep1(const Sweep1Args a
   LaneWalk w;
   Half A, B;
   unsigned k = 0;
-  prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE, IA>(A, g, M, F, a.u, X, wr, rs, w, blockIdx.x, 0, 0, pol);
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
-    prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
+    prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE, IA>(B, g, M, F, a.u, X, wr, rs, w, it, k, 1, pol);
     sweep1_half<MT, BMAX, HIST, WRITEJ, WRITEG>(A, hist_sm, hl, a, SAMPLE);
-    prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+    prepare<FT, MT, HIST, SAMPLE, !SAMPLE, SAMPLE, IA>(A, g, M, F, a.u, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
     sweep1_half<MT, BMAX, HIST, WRITEJ, WRITEG>(B, hist_sm, hl, a, SAMPLE);
     if (HIST && ++pending == flush_every<BMAX, kSweep1Threads>()) {
       hist_flush<BMAX, kSweep1Threads>(hist_sm, a.ghist, a.B);
@@ -896,7 +909,7 @@ __device__ __forceinline__ void sweep2_half(const Half& H, const float* tsm, con
   }
 }
 
-template <typename FT, typename MT, int BMAX, int MODE>
+template <typename FT, typename MT, int BMAX, int MODE, bool IA>
 __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2Args a) {
   using C = S2Cfg<FT, BMAX, MODE>;
   constexpr bool MI = C::MI, GATHER = C::GATHER, VEC = C::VEC, BWD = C::BWD, XS = C::XS, MSE = C::MSE;
@@ -934,14 +947,14 @@ __global__ void __launch_bounds__(sweep2_threads(MODE), 1) k_sweep2(const Sweep2
   LaneWalk w;
   Half A, B;
   unsigned k = 0;
-  if constexpr (GATHER) prepare<FT, MT, LF, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
+  if constexpr (GATHER) prepare<FT, MT, LF, VEC, XS, GATHER, IA>(A, g, M, F, U, X, wr, rs, w, blockIdx.x, 0, 0, pol);
   int pending = 0;
   for (unsigned it = blockIdx.x; it < a.nIter; it += gridDim.x, ++k) {
     if constexpr (GATHER) {
       // gathers of the next half are in flight while the current one computes
-      prepare<FT, MT, LF, VEC, XS, GATHER>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
+      prepare<FT, MT, LF, VEC, XS, GATHER, IA>(B, g, M, F, U, X, wr, rs, w, it, k, 1, pol);
       sweep2_half<MT, BMAX, MI, GATHER, BWD, MSE>(A, tsm, a, acc);
-      prepare<FT, MT, LF, VEC, XS, GATHER>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
+      prepare<FT, MT, LF, VEC, XS, GATHER, IA>(A, g, M, F, U, X, wr, rs, w, it + gridDim.x, k + 1, 0, pol);
       sweep2_half<MT, BMAX, MI, GATHER, BWD, MSE>(B, tsm, a, acc);
     } else {
       prepare_chunk<FT, MI, VEC, XS>(A, B, g, F, U, X, wr, rs, it, k, pol);
@@ -1040,7 +1053,8 @@ cudaError_t launch_zero_u64(unsigned long long* p, int n, cudaStream_t s) {
 
 template <typename FT, typename MT, int BMAX, int MODE>
 static cudaError_t run_sweep1(const Sweep1Args& a, int grid, cudaStream_t s, int* occ) {
-  auto k = k_sweep1<FT, MT, BMAX, MODE>;
+  constexpr bool SAMPLE = S1Cfg<FT, BMAX, MODE>::SAMPLE;
+  auto k = (SAMPLE && a.g.ia) ? k_sweep1<FT, MT, BMAX, MODE, SAMPLE> : k_sweep1<FT, MT, BMAX, MODE, false>;
   const size_t smem = S1Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -1093,7 +1107,8 @@ int sweep1_ctas_per_sm(int mode, int ft, int mt, int bmax) {
 
 template <typename FT, typename MT, int BMAX, int MODE>
 static cudaError_t run_sweep2(const Sweep2Args& a, int grid, cudaStream_t s, int* occ) {
-  auto k = k_sweep2<FT, MT, BMAX, MODE>;
+  constexpr bool GATHER = S2Cfg<FT, BMAX, MODE>::GATHER;
+  auto k = (GATHER && a.g.ia) ? k_sweep2<FT, MT, BMAX, MODE, GATHER> : k_sweep2<FT, MT, BMAX, MODE, false>;
   const size_t smem = S2Cfg<FT, BMAX, MODE>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
