@@ -125,6 +125,19 @@ __device__ __forceinline__ void stage_slope(float* slot, const float* src, const
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
+// Streamed (J, F) reads of the staged halo positions: read once per CTA, so
+// they bypass L1 (no allocation) and leave it to the MI table cells.
+__device__ __forceinline__ float ld_stream(const float* p) {
+  float v;
+  asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_stream(const __half* p) {
+  unsigned short v;
+  asm("ld.global.nc.L1::no_allocate.b16 %0, [%1];" : "=h"(v) : "l"(p));
+  return __half2float(__ushort_as_half(v));
+}
+
 // all but the most recent group of this thread's copies have landed
 __device__ __forceinline__ void slope_wait_prev() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 
@@ -810,8 +823,6 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   // from M and u like the sweeps do
   auto sample = [&](int x, int y, int z, size_t lin, float* dq, auto grad) -> float {
     constexpr bool GRAD = decltype(grad)::value;
-    long long P[3];
-    anchor(g, x, y, z, P);
     float u0 = 0.0f, u1 = 0.0f, u2 = 0.0f;
     if (a.u) {
       u0 = __ldg(a.u + 3 * lin);
@@ -820,7 +831,13 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
     }
     int b[3];
     float r[3], m[8];
-    cell_of(g, P, u0, u1, u2, b, r);
+    if (g.ia) {
+      cell_of_int(g, x, y, z, u0, u1, u2, b, r);
+    } else {
+      long long P[3];
+      anchor(g, x, y, z, P);
+      cell_of(g, P, u0, u1, u2, b, r);
+    }
     gather8<FT>(Mp, g, b, m);
 #pragma unroll
     for (int q = 0; q < 8; ++q) m[q] = tap_value<FT>(m[q]);
@@ -845,9 +862,9 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
           const int y = (int)fast_div((unsigned)soff[i], g.divW_m, g.divW_s);
           v.x = sample(soff[i] - y * g.fW, y, zp, base + soff[i], nullptr, std::false_type{});
         } else {
-          v.x = __ldg(a.J + base + soff[i]);
+          v.x = ld_stream(a.J + base + soff[i]);
         }
-        v.y = load1(F + base + soff[i]);
+        v.y = ld_stream(F + base + soff[i]);
       }
       nxt[i] = v;
     }
