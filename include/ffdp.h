@@ -41,7 +41,7 @@
  *   on the device.
  *
  *   Limits: each dimension in [2, 2^20]; D*H*W < 2^32 voxels; bins in [8, 64];
- *   LNCC window odd in [3, 9]; channels of a sampled volume in [1, 4]; a
+ *   LNCC window odd and >= 3; channels of a sampled volume in [1, 4]; a
  *   moving or sampled volume below 2^31 voxels.
  */
 #ifndef FFDP_H
@@ -87,8 +87,11 @@ typedef struct {
   float f_lo, f_hi, m_lo, m_hi;
 } ffdp_mi_params;
 
-/* LNCC: odd window in [3, 9]; cc = cross^2 / (varF varJ + eps) with
- * zero-padded window sums and divisor window^3. */
+/* LNCC: odd window >= 3; cc = cross^2 / (varF varJ + eps) with zero-padded
+ * window sums and divisor window^3.  Windows up to 9 run in tiled kernels that
+ * keep every window sum on chip; wider ones run as separable box sums, one
+ * pass per axis, through two [5][N] float buffers of the workspace (40 bytes
+ * per voxel more).  A window wider than the grid sums what lies inside it. */
 typedef struct {
   int window;
   float eps;
@@ -128,8 +131,10 @@ enum {
  * sums read their halo instead of re-sampling it and the sampler backward,
  * done in the window kernel's epilogue, reads the slope instead of gathering
  * M again; the paper's fused LNCC keeps five such intermediates.  An MI-only
- * objective with store_slope = 1 holds the same two buffers.  Queries the
- * current device's SM count. */
+ * objective with store_slope = 1 holds the same two buffers.  An LNCC window
+ * above 9 (the LNCC op or an objective with LNCC) adds 40 bytes per voxel
+ * for the separable window-sum passes.  Queries the current device's SM
+ * count. */
 size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void *params);
 
 /* Design 1, forward: J[i] = M(A x_i + t + S u_i) for every fixed voxel i.

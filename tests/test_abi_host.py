@@ -89,9 +89,10 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     mp = ffdp.mi_params(32, (0, 1), (2, 1))
     st = lib.ffdp_mi_fwd_bwd(fake, 0, fake, good, ctypes.byref(mp), fake, fake, ws, 1 << 30, None)
     assert st == 1
-    lp = ffdp.lncc_params(11)
-    st = lib.ffdp_lncc_fwd_bwd(fake, 0, fake, good, ctypes.byref(lp), fake, fake, ws, 1 << 30, None)
-    assert st == 1
+    for w in (10, 1, -3):  # even, below 3
+        lp = ffdp.lncc_params(w)
+        st = lib.ffdp_lncc_fwd_bwd(fake, 0, fake, good, ctypes.byref(lp), fake, fake, ws, 1 << 30, None)
+        assert st == 1
     assert lib.ffdp_launch_count() == n0
     assert len(lib.ffdp_last_error()) > 0
 
@@ -110,6 +111,23 @@ def test_workspace_is_o1_for_mi_and_sampler(lib):
     c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (64, 64, 64), q)
     assert c >= 4 * 64 ** 3
     assert ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (1, 64, 64), q) == 0
+
+
+def test_wide_lncc_windows_take_two_five_channel_buffers(lib):
+    # windows above 9 run as separable box-sum passes through two [5][N]
+    # float buffers (40 bytes per voxel); any odd window >= 3 is accepted
+    from voxel_grid_sampler_gb300 import ffdp
+    dims = (20, 30, 40)
+    N = 20 * 30 * 40
+    tiled = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(9))
+    for w in (11, 13, 61, 1001):
+        wide = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(w))
+        assert wide - tiled >= 40 * N and wide - tiled < 40 * N + 1024
+    q9 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 9)
+    q11 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 11)
+    o9 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q9)
+    o11 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q11)
+    assert o11 - o9 >= 40 * N and o11 - o9 < 40 * N + 1024
 
 
 @nogpu

@@ -110,7 +110,10 @@ def test_mi_is_deterministic_and_order_free(ffdp):
 
 
 # --------------------------------------------------------------------- LNCC
-LNCC_CASES = [((20, 37, 70), 5), ((9, 16, 32), 3), ((13, 17, 45), 7), ((11, 12, 40), 9), ((70, 17, 6), 5)]
+LNCC_CASES = [((20, 37, 70), 5), ((9, 16, 32), 3), ((13, 17, 45), 7), ((11, 12, 40), 9), ((70, 17, 6), 5),
+              # windows above 9: the separable wide-window passes; 13 and 21
+              # are wider than some axes (clipped sums, divisor still w^3)
+              ((20, 37, 70), 11), ((9, 16, 32), 13), ((13, 17, 45), 21)]
 
 
 @pytest.mark.parametrize("shape,w", LNCC_CASES)
@@ -147,6 +150,10 @@ OBJ_CASES = [
     ((19, 37, 100), (19, 37, 100), np.float32, 1.0, 1.0, 64, 5),
     ((12, 16, 64), (12, 16, 64), np.float32, 0.5, 1.0, 32, 9),
     ((10, 48, 96), (10, 48, 96), np.float16, 0.0, 1.0, 32, 3),
+    # windows above 9 (wide-window passes), with and without the MI term
+    ((16, 18, 40), (16, 18, 40), np.float32, 1.0, 1.0, 64, 11),
+    ((15, 17, 33), (15, 17, 33), np.float16, 1.0, 0.5, 32, 13),
+    ((12, 16, 64), (12, 16, 64), np.float32, 0.0, 1.0, 32, 11),
 ]
 
 

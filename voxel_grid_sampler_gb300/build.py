@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libffdp.so")
-SOURCES = ["ffdp_api.cu", "k_sweep.cu", "k_lncc.cu", "k_channels.cu", "k_reg.cu"]
+SOURCES = ["ffdp_api.cu", "k_sweep.cu", "k_lncc.cu", "k_lncc_wide.cu", "k_channels.cu", "k_reg.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

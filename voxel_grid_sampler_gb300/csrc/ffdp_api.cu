@@ -6,6 +6,7 @@
 // Registration", Key designs items 1 (fused_grid_sampler(I; A, t, [u], S,
 // x_bounds)) and 2 (implicit-Parzen MI, fused LNCC); "Background" for the
 // objective L = C(F, M o phi), phi(x) = Ax + t + u(x).
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cmath>
@@ -276,8 +277,7 @@ ffdp_status check_mi(const ffdp_mi_params* p) {
 
 ffdp_status check_lncc(const ffdp_lncc_params* p) {
   if (!p) return fail(FFDP_ERR_INVALID_ARGUMENT, "null LNCC params");
-  if (p->window < 3 || p->window > 9 || (p->window & 1) == 0)
-    return fail(FFDP_ERR_INVALID_ARGUMENT, "window must be odd in [3, 9]");
+  if (p->window < 3 || (p->window & 1) == 0) return fail(FFDP_ERR_INVALID_ARGUMENT, "window must be odd and >= 3");
   if (!std::isfinite(p->eps) || p->eps < 0.0f) return fail(FFDP_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
   return FFDP_OK;
 }
@@ -296,8 +296,20 @@ int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
 
 // Workspace layout (byte offsets, 256-aligned).
 struct Ws {
-  size_t hist, table, table2, scalars, partials, J, DG, total;
+  size_t hist, table, table2, scalars, partials, J, DG, WA, WB, total;
 };
+
+// The LNCC window runs through the wide-window passes (two [5][N] buffers).
+bool lncc_wide(int window) { return window > kLnccTiledMaxWindow; }
+
+// Window radius of the wide-window passes: a radius at or beyond the largest
+// grid extent sums the same (clipped) terms, so it is capped there; the
+// divisor stays the true window^3.
+int wide_radius(int window, const Geom& g) {
+  const int R = (window - 1) / 2;
+  const int e = std::max(g.fW, std::max(g.fH, g.fD));
+  return R < e ? R : e;
+}
 
 size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -306,7 +318,7 @@ size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
 bool lncc_recompute(int window) { return kLnccRecompute && window <= 7; }
 
 // ln: LNCC on; store: J and dJ/dq per voxel.
-Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N) {
+Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N, bool wide = false) {
   const bool needJ = store;
   Ws w;
   size_t o = 0;
@@ -325,6 +337,10 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t 
   if (needJ) o = al(o + (size_t)N * sizeof(float));
   w.DG = o;  // dJ/dq, [N][3]
   if (needJ) o = al(o + (size_t)N * 3 * sizeof(float));
+  w.WA = o;  // wide-window LNCC: window sums, then g-terms, [5][N] each
+  if (wide) o = al(o + (size_t)N * 5 * sizeof(float));
+  w.WB = o;
+  if (wide) o = al(o + (size_t)N * 5 * sizeof(float));
   w.total = o;
   return w;
 }
@@ -400,7 +416,7 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
     case FFDP_OP_LNCC: {
       const ffdp_lncc_params* p = static_cast<const ffdp_lncc_params*>(params);
       if (check_lncc(p) != FFDP_OK) return 0;
-      return ws_layout(false, 32, max_parts(), false, false, N).total;
+      return ws_layout(false, 32, max_parts(), false, false, N, lncc_wide(p->window)).total;
     }
     case FFDP_OP_OBJECTIVE: {
       const ffdp_objective_params* p = static_cast<const ffdp_objective_params*>(params);
@@ -409,7 +425,8 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
       if (mi && check_mi(&p->mi) != FFDP_OK) return 0;
       if (ln && check_lncc(&p->lncc) != FFDP_OK) return 0;
       return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln,
-                       (ln && !lncc_recompute(p->lncc.window)) || (mi && !ln && p->store_slope != 0), N).total;
+                       (ln && !lncc_recompute(p->lncc.window)) || (mi && !ln && p->store_slope != 0), N,
+                       ln && lncc_wide(p->lncc.window)).total;
     }
     case FFDP_OP_SAMPLE_CHANNELS_BWD:
     case FFDP_OP_MSE:
@@ -561,10 +578,36 @@ extern "C" ffdp_status ffdp_lncc_fwd_bwd(const void* F, ffdp_dtype ft, const flo
   FFDP_TRY(check_lncc(p));
   if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
-  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims));
+  const bool wide = lncc_wide(p->window);
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims), wide);
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (wide) {
+    WideArgs a{};
+    make_grid_only(dims, a.g);
+    a.F = F;
+    a.J = J;
+    a.dJ = dJ;
+    a.partials = reinterpret_cast<double*>(wb + w.partials);
+    a.bufA = reinterpret_cast<float*>(wb + w.WA);
+    a.bufB = reinterpret_cast<float*>(wb + w.WB);
+    a.R = wide_radius(p->window, a.g);
+    a.eps = p->eps;
+    a.inv_n = (float)(1.0 / ((double)p->window * p->window * p->window));
+    a.gscale = (float)(-1.0 / (double)a.g.N);
+    const int grid = persistent_grid((unsigned)((a.g.N + 255) / 256), kWideCtasPerSm);
+    FFDP_CUDA(launch_lncc_wide(LN_DJ, ft, 0, a, grid, s), "wide-window LNCC launch");
+    FinishArgs f{};
+    f.partials = a.partials;
+    f.nparts = grid;
+    f.loss = loss;
+    f.nloss = 1;
+    f.has_lncc = 1;
+    f.N = (double)a.g.N;
+    FFDP_CUDA(launch_finish(f, s), "finish launch");
+    return FFDP_OK;
+  }
   LnccArgs a{};
   make_grid_only(dims, a.g);
   a.F = F;
@@ -613,7 +656,8 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   const uint64_t N = nvox(fdims);
   const bool rc = ln && lncc_recompute(p->lncc.window);  // LNCC samples J on chip
   const bool store = (ln && !rc) || (mi && !ln && p->store_slope != 0);
-  const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N);
+  const bool wide = ln && lncc_wide(p->lncc.window);
+  const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N, wide);
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -663,7 +707,29 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
     FFDP_CUDA(launch_finalize(bmax, fa, s), "MI finalize launch");
   }
   int nparts = 0;
-  if (ln) {
+  if (wide) {
+    // wide window: separable box-sum passes, then g = dL/dJ (LNCC + MI term)
+    // and the sampler backward from the stored slope
+    WideArgs a{};
+    a.g = g;
+    a.F = F;
+    a.J = Jbuf;
+    a.dJdq = DGbuf;
+    a.du = du;
+    a.T = bmax == 64 ? table2 : table;
+    a.partials = partials;
+    a.bufA = reinterpret_cast<float*>(wb + w.WA);
+    a.bufB = reinterpret_cast<float*>(wb + w.WB);
+    a.bf = bf;
+    a.bj = bj;
+    a.R = wide_radius(p->lncc.window, g);
+    a.eps = p->lncc.eps;
+    a.inv_n = (float)(1.0 / ((double)p->lncc.window * p->lncc.window * p->lncc.window));
+    a.gscale = (float)(-(double)p->w_lncc / (double)N);
+    const int grid = persistent_grid((unsigned)((N + 255) / 256), kWideCtasPerSm);
+    FFDP_CUDA(launch_lncc_wide(LN_DU, ft, mi ? bmax : 0, a, grid, s), "wide-window LNCC launch");
+    nparts = grid;
+  } else if (ln) {
     // LNCC window kernel: g = dL/dJ (LNCC term + MI term from on-chip J, F),
     // then the sampler backward from the stored slope (du, affine partials)
     LnccArgs a{};

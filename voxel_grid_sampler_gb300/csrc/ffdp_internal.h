@@ -118,6 +118,27 @@ struct LnccArgs {
   long long per;       // (column, plane) pairs per CTA
 };
 
+// LNCC for windows above kLnccTiledMaxWindow: separable box sums through two
+// [5][N] float buffers of the workspace (k_lncc_wide.cu).
+constexpr int kLnccTiledMaxWindow = 9;
+struct WideArgs {
+  const void* F;
+  const float* J;
+  const float* dJdq;  // LN_DU: [N][3] stored slope of J
+  float* du;          // LN_DU: [N][3] or NULL (affine partials only)
+  float* dJ;          // LN_DJ: [N] dL/dJ or NULL
+  const float* T;     // MI polynomial cells (B > 0)
+  double* partials;   // [grid][kPartialStride]: kPCC from the cc pass, the affine slots from the last pass
+  float* bufA;        // [5][N]
+  float* bufB;        // [5][N]
+  Geom g;             // fixed-grid extents always valid; K and ctr for LN_DU
+  BinMap bf, bj;
+  int R;              // window radius
+  float eps;
+  float inv_n;        // 1 / window^3
+  float gscale;       // -w_lncc / N
+};
+
 // Reduction of per-CTA partials into dA, dt and the loss values.
 struct FinishArgs {
   const double* partials;
@@ -165,6 +186,8 @@ cudaError_t launch_sweep1(int mode, int ft, int mt, int bmax, const Sweep1Args& 
 cudaError_t launch_sweep2(int mode, int ft, int mt, int bmax, const Sweep2Args& a, int grid, cudaStream_t s);
 cudaError_t launch_finalize(int bmax, const FinalizeArgs& a, cudaStream_t s);
 cudaError_t launch_lncc(int mode, int ft, int mt, int bmax_or0, const LnccArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_lncc_wide(int mode, int ft, int bmax_or0, const WideArgs& a, int grid, cudaStream_t s);
+constexpr int kWideCtasPerSm = 8;  // resident 256-thread CTAs per SM of the wide-window passes
 cudaError_t launch_finish(const FinishArgs& a, cudaStream_t s);
 cudaError_t launch_chan_fwd(int C, int compose, const ChanArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_chan_bwd(int C, int compose, const ChanArgs& a, int grid, cudaStream_t s);

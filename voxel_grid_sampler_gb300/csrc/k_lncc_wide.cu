@@ -1,0 +1,291 @@
+// k_lncc_wide.cu -- LNCC for windows wider than the tiled kernels keep on chip
+// (w > kLnccTiledMaxWindow).
+//
+// Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
+// Registration", Key designs item 2 (LNCC from the window sums of I, J, I^2,
+// J^2, IJ, and its gradient through the same window sums).  The definitions
+// are those of the tiled kernels (zero padding, window w = 2R + 1, n = w^3):
+//   cross = S_FJ - S_F S_J / n,  vF = S_FF - S_F^2 / n,  vJ = S_JJ - S_J^2 / n
+//   (variances clamped at 0), cc = cross^2 / (vF vJ + eps),
+//   D = vF vJ + eps, A1 = 2 cross / D, A2 = cross^2 vF / D^2, s = -w_lncc / N:
+//   g_FJ = s A1,  g_JJ = -s A2,  g_J = s (2 A2 S_J - A1 S_F) / n,
+//   dJ_m = sum_{k in window(m)} g_J(k) + 2 J_m g_JJ(k) + F_m g_FJ(k).
+//
+// A window of w^3 voxels with a 2R halo around a 32-wide tile no longer fits
+// the register history or the plane ring of the tiled kernels, so the window
+// sums run as separable box sums, one grid-stride pass per axis, through two
+// [5][N] float buffers A and B of the workspace:
+//   1. x sums of J, F, J^2, F^2, FJ                     J, F -> A[0..4]
+//   2. y sums                                           A    -> B[0..4]
+//   3. z sums, cc (per-CTA partials), g_J, g_JJ, g_FJ    B    -> A[0..2]
+//   4. x sums of the three g-terms                      A    -> B[0..2]
+//   5. y sums                                           B    -> A[0..2]
+//   6. z sums, dJ (+ the MI term from the polynomial cells), then dJ stored
+//      or the sampler backward from the stored slope: du = K^T (g dJ/dq) and
+//      the affine moments, per-CTA fp64 partials.
+// Each window sum adds the terms inside the grid directly (no running sums:
+// no drift over long axes), min(w, extent) loads per channel and output.  A
+// warp's lanes hold 32 consecutive x, so every load is coalesced and the
+// w-fold reuse of an input is served by L1 / L2.
+#include "ffdp_internal.h"
+#include "ffdp_lncc.cuh"
+
+namespace ffdp {
+
+constexpr int kWideThreads = 256;
+
+// Window range [lo, hi] along AXIS (0 = x, 1 = y, 2 = z) of voxel lin, clipped
+// to the grid, and the element stride of that axis.
+template <int AXIS>
+__device__ __forceinline__ void axis_window(const Geom& g, unsigned lin, int R, int& lo, int& hi, long long& st) {
+  int ix, iy, iz;
+  lin_to_xyz(g, lin, ix, iy, iz);
+  const int c = AXIS == 0 ? ix : (AXIS == 1 ? iy : iz);
+  const int n = AXIS == 0 ? g.fW : (AXIS == 1 ? g.fH : g.fD);
+  lo = c - R < 0 ? -c : -R;
+  hi = c + R > n - 1 ? n - 1 - c : R;
+  st = AXIS == 0 ? 1ll : (AXIS == 1 ? (long long)g.fW : (long long)g.fW * g.fH);
+}
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// pass 1: x sums of the five products of (J, F)
+template <typename FT>
+__global__ void __launch_bounds__(kWideThreads) k_wide_prod_x(const WideArgs a) {
+  const Geom& g = a.g;
+  const size_t N = g.N;
+  const FT* __restrict__ F = static_cast<const FT*>(a.F);
+  for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
+    int lo, hi;
+    long long st;
+    axis_window<0>(g, (unsigned)lin, a.R, lo, hi, st);
+    float sJ = 0.f, sF = 0.f, sJJ = 0.f, sFF = 0.f, sFJ = 0.f;
+    for (int k = lo; k <= hi; ++k) {
+      const float j = __ldg(a.J + lin + k), f = load1(F + lin + k);
+      sJ += j;
+      sF += f;
+      sJJ = fmaf(j, j, sJJ);
+      sFF = fmaf(f, f, sFF);
+      sFJ = fmaf(f, j, sFJ);
+    }
+    a.bufA[lin] = sJ;
+    a.bufA[N + lin] = sF;
+    a.bufA[2 * N + lin] = sJJ;
+    a.bufA[3 * N + lin] = sFF;
+    a.bufA[4 * N + lin] = sFJ;
+  }
+}
+
+// passes 2, 4, 5: window sums of C channels ([C][N]) along AXIS
+template <int C, int AXIS>
+__global__ void __launch_bounds__(kWideThreads) k_wide_box(const float* __restrict__ in, float* __restrict__ out,
+                                                           const Geom g, int R) {
+  const size_t N = g.N;
+  for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
+    int lo, hi;
+    long long st;
+    axis_window<AXIS>(g, (unsigned)lin, R, lo, hi, st);
+    float s[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) s[c] = 0.f;
+    const float* p = in + lin + (long long)lo * st;
+    for (int k = lo; k <= hi; ++k, p += st) {
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[c] += __ldg(p + c * N);
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) out[c * N + lin] = s[c];
+  }
+}
+
+// pass 3: z sums of the five channels, cc and the three g-terms
+__global__ void __launch_bounds__(kWideThreads) k_wide_cc(const WideArgs a) {
+  __shared__ double red[kWideThreads / 32];
+  const Geom& g = a.g;
+  const size_t N = g.N;
+  const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
+  double cc_d = 0.0;
+  float cc_f = 0.0f;
+  int cnt = 0;
+  for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
+    int lo, hi;
+    long long st;
+    axis_window<2>(g, (unsigned)lin, a.R, lo, hi, st);
+    float s[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    const float* p = a.bufB + lin + (long long)lo * st;
+    for (int k = lo; k <= hi; ++k, p += st) {
+#pragma unroll
+      for (int c = 0; c < 5; ++c) s[c] += __ldg(p + c * N);
+    }
+    const float SJ = s[0], SF = s[1];
+    const float vJ = fmaxf(fmaf(SJ * SJ, -inv_n, s[2]), 0.0f);
+    const float vF = fmaxf(fmaf(SF * SF, -inv_n, s[3]), 0.0f);
+    const float cross = fmaf(-SJ * SF, inv_n, s[4]);
+    const float rD = rcp_approx(fmaf(vJ, vF, eps));
+    const float A1 = 2.0f * cross * rD;
+    const float cc = cross * cross * rD;
+    const float A2 = cc * vF * rD;
+    a.bufA[lin] = gs * (2.0f * A2 * SJ - A1 * SF) * inv_n;
+    a.bufA[N + lin] = -gs * A2;
+    a.bufA[2 * N + lin] = gs * A1;
+    cc_f += cc;
+    if (++cnt == 64) {
+      cc_d += (double)cc_f;
+      cc_f = 0.0f;
+      cnt = 0;
+    }
+  }
+  cc_d = warp_sum_d(cc_d + (double)cc_f);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cc_d;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < kWideThreads / 32; ++w) t += red[w];
+    a.partials[(size_t)blockIdx.x * kPartialStride + kPCC] = t;
+  }
+}
+
+// pass 6: z sums of the g-terms, dJ, and dJ or the sampler backward
+template <typename FT, int BMAX, bool DU>
+__global__ void __launch_bounds__(kWideThreads) k_wide_fin(const WideArgs a) {
+  constexpr bool MI = BMAX != 0;
+  __shared__ double red[kWideThreads / 32][12];
+  const Geom& g = a.g;
+  const size_t N = g.N;
+  const FT* __restrict__ F = static_cast<const FT*>(a.F);
+  // affine moments: e_r and e_r (i_c - ctr_c), fp32 runs folded into fp64
+  float S[3] = {0.f, 0.f, 0.f}, Mo[3][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
+  double Sd[3] = {0.0, 0.0, 0.0}, Md[3][3] = {{0.0, 0.0, 0.0}, {0.0, 0.0, 0.0}, {0.0, 0.0, 0.0}};
+  int cnt = 0;
+  auto fold = [&] {
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      Sd[r] += (double)S[r];
+      S[r] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        Md[r][c] += (double)Mo[r][c];
+        Mo[r][c] = 0.f;
+      }
+    }
+  };
+  for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
+    int ix, iy, iz;
+    lin_to_xyz(g, (unsigned)lin, ix, iy, iz);
+    const int lo = iz - a.R < 0 ? -iz : -a.R;
+    const int hi = iz + a.R > g.fD - 1 ? g.fD - 1 - iz : a.R;
+    const long long st = (long long)g.fW * g.fH;
+    float GJ = 0.f, GJJ = 0.f, GFJ = 0.f;
+    const float* p = a.bufA + lin + (long long)lo * st;
+    for (int k = lo; k <= hi; ++k, p += st) {
+      GJ += __ldg(p);
+      GJJ += __ldg(p + N);
+      GFJ += __ldg(p + 2 * N);
+    }
+    const float jv = __ldg(a.J + lin), fv = load1(F + lin);
+    float gv = fmaf(fv, GFJ, fmaf(2.0f * jv, GJJ, GJ));
+    if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
+    if constexpr (!DU) {
+      if (a.dJ) a.dJ[lin] = gv;
+    } else {
+      const float e[3] = {gv * __ldg(a.dJdq + 3 * lin), gv * __ldg(a.dJdq + 3 * lin + 1),
+                          gv * __ldg(a.dJdq + 3 * lin + 2)};
+      if (a.du) {
+        const float* K = g.K;
+        float* d = a.du + 3 * lin;
+        if (g.k_diag) {
+          d[0] = K[0] * e[0];
+          d[1] = K[4] * e[1];
+          d[2] = K[8] * e[2];
+        } else {
+          d[0] = fmaf(K[0], e[0], fmaf(K[3], e[1], K[6] * e[2]));
+          d[1] = fmaf(K[1], e[0], fmaf(K[4], e[1], K[7] * e[2]));
+          d[2] = fmaf(K[2], e[0], fmaf(K[5], e[1], K[8] * e[2]));
+        }
+      }
+      const float cx[3] = {(float)ix - g.ctr[0], (float)iy - g.ctr[1], (float)iz - g.ctr[2]};
+#pragma unroll
+      for (int r = 0; r < 3; ++r) {
+        S[r] += e[r];
+#pragma unroll
+        for (int c = 0; c < 3; ++c) Mo[r][c] = fmaf(e[r], cx[c], Mo[r][c]);
+      }
+      if (++cnt == 32) {
+        fold();
+        cnt = 0;
+      }
+    }
+  }
+  if constexpr (DU) {
+    fold();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      const double s = warp_sum_d(Sd[r]);
+      if (lane == 0) red[wid][kPS + r] = s;
+#pragma unroll
+      for (int c = 0; c < 3; ++c) {
+        const double m = warp_sum_d(Md[r][c]);
+        if (lane == 0) red[wid][kPM + 3 * r + c] = m;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 12) {
+      double t = 0.0;
+      for (int w = 0; w < kWideThreads / 32; ++w) t += red[w][threadIdx.x];
+      a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = t;
+    }
+  }
+}
+
+namespace {
+
+template <typename FT, int BMAX, bool DU>
+cudaError_t run_wide(const WideArgs& a, int grid, cudaStream_t s) {
+  const Geom& g = a.g;
+  note_launch_begin("k_wide_prod_x", s);
+  k_wide_prod_x<FT><<<grid, kWideThreads, 0, s>>>(a);
+  note_launch_end(s);
+  note_launch_begin("k_wide_box", s);
+  k_wide_box<5, 1><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
+  note_launch_end(s);
+  note_launch_begin("k_wide_cc", s);
+  k_wide_cc<<<grid, kWideThreads, 0, s>>>(a);
+  note_launch_end(s);
+  note_launch_begin("k_wide_box", s);
+  k_wide_box<3, 0><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
+  note_launch_end(s);
+  note_launch_begin("k_wide_box", s);
+  k_wide_box<3, 1><<<grid, kWideThreads, 0, s>>>(a.bufB, a.bufA, g, a.R);
+  note_launch_end(s);
+  note_launch_begin("k_wide_fin", s);
+  k_wide_fin<FT, BMAX, DU><<<grid, kWideThreads, 0, s>>>(a);
+  note_launch_end(s);
+  return cudaGetLastError();
+}
+
+template <typename FT, int BMAX>
+cudaError_t run_wide_mode(int mode, const WideArgs& a, int grid, cudaStream_t s) {
+  return mode == LN_DU ? run_wide<FT, BMAX, true>(a, grid, s) : run_wide<FT, BMAX, false>(a, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_lncc_wide(int mode, int ft, int bmax, const WideArgs& a, int grid, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  FFDP_DT_SWITCH(ft, FT, {
+    if (bmax == 0)
+      e = run_wide_mode<FT, 0>(mode, a, grid, s);
+    else if (bmax == 32)
+      e = run_wide_mode<FT, 32>(mode, a, grid, s);
+    else
+      e = run_wide_mode<FT, 64>(mode, a, grid, s);
+  });
+  return e;
+}
+
+}  // namespace ffdp
