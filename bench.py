@@ -310,9 +310,9 @@ def run_gpu(args, ws, rank, local):
     F, M, u = pair.F, pair.M, pair.u
     N = F.numel()
     T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
-    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
-                              store_slope=bool(args.store_slope))
-    wsbuf = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P, dev)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    stored = bool(args.store_slope)  # ffdp_objective_stored (MI only: J and slope kept) or ffdp_objective
+    wsbuf = ffdp.workspace(_ws_op(stored), F.shape, P, dev)
     loss = torch.empty(3, device=dev)
     du = torch.empty(tuple(F.shape) + (3,), device=dev)
     dA = torch.empty(9, device=dev)
@@ -320,7 +320,7 @@ def run_gpu(args, ws, rank, local):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, wsbuf, stream)
+        ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, store_slope=stored)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -336,12 +336,10 @@ def run_gpu(args, ws, rank, local):
     # the other MI mode of an MI-only objective, timed the same way for reference
     alt = None
     if wl.w_lncc == 0.0:
-        P2 = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
-                                   store_slope=not args.store_slope)
-        ws2 = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P2, dev)
+        ws2 = ffdp.workspace(_ws_op(not stored), F.shape, P, dev)
 
         def step2():
-            ffdp.ffdp_objective(F, M, u, T, P2, loss, du, dA, dt, ws2, stream)
+            ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, ws2, stream, store_slope=not stored)
         for _ in range(3):
             step2()
         torch.cuda.synchronize(dev)
@@ -356,7 +354,7 @@ def run_gpu(args, ws, rank, local):
     if args.no_e2e:
         ms_e2e, h2d, d2h = float("nan"), 0, 0
     else:
-        ms_e2e, h2d, d2h = _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws)
+        ms_e2e, h2d, d2h = _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws, stored)
     out = _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h, alt)
     # ---- the gigavoxel workload, timed the same way, on the same line
     if out is not None and args.workload == 4 and not args.shape and not args.no_workload5 and ws == 1:
@@ -382,16 +380,15 @@ def _workload5(args, dev, stream):
     F, M, u = pair.F, pair.M, pair.u
     N = F.numel()
     T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
-    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
-                              store_slope=True)
-    wsbuf = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE, F.shape, P, dev)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    wsbuf = ffdp.workspace(ffdp.FFDP_OP_OBJECTIVE_STORED, F.shape, P, dev)
     loss = torch.empty(3, device=dev)
     du = torch.empty(tuple(F.shape) + (3,), device=dev)
     dA = torch.empty(9, device=dev)
     dt = torch.empty(3, device=dev)
 
     def step():
-        ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, wsbuf, stream)
+        ffdp.ffdp_objective(F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, store_slope=True)
 
     for _ in range(3):
         step()
@@ -416,7 +413,12 @@ def _workload5(args, dev, stream):
     return res
 
 
-def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
+def _ws_op(stored):
+    from voxel_grid_sampler_gb300 import ffdp
+    return ffdp.FFDP_OP_OBJECTIVE_STORED if stored else ffdp.FFDP_OP_OBJECTIVE
+
+
+def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws, stored):
     """End to end through ffdp_objective with host buffers: every step copies F,
     M and u in from pinned host memory and du, the losses, dA and dt out.
     Double-buffered on three streams (copy in / compute / copy out, ordered
@@ -451,7 +453,8 @@ def _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws):
         comp.wait_event(b["ev_in"])
         if b["used"]:
             comp.wait_event(b["ev_out"])  # this set's previous results are copied out
-        ffdp.ffdp_objective(b["F"], b["M"], b["u"], T, P, b["loss"], b["du"], b["dA"], b["dt"], wsbuf, comp)
+        ffdp.ffdp_objective(b["F"], b["M"], b["u"], T, P, b["loss"], b["du"], b["dA"], b["dt"], wsbuf, comp,
+                            store_slope=stored)
         with torch.cuda.stream(comp):
             b["small"][0:3].copy_(b["loss"])
             b["small"][3:12].copy_(b["dA"])

@@ -98,18 +98,11 @@ typedef struct {
 } ffdp_lncc_params;
 
 /* Objective L = w_mi * (-MI) + w_lncc * (-LNCC).  A weight of 0 disables (does
- * not evaluate) that term; at least one weight must be non-zero.
- * store_slope (MI-only objectives): 0 = fully implicit, the workspace does not
- * grow with the volume and the gradient pass samples M again; 1 = the first
- * pass also stores J and its slope dJ/dp in the workspace (16 bytes per
- * voxel) and the gradient pass streams them instead of gathering M (faster
- * where the memory is available).  Objectives with LNCC always store them.
- * The results are the same in both modes up to rounding. */
+ * not evaluate) that term; at least one weight must be non-zero. */
 typedef struct {
   float w_mi, w_lncc;
   ffdp_mi_params mi;
   ffdp_lncc_params lncc;
-  int store_slope;
 } ffdp_objective_params;
 
 /* Operation codes for ffdp_workspace_bytes. */
@@ -121,7 +114,8 @@ enum {
   FFDP_OP_SAMPLE_CHANNELS_BWD = 5, /* params: NULL */
   FFDP_OP_MSE = 6,             /* params: NULL */
   FFDP_OP_OBJECTIVE_MSE = 7,   /* params: NULL */
-  FFDP_OP_SOBOLEV = 8          /* params: NULL (regulariser and Adam step) */
+  FFDP_OP_SOBOLEV = 8,         /* params: NULL (regulariser and Adam step) */
+  FFDP_OP_OBJECTIVE_STORED = 9 /* params: const ffdp_objective_params* (ffdp_objective_stored) */
 };
 
 /* Bytes of device workspace a call of `op` on fixed grid `fixed` needs (0 for
@@ -131,7 +125,7 @@ enum {
  * sums read their halo instead of re-sampling it and the sampler backward,
  * done in the window kernel's epilogue, reads the slope instead of gathering
  * M again; the paper's fused LNCC keeps five such intermediates.  An MI-only
- * objective with store_slope = 1 holds the same two buffers.  An LNCC window
+ * objective through ffdp_objective_stored holds the same two buffers.  An LNCC window
  * above 9 (the LNCC op or an objective with LNCC) adds 40 bytes per voxel
  * for the separable window-sum passes.  Queries the current device's SM
  * count. */
@@ -178,6 +172,21 @@ ffdp_status ffdp_objective(const void *F, ffdp_dtype ft, ffdp_dims fdims, const 
                            const ffdp_transform *T, const ffdp_objective_params *p, float *loss,
                            float *du, float *dA, float *dt, void *ws, size_t ws_bytes,
                            void *stream);
+
+/* ffdp_objective with the warped image kept for an MI-only objective: the
+ * first pass also stores J and its slope dJ/dp in the workspace (16 bytes per
+ * voxel, ffdp_workspace_bytes(FFDP_OP_OBJECTIVE_STORED, fdims, p)) and the
+ * gradient pass streams them instead of gathering M again -- faster where the
+ * memory is available (ffdp_objective keeps an MI-only objective fully
+ * implicit: its workspace does not grow with the volume).  Objectives with
+ * LNCC store J and its slope in either entry point, so for them the two calls
+ * are the same.  Results equal ffdp_objective's up to rounding; arguments,
+ * outputs and errors are as for ffdp_objective. */
+ffdp_status ffdp_objective_stored(const void *F, ffdp_dtype ft, ffdp_dims fdims, const void *M,
+                                  ffdp_dtype mt, ffdp_dims mdims, const float *u,
+                                  const ffdp_transform *T, const ffdp_objective_params *p,
+                                  float *loss, float *du, float *dA, float *dt, void *ws,
+                                  size_t ws_bytes, void *stream);
 
 /* ---- warp composition, image gradient, MSE -----------------------------
  * "Background" of the paper: the similarity C may be MSE, LNCC or MI, and
@@ -277,7 +286,7 @@ ffdp_status ffdp_sobolev_adam_step(const float *u, float *u_out, const float *g,
  * the library image instead: ffdp_static_scratch_bytes() bytes (512 KiB) that
  * every GPU loading the library holds until the process exits.  It never
  * calls an allocator.
- *   - MI only and implicit: p->w_lncc and p->store_slope must be 0 (per-voxel
+ *   - MI only and implicit, as ffdp_objective: p->w_lncc must be 0 (per-voxel
  *     images do not fit); a call whose scratch need (ffdp_workspace_bytes of
  *     the MI-only objective) exceeds the static scratch returns
  *     FFDP_ERR_UNSUPPORTED.

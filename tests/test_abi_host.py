@@ -113,6 +113,31 @@ def test_workspace_is_o1_for_mi_and_sampler(lib):
     assert ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (1, 64, 64), q) == 0
 
 
+def test_objective_params_are_the_contract_struct(lib):
+    # {w_mi, w_lncc, mi {bins, f_lo, f_hi, m_lo, m_hi}, lncc {window, eps}}: no
+    # trailing field, so a caller laying the struct out as the boundary
+    # specifies passes exactly what the library reads
+    from voxel_grid_sampler_gb300 import ffdp
+    names = [f[0] for f in ffdp.ffdp_objective_params._fields_]
+    assert names == ["w_mi", "w_lncc", "mi", "lncc"]
+    assert ctypes.sizeof(ffdp.ffdp_objective_params) == 4 + 4 + 20 + 8
+
+
+def test_stored_objective_workspace(lib):
+    # ffdp_objective_stored: an MI-only objective keeps J and its slope (16
+    # bytes per voxel); with LNCC both entry points hold the same buffers
+    from voxel_grid_sampler_gb300 import ffdp
+    dims = (40, 50, 60)
+    N = 40 * 50 * 60
+    p = ffdp.objective_params(1.0, 0.0, 32, (0, 1), (0, 1), 5)
+    a = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, p)
+    b = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE_STORED, dims, p)
+    assert 16 * N <= b - a <= 16 * N + 1024
+    q = ffdp.objective_params(1.0, 1.0, 32, (0, 1), (0, 1), 5)
+    assert (ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q) ==
+            ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE_STORED, dims, q))
+
+
 def test_wide_lncc_windows_take_two_five_channel_buffers(lib):
     # windows above 9 run as separable box-sum passes through two [5][N]
     # float buffers (40 bytes per voxel); any odd window >= 3 is accepted

@@ -62,8 +62,8 @@ def test_objective_on_extreme_grids(ffdp, shape):
     mr = (float(M.min()), float(M.max()))
     To = oracle_T(A, t)
     for wmi, wln, store in ((1.0, 1.0, False), (1.0, 0.0, True), (1.0, 0.0, False)):
-        P = ffdp.objective_params(wmi, wln, 32, fr, mr, 5, 1e-5, store_slope=store)
-        loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P)
+        P = ffdp.objective_params(wmi, wln, 32, fr, mr, 5, 1e-5)
+        loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P, store_slope=store)
         ref = oracle.objective(F, M, u, To, oracle.ObjectiveParams(wmi, wln, 32, fr, mr, 5, 1e-5))
         l = host(loss)
         for k in range(3):

@@ -168,8 +168,8 @@ def test_objective(ffdp, fs, ms, dt_, wmi, wln, B, w, store):
     fr = (float(F.min()), float(F.max()))
     mr = (float(M.min()), float(M.max()))
     T = ffdp.transform(A, t, S, xmin, xmax)
-    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5, store_slope=store)
-    loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P)
+    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5)
+    loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P, store_slope=store)
     ref = oracle.objective(F, M, u, oracle_T(A, t, S, xmin, xmax),
                            oracle.ObjectiveParams(wmi, wln, B, fr, mr, w, 1e-5))
     l = host(loss)
@@ -208,8 +208,8 @@ def test_objective_large(ffdp, fs, dt_, wmi, wln, B, w, store):
     fr = (float(F.min()), float(F.max()))
     mr = (float(M.min()), float(M.max()))
     T = ffdp.transform(A, t, S, xmin, xmax)
-    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5, store_slope=store)
-    loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P)
+    P = ffdp.objective_params(wmi, wln, B, fr, mr, w, 1e-5)
+    loss, du, dA, dt = ffdp.ffdp_objective(_cuda(F), _cuda(M), _cuda(u), T, P, store_slope=store)
     ref = oracle.objective(F, M, u, oracle_T(A, t, S, xmin, xmax),
                            oracle.ObjectiveParams(wmi, wln, B, fr, mr, w, 1e-5))
     l = host(loss)
@@ -240,9 +240,8 @@ def test_workspace_is_independent_of_volume_size_for_mi(ffdp):
     a = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (64, 64, 64), p)
     b = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), p)
     assert a == b and a < (1 << 20)
-    # stored J and slope: 16 bytes per voxel on top
-    q = ffdp.objective_params(1.0, 0.0, 64, (0, 1), (0, 1), 5, store_slope=True)
-    c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, (512, 512, 512), q)
+    # stored J and slope (ffdp_objective_stored): 16 bytes per voxel on top
+    c = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE_STORED, (512, 512, 512), p)
     assert 16 * 512 ** 3 <= c - a <= 16 * 512 ** 3 + 4096
     # LNCC on: the same two per-voxel buffers (the sampler backward runs in the
     # window kernel's epilogue), plus the 64-bin polynomial cells

@@ -29,9 +29,8 @@ def ffdp():
 def _run_gpu(ffdp, pair, store_slope=False):
     wl = pair.workload
     T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
-    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps,
-                              store_slope=store_slope)
-    loss, du, dA, dt = ffdp.ffdp_objective(pair.F, pair.M, pair.u, T, P)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    loss, du, dA, dt = ffdp.ffdp_objective(pair.F, pair.M, pair.u, T, P, store_slope=store_slope)
     J = ffdp.ffdp_grid_sample_fwd(pair.M, pair.F.shape, pair.u, T)
     torch.cuda.synchronize()
     return loss.cpu().numpy(), du, dA.cpu().numpy(), dt.cpu().numpy(), J

@@ -75,8 +75,3 @@ def test_static_scratch_objective_rejects_lncc_and_reports_its_size():
     with pytest.raises(ffdp.FfdpError) as ei:
         ffdp.ffdp_objective_mi_static(F, M, u, T, P, *out)
     assert ei.value.status == 2 and "MI only" in str(ei.value)
-    # stored J and slope would need per-voxel memory: rejected the same way
-    P = ffdp.objective_params(1.0, 0.0, 32, pair.f_range, pair.m_range, 5, store_slope=True)
-    with pytest.raises(ffdp.FfdpError) as ei:
-        ffdp.ffdp_objective_mi_static(F, M, u, T, P, *out)
-    assert ei.value.status == 2 and "store_slope" in str(ei.value)

@@ -418,14 +418,16 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
       if (check_lncc(p) != FFDP_OK) return 0;
       return ws_layout(false, 32, max_parts(), false, false, N, lncc_wide(p->window)).total;
     }
-    case FFDP_OP_OBJECTIVE: {
+    case FFDP_OP_OBJECTIVE:
+    case FFDP_OP_OBJECTIVE_STORED: {
       const ffdp_objective_params* p = static_cast<const ffdp_objective_params*>(params);
       if (!p) return 0;
       const bool mi = p->w_mi != 0.0f, ln = p->w_lncc != 0.0f;
       if (mi && check_mi(&p->mi) != FFDP_OK) return 0;
       if (ln && check_lncc(&p->lncc) != FFDP_OK) return 0;
+      const bool store_slope = op == FFDP_OP_OBJECTIVE_STORED;
       return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln,
-                       (ln && !lncc_recompute(p->lncc.window)) || (mi && !ln && p->store_slope != 0), N,
+                       (ln && !lncc_recompute(p->lncc.window)) || (mi && !ln && store_slope), N,
                        ln && lncc_wide(p->lncc.window)).total;
     }
     case FFDP_OP_SAMPLE_CHANNELS_BWD:
@@ -632,11 +634,15 @@ extern "C" ffdp_status ffdp_lncc_fwd_bwd(const void* F, ffdp_dtype ft, const flo
   return FFDP_OK;
 }
 
-extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M,
-                                      ffdp_dtype mt, ffdp_dims mdims, const float* u,
-                                      const ffdp_transform* T, const ffdp_objective_params* p, float* loss,
-                                      float* du, float* dA, float* dt, void* ws, size_t ws_bytes,
-                                      void* stream) {
+namespace {
+
+// The objective pipeline of ffdp_objective (store_slope = false) and
+// ffdp_objective_stored (store_slope = true: an MI-only objective keeps J and
+// its slope for a streaming gradient pass).
+ffdp_status objective(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M, ffdp_dtype mt,
+                      ffdp_dims mdims, const float* u, const ffdp_transform* T, const ffdp_objective_params* p,
+                      float* loss, float* du, float* dA, float* dt, void* ws, size_t ws_bytes, void* stream,
+                      bool store_slope) {
   g_err[0] = '\0';
   if (!F || !M || !T || !p || !loss) return fail(FFDP_ERR_INVALID_ARGUMENT, "null F, M, T, params or loss");
   FFDP_TRY(check_dtype(ft, "F"));
@@ -655,7 +661,7 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   const int bmax = mi ? bmax_of(p->mi.bins) : 32;
   const uint64_t N = nvox(fdims);
   const bool rc = ln && lncc_recompute(p->lncc.window);  // LNCC samples J on chip
-  const bool store = (ln && !rc) || (mi && !ln && p->store_slope != 0);
+  const bool store = (ln && !rc) || (mi && !ln && store_slope);
   const bool wide = ln && lncc_wide(p->lncc.window);
   const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N, wide);
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
@@ -799,6 +805,24 @@ extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fd
   }
   FFDP_CUDA(launch_finish(f, s), "finish launch");
   return FFDP_OK;
+}
+
+}  // namespace
+
+extern "C" ffdp_status ffdp_objective(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M,
+                                      ffdp_dtype mt, ffdp_dims mdims, const float* u,
+                                      const ffdp_transform* T, const ffdp_objective_params* p, float* loss,
+                                      float* du, float* dA, float* dt, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  return objective(F, ft, fdims, M, mt, mdims, u, T, p, loss, du, dA, dt, ws, ws_bytes, stream, false);
+}
+
+extern "C" ffdp_status ffdp_objective_stored(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void* M,
+                                             ffdp_dtype mt, ffdp_dims mdims, const float* u,
+                                             const ffdp_transform* T, const ffdp_objective_params* p,
+                                             float* loss, float* du, float* dA, float* dt, void* ws,
+                                             size_t ws_bytes, void* stream) {
+  return objective(F, ft, fdims, M, mt, mdims, u, T, p, loss, du, dA, dt, ws, ws_bytes, stream, true);
 }
 
 // ------------------------------------------- C-channel sampler (composition)
@@ -1089,11 +1113,6 @@ extern "C" ffdp_status ffdp_objective_mi_static(const void* F, ffdp_dtype ft, ff
     return fail(FFDP_ERR_UNSUPPORTED,
                 "the workspace-free objective evaluates MI only (w_lncc must be 0): LNCC keeps a "
                 "per-voxel image that does not fit the %zu-byte static scratch",
-                kStaticScratchBytes);
-  if (p->store_slope != 0)
-    return fail(FFDP_ERR_UNSUPPORTED,
-                "the workspace-free objective is implicit (store_slope must be 0): stored J and "
-                "dJ/dp do not fit the %zu-byte static scratch",
                 kStaticScratchBytes);
   const size_t need = ffdp_workspace_bytes(FFDP_OP_OBJECTIVE, fdims, p);
   if (need == 0) {

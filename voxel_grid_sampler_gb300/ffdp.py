@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libffdp.so")
 FFDP_F32, FFDP_F16 = 0, 1
 FFDP_OP_GRID_SAMPLE_BWD, FFDP_OP_MI, FFDP_OP_LNCC, FFDP_OP_OBJECTIVE = 1, 2, 3, 4
 FFDP_OP_SAMPLE_CHANNELS_BWD, FFDP_OP_MSE, FFDP_OP_OBJECTIVE_MSE, FFDP_OP_SOBOLEV = 5, 6, 7, 8
+FFDP_OP_OBJECTIVE_STORED = 9
 STATUS = {0: "FFDP_OK", 1: "FFDP_ERR_INVALID_ARGUMENT", 2: "FFDP_ERR_UNSUPPORTED",
           3: "FFDP_ERR_WORKSPACE", 4: "FFDP_ERR_CUDA", 5: "FFDP_ERR_INTERNAL"}
 
@@ -57,7 +58,7 @@ class ffdp_sobolev_adam_params(ctypes.Structure):
 
 class ffdp_objective_params(ctypes.Structure):
     _fields_ = [("w_mi", ctypes.c_float), ("w_lncc", ctypes.c_float), ("mi", ffdp_mi_params),
-                ("lncc", ffdp_lncc_params), ("store_slope", ctypes.c_int)]
+                ("lncc", ffdp_lncc_params)]
 
 
 _lib = None
@@ -84,10 +85,11 @@ def lib() -> ctypes.CDLL:
         L.ffdp_lncc_fwd_bwd.argtypes = [_vp, ctypes.c_int, _vp, ffdp_dims,
                                         ctypes.POINTER(ffdp_lncc_params), _vp, _vp, _vp, ctypes.c_size_t,
                                         _vp]
-        L.ffdp_objective.argtypes = [_vp, ctypes.c_int, ffdp_dims, _vp, ctypes.c_int, ffdp_dims, _vp,
-                                     ctypes.POINTER(ffdp_transform),
-                                     ctypes.POINTER(ffdp_objective_params), _vp, _vp, _vp, _vp, _vp,
-                                     ctypes.c_size_t, _vp]
+        for f in ("ffdp_objective", "ffdp_objective_stored"):
+            getattr(L, f).argtypes = [_vp, ctypes.c_int, ffdp_dims, _vp, ctypes.c_int, ffdp_dims, _vp,
+                                      ctypes.POINTER(ffdp_transform),
+                                      ctypes.POINTER(ffdp_objective_params), _vp, _vp, _vp, _vp, _vp,
+                                      ctypes.c_size_t, _vp]
         L.ffdp_sample_channels_fwd.argtypes = [_vp, ctypes.c_int, ffdp_dims, ffdp_dims, _vp,
                                                ctypes.POINTER(ffdp_transform), ctypes.c_int, _vp, _vp]
         L.ffdp_sample_channels_bwd.argtypes = [_vp, ctypes.c_int, ffdp_dims, ffdp_dims, _vp,
@@ -102,7 +104,7 @@ def lib() -> ctypes.CDLL:
                                              ctypes.POINTER(ffdp_sobolev_adam_params), _vp, _vp, ctypes.c_size_t,
                                              _vp]
         for f in ("ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd", "ffdp_mi_fwd_bwd",
-                  "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_sample_channels_fwd",
+                  "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_objective_stored", "ffdp_sample_channels_fwd",
                   "ffdp_sample_channels_bwd", "ffdp_mse_fwd_bwd", "ffdp_objective_mse",
                   "ffdp_sobolev_fwd_bwd", "ffdp_sobolev_adam_step"):
             getattr(L, f).restype = ctypes.c_int
@@ -154,10 +156,9 @@ def lncc_params(window, eps=1e-5) -> ffdp_lncc_params:
     return ffdp_lncc_params(int(window), float(eps))
 
 
-def objective_params(w_mi, w_lncc, bins, f_range, m_range, window, eps=1e-5,
-                     store_slope=False) -> ffdp_objective_params:
+def objective_params(w_mi, w_lncc, bins, f_range, m_range, window, eps=1e-5) -> ffdp_objective_params:
     return ffdp_objective_params(float(w_mi), float(w_lncc), mi_params(bins, f_range, m_range),
-                                 lncc_params(window, eps), 1 if store_slope else 0)
+                                 lncc_params(window, eps))
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -272,7 +273,9 @@ def ffdp_lncc_fwd_bwd(F, J, params: ffdp_lncc_params, loss=None, dJ=None, ws=Non
 
 
 def ffdp_objective(F, M, u, T: ffdp_transform, params: ffdp_objective_params, loss=None, du=None,
-                   dA=None, dt=None, ws=None, stream=None, want_du=True):
+                   dA=None, dt=None, ws=None, stream=None, want_du=True, store_slope=False):
+    """The fused objective; store_slope selects ffdp_objective_stored (an MI-only
+    objective keeps J and its slope in the workspace for a streaming gradient pass)."""
     _dev(F, "F", ndim=3)
     _dev(M, "M", ndim=3)
     _dev(u, "u", torch.float32, 4)
@@ -286,11 +289,12 @@ def ffdp_objective(F, M, u, T: ffdp_transform, params: ffdp_objective_params, lo
     if dt is None:
         dt = torch.empty(3, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = workspace(FFDP_OP_OBJECTIVE, F.shape, params, dev)
-    _check(lib().ffdp_objective(_ptr(F), _dtype_code(F), dims_of(F.shape), _ptr(M), _dtype_code(M),
-                                dims_of(M.shape), _ptr(u), ctypes.byref(T), ctypes.byref(params),
-                                _ptr(loss), _ptr(du), _ptr(dA), _ptr(dt), _ptr(ws), ws.numel(),
-                                _stream(stream)))
+        ws = workspace(FFDP_OP_OBJECTIVE_STORED if store_slope else FFDP_OP_OBJECTIVE, F.shape, params, dev)
+    fn = lib().ffdp_objective_stored if store_slope else lib().ffdp_objective
+    _check(fn(_ptr(F), _dtype_code(F), dims_of(F.shape), _ptr(M), _dtype_code(M),
+              dims_of(M.shape), _ptr(u), ctypes.byref(T), ctypes.byref(params),
+              _ptr(loss), _ptr(du), _ptr(dA), _ptr(dt), _ptr(ws), ws.numel(),
+              _stream(stream)))
     return loss, du, dA, dt
 
 
