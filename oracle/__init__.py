@@ -393,13 +393,15 @@ def objective(F, M, u, T: Transform, p: ObjectiveParams, want_du: bool = True):
 
 
 def objective_mi_slabs(F, M, u, T: Transform, p: ObjectiveParams, slab: int = 16,
-                       du_index=None):
+                       du_index=None, on_slab=None):
     """MI-only objective evaluated slab by slab, so no N-sized double array is held.
 
     The histogram is accumulated over z-slabs and merged with the slab weights
     N_h/N implied by plain accumulation (design 5's partial-aggregation
     identity).  Returns dict(loss, dA, dt, du_samples) where du_samples holds
-    du at the flat voxel indices ``du_index`` (sorted or not)."""
+    du at the flat voxel indices ``du_index`` (sorted or not).  on_slab, if
+    given, is called as on_slab(z0, z1, du, J) with each slab's du
+    [z1-z0, H, W, 3] and J [z1-z0, H, W] (float64) as they are computed."""
     F32 = _f32(F)
     shape = F32.shape
     D, H, W = shape
@@ -425,8 +427,10 @@ def objective_mi_slabs(F, M, u, T: Transform, p: ObjectiveParams, slab: int = 16
         z1 = min(D, z0 + slab)
         J = grid_sample(M32, shape, u32, T, z0, z1)
         gJ = p.w_mi * mi_grad(F32[z0:z1], J, B, p.f_range, p.m_range, P, PF, PJ, N)
-        du, dA, dt = grid_sample_bwd(M32, shape, u32, T, gJ, z0, z1, want_du=idx is not None,
-                                     dA=dA, dt=dt)
+        du, dA, dt = grid_sample_bwd(M32, shape, u32, T, gJ, z0, z1,
+                                     want_du=idx is not None or on_slab is not None, dA=dA, dt=dt)
+        if on_slab is not None:
+            on_slab(z0, z1, du, J)
         if idx is not None:
             sel = (idx >= z0 * plane) & (idx < z1 * plane)
             du_s[sel] = du.reshape(-1, 3)[idx[sel] - z0 * plane]
