@@ -113,7 +113,10 @@ def test_mi_is_deterministic_and_order_free(ffdp):
 LNCC_CASES = [((20, 37, 70), 5), ((9, 16, 32), 3), ((13, 17, 45), 7), ((11, 12, 40), 9), ((70, 17, 6), 5),
               # windows above 9: the separable wide-window passes; 13 and 21
               # are wider than some axes (clipped sums, divisor still w^3)
-              ((20, 37, 70), 11), ((9, 16, 32), 13), ((13, 17, 45), 21)]
+              ((20, 37, 70), 11), ((9, 16, 32), 13), ((13, 17, 45), 21),
+              # wider than every axis: every window holds the whole grid (the
+              # radius is capped at the largest extent, the divisor stays w^3)
+              ((9, 16, 32), 101)]
 
 
 @pytest.mark.parametrize("shape,w", LNCC_CASES)
@@ -126,6 +129,18 @@ def test_lncc_fwd_bwd(ffdp, shape, w, fdt):
     r = oracle.lncc(F, J.astype(np.float64), w, 1e-5)
     assert rel_err(host(loss)[0], -r["lncc"]) <= TOL_LOSS
     assert rel_l2(host(dJ), r["dJ"]) <= TOL_GRAD
+
+
+def test_wide_window_loss_only_matches_full_call(ffdp):
+    # the wide-window passes without a dL/dJ output give the same loss
+    F = _vol((14, 19, 45), 15, 0.0, 1.0)
+    J = (0.6 * F.astype(np.float64) + 0.4 * _vol((14, 19, 45), 16)).astype(np.float32)
+    p = ffdp.lncc_params(15, 1e-5)
+    l1, dJ = ffdp.ffdp_lncc_fwd_bwd(_cuda(F), _cuda(J), p)
+    l2, none = ffdp.ffdp_lncc_fwd_bwd(_cuda(F), _cuda(J), p, want_grad=False)
+    assert none is None and host(l1)[0] == host(l2)[0]
+    r = oracle.lncc(F, J.astype(np.float64), 15, 1e-5)
+    assert rel_err(host(l2)[0], -r["lncc"]) <= TOL_LOSS
 
 
 def test_lncc_of_scaled_image_is_one(ffdp):
