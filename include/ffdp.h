@@ -88,10 +88,10 @@ typedef struct {
 } ffdp_mi_params;
 
 /* LNCC: odd window >= 3; cc = cross^2 / (varF varJ + eps) with zero-padded
- * window sums and divisor window^3.  Windows up to 9 run in tiled kernels that
- * keep every window sum on chip; wider ones run as separable box sums, one
- * pass per axis, through two [5][N] float buffers of the workspace (40 bytes
- * per voxel more).  A window wider than the grid sums what lies inside it. */
+ * window sums and divisor window^3.  Windows up to 7 run in a tiled kernel
+ * that keeps every window sum on chip; wider ones run as separable box sums,
+ * one pass per axis, through two [5][N] float buffers of the workspace (40
+ * bytes per voxel more).  A window wider than the grid sums what lies inside it. */
 typedef struct {
   int window;
   float eps;
@@ -126,7 +126,7 @@ enum {
  * done in the window kernel's epilogue, reads the slope instead of gathering
  * M again; the paper's fused LNCC keeps five such intermediates.  An MI-only
  * objective through ffdp_objective_stored holds the same two buffers.  An LNCC window
- * above 9 (the LNCC op or an objective with LNCC) adds 40 bytes per voxel
+ * above 7 (the LNCC op or an objective with LNCC) adds 40 bytes per voxel
  * for the separable window-sum passes.  Queries the current device's SM
  * count. */
 size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void *params);

@@ -139,20 +139,20 @@ def test_stored_objective_workspace(lib):
 
 
 def test_wide_lncc_windows_take_two_five_channel_buffers(lib):
-    # windows above 9 run as separable box-sum passes through two [5][N]
+    # windows above 7 run as separable box-sum passes through two [5][N]
     # float buffers (40 bytes per voxel); any odd window >= 3 is accepted
     from voxel_grid_sampler_gb300 import ffdp
     dims = (20, 30, 40)
     N = 20 * 30 * 40
-    tiled = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(9))
-    for w in (11, 13, 61, 1001):
+    tiled = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(7))
+    for w in (9, 11, 13, 61, 1001):
         wide = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(w))
         assert wide - tiled >= 40 * N and wide - tiled < 40 * N + 1024
+    q7 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 7)
     q9 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 9)
-    q11 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 11)
+    o7 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q7)
     o9 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q9)
-    o11 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q11)
-    assert o11 - o9 >= 40 * N and o11 - o9 < 40 * N + 1024
+    assert o9 - o7 >= 40 * N and o9 - o7 < 40 * N + 1024
 
 
 @nogpu

@@ -111,7 +111,7 @@ def test_mi_is_deterministic_and_order_free(ffdp):
 
 # --------------------------------------------------------------------- LNCC
 LNCC_CASES = [((20, 37, 70), 5), ((9, 16, 32), 3), ((13, 17, 45), 7), ((11, 12, 40), 9), ((70, 17, 6), 5),
-              # windows above 9: the separable wide-window passes; 13 and 21
+              # windows above 7: the separable wide-window passes; 13 and 21
               # are wider than some axes (clipped sums, divisor still w^3)
               ((20, 37, 70), 11), ((9, 16, 32), 13), ((13, 17, 45), 21),
               # wider than every axis: every window holds the whole grid (the
@@ -157,7 +157,7 @@ OBJ_CASES = [
     ((18, 21, 35), (18, 21, 35), np.float32, 0.7, 0.0, 64, 5),
     ((18, 21, 35), (18, 21, 35), np.float32, 0.0, 1.3, 32, 7),
     ((17, 19, 37), (17, 19, 37), np.float16, 1.0, 0.5, 48, 3),
-    # window 9 (the shared-memory plane-ring kernel) with the MI term fused, both table sizes
+    # window 9 (the separable wide-window passes) with the MI term fused, both table sizes
     ((16, 18, 40), (16, 18, 40), np.float32, 1.0, 1.0, 64, 9),
     ((15, 17, 33), (15, 17, 33), np.float16, 1.0, 0.5, 32, 9),
     # rows a multiple of 4 voxels: full tiles stage the stored slope by 16-byte
@@ -165,7 +165,7 @@ OBJ_CASES = [
     ((19, 37, 100), (19, 37, 100), np.float32, 1.0, 1.0, 64, 5),
     ((12, 16, 64), (12, 16, 64), np.float32, 0.5, 1.0, 32, 9),
     ((10, 48, 96), (10, 48, 96), np.float16, 0.0, 1.0, 32, 3),
-    # windows above 9 (wide-window passes), with and without the MI term
+    # windows above 7 (wide-window passes), with and without the MI term
     ((16, 18, 40), (16, 18, 40), np.float32, 1.0, 1.0, 64, 11),
     ((15, 17, 33), (15, 17, 33), np.float16, 1.0, 0.5, 32, 13),
     ((12, 16, 64), (12, 16, 64), np.float32, 0.0, 1.0, 32, 11),

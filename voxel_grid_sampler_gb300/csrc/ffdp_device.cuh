@@ -13,7 +13,6 @@
 namespace ffdp {
 
 // ---------------------------------------------------------------- constants
-constexpr int kThreads = 256;           // threads per CTA of the LNCC kernel
 #ifndef FFDP_SWEEP1_THREADS
 #define FFDP_SWEEP1_THREADS 640
 #endif

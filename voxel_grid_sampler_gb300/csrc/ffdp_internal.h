@@ -120,7 +120,7 @@ struct LnccArgs {
 
 // LNCC for windows above kLnccTiledMaxWindow: separable box sums through two
 // [5][N] float buffers of the workspace (k_lncc_wide.cu).
-constexpr int kLnccTiledMaxWindow = 9;
+constexpr int kLnccTiledMaxWindow = 7;  // tiled register-history kernel (radius <= 3)
 struct WideArgs {
   const void* F;
   const float* J;

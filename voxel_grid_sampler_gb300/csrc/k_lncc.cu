@@ -1,6 +1,8 @@
-// k_lncc.cu -- fused LNCC forward + backward on a materialised warped image J,
-// optionally adding the MI partial gradient: writes g = dL/dJ per voxel (the
-// sampler backward of g runs in the linear gradient sweep).
+// k_lncc.cu -- fused LNCC forward + backward for windows up to 7 on a
+// materialised warped image J: writes g = dL/dJ per voxel (stand-alone LNCC)
+// or, in the objective, adds the MI partial gradient and runs the sampler
+// backward (du and the affine partials) from the stored slope in its epilogue.
+// Wider windows run as separable passes (k_lncc_wide.cu).
 //
 // Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
 // Registration", Key designs item 2: all LNCC intermediates (the window sums
@@ -12,23 +14,13 @@
 //   s = -w_lncc / N:  g_FJ = s A1,  g_JJ = -s A2,  g_J = s (2 A2 S_J - A1 S_F) / n,
 //   dJ_m = sum_{k in window(m)} g_J(k) + 2 J_m g_JJ(k) + F_m g_FJ(k).
 //
-// Work layout.  A CTA owns a 32 x TY column of output voxels and streams a
-// z-range of planes.  (J, F) planes with a 2R halo sit in a ring of w planes
-// in shared memory as interleaved pairs, so that the five window sums run on
-// packed fp32 pairs ((S_J, S_F), (S_JJ, S_FF)) plus S_FJ.  Per incoming plane:
-//   [B] z sums of the products over the ring (direct, w terms),
-//   [C] x sums (runs of 4 outputs per thread, sliding),
-//   [D] y sums (runs of 4 rows per thread, sliding) -> cc and the g-terms of
-//       plane zc = zi - R on the R-halo region,
-//   [E] x sums and [F] y sums of the g-terms -> their 2-D window sums at the
-//       output columns, kept in a ring of w planes,
-//   [G] z sums over that ring give dJ at plane zo = zi - 2R; the MI term
-//       (from the on-chip J and F) is added and g is stored.
-// The next plane is fetched into registers during a step and written to the
-// ring after [B], so global latency overlaps the shared-memory work.  The
-// first window pass uses direct fp32 sums in z (no sliding add/subtract) to
-// keep rounding low in flat regions.  CTAs are persistent over tiles, so the
-// per-CTA partial records stay O(#SMs).
+// Work layout (k_lncc_rh, below).  A CTA owns a 32 x TY column of output
+// voxels and streams a z segment of planes; each thread keeps the (J, F) of
+// its staged positions of the 2R-halo plane for the last w planes in
+// registers, so the z window sums need no shared memory and shared memory
+// carries only the x and y passes.  The five window sums run on packed fp32
+// pairs ((S_J, S_F), (S_JJ, S_FF)) plus S_FJ.  CTAs are persistent over
+// tiles, so the per-CTA partial records stay O(#SMs).
 #include <type_traits>
 
 #include "ffdp_internal.h"
@@ -47,21 +39,9 @@ struct LT {
   static constexpr int E1W = kTX + 2 * R;
   static constexpr int E1H = TY + 2 * R;
   static constexpr int E1S = (E1W + 3) & ~3;
-  static constexpr int E2S = E2W;
-  static constexpr int NIN = ((4 + 2 * R) + 3) & ~3;  // inputs of a 4-output sliding run, rounded to 4
-  static constexpr int RING = W * E2H * E2S * 2;
-  static constexpr int ZB = E2H * E2S * 5;
   static constexpr int XB = E2H * E1S * 5;
-  static constexpr int GR = W * TY * kTX * 3;
   static constexpr int PAD = 32;
-  static constexpr int OFF_RING = 0;
-  static constexpr int OFF_Z = OFF_RING + RING + PAD;
-  static constexpr int OFF_X = OFF_Z + ZB + PAD;
-  static constexpr int OFF_G = OFF_X + XB + PAD;
-  static constexpr int TOTAL = OFF_G + GR + PAD;
-  static_assert(E1H * E1S * 3 <= ZB, "g-term plane must fit in the z buffer");
   static_assert(E1H * kTX * 3 <= XB, "g-term x buffer must fit in the x buffer");
-  static_assert((OFF_Z % 4) == 0 && (OFF_X % 4) == 0 && (OFF_G % 4) == 0, "16-byte alignment");
   static_assert((TY % 4) == 0, "TY multiple of 4");
 };
 
@@ -234,439 +214,6 @@ struct DuAcc {
     }
   }
 };
-
-template <typename FT, int BMAX, int R, bool DU>
-__global__ void __launch_bounds__(kThreads, R <= 3 ? 2 : 1) k_lncc(const LnccArgs a) {
-  using L = LT<R>;
-  constexpr int W = L::W, TY = L::TY, E2H = L::E2H, E2W = L::E2W, E2S = L::E2S;
-  constexpr int E1W = L::E1W, E1H = L::E1H, E1S = L::E1S, NIN = L::NIN;
-  constexpr bool MI = BMAX != 0;
-  constexpr int NSTG = (E2H * E2W + kThreads - 1) / kThreads;
-  constexpr int NOUT = (kTX * TY) / kThreads;  // output positions per thread (2 or 1)
-  static_assert(NOUT >= 1 && NOUT * kThreads == kTX * TY, "tile / thread mismatch");
-
-  extern __shared__ float4 sm4[];
-  float* sm = reinterpret_cast<float*>(sm4);
-  __shared__ double wsum[kThreads / 32][13];
-  float2* ring = reinterpret_cast<float2*>(sm + L::OFF_RING);
-  float2* zP = reinterpret_cast<float2*>(sm + L::OFF_Z);
-  float2* zQ = zP + E2H * E2S;
-  float* zX = sm + L::OFF_Z + 4 * E2H * E2S;
-  float2* xP = reinterpret_cast<float2*>(sm + L::OFF_X);
-  float2* xQ = xP + E2H * E1S;
-  float* xX = sm + L::OFF_X + 4 * E2H * E1S;
-  float2* gP = reinterpret_cast<float2*>(sm + L::OFF_Z);
-  float* gX = sm + L::OFF_Z + 2 * E1H * E1S;
-  float2* gxP = reinterpret_cast<float2*>(sm + L::OFF_X);
-  float* gxX = sm + L::OFF_X + 2 * E1H * kTX;
-  float2* grP = reinterpret_cast<float2*>(sm + L::OFF_G);
-  float* grX = sm + L::OFF_G + W * TY * kTX * 2;
-  float* slope = sm + L::TOTAL;  // LN_DU only
-
-  const Geom& g = a.g;
-  const int tid = threadIdx.x;
-  const FT* __restrict__ F = static_cast<const FT*>(a.F);
-  const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
-  const float2 ninv2 = make_float2(-inv_n, -inv_n);
-  const size_t plane = (size_t)g.fW * g.fH;
-  float cc_acc = 0.0f;
-  if ((tid & 31) == 0)
-    for (int q = 0; q < 13; ++q) wsum[tid >> 5][q] = 0.0;
-  DuAcc<NOUT> dacc;
-  dacc.clear();
-
-  // this thread's staged elements of a halo plane: in-plane offset, or -1
-  // where the element lies outside the grid (read as zero)
-  float2 stg[NSTG];
-  int soff[NSTG];
-  auto load_plane = [&](int zp) {
-    const bool zin = zp >= 0 && zp < g.fD;
-    const size_t base = (size_t)zp * plane;
-#pragma unroll
-    for (int i = 0; i < NSTG; ++i) {
-      float2 v = make_float2(0.0f, 0.0f);
-      if (zin && soff[i] >= 0) {
-        v.x = __ldg(a.J + base + soff[i]);
-        v.y = load1(F + base + soff[i]);
-      }
-      stg[i] = v;
-    }
-  };
-  auto store_plane = [&](int slot) {
-    float2* dst = ring + slot * (E2H * E2S);
-#pragma unroll
-    for (int i = 0; i < NSTG; ++i) {
-      const int e = tid + i * kThreads;
-      if (e < E2H * E2W) dst[e] = stg[i];
-    }
-  };
-
-  LnccSegs seg(a);
-  int tx, ty, z0, z1;
-  while (seg.next(tx, ty, z0, z1)) {
-    const int x0 = tx * kTX, y0 = ty * TY;
-    const int nsteps = (z1 - z0) + 4 * R;
-    // LN_DU: the tile's slope (plane stride slope_plane) and its staging slots;
-    // slot_rd is the slot of the current step's output plane (s mod 3)
-    const bool full = x0 + kTX <= g.fW && y0 + TY <= g.fH && (g.fW & 3) == 0;
-    const size_t slope_plane = 3 * (size_t)g.fW * g.fH;
-    const float* slope_tile = DU ? a.dJdq + 3 * ((size_t)y0 * g.fW + x0) : nullptr;
-    int slot_rd = 2;
-
-    // output positions of this thread (one column: kThreads is a multiple of kTX)
-    int oX[NOUT], oY[NOUT];
-#pragma unroll
-    for (int k = 0; k < NOUT; ++k) {
-      const int e = tid + k * kThreads;
-      oY[k] = y0 + e / kTX;
-      oX[k] = x0 + (e % kTX);
-    }
-    auto fold_du = [&] {
-      float cy[NOUT];
-#pragma unroll
-      for (int k = 0; k < NOUT; ++k) cy[k] = (float)oY[k] - g.ctr[1];
-      dacc.fold(wsum[tid >> 5], tid & 31, (float)oX[0] - g.ctr[0], cy);
-    };
-#pragma unroll
-    for (int i = 0; i < NSTG; ++i) {
-      const int e = tid + i * kThreads;
-      const int ey = e / E2W, ex = e - ey * E2W;
-      const int x = x0 - 2 * R + ex, y = y0 - 2 * R + ey;
-      soff[i] = (e < E2H * E2W && (unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) ? y * g.fW + x : -1;
-    }
-
-    __syncthreads();  // previous tile finished with every buffer
-    load_plane(z0 - 2 * R);
-    store_plane(0);
-    if (nsteps > 1) load_plane(z0 - 2 * R + 1);
-    __syncthreads();
-
-    for (int s = 0; s < nsteps; ++s) {
-      const int zi = z0 - 2 * R + s;
-      const bool pass1 = s >= 2 * R;
-      const bool pass2 = s >= 4 * R;
-      if constexpr (DU) {
-        slot_rd = slot_rd == 2 ? 0 : slot_rd + 1;
-        const int sn = s + 1;  // the output plane of the next step
-        const float* src = (sn >= 4 * R && sn < nsteps) ? slope_tile + (size_t)(zi + 1 - 2 * R) * slope_plane : nullptr;
-        stage_slope<TY, kThreads>(slope + (slot_rd == 2 ? 0 : slot_rd + 1) * SlopeStage<TY>::SLOT, src,
-                                  g, x0, y0, full, tid);
-      }
-      // (J, F) at this thread's outputs of plane zo = zi - 2R: the ring slot
-      // about to be overwritten.
-      float2 jfo[NOUT];
-      if (pass2) {
-        const float2* src = ring + ((s + 1) % W) * (E2H * E2S);
-#pragma unroll
-        for (int k = 0; k < NOUT; ++k) {
-          const int e = tid + k * kThreads;
-          jfo[k] = src[(e / kTX + 2 * R) * E2S + (e % kTX) + 2 * R];
-        }
-      }
-      // [B] z sums over the ring: (S_J, S_F), (S_JJ, S_FF), S_FJ
-      if (pass1) {
-        constexpr int BG = E2W / 4;
-        for (int it = tid; it < E2H * BG; it += kThreads) {
-          const int row = it / BG, c4 = it - row * BG;
-          float2 sP[4], sQ[4];
-          float sX[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            sP[i] = make_float2(0.f, 0.f);
-            sQ[i] = make_float2(0.f, 0.f);
-            sX[i] = 0.f;
-          }
-#pragma unroll
-          for (int k = 0; k < W; ++k) {
-            const float4* src = reinterpret_cast<const float4*>(ring + k * (E2H * E2S) + row * E2S + 4 * c4);
-            const float4 v0 = src[0], v1 = src[1];
-            const float2 p[4] = {make_float2(v0.x, v0.y), make_float2(v0.z, v0.w), make_float2(v1.x, v1.y),
-                                 make_float2(v1.z, v1.w)};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              sP[i] = add2(sP[i], p[i]);
-              sQ[i] = fma2(p[i], p[i], sQ[i]);
-              sX[i] = fmaf(p[i].x, p[i].y, sX[i]);
-            }
-          }
-          float4* dP = reinterpret_cast<float4*>(zP + row * E2S + 4 * c4);
-          float4* dQ = reinterpret_cast<float4*>(zQ + row * E2S + 4 * c4);
-          dP[0] = make_float4(sP[0].x, sP[0].y, sP[1].x, sP[1].y);
-          dP[1] = make_float4(sP[2].x, sP[2].y, sP[3].x, sP[3].y);
-          dQ[0] = make_float4(sQ[0].x, sQ[0].y, sQ[1].x, sQ[1].y);
-          dQ[1] = make_float4(sQ[2].x, sQ[2].y, sQ[3].x, sQ[3].y);
-          *reinterpret_cast<float4*>(zX + row * E2S + 4 * c4) = make_float4(sX[0], sX[1], sX[2], sX[3]);
-        }
-      }
-      if constexpr (DU) slope_wait_prev();
-      __syncthreads();
-      // the oldest ring slot is free: write the staged plane, fetch the next
-      if (s + 1 < nsteps) {
-        store_plane((s + 1) % W);
-        if (s + 2 < nsteps) load_plane(zi + 2);
-      }
-      if (!pass1) {
-        __syncthreads();
-        continue;
-      }
-      // [C] x sums, 4 outputs per item (sliding)
-      {
-        constexpr int XG = E1S / 4;
-        for (int it = tid; it < E2H * XG; it += kThreads) {
-          const int row = it / XG, g4 = it - row * XG;
-          float2 vP[NIN], vQ[NIN];
-          float vX[NIN];
-          const float4* sP4 = reinterpret_cast<const float4*>(zP + row * E2S + 4 * g4);
-          const float4* sQ4 = reinterpret_cast<const float4*>(zQ + row * E2S + 4 * g4);
-          const float4* sX4 = reinterpret_cast<const float4*>(zX + row * E2S + 4 * g4);
-#pragma unroll
-          for (int k = 0; k < NIN / 2; ++k) {
-            const float4 p = sP4[k], q = sQ4[k];
-            vP[2 * k] = make_float2(p.x, p.y);
-            vP[2 * k + 1] = make_float2(p.z, p.w);
-            vQ[2 * k] = make_float2(q.x, q.y);
-            vQ[2 * k + 1] = make_float2(q.z, q.w);
-          }
-#pragma unroll
-          for (int k = 0; k < NIN / 4; ++k) {
-            const float4 x = sX4[k];
-            vX[4 * k] = x.x;
-            vX[4 * k + 1] = x.y;
-            vX[4 * k + 2] = x.z;
-            vX[4 * k + 3] = x.w;
-          }
-          float2 aP = vP[0], aQ = vQ[0];
-          float aX = vX[0];
-#pragma unroll
-          for (int k = 1; k <= 2 * R; ++k) {
-            aP = add2(aP, vP[k]);
-            aQ = add2(aQ, vQ[k]);
-            aX += vX[k];
-          }
-          float2 oP[4], oQ[4];
-          float oXv[4];
-          oP[0] = aP;
-          oQ[0] = aQ;
-          oXv[0] = aX;
-#pragma unroll
-          for (int j = 1; j < 4; ++j) {
-            aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
-            aQ = sub2(add2(aQ, vQ[2 * R + j]), vQ[j - 1]);
-            aX = (aX + vX[2 * R + j]) - vX[j - 1];
-            oP[j] = aP;
-            oQ[j] = aQ;
-            oXv[j] = aX;
-          }
-          float4* dP = reinterpret_cast<float4*>(xP + row * E1S + 4 * g4);
-          float4* dQ = reinterpret_cast<float4*>(xQ + row * E1S + 4 * g4);
-          dP[0] = make_float4(oP[0].x, oP[0].y, oP[1].x, oP[1].y);
-          dP[1] = make_float4(oP[2].x, oP[2].y, oP[3].x, oP[3].y);
-          dQ[0] = make_float4(oQ[0].x, oQ[0].y, oQ[1].x, oQ[1].y);
-          dQ[1] = make_float4(oQ[2].x, oQ[2].y, oQ[3].x, oQ[3].y);
-          *reinterpret_cast<float4*>(xX + row * E1S + 4 * g4) = make_float4(oXv[0], oXv[1], oXv[2], oXv[3]);
-        }
-      }
-      __syncthreads();
-      // [D] y sums -> window sums at plane zc on the R-halo region; cc and g-terms
-      {
-        constexpr int YR = (E1H + 3) / 4;
-        const int zc = zi - R;
-        const bool zin = zc >= 0 && zc < g.fD;
-        const bool zown = zc >= z0 && zc < z1;
-        for (int it = tid; it < E1W * YR; it += kThreads) {
-          const int x1 = it % E1W, r4 = it / E1W;
-          const int ys = 4 * r4;
-          float2 vP[4 + 2 * R], vQ[4 + 2 * R];
-          float vX[4 + 2 * R];
-#pragma unroll
-          for (int k = 0; k < 4 + 2 * R; ++k) {
-            const int row = ys + k;
-            if (row < E2H) {
-              vP[k] = xP[row * E1S + x1];
-              vQ[k] = xQ[row * E1S + x1];
-              vX[k] = xX[row * E1S + x1];
-            } else {
-              vP[k] = vQ[k] = make_float2(0.f, 0.f);
-              vX[k] = 0.f;
-            }
-          }
-          float2 aP = vP[0], aQ = vQ[0];
-          float aX = vX[0];
-#pragma unroll
-          for (int k = 1; k <= 2 * R; ++k) {
-            aP = add2(aP, vP[k]);
-            aQ = add2(aQ, vQ[k]);
-            aX += vX[k];
-          }
-          const int x = x0 - R + x1;
-          const bool xin = (unsigned)x < (unsigned)g.fW;
-          const bool xown = x1 >= R && x1 < R + kTX;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j > 0) {
-              aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
-              aQ = sub2(add2(aQ, vQ[2 * R + j]), vQ[j - 1]);
-              aX = (aX + vX[2 * R + j]) - vX[j - 1];
-            }
-            const int y1 = ys + j;
-            if (y1 < E1H) {
-              const int y = y0 - R + y1;
-              float2 gpair = make_float2(0.f, 0.f);
-              float gfj = 0.f;
-              if (zin && xin && (unsigned)y < (unsigned)g.fH) {
-                // aP = (S_J, S_F), aQ = (S_JJ, S_FF), aX = S_FJ
-                // (vJ, vF), clamped at 0 (exact variances are; fp32 cancellation in
-                // flat windows can leave small negatives) so that vF vJ + eps >= eps
-                float2 v = fma2(mul2(aP, aP), ninv2, aQ);
-                v = make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f));
-                const float cross = fmaf(-aP.x * aP.y, inv_n, aX);
-                const float D = fmaf(v.x, v.y, eps);
-                const float rD = rcp_approx(D);
-                const float A1 = 2.0f * cross * rD;
-                const float cc = cross * cross * rD;
-                const float A2 = cc * v.y * rD;
-                gfj = gs * A1;
-                gpair.y = -gs * A2;
-                gpair.x = gs * (2.0f * A2 * aP.x - A1 * aP.y) * inv_n;
-                if (zown && xown && y1 >= R && y1 < R + TY) cc_acc += cc;
-              }
-              gP[y1 * E1S + x1] = gpair;
-              gX[y1 * E1S + x1] = gfj;
-            }
-          }
-        }
-      }
-      __syncthreads();
-      // [E] x sums of the g-terms onto the 32 output columns
-      {
-        constexpr int XG2 = kTX / 4;
-        for (int it = tid; it < E1H * XG2; it += kThreads) {
-          const int row = it / XG2, g4 = it - row * XG2;
-          float2 vP[NIN];
-          float vX[NIN];
-          const float4* sP4 = reinterpret_cast<const float4*>(gP + row * E1S + 4 * g4);
-          const float4* sX4 = reinterpret_cast<const float4*>(gX + row * E1S + 4 * g4);
-#pragma unroll
-          for (int k = 0; k < NIN / 2; ++k) {
-            const float4 p = sP4[k];
-            vP[2 * k] = make_float2(p.x, p.y);
-            vP[2 * k + 1] = make_float2(p.z, p.w);
-          }
-#pragma unroll
-          for (int k = 0; k < NIN / 4; ++k) {
-            const float4 x = sX4[k];
-            vX[4 * k] = x.x;
-            vX[4 * k + 1] = x.y;
-            vX[4 * k + 2] = x.z;
-            vX[4 * k + 3] = x.w;
-          }
-          float2 aP = vP[0];
-          float aX = vX[0];
-#pragma unroll
-          for (int k = 1; k <= 2 * R; ++k) {
-            aP = add2(aP, vP[k]);
-            aX += vX[k];
-          }
-          float2 oP[4];
-          float oXv[4];
-          oP[0] = aP;
-          oXv[0] = aX;
-#pragma unroll
-          for (int j = 1; j < 4; ++j) {
-            aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
-            aX = (aX + vX[2 * R + j]) - vX[j - 1];
-            oP[j] = aP;
-            oXv[j] = aX;
-          }
-          float4* dP = reinterpret_cast<float4*>(gxP + row * kTX + 4 * g4);
-          dP[0] = make_float4(oP[0].x, oP[0].y, oP[1].x, oP[1].y);
-          dP[1] = make_float4(oP[2].x, oP[2].y, oP[3].x, oP[3].y);
-          *reinterpret_cast<float4*>(gxX + row * kTX + 4 * g4) = make_float4(oXv[0], oXv[1], oXv[2], oXv[3]);
-        }
-      }
-      __syncthreads();
-      // [F] y sums of the g-terms -> 2-D window sums at the outputs, into the ring
-      {
-        float2* rP = grP + (s % W) * (TY * kTX);
-        float* rX = grX + (s % W) * (TY * kTX);
-        for (int it = tid; it < kTX * (TY / 4); it += kThreads) {
-          const int x = it % kTX, r4 = it / kTX;
-          const int ys = 4 * r4;
-          float2 vP[4 + 2 * R];
-          float vX[4 + 2 * R];
-#pragma unroll
-          for (int k = 0; k < 4 + 2 * R; ++k) {
-            vP[k] = gxP[(ys + k) * kTX + x];
-            vX[k] = gxX[(ys + k) * kTX + x];
-          }
-          float2 aP = vP[0];
-          float aX = vX[0];
-#pragma unroll
-          for (int k = 1; k <= 2 * R; ++k) {
-            aP = add2(aP, vP[k]);
-            aX += vX[k];
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j > 0) {
-              aP = sub2(add2(aP, vP[2 * R + j]), vP[j - 1]);
-              aX = (aX + vX[2 * R + j]) - vX[j - 1];
-            }
-            rP[(ys + j) * kTX + x] = aP;
-            rX[(ys + j) * kTX + x] = aX;
-          }
-        }
-      }
-      __syncthreads();
-      // [G] z sums over the g-term ring -> dJ at plane zo, then the epilogue
-      if (pass2) {
-        const int zo = zi - 2 * R;
-#pragma unroll
-        for (int k = 0; k < NOUT; ++k) {
-          const int e = tid + k * kThreads;
-          float2 bP = grP[e];
-          float bX = grX[e];
-#pragma unroll
-          for (int q = 1; q < W; ++q) {
-            bP = add2(bP, grP[q * (TY * kTX) + e]);
-            bX += grX[q * (TY * kTX) + e];
-          }
-          const float jv = jfo[k].x, fv = jfo[k].y;
-          const int X = oX[k], Y = oY[k];
-          if (X < g.fW && Y < g.fH) {
-            float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
-            if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
-            const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
-            if constexpr (DU)
-              dacc.add(a, k, lin, slope + slot_rd * SlopeStage<TY>::SLOT + 3 * e, (float)zo - g.ctr[2], gv);
-            else if (a.dJ)
-              a.dJ[lin] = gv;
-          }
-        }
-      }
-      // fold the fp32 cc (and affine) partials into fp64 every 32 planes
-      // (uniform across the CTA)
-      if ((s & 31) == 31) {
-        const float v = warp_sum(cc_acc);
-        if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
-        cc_acc = 0.0f;
-        if constexpr (DU) fold_du();
-      }
-    }
-    if constexpr (DU) fold_du();  // the next segment has other columns and rows
-  }
-  {
-    const float v = warp_sum(cc_acc);
-    if ((tid & 31) == 0) wsum[tid >> 5][12] += (double)v;
-  }
-  __syncthreads();
-  if (tid < kPartialStride) {
-    double s = 0.0;
-    if (tid == kPCC || (DU && tid < 12))
-      for (int k = 0; k < kThreads / 32; ++k) s += wsum[k][tid];
-    a.partials[(size_t)blockIdx.x * kPartialStride + tid] = s;
-  }
-}
 
 // ------------------------------------------------- register-history variant
 // Same mathematics and tiling, for R <= 3.  Each thread stages NSTG fixed
@@ -1156,27 +703,18 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
 
 template <int R, bool DU>
 static size_t smem_of() {
-  const size_t stage = (DU && !(kLnccRecompute && R <= 3)) ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0;
-  if constexpr (R <= 3)
-    return ((size_t)LTR<R>::TOTAL + stage) * sizeof(float);
-  else
-    return ((size_t)LT<R>::TOTAL + stage) * sizeof(float);
+  const size_t stage = (DU && !kLnccRecompute) ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0;
+  return ((size_t)LTR<R>::TOTAL + stage) * sizeof(float);
 }
 
 // occ != nullptr: report resident CTAs per SM instead of launching.
 template <typename FT, int BMAX, int R, bool DU>
 static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
-  // radius <= 3: register-history kernel; radius 4: shared-memory plane ring
-  auto k = [] {
-    if constexpr (R <= 3)
-      return k_lncc_rh<FT, BMAX, R, DU>;
-    else
-      return k_lncc<FT, BMAX, R, DU>;
-  }();
+  auto k = k_lncc_rh<FT, BMAX, R, DU>;
   const size_t smem = smem_of<R, DU>();
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  constexpr int nt = R <= 3 ? kLnccRHThreads : kThreads;
+  constexpr int nt = kLnccRHThreads;
   if (occ) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, nt, smem);
   note_launch_begin("k_lncc", s);
   k<<<grid, nt, smem, s>>>(a);
@@ -1209,7 +747,6 @@ static cudaError_t dispatch_lncc(int mode, int ft, int mt, int bmax, const LnccA
     case 1: return dispatch_r<1>(mode, ft, bmax, a, grid, s, occ);
     case 2: return dispatch_r<2>(mode, ft, bmax, a, grid, s, occ);
     case 3: return dispatch_r<3>(mode, ft, bmax, a, grid, s, occ);
-    case 4: return dispatch_r<4>(mode, ft, bmax, a, grid, s, occ);
   }
   return cudaErrorInvalidValue;
 }
@@ -1219,9 +756,9 @@ cudaError_t launch_lncc(int mode, int ft, int mt, int bmax, const LnccArgs& a, i
 }
 
 int lncc_ctas_per_sm(int mode, int ft, int mt, int bmax, int R) {
-  static OccCache<2 * 2 * 3 * 5> cache;
+  static OccCache<2 * 2 * 3 * 4> cache;
   const int bidx = bmax == 0 ? 0 : (bmax == 32 ? 1 : 2);
-  return cache.get(((mode * 2 + ft) * 3 + bidx) * 5 + (R >= 0 && R <= 4 ? R : 0), [&] {
+  return cache.get(((mode * 2 + ft) * 3 + bidx) * 4 + (R >= 0 && R <= 3 ? R : 0), [&] {
     int occ = 0;
     LnccArgs dummy{};
     return dispatch_lncc(mode, ft, mt, bmax, dummy, 0, 0, R, &occ) == cudaSuccess ? occ : 1;

@@ -23,10 +23,12 @@
 //   6. z sums, dJ (+ the MI term from the polynomial cells), then dJ stored
 //      or the sampler backward from the stored slope: du = K^T (g dJ/dq) and
 //      the affine moments, per-CTA fp64 partials.
-// Each window sum adds the terms inside the grid directly (no running sums:
-// no drift over long axes), min(w, extent) loads per channel and output.  A
-// warp's lanes hold 32 consecutive x, so every load is coalesced and the
-// w-fold reuse of an input is served by L1 / L2.
+// The x sums add the terms inside the grid directly (min(w, extent) loads per
+// channel and output, the w-fold reuse of an input served by L1).  The y and z
+// sums run along lines: a thread owns 16 consecutive outputs of a line, sums
+// the first window directly and slides it along the rest, so the drift of the
+// running sum is bounded by 16 steps and each input is loaded about twice.  A
+// warp's lanes hold 32 consecutive x, so every load is coalesced.
 #include "ffdp_internal.h"
 #include "ffdp_lncc.cuh"
 
@@ -80,20 +82,106 @@ __global__ void __launch_bounds__(kWideThreads) k_wide_prod_x(const WideArgs a) 
   }
 }
 
-// passes 2, 4, 5: window sums of C channels ([C][N]) along AXIS
-template <int C, int AXIS>
-__global__ void __launch_bounds__(kWideThreads) k_wide_box(const float* __restrict__ in, float* __restrict__ out,
-                                                           const Geom g, int R) {
+// Runs along y or z: a thread owns kRun consecutive outputs of one grid line
+// along AXIS and slides its window sums along them (one add and one subtract
+// per output after the first full sum), so a y or z pass loads each input
+// about twice instead of w times.  Lanes of a warp hold consecutive x, so every
+// load is coalesced.
+constexpr int kRun = 16;
+
+struct Run {
+  size_t base;    // linear index of the run's first output
+  long long st;   // element stride along the axis
+  int p0, n;      // axis coordinate of the first output, outputs in the run
+  int ext;        // grid extent along the axis
+  int x, y, z;    // coordinates of the first output
+};
+
+// Decodes work item `item` (x fastest) into the run it owns; false past the
+// last run.
+template <int AXIS>
+__device__ __forceinline__ bool run_of(const Geom& g, size_t item, Run& r) {
+  const int W = g.fW, H = g.fH, D = g.fD;
+  r.ext = AXIS == 1 ? H : D;
+  const int nch = (r.ext + kRun - 1) / kRun;
+  r.x = (int)(item % (size_t)W);
+  const size_t rest = item / (size_t)W;
+  int c;
+  if (AXIS == 1) {
+    c = (int)(rest % (size_t)nch);
+    r.z = (int)(rest / (size_t)nch);
+    if (r.z >= D) return false;
+    r.y = c * kRun;
+  } else {
+    r.y = (int)(rest % (size_t)H);
+    c = (int)(rest / (size_t)H);
+    if (c >= nch) return false;
+    r.z = c * kRun;
+  }
+  r.p0 = c * kRun;
+  r.n = min(kRun, r.ext - r.p0);
+  r.st = AXIS == 1 ? (long long)W : (long long)W * H;
+  r.base = ((size_t)r.z * H + r.y) * W + r.x;
+  return true;
+}
+
+template <int AXIS>
+__device__ __forceinline__ size_t runs_total(const Geom& g) {
+  const int ext = AXIS == 1 ? g.fH : g.fD;
+  const size_t nch = (size_t)((ext + kRun - 1) / kRun);
+  return AXIS == 1 ? (size_t)g.fW * nch * g.fD : (size_t)g.fW * g.fH * nch;
+}
+
+// Window sums of C channels ([C][N], channel stride N) over the run's
+// outputs: emit(i, s) receives output i's sums.  The first output's window is
+// summed directly; each next one adds the entering and drops the leaving
+// input (zero padding outside the grid).
+template <int C, class Emit>
+__device__ __forceinline__ void run_sums(const float* __restrict__ in, size_t N, const Run& r, int R, Emit&& emit) {
+  float s[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) s[c] = 0.f;
+  {
+    const int lo = r.p0 - R < 0 ? -r.p0 : -R;
+    const int hi = r.p0 + R > r.ext - 1 ? r.ext - 1 - r.p0 : R;
+    const float* p = in + r.base + (long long)lo * r.st;
+    for (int k = lo; k <= hi; ++k, p += r.st) {
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[c] += __ldg(p + c * N);
+    }
+  }
+  emit(0, s);
+  for (int i = 1; i < r.n; ++i) {
+    const int pin = r.p0 + i + R, pout = r.p0 + i - R - 1;
+    if (pin < r.ext) {
+      const float* p = in + r.base + (long long)(i + R) * r.st;
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[c] += __ldg(p + c * N);
+    }
+    if (pout >= 0) {
+      const float* p = in + r.base + (long long)(i - R - 1) * r.st;
+#pragma unroll
+      for (int c = 0; c < C; ++c) s[c] -= __ldg(p + c * N);
+    }
+    emit(i, s);
+  }
+}
+
+// pass 4: window sums of C channels along x, direct (the w inputs of
+// neighbouring lanes overlap and come from L1)
+template <int C>
+__global__ void __launch_bounds__(kWideThreads) k_wide_box_x(const float* __restrict__ in, float* __restrict__ out,
+                                                             const Geom g, int R) {
   const size_t N = g.N;
   for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
     int lo, hi;
     long long st;
-    axis_window<AXIS>(g, (unsigned)lin, R, lo, hi, st);
+    axis_window<0>(g, (unsigned)lin, R, lo, hi, st);
     float s[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) s[c] = 0.f;
-    const float* p = in + lin + (long long)lo * st;
-    for (int k = lo; k <= hi; ++k, p += st) {
+    const float* p = in + lin + lo;
+    for (int k = lo; k <= hi; ++k, ++p) {
 #pragma unroll
       for (int c = 0; c < C; ++c) s[c] += __ldg(p + c * N);
     }
@@ -102,44 +190,53 @@ __global__ void __launch_bounds__(kWideThreads) k_wide_box(const float* __restri
   }
 }
 
-// pass 3: z sums of the five channels, cc and the three g-terms
+// passes 2, 5: window sums of C channels along y, by runs
+template <int C>
+__global__ void __launch_bounds__(kWideThreads) k_wide_box_y(const float* __restrict__ in, float* __restrict__ out,
+                                                             const Geom g, int R) {
+  const size_t N = g.N, total = runs_total<1>(g);
+  for (size_t item = (size_t)blockIdx.x * kWideThreads + threadIdx.x; item < total;
+       item += (size_t)gridDim.x * kWideThreads) {
+    Run r;
+    if (!run_of<1>(g, item, r)) continue;
+    run_sums<C>(in, N, r, R, [&](int i, const float* s) {
+      const size_t o = r.base + (size_t)i * r.st;
+#pragma unroll
+      for (int c = 0; c < C; ++c) out[c * N + o] = s[c];
+    });
+  }
+}
+
+// pass 3: z sums of the five channels by runs, cc and the three g-terms
 __global__ void __launch_bounds__(kWideThreads) k_wide_cc(const WideArgs a) {
   __shared__ double red[kWideThreads / 32];
   const Geom& g = a.g;
-  const size_t N = g.N;
+  const size_t N = g.N, total = runs_total<2>(g);
   const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
   double cc_d = 0.0;
-  float cc_f = 0.0f;
-  int cnt = 0;
-  for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
-    int lo, hi;
-    long long st;
-    axis_window<2>(g, (unsigned)lin, a.R, lo, hi, st);
-    float s[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-    const float* p = a.bufB + lin + (long long)lo * st;
-    for (int k = lo; k <= hi; ++k, p += st) {
-#pragma unroll
-      for (int c = 0; c < 5; ++c) s[c] += __ldg(p + c * N);
-    }
-    const float SJ = s[0], SF = s[1];
-    const float vJ = fmaxf(fmaf(SJ * SJ, -inv_n, s[2]), 0.0f);
-    const float vF = fmaxf(fmaf(SF * SF, -inv_n, s[3]), 0.0f);
-    const float cross = fmaf(-SJ * SF, inv_n, s[4]);
-    const float rD = rcp_approx(fmaf(vJ, vF, eps));
-    const float A1 = 2.0f * cross * rD;
-    const float cc = cross * cross * rD;
-    const float A2 = cc * vF * rD;
-    a.bufA[lin] = gs * (2.0f * A2 * SJ - A1 * SF) * inv_n;
-    a.bufA[N + lin] = -gs * A2;
-    a.bufA[2 * N + lin] = gs * A1;
-    cc_f += cc;
-    if (++cnt == 64) {
-      cc_d += (double)cc_f;
-      cc_f = 0.0f;
-      cnt = 0;
-    }
+  for (size_t item = (size_t)blockIdx.x * kWideThreads + threadIdx.x; item < total;
+       item += (size_t)gridDim.x * kWideThreads) {
+    Run r;
+    if (!run_of<2>(g, item, r)) continue;
+    float cc_f = 0.0f;  // at most kRun terms, then folded
+    run_sums<5>(a.bufB, N, r, a.R, [&](int i, const float* s) {
+      const size_t o = r.base + (size_t)i * r.st;
+      const float SJ = s[0], SF = s[1];
+      const float vJ = fmaxf(fmaf(SJ * SJ, -inv_n, s[2]), 0.0f);
+      const float vF = fmaxf(fmaf(SF * SF, -inv_n, s[3]), 0.0f);
+      const float cross = fmaf(-SJ * SF, inv_n, s[4]);
+      const float rD = rcp_approx(fmaf(vJ, vF, eps));
+      const float A1 = 2.0f * cross * rD;
+      const float cc = cross * cross * rD;
+      const float A2 = cc * vF * rD;
+      a.bufA[o] = gs * (2.0f * A2 * SJ - A1 * SF) * inv_n;
+      a.bufA[N + o] = -gs * A2;
+      a.bufA[2 * N + o] = gs * A1;
+      cc_f += cc;
+    });
+    cc_d += (double)cc_f;
   }
-  cc_d = warp_sum_d(cc_d + (double)cc_f);
+  cc_d = warp_sum_d(cc_d);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cc_d;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -149,88 +246,74 @@ __global__ void __launch_bounds__(kWideThreads) k_wide_cc(const WideArgs a) {
   }
 }
 
-// pass 6: z sums of the g-terms, dJ, and dJ or the sampler backward
+// pass 6: z sums of the g-terms by runs, dJ, and dJ or the sampler backward
 template <typename FT, int BMAX, bool DU>
 __global__ void __launch_bounds__(kWideThreads) k_wide_fin(const WideArgs a) {
   constexpr bool MI = BMAX != 0;
   __shared__ double red[kWideThreads / 32][12];
   const Geom& g = a.g;
-  const size_t N = g.N;
+  const size_t N = g.N, total = runs_total<2>(g);
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
-  // affine moments: e_r and e_r (i_c - ctr_c), fp32 runs folded into fp64
-  float S[3] = {0.f, 0.f, 0.f}, Mo[3][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
+  // affine moments e_r and e_r (i_c - ctr_c): fp32 over one run, then fp64
   double Sd[3] = {0.0, 0.0, 0.0}, Md[3][3] = {{0.0, 0.0, 0.0}, {0.0, 0.0, 0.0}, {0.0, 0.0, 0.0}};
-  int cnt = 0;
-  auto fold = [&] {
+  for (size_t item = (size_t)blockIdx.x * kWideThreads + threadIdx.x; item < total;
+       item += (size_t)gridDim.x * kWideThreads) {
+    Run r;
+    if (!run_of<2>(g, item, r)) continue;
+    float S[3] = {0.f, 0.f, 0.f}, Mo[3][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
+    const float cx = (float)r.x - g.ctr[0], cy = (float)r.y - g.ctr[1];
+    run_sums<3>(a.bufA, N, r, a.R, [&](int i, const float* s) {
+      const size_t o = r.base + (size_t)i * r.st;
+      const float jv = __ldg(a.J + o), fv = load1(F + o);
+      float gv = fmaf(fv, s[2], fmaf(2.0f * jv, s[1], s[0]));
+      if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
+      if constexpr (!DU) {
+        if (a.dJ) a.dJ[o] = gv;
+      } else {
+        const float e[3] = {gv * __ldg(a.dJdq + 3 * o), gv * __ldg(a.dJdq + 3 * o + 1),
+                            gv * __ldg(a.dJdq + 3 * o + 2)};
+        if (a.du) {
+          const float* K = g.K;
+          float* d = a.du + 3 * o;
+          if (g.k_diag) {
+            d[0] = K[0] * e[0];
+            d[1] = K[4] * e[1];
+            d[2] = K[8] * e[2];
+          } else {
+            d[0] = fmaf(K[0], e[0], fmaf(K[3], e[1], K[6] * e[2]));
+            d[1] = fmaf(K[1], e[0], fmaf(K[4], e[1], K[7] * e[2]));
+            d[2] = fmaf(K[2], e[0], fmaf(K[5], e[1], K[8] * e[2]));
+          }
+        }
+        const float cz = (float)(r.z + i) - g.ctr[2];
 #pragma unroll
-    for (int r = 0; r < 3; ++r) {
-      Sd[r] += (double)S[r];
-      S[r] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        Md[r][c] += (double)Mo[r][c];
-        Mo[r][c] = 0.f;
-      }
-    }
-  };
-  for (size_t lin = (size_t)blockIdx.x * kWideThreads + threadIdx.x; lin < N; lin += (size_t)gridDim.x * kWideThreads) {
-    int ix, iy, iz;
-    lin_to_xyz(g, (unsigned)lin, ix, iy, iz);
-    const int lo = iz - a.R < 0 ? -iz : -a.R;
-    const int hi = iz + a.R > g.fD - 1 ? g.fD - 1 - iz : a.R;
-    const long long st = (long long)g.fW * g.fH;
-    float GJ = 0.f, GJJ = 0.f, GFJ = 0.f;
-    const float* p = a.bufA + lin + (long long)lo * st;
-    for (int k = lo; k <= hi; ++k, p += st) {
-      GJ += __ldg(p);
-      GJJ += __ldg(p + N);
-      GFJ += __ldg(p + 2 * N);
-    }
-    const float jv = __ldg(a.J + lin), fv = load1(F + lin);
-    float gv = fmaf(fv, GFJ, fmaf(2.0f * jv, GJJ, GJ));
-    if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
-    if constexpr (!DU) {
-      if (a.dJ) a.dJ[lin] = gv;
-    } else {
-      const float e[3] = {gv * __ldg(a.dJdq + 3 * lin), gv * __ldg(a.dJdq + 3 * lin + 1),
-                          gv * __ldg(a.dJdq + 3 * lin + 2)};
-      if (a.du) {
-        const float* K = g.K;
-        float* d = a.du + 3 * lin;
-        if (g.k_diag) {
-          d[0] = K[0] * e[0];
-          d[1] = K[4] * e[1];
-          d[2] = K[8] * e[2];
-        } else {
-          d[0] = fmaf(K[0], e[0], fmaf(K[3], e[1], K[6] * e[2]));
-          d[1] = fmaf(K[1], e[0], fmaf(K[4], e[1], K[7] * e[2]));
-          d[2] = fmaf(K[2], e[0], fmaf(K[5], e[1], K[8] * e[2]));
+        for (int q = 0; q < 3; ++q) {
+          S[q] += e[q];
+          Mo[q][2] = fmaf(e[q], cz, Mo[q][2]);
         }
       }
-      const float cx[3] = {(float)ix - g.ctr[0], (float)iy - g.ctr[1], (float)iz - g.ctr[2]};
+    });
+    if constexpr (DU) {
+      // the run's x and y are fixed: their moments follow from the sums
 #pragma unroll
-      for (int r = 0; r < 3; ++r) {
-        S[r] += e[r];
-#pragma unroll
-        for (int c = 0; c < 3; ++c) Mo[r][c] = fmaf(e[r], cx[c], Mo[r][c]);
-      }
-      if (++cnt == 32) {
-        fold();
-        cnt = 0;
+      for (int q = 0; q < 3; ++q) {
+        Sd[q] += (double)S[q];
+        Md[q][0] += (double)(S[q] * cx);
+        Md[q][1] += (double)(S[q] * cy);
+        Md[q][2] += (double)Mo[q][2];
       }
     }
   }
   if constexpr (DU) {
-    fold();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
-    for (int r = 0; r < 3; ++r) {
-      const double s = warp_sum_d(Sd[r]);
-      if (lane == 0) red[wid][kPS + r] = s;
+    for (int q = 0; q < 3; ++q) {
+      const double sv = warp_sum_d(Sd[q]);
+      if (lane == 0) red[wid][kPS + q] = sv;
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
-        const double m = warp_sum_d(Md[r][c]);
-        if (lane == 0) red[wid][kPM + 3 * r + c] = m;
+        const double m = warp_sum_d(Md[q][c]);
+        if (lane == 0) red[wid][kPM + 3 * q + c] = m;
       }
     }
     __syncthreads();
@@ -251,16 +334,16 @@ cudaError_t run_wide(const WideArgs& a, int grid, cudaStream_t s) {
   k_wide_prod_x<FT><<<grid, kWideThreads, 0, s>>>(a);
   note_launch_end(s);
   note_launch_begin("k_wide_box", s);
-  k_wide_box<5, 1><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
+  k_wide_box_y<5><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
   note_launch_end(s);
   note_launch_begin("k_wide_cc", s);
   k_wide_cc<<<grid, kWideThreads, 0, s>>>(a);
   note_launch_end(s);
   note_launch_begin("k_wide_box", s);
-  k_wide_box<3, 0><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
+  k_wide_box_x<3><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
   note_launch_end(s);
   note_launch_begin("k_wide_box", s);
-  k_wide_box<3, 1><<<grid, kWideThreads, 0, s>>>(a.bufB, a.bufA, g, a.R);
+  k_wide_box_y<3><<<grid, kWideThreads, 0, s>>>(a.bufB, a.bufA, g, a.R);
   note_launch_end(s);
   note_launch_begin("k_wide_fin", s);
   k_wide_fin<FT, BMAX, DU><<<grid, kWideThreads, 0, s>>>(a);
