@@ -1,4 +1,4 @@
-// k_lncc_wide.cu -- LNCC for windows wider than the tiled kernels keep on chip
+// k_lncc_wide.cu -- LNCC for windows wider than the tiled kernel keeps on chip
 // (w > kLnccTiledMaxWindow).
 //
 // Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
@@ -12,7 +12,7 @@
 //   dJ_m = sum_{k in window(m)} g_J(k) + 2 J_m g_JJ(k) + F_m g_FJ(k).
 //
 // A window of w^3 voxels with a 2R halo around a 32-wide tile no longer fits
-// the register history or the plane ring of the tiled kernels, so the window
+// the register history of the tiled kernel, so the window
 // sums run as separable box sums, one grid-stride pass per axis, through two
 // [5][N] float buffers A and B of the workspace:
 //   1. x sums of J, F, J^2, F^2, FJ                     J, F -> A[0..4]
