@@ -180,6 +180,28 @@ def oracle_sample(pair, ds, threads=None):
     return F.size, dt, oracle.max_threads()
 
 
+def _cpu_small(dev):
+    """The oracle on the two small workloads in full (64^3 MI 32 + LNCC 5; 160x192x224
+    MI 32), on one thread and on every host thread: context for the CPU baseline."""
+    import oracle
+    from voxel_grid_sampler_gb300 import synth
+    cores = len(os.sched_getaffinity(0))
+    res = {}
+    try:
+        for k in (1, 2):
+            pair = synth.make_pair(k, device=dev)
+            name = pair.workload.name
+            r = {}
+            for th in (1, cores):
+                n, t, used = oracle_sample(pair, pair.F.shape[0], threads=th)
+                r["threads_%d" % used] = {"value": n / t / 1e9, "unit": UNIT, "s": t}
+            res[name] = r
+            del pair
+    finally:
+        oracle.set_threads(cores)
+    return res
+
+
 def _sample_planes(pair, budget_s=12.0):
     """Planes of the bounded CPU sample: ~budget_s seconds of oracle work."""
     import oracle
@@ -537,6 +559,8 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
         out["cpu_baseline"] = {"value": n / t / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": "oracle objective on fixed planes z<%d of the %s pair "
                                          "(%d voxels, %.1f s)" % (ds, "x".join(map(str, F.shape)), n, t)}
+        if not args.shape:
+            out["cpu_small"] = _cpu_small(F.device)
     return out
 
 
