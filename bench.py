@@ -50,9 +50,19 @@ SINGLE_PASS_BYTES = {4: 4 + 4 + 12 + 12, 5: 2 + 2 + 12 + 12}
 KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc": 4 + 4 + 12 + 12},
                 5: {"k_sweep1": 2 + 12 + 2, "k_sweep2": 2 + 12 + 2 + 12}}
 KERNEL_BYTES_STORED = {5: {"k_sweep1": 2 + 12 + 2 + 4 + 12, "k_sweep2": 2 + 4 + 12 + 12}}
+# LNCC windows above 7 (--window): separable passes through two [5][N]
+# buffers instead of k_lncc -- x sums of the products (J, F read, 5 sums
+# written), y sums (5 + 5), z sums with cc and the g-terms (5 + 3), x and y
+# sums of the g-terms (3 + 3 each), z sums with dL/dJ and the sampler backward
+# (3 sums, F, J, dJ/dq read, du written)
+KERNEL_BYTES_WIDE = {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_wide_prod_x": 4 + 4 + 20, "k_wide_y": 20 + 20,
+                     "k_wide_cc": 20 + 12, "k_wide_gx": 12 + 12, "k_wide_gy": 12 + 12,
+                     "k_wide_fin": 12 + 4 + 4 + 12 + 12}
 
 
 def _kernel_bytes(args, wl):
+    if wl.w_lncc != 0.0 and _window(args, wl) > 7:
+        return KERNEL_BYTES_WIDE
     if wl.w_lncc == 0.0 and args.store_slope and args.workload in KERNEL_BYTES_STORED:
         return KERNEL_BYTES_STORED[args.workload]
     return KERNEL_BYTES[args.workload]
@@ -158,7 +168,12 @@ def _crop_transform(pair, ds):
     return xmax
 
 
-def oracle_sample(pair, ds, threads=None):
+def _window(args, wl):
+    """LNCC window of the run: the workload's, or --window."""
+    return args.window if getattr(args, "window", 0) else wl.window
+
+
+def oracle_sample(pair, ds, threads=None, window=None):
     """Time the CPU oracle on the first ds planes of the workload (one fwd+bwd)."""
     import oracle
     wl = pair.workload
@@ -170,7 +185,8 @@ def oracle_sample(pair, ds, threads=None):
     xmax = _crop_transform(pair, ds)
     T = oracle.Transform(pair.A.astype(np.float64), pair.t.astype(np.float64), pair.S.astype(np.float64),
                          pair.xmin.astype(np.float64), xmax.astype(np.float32).astype(np.float64))
-    P = oracle.ObjectiveParams(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    P = oracle.ObjectiveParams(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, window or wl.window,
+                               wl.eps)
     t0 = time.perf_counter()
     if wl.w_lncc != 0.0:
         oracle.objective(F, M, u, T, P)
@@ -202,10 +218,10 @@ def _cpu_small(dev):
     return res
 
 
-def _sample_planes(pair, budget_s=12.0):
+def _sample_planes(pair, budget_s=12.0, window=None):
     """Planes of the bounded CPU sample: ~budget_s seconds of oracle work."""
     import oracle
-    n1, t1, _ = oracle_sample(pair, 2)
+    n1, t1, _ = oracle_sample(pair, 2, window=window)
     per_plane = t1 / 2.0
     ds = int(max(2, min(pair.F.shape[0], budget_s / max(per_plane, 1e-3))))
     return ds
@@ -220,13 +236,14 @@ def run_reference(args, ws, rank, local):
     pair.F, pair.M, pair.u = pair.F.cpu(), pair.M.cpu(), pair.u.cpu()
     # each step a bounded sample so that warm-up + timed steps end within ~3 minutes
     budget = min(args.ref_step_s, 150.0 / max(1, args.steps + args.warmup))
-    ds = _sample_planes(pair, budget_s=budget)
+    win = _window(args, pair.workload)
+    ds = _sample_planes(pair, budget_s=budget, window=win)
     for _ in range(args.warmup):
-        oracle_sample(pair, ds)
+        oracle_sample(pair, ds, window=win)
     times = []
     cores = 1
     for _ in range(args.steps):
-        n, t, cores = oracle_sample(pair, ds)
+        n, t, cores = oracle_sample(pair, ds, window=win)
         times.append(t)
     t = sum(times) / len(times)
     value = n / t / 1e9
@@ -235,7 +252,7 @@ def run_reference(args, ws, rank, local):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "shape": list(pair.F.shape), "sample_planes": ds},
+        "config": {"workload": wl.name, "shape": list(pair.F.shape), "lncc_window": win, "sample_planes": ds},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "oracle objective on fixed planes z<%d of the %s pair (%d voxels)"
                                    % (ds, "x".join(map(str, pair.F.shape)), n)},
@@ -332,7 +349,7 @@ def run_gpu(args, ws, rank, local):
     F, M, u = pair.F, pair.M, pair.u
     N = F.numel()
     T = ffdp.transform(pair.A, pair.t, pair.S, pair.xmin, pair.xmax)
-    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, wl.window, wl.eps)
+    P = ffdp.objective_params(wl.w_mi, wl.w_lncc, wl.bins, pair.f_range, pair.m_range, _window(args, wl), wl.eps)
     stored = bool(args.store_slope)  # ffdp_objective_stored (MI only: J and slope kept) or ffdp_objective
     wsbuf = ffdp.workspace(_ws_op(stored), F.shape, P, dev)
     loss = torch.empty(3, device=dev)
@@ -379,7 +396,8 @@ def run_gpu(args, ws, rank, local):
         ms_e2e, h2d, d2h = _e2e(args, F, M, u, T, P, loss, du, dA, dt, wsbuf, stream, dev, ws, stored)
     out = _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e, h2d, d2h, alt)
     # ---- the gigavoxel workload, timed the same way, on the same line
-    if out is not None and args.workload == 4 and not args.shape and not args.no_workload5 and ws == 1:
+    if (out is not None and args.workload == 4 and not args.shape and not args.window and not args.no_workload5
+            and ws == 1):
         del pair, F, M, u, wsbuf, du, step
         torch.cuda.empty_cache()
         out["workload5"] = _workload5(args, dev, stream)
@@ -530,7 +548,7 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32" if wl.dtype == "f32" else "f32 (f16 storage)",
         "data": "synthetic",
-        "config": {"workload": wl.name, "shape": list(F.shape), "voxels": N,
+        "config": {"workload": wl.name, "shape": list(F.shape), "voxels": N, "lncc_window": _window(args, wl),
                    "l2": "inputs larger than L2 (%.2f GB algorithmic bytes per step)"
                          % (ALGO_BYTES[args.workload] * N / 1e9),
                    "parallelism": "independent pair per rank" if ws > 1 else "single GPU",
@@ -554,12 +572,12 @@ def _rest(args, ws, rank, pair, wl, F, N, ms, kern, launches, clk, loss, ms_e2e,
         "loss": [float(x) for x in loss.tolist()],
     }
     if ws == 1 and not args.no_cpu_baseline:
-        ds = _sample_planes(pair, budget_s=args.cpu_budget_s)
-        n, t, cores = oracle_sample(pair, ds)
+        ds = _sample_planes(pair, budget_s=args.cpu_budget_s, window=_window(args, wl))
+        n, t, cores = oracle_sample(pair, ds, window=_window(args, wl))
         out["cpu_baseline"] = {"value": n / t / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": "oracle objective on fixed planes z<%d of the %s pair "
                                          "(%d voxels, %.1f s)" % (ds, "x".join(map(str, F.shape)), n, t)}
-        if not args.shape:
+        if not args.shape and not args.window:
             out["cpu_small"] = _cpu_small(F.device)
     return out
 
@@ -747,6 +765,8 @@ def main():
     ap.add_argument("--no-workload5", action="store_true",
                     help="skip the 1024^3 leg that the default workload-4 line carries")
     ap.add_argument("--shape", type=int, default=0, help="cube edge overriding the workload size (profiling)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="LNCC window overriding the workload's (odd >= 3; above 7 the separable passes run)")
     ap.add_argument("--store-slope", type=int, default=1, choices=[0, 1],
                     help="MI-only objectives: store J and dJ/dp (1) or stay implicit (0)")
     ap.add_argument("--path", default="objective", choices=["objective", "mse", "compose", "adam"],

@@ -250,12 +250,16 @@ __global__ void __launch_bounds__(kWideThreads) k_wide_cc(const WideArgs a) {
 template <typename FT, int BMAX, bool DU>
 __global__ void __launch_bounds__(kWideThreads) k_wide_fin(const WideArgs a) {
   constexpr bool MI = BMAX != 0;
-  __shared__ double red[kWideThreads / 32][12];
+  // affine moments e_r and e_r (i_c - ctr_c): fp32 over one run, then added
+  // to the thread's fp64 slots here (slot kPS + r, kPM + 3 r + c), which keeps
+  // them out of the registers of the run loop
+  __shared__ double acc[DU ? 12 : 1][kWideThreads];
   const Geom& g = a.g;
   const size_t N = g.N, total = runs_total<2>(g);
   const FT* __restrict__ F = static_cast<const FT*>(a.F);
-  // affine moments e_r and e_r (i_c - ctr_c): fp32 over one run, then fp64
-  double Sd[3] = {0.0, 0.0, 0.0}, Md[3][3] = {{0.0, 0.0, 0.0}, {0.0, 0.0, 0.0}, {0.0, 0.0, 0.0}};
+  const int tid = threadIdx.x;
+  if constexpr (DU)
+    for (int c = 0; c < 12; ++c) acc[c][tid] = 0.0;
   for (size_t item = (size_t)blockIdx.x * kWideThreads + threadIdx.x; item < total;
        item += (size_t)gridDim.x * kWideThreads) {
     Run r;
@@ -297,30 +301,22 @@ __global__ void __launch_bounds__(kWideThreads) k_wide_fin(const WideArgs a) {
       // the run's x and y are fixed: their moments follow from the sums
 #pragma unroll
       for (int q = 0; q < 3; ++q) {
-        Sd[q] += (double)S[q];
-        Md[q][0] += (double)(S[q] * cx);
-        Md[q][1] += (double)(S[q] * cy);
-        Md[q][2] += (double)Mo[q][2];
+        acc[kPS + q][tid] += (double)S[q];
+        acc[kPM + 3 * q][tid] += (double)(S[q] * cx);
+        acc[kPM + 3 * q + 1][tid] += (double)(S[q] * cy);
+        acc[kPM + 3 * q + 2][tid] += (double)Mo[q][2];
       }
     }
   }
   if constexpr (DU) {
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-#pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      const double sv = warp_sum_d(Sd[q]);
-      if (lane == 0) red[wid][kPS + q] = sv;
-#pragma unroll
-      for (int c = 0; c < 3; ++c) {
-        const double m = warp_sum_d(Md[q][c]);
-        if (lane == 0) red[wid][kPM + 3 * q + c] = m;
-      }
-    }
+    // each warp sums a slot over the CTA's threads (warp w takes slots w, w + 8)
     __syncthreads();
-    if (threadIdx.x < 12) {
+    const int lane = tid & 31, wid = tid >> 5;
+    for (int c = wid; c < 12; c += kWideThreads / 32) {
       double t = 0.0;
-      for (int w = 0; w < kWideThreads / 32; ++w) t += red[w][threadIdx.x];
-      a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = t;
+      for (int k = lane; k < kWideThreads; k += 32) t += acc[c][k];
+      t = warp_sum_d(t);
+      if (lane == 0) a.partials[(size_t)blockIdx.x * kPartialStride + c] = t;
     }
   }
 }
@@ -333,16 +329,16 @@ cudaError_t run_wide(const WideArgs& a, int grid, cudaStream_t s) {
   note_launch_begin("k_wide_prod_x", s);
   k_wide_prod_x<FT><<<grid, kWideThreads, 0, s>>>(a);
   note_launch_end(s);
-  note_launch_begin("k_wide_box", s);
+  note_launch_begin("k_wide_y", s);
   k_wide_box_y<5><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
   note_launch_end(s);
   note_launch_begin("k_wide_cc", s);
   k_wide_cc<<<grid, kWideThreads, 0, s>>>(a);
   note_launch_end(s);
-  note_launch_begin("k_wide_box", s);
+  note_launch_begin("k_wide_gx", s);
   k_wide_box_x<3><<<grid, kWideThreads, 0, s>>>(a.bufA, a.bufB, g, a.R);
   note_launch_end(s);
-  note_launch_begin("k_wide_box", s);
+  note_launch_begin("k_wide_gy", s);
   k_wide_box_y<3><<<grid, kWideThreads, 0, s>>>(a.bufB, a.bufA, g, a.R);
   note_launch_end(s);
   note_launch_begin("k_wide_fin", s);

@@ -11,7 +11,6 @@ from __future__ import annotations
 
 import ctypes
 import os
-from dataclasses import dataclass
 
 import numpy as np
 import torch
@@ -442,15 +441,6 @@ def timing_read(max_kernels: int = 32) -> dict:
         nm = names.raw[64 * k:64 * k + 64].split(b"\0", 1)[0].decode()
         out[nm] = (int(counts[k]), float(ms[k]))
     return out
-
-
-@dataclass
-class Declared:
-    """Entry points declared in include/ffdp.h (for the symbol check)."""
-    names: tuple = ("ffdp_workspace_bytes", "ffdp_grid_sample_fwd", "ffdp_grid_sample_bwd",
-                    "ffdp_mi_fwd_bwd", "ffdp_lncc_fwd_bwd", "ffdp_objective", "ffdp_status_string",
-                    "ffdp_last_error", "ffdp_launch_count", "ffdp_timing_enable", "ffdp_timing_read",
-                    "ffdp_device_error", "ffdp_test_ring_stall")
 
 
 def ffdp_objective_mi_static(F, M, u, T: ffdp_transform, params: ffdp_objective_params, loss, du, dA, dt,
