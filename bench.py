@@ -42,12 +42,16 @@ ALGO_BYTES = {4: 2 * (4 + 12 + 4) + 12, 5: 2 * (2 + 12 + 2) + 12}
 SINGLE_PASS_BYTES = {4: 4 + 4 + 12 + 12, 5: 2 + 2 + 12 + 12}
 # Algorithmic bytes per voxel of each kernel of the objective:
 #   k_sweep1  F + u + M read (+ J and dJ/dq written when LNCC is on)
-#   k_lncc    F + J + dJ/dq read, du written (window sums, dL/dJ and the
-#             sampler backward in one kernel)
+#   k_lncc_fw J + F read, the three g-terms written (forward window sums, cc)
+#   k_lncc_bw g-terms + J + F + dJ/dq read, du written (backward window sums,
+#             dL/dJ with the MI term, the sampler backward)
+#   k_lncc    (the fused kernel of the FFDP_LNCC_FUSED build) F + J + dJ/dq
+#             read, du written
 #   k_sweep2  MI: F + u + M read, du written
 #   (MI-only with stored J and slope: k_sweep1 also writes J + dJ/dq; k_sweep2
 #   reads F + J + dJ/dq and writes du)
-KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc": 4 + 4 + 12 + 12},
+KERNEL_BYTES = {4: {"k_sweep1": 4 + 12 + 4 + 4 + 12, "k_lncc_fw": 4 + 4 + 12, "k_lncc_bw": 12 + 4 + 4 + 12 + 12,
+                    "k_lncc": 4 + 4 + 12 + 12},
                 5: {"k_sweep1": 2 + 12 + 2, "k_sweep2": 2 + 12 + 2 + 12}}
 KERNEL_BYTES_STORED = {5: {"k_sweep1": 2 + 12 + 2 + 4 + 12, "k_sweep2": 2 + 4 + 12 + 12}}
 # LNCC windows above 7 (--window): separable passes through two [5][N]

@@ -123,8 +123,10 @@ enum {
  * independent of the volume size.  An objective with LNCC enabled also holds
  * the warped image J and its slope dJ/dp (16 bytes per voxel): the window
  * sums read their halo instead of re-sampling it and the sampler backward,
- * done in the window kernel's epilogue, reads the slope instead of gathering
- * M again; the paper's fused LNCC keeps five such intermediates.  An MI-only
+ * done in the backward window kernel, reads the slope instead of gathering M
+ * again; the paper's fused LNCC keeps five such intermediates.  LNCC windows
+ * up to 7 (the LNCC op and the objective) also hold the three g-terms the
+ * forward window kernel hands to the backward one (12 bytes per voxel).  An MI-only
  * objective through ffdp_objective_stored holds the same two buffers.  An LNCC window
  * above 7 (the LNCC op or an objective with LNCC) adds 40 bytes per voxel
  * for the separable window-sum passes.  Queries the current device's SM

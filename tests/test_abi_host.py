@@ -139,20 +139,23 @@ def test_stored_objective_workspace(lib):
 
 
 def test_wide_lncc_windows_take_two_five_channel_buffers(lib):
-    # windows above 7 run as separable box-sum passes through two [5][N]
-    # float buffers (40 bytes per voxel); any odd window >= 3 is accepted
+    # windows up to 7 run as the forward / backward window-kernel pair, which
+    # hands the three g-terms over in the workspace (12 bytes per voxel);
+    # wider ones as separable box-sum passes through two [5][N] float buffers
+    # (40 bytes per voxel); any odd window >= 3 is accepted
     from voxel_grid_sampler_gb300 import ffdp
     dims = (20, 30, 40)
     N = 20 * 30 * 40
     tiled = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(7))
+    assert 12 * N <= tiled < 12 * N + (1 << 20)
     for w in (9, 11, 13, 61, 1001):
         wide = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_LNCC, dims, ffdp.lncc_params(w))
-        assert wide - tiled >= 40 * N and wide - tiled < 40 * N + 1024
+        assert wide - tiled >= 28 * N and wide - tiled < 28 * N + 1024
     q7 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 7)
     q9 = ffdp.objective_params(1.0, 1.0, 64, (0, 1), (0, 1), 9)
     o7 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q7)
     o9 = ffdp.ffdp_workspace_bytes(ffdp.FFDP_OP_OBJECTIVE, dims, q9)
-    assert o9 - o7 >= 40 * N and o9 - o7 < 40 * N + 1024
+    assert o9 - o7 >= 28 * N and o9 - o7 < 28 * N + 1024
 
 
 @nogpu

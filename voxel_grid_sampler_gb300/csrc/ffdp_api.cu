@@ -296,11 +296,15 @@ int bmax_of(int bins) { return bins <= 32 ? 32 : 64; }
 
 // Workspace layout (byte offsets, 256-aligned).
 struct Ws {
-  size_t hist, table, table2, scalars, partials, J, DG, WA, WB, total;
+  size_t hist, table, table2, scalars, partials, J, DG, WA, WB, GS, total;
 };
 
 // The LNCC window runs through the wide-window passes (two [5][N] buffers).
 bool lncc_wide(int window) { return window > kLnccTiledMaxWindow; }
+
+// The tiled LNCC runs as the forward / backward kernel pair, with the g-terms
+// ([3][N]) in the workspace.
+bool lncc_split(int window) { return kLnccSplit && !kLnccRecompute && !lncc_wide(window); }
 
 // Window radius of the wide-window passes: a radius at or beyond the largest
 // grid extent sums the same (clipped) terms, so it is capped there; the
@@ -318,7 +322,8 @@ size_t al(size_t x) { return (x + 255) & ~(size_t)255; }
 bool lncc_recompute(int window) { return kLnccRecompute && window <= 7; }
 
 // ln: LNCC on; store: J and dJ/dq per voxel.
-Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N, bool wide = false) {
+Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t N, bool wide = false,
+             bool split = false) {
   const bool needJ = store;
   Ws w;
   size_t o = 0;
@@ -341,6 +346,8 @@ Ws ws_layout(bool mi, int bmax, size_t max_parts, bool ln, bool store, uint64_t 
   if (wide) o = al(o + (size_t)N * 5 * sizeof(float));
   w.WB = o;
   if (wide) o = al(o + (size_t)N * 5 * sizeof(float));
+  w.GS = o;  // split LNCC: the g-terms, [3][N]
+  if (split) o = al(o + (size_t)N * 3 * sizeof(float));
   w.total = o;
   return w;
 }
@@ -416,7 +423,7 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
     case FFDP_OP_LNCC: {
       const ffdp_lncc_params* p = static_cast<const ffdp_lncc_params*>(params);
       if (check_lncc(p) != FFDP_OK) return 0;
-      return ws_layout(false, 32, max_parts(), false, false, N, lncc_wide(p->window)).total;
+      return ws_layout(false, 32, max_parts(), false, false, N, lncc_wide(p->window), lncc_split(p->window)).total;
     }
     case FFDP_OP_OBJECTIVE:
     case FFDP_OP_OBJECTIVE_STORED: {
@@ -428,7 +435,7 @@ extern "C" size_t ffdp_workspace_bytes(int op, ffdp_dims fixed, const void* para
       const bool store_slope = op == FFDP_OP_OBJECTIVE_STORED;
       return ws_layout(mi, mi ? bmax_of(p->mi.bins) : 32, max_parts(), ln,
                        (ln && !lncc_recompute(p->lncc.window)) || (mi && !ln && store_slope), N,
-                       ln && lncc_wide(p->lncc.window)).total;
+                       ln && lncc_wide(p->lncc.window), ln && lncc_split(p->lncc.window)).total;
     }
     case FFDP_OP_SAMPLE_CHANNELS_BWD:
     case FFDP_OP_MSE:
@@ -581,7 +588,7 @@ extern "C" ffdp_status ffdp_lncc_fwd_bwd(const void* F, ffdp_dtype ft, const flo
   if (!aligned16(F) || !aligned16(J) || (dJ && !aligned16(dJ)))
     return fail(FFDP_ERR_INVALID_ARGUMENT, "F, J and dJ must be 16-byte aligned");
   const bool wide = lncc_wide(p->window);
-  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims), wide);
+  const Ws w = ws_layout(false, 32, max_parts(), false, false, nvox(dims), wide, lncc_split(p->window));
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -615,6 +622,7 @@ extern "C" ffdp_status ffdp_lncc_fwd_bwd(const void* F, ffdp_dtype ft, const flo
   a.F = F;
   a.J = J;
   a.dJ = dJ;
+  a.gbuf = reinterpret_cast<float*>(wb + w.GS);
   a.partials = reinterpret_cast<double*>(wb + w.partials);
   a.R = (p->window - 1) / 2;
   a.eps = p->eps;
@@ -663,7 +671,7 @@ ffdp_status objective(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void*
   const bool rc = ln && lncc_recompute(p->lncc.window);  // LNCC samples J on chip
   const bool store = (ln && !rc) || (mi && !ln && store_slope);
   const bool wide = ln && lncc_wide(p->lncc.window);
-  const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N, wide);
+  const Ws w = ws_layout(mi, bmax, max_parts(), ln, store, N, wide, ln && lncc_split(p->lncc.window));
   FFDP_TRY(check_ws(ws, ws_bytes, w.total));
   char* wb = static_cast<char*>(ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -746,6 +754,7 @@ ffdp_status objective(const void* F, ffdp_dtype ft, ffdp_dims fdims, const void*
     a.M = M;
     a.u = u;
     a.du = du;
+    a.gbuf = reinterpret_cast<float*>(wb + w.GS);
     a.T = bmax == 64 ? table2 : table;  // polynomial cells
     a.partials = partials;
     a.bf = bf;

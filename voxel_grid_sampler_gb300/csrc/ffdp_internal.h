@@ -39,6 +39,20 @@ __host__ __device__ constexpr int sweep2_threads(int mode) {
 constexpr int kSweep2Modes = 6;
 enum LnccMode { LN_DJ = 0, LN_DU = 1 };  // write dL/dJ; or du and affine partials from the stored slope
 
+// LNCC window sums (windows up to 7) as two kernels: a forward one that stores
+// the three g-terms per voxel (12 B/voxel of workspace) and a backward one
+// that sums them over the window and runs the epilogue.  FFDP_LNCC_FUSED
+// builds the single fused register-history kernel instead (the halo-recompute
+// build always uses it).
+#ifdef FFDP_LNCC_FUSED
+constexpr bool kLnccSplit = false;
+#else
+constexpr bool kLnccSplit = true;
+#endif
+#ifndef FFDP_LNCC_SPLIT_MINB
+#define FFDP_LNCC_SPLIT_MINB 3
+#endif
+
 // Compile-time variant of the LNCC objective path (FFDP_LNCC_RECOMPUTE): the
 // window kernel samples J (and, at its output voxels, the slope dJ/dq) from M
 // and u on chip instead of reading the J and slope that the histogram sweep
@@ -105,6 +119,7 @@ struct LnccArgs {
   const float* u;     //                                and the displacement (NULL: 0)
   float* du;          // LN_DU: [N][3] or NULL (affine partials only)
   float* dJ;          // LN_DJ: [N] dL/dJ or NULL
+  float* gbuf;        // split variant: [3][N] g-terms written by the forward kernel
   const float* T;
   double* partials;
   Geom g;          // fixed-grid extents always valid; K and ctr for LN_DU

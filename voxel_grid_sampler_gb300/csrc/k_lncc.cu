@@ -1,7 +1,7 @@
-// k_lncc.cu -- fused LNCC forward + backward for windows up to 7 on a
-// materialised warped image J: writes g = dL/dJ per voxel (stand-alone LNCC)
-// or, in the objective, adds the MI partial gradient and runs the sampler
-// backward (du and the affine partials) from the stored slope in its epilogue.
+// k_lncc.cu -- LNCC forward + backward for windows up to 7 on a materialised
+// warped image J: writes g = dL/dJ per voxel (stand-alone LNCC) or, in the
+// objective, adds the MI partial gradient and runs the sampler backward (du
+// and the affine partials) from the stored slope.
 // Wider windows run as separable passes (k_lncc_wide.cu).
 //
 // Paper: "A Scalable Distributed Framework for Multimodal GigaVoxel Image
@@ -14,13 +14,20 @@
 //   s = -w_lncc / N:  g_FJ = s A1,  g_JJ = -s A2,  g_J = s (2 A2 S_J - A1 S_F) / n,
 //   dJ_m = sum_{k in window(m)} g_J(k) + 2 J_m g_JJ(k) + F_m g_FJ(k).
 //
-// Work layout (k_lncc_rh, below).  A CTA owns a 32 x TY column of output
-// voxels and streams a z segment of planes; each thread keeps the (J, F) of
-// its staged positions of the 2R-halo plane for the last w planes in
-// registers, so the z window sums need no shared memory and shared memory
-// carries only the x and y passes.  The five window sums run on packed fp32
-// pairs ((S_J, S_F), (S_JJ, S_FF)) plus S_FJ.  CTAs are persistent over
-// tiles, so the per-CTA partial records stay O(#SMs).
+// Work layout.  A CTA owns a 32 x TY column of output voxels and streams a z
+// segment of planes; each thread keeps the values of its staged positions of
+// the halo plane for the last w planes in registers, so the z window sums
+// need no shared memory and shared memory carries only the x and y passes.
+// The five window sums run on packed fp32 pairs ((S_J, S_F), (S_JJ, S_FF))
+// plus S_FJ.  CTAs are persistent over tiles, so the per-CTA partial records
+// stay O(#SMs).  Two forms:
+//   * split (the default): k_lncc_fw computes the window sums, cc and the
+//     three g-terms at the tile's own outputs (an R halo) and stores the
+//     g-terms; k_lncc_bw sums them over the window (an R halo again) and runs
+//     the epilogue.  Each kernel holds about half the state of the fused one
+//     (80 registers, three CTAs per SM) and has two barriers per plane.
+//   * fused (FFDP_LNCC_FUSED, and the halo-recompute build): k_lncc_rh does
+//     both halves per plane on a 2R halo, the g-terms never leaving the chip.
 #include <type_traits>
 
 #include "ffdp_internal.h"
@@ -148,6 +155,52 @@ struct LnccSegs {
     return true;
   }
 };
+
+// Plane-synchronous work order: in full rounds every CTA takes one whole tile
+// column (all planes), so neighbouring tiles pass the same planes at about the
+// same time and read each other's halo rows from L2; the columns left over
+// after the last full round are shared as equal runs of (column, plane) pairs.
+struct LnccSegsSync {
+  long long u, end;
+  int D, tilesX, G, b, r, rounds;
+  __device__ explicit LnccSegsSync(const LnccArgs& a) : D(a.g.fD), tilesX(a.tilesX) {
+    const int ncols = a.tilesX * a.tilesY;
+    G = gridDim.x;
+    b = blockIdx.x;
+    rounds = ncols / G;
+    r = 0;
+    const long long rem = (long long)(ncols - rounds * G) * D;
+    const long long per = (rem + G - 1) / G;
+    const long long base = (long long)rounds * G * D;
+    u = base + (long long)b * per;
+    end = min(base + rem, u + per);
+  }
+  __device__ bool next(int& tx, int& ty, int& z0, int& z1) {
+    if (r < rounds) {
+      const int col = r * G + b;
+      ++r;
+      tx = col % tilesX;
+      ty = col / tilesX;
+      z0 = 0;
+      z1 = D;
+      return true;
+    }
+    if (u >= end) return false;
+    const long long col = u / D;
+    z0 = (int)(u - col * D);
+    z1 = (int)min((long long)D, z0 + (end - u));
+    tx = (int)(col % tilesX);
+    ty = (int)(col / tilesX);
+    u += z1 - z0;
+    return true;
+  }
+};
+// The split forward kernel takes the plane-synchronous order (its halo reads
+// then come from L2: 1.14 -> 1.12 ms at 512^3); the backward kernel keeps the
+// equal runs (plane-synchronous, its sampler-backward epilogue slowed from
+// 1.72 to 2.35 ms, as in the fused kernel).
+using SegsFw = LnccSegsSync;
+using SegsBw = LnccSegs;
 
 // Sampler backward in the window kernel's epilogue (LN_DU), from the slope
 // dJ/dq that the sampling sweep stored: per voxel e = g dJ/dq with g = dL/dJ,
@@ -701,6 +754,501 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_MINB) k_lncc_rh(cons
   }
 }
 
+// ---------------------------------------------------------- split variant
+// The same mathematics in two kernels, so that each holds half the state:
+//   forward (k_lncc_fw): the five window sums at the tile's own outputs only
+//     (an R halo instead of 2R), cc and the three g-terms, stored per voxel
+//     ([3][N], 12 B/voxel of workspace);
+//   backward (k_lncc_bw): the window sums of the stored g-terms at the tile's
+//     outputs (again an R halo), dL/dJ with the MI term, then dL/dJ stored or
+//     the sampler backward from the stored slope.
+// Each has two barriers per plane, and in both the thread that owns an output
+// does its y sums itself (no work items in that pass).
+template <int R>
+struct LTS {
+  static constexpr int W = 2 * R + 1;
+  static constexpr int TY = lncc_ty(R);
+  static constexpr int HW = kTX + 2 * R;  // R-halo plane: HH rows of HW columns
+  static constexpr int HH = TY + 2 * R;
+  static constexpr int NOUT = TY * kTX / kLnccRHThreads;
+  static constexpr int NCORE = TY * kTX;
+  static constexpr int NHALO = HH * HW - NCORE;
+  static constexpr int NEXTRA = (NHALO + kLnccRHThreads - 1) / kLnccRHThreads;
+  static constexpr int NSTG = NOUT + NEXTRA;
+  static constexpr int XG = kTX / 2;  // 2-output x items per row
+  static_assert(NOUT * kLnccRHThreads == NCORE, "outputs per thread");
+  // row stride of the halo plane in the x pass: a row continues the bank
+  // sequence of the previous one for the 16-byte pair loads and the 8-byte
+  // scalar-pair loads (as in the register-history kernel)
+  static constexpr int zs_of(int s) { return (s % 2 == 0 && ((s / 2 - XG) % 16 + 16) % 16 == 0) ? s : zs_of(s + 1); }
+  static constexpr int ZS = zs_of(HW);
+  // forward: z sums (5 channels) on the halo plane, x sums (5) on HH x 32
+  static constexpr int FW_Z = HH * ZS * 5;
+  static constexpr int FW_TOTAL = FW_Z + HH * kTX * 5;
+  // backward: g-terms (3 channels) on the halo plane, x sums (3) on HH x 32
+  static constexpr int BW_G = HH * ZS * 3;
+  static constexpr int BW_TOTAL = BW_G + HH * kTX * 3;
+};
+
+// Halo position h (outside the output core) of the R-halo plane: the top and
+// bottom R rows in full, then the R columns on either side of the core rows.
+template <int R>
+__device__ __forceinline__ void halo_pos_r(int h, int& row, int& col) {
+  using S = LTS<R>;
+  constexpr int STRIP = R * S::HW;
+  if (h < STRIP) {
+    row = h / S::HW;
+    col = h - row * S::HW;
+  } else if (h < 2 * STRIP) {
+    h -= STRIP;
+    row = R + S::TY + h / S::HW;
+    col = h % S::HW;
+  } else {
+    h -= 2 * STRIP;
+    row = R + h / (2 * R);
+    const int c = h % (2 * R);
+    col = c < R ? c : kTX + c;
+  }
+}
+
+// Staged positions of a thread on the R-halo plane (its own outputs first):
+// shared-memory index (-1: no position).
+template <int R>
+__device__ __forceinline__ void split_stage_idx(int tid, int sidx[LTS<R>::NSTG]) {
+  using S = LTS<R>;
+  const int ox = tid & 31, oy0 = (tid >> 5) * S::NOUT;
+#pragma unroll
+  for (int i = 0; i < S::NSTG; ++i) {
+    int row, col;
+    if (i < S::NOUT) {
+      row = oy0 + i + R;
+      col = ox + R;
+    } else {
+      const int h = tid + (i - S::NOUT) * kLnccRHThreads;
+      if (h < S::NHALO) {
+        halo_pos_r<R>(h, row, col);
+      } else {
+        row = -1;
+        col = 0;
+      }
+    }
+    sidx[i] = row < 0 ? -1 : row * S::ZS + col;
+  }
+}
+
+// In-plane offsets of the staged positions for the tile at (x0, y0): -1
+// outside the grid (read as zero), -2 no position.
+template <int R>
+__device__ __forceinline__ void split_stage_off(const Geom& g, int x0, int y0, const int sidx[LTS<R>::NSTG],
+                                                int soff[LTS<R>::NSTG]) {
+  using S = LTS<R>;
+#pragma unroll
+  for (int i = 0; i < S::NSTG; ++i) {
+    soff[i] = -2;
+    if (sidx[i] >= 0) {
+      const int row = sidx[i] / S::ZS, col = sidx[i] - row * S::ZS;
+      const int x = x0 - R + col, y = y0 - R + row;
+      soff[i] = ((unsigned)x < (unsigned)g.fW && (unsigned)y < (unsigned)g.fH) ? y * g.fW + x : -1;
+    }
+  }
+}
+
+template <typename FT, int R>
+__global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_fw(const LnccArgs a) {
+  using S = LTS<R>;
+  constexpr int W = S::W, TY = S::TY, NOUT = S::NOUT, NSTG = S::NSTG, ZS = S::ZS, HH = S::HH, XG = S::XG;
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  __shared__ double wsum[kLnccRHThreads / 32];
+  float2* zP = reinterpret_cast<float2*>(sm);
+  float2* zQ = zP + HH * ZS;
+  float* zX = sm + 4 * HH * ZS;
+  float2* xP = reinterpret_cast<float2*>(sm + S::FW_Z);
+  float2* xQ = xP + HH * kTX;
+  float* xX = sm + S::FW_Z + 4 * HH * kTX;
+
+  const Geom& g = a.g;
+  const int tid = threadIdx.x;
+  const FT* __restrict__ F = static_cast<const FT*>(a.F);
+  const float inv_n = a.inv_n, eps = a.eps, gs = a.gscale;
+  const float2 ninv2 = make_float2(-inv_n, -inv_n);
+  const size_t plane = (size_t)g.fW * g.fH, N = (size_t)g.N;
+  float cc_acc = 0.0f;
+  if ((tid & 31) == 0) wsum[tid >> 5] = 0.0;
+  const int ox = tid & 31, oy0 = (tid >> 5) * NOUT;
+  int sidx[NSTG], soff[NSTG];
+  split_stage_idx<R>(tid, sidx);
+  float2 hist[W][NSTG];
+  float2 nxt[NSTG];
+  auto load_plane = [&](int zp) {
+    const bool zin = zp >= 0 && zp < g.fD;
+    const size_t base = (size_t)zp * plane;
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      float2 v = make_float2(0.0f, 0.0f);
+      if (zin && soff[i] >= 0) {
+        v.x = ld_stream(a.J + base + soff[i]);
+        v.y = ld_stream(F + base + soff[i]);
+      }
+      nxt[i] = v;
+    }
+  };
+
+  SegsFw seg(a);
+  int tx, ty, z0, z1;
+  while (seg.next(tx, ty, z0, z1)) {
+    const int x0 = tx * kTX, y0 = ty * TY;
+    const int nsteps = (z1 - z0) + 2 * R;
+    split_stage_off<R>(g, x0, y0, sidx, soff);
+    load_plane(z0 - R);
+    for (int s0 = 0; s0 < nsteps; s0 += W) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const int s = s0 + j;
+        if (s < nsteps) {
+          const int zi = z0 - R + s;  // newest plane; outputs at zc = zi - R
+          const bool out = s >= 2 * R;
+#pragma unroll
+          for (int i = 0; i < NSTG; ++i) hist[j][i] = nxt[i];
+          if (s + 1 < nsteps) load_plane(zi + 1);
+          if (out) {
+            // z sums over the register history -> halo plane
+#pragma unroll
+            for (int i = 0; i < NSTG; ++i) {
+              if (sidx[i] >= 0) {
+                float2 sP = hist[0][i];
+                float2 sQ = mul2(hist[0][i], hist[0][i]);
+                float sX = hist[0][i].x * hist[0][i].y;
+#pragma unroll
+                for (int q = 1; q < W; ++q) {
+                  sP = add2(sP, hist[q][i]);
+                  sQ = fma2(hist[q][i], hist[q][i], sQ);
+                  sX = fmaf(hist[q][i].x, hist[q][i].y, sX);
+                }
+                zP[sidx[i]] = sP;
+                zQ[sidx[i]] = sQ;
+                zX[sidx[i]] = sX;
+              }
+            }
+          }
+          __syncthreads();
+          if (out) {
+            // x sums onto the 32 output columns of every halo row, 2 per item
+            constexpr int NI = 2 + 2 * R;
+            for (int it = tid; it < HH * XG; it += kLnccRHThreads) {
+              const int row = it / XG, g2 = it - row * XG;
+              float2 vP[NI], vQ[NI];
+              float vX[NI];
+              const float4* sP4 = reinterpret_cast<const float4*>(zP + row * ZS + 2 * g2);
+              const float4* sQ4 = reinterpret_cast<const float4*>(zQ + row * ZS + 2 * g2);
+              const float2* sX2 = reinterpret_cast<const float2*>(zX + row * ZS + 2 * g2);
+#pragma unroll
+              for (int k = 0; k < NI / 2; ++k) {
+                const float4 p = sP4[k], q = sQ4[k];
+                const float2 x = sX2[k];
+                vP[2 * k] = make_float2(p.x, p.y);
+                vP[2 * k + 1] = make_float2(p.z, p.w);
+                vQ[2 * k] = make_float2(q.x, q.y);
+                vQ[2 * k + 1] = make_float2(q.z, q.w);
+                vX[2 * k] = x.x;
+                vX[2 * k + 1] = x.y;
+              }
+              float2 aP = vP[0], aQ = vQ[0];
+              float aX = vX[0];
+#pragma unroll
+              for (int k = 1; k <= 2 * R; ++k) {
+                aP = add2(aP, vP[k]);
+                aQ = add2(aQ, vQ[k]);
+                aX += vX[k];
+              }
+              const float2 bP = sub2(add2(aP, vP[2 * R + 1]), vP[0]);
+              const float2 bQ = sub2(add2(aQ, vQ[2 * R + 1]), vQ[0]);
+              const float bX = (aX + vX[2 * R + 1]) - vX[0];
+              *reinterpret_cast<float4*>(xP + row * kTX + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
+              *reinterpret_cast<float4*>(xQ + row * kTX + 2 * g2) = make_float4(aQ.x, aQ.y, bQ.x, bQ.y);
+              *reinterpret_cast<float2*>(xX + row * kTX + 2 * g2) = make_float2(aX, bX);
+            }
+          }
+          __syncthreads();
+          if (out) {
+            // y sums at the thread's own outputs, cc and the g-terms
+            const int zc = zi - R;
+            float2 vP[NOUT + 2 * R], vQ[NOUT + 2 * R];
+            float vX[NOUT + 2 * R];
+#pragma unroll
+            for (int k = 0; k < NOUT + 2 * R; ++k) {
+              vP[k] = xP[(oy0 + k) * kTX + ox];
+              vQ[k] = xQ[(oy0 + k) * kTX + ox];
+              vX[k] = xX[(oy0 + k) * kTX + ox];
+            }
+            float2 aP = vP[0], aQ = vQ[0];
+            float aX = vX[0];
+#pragma unroll
+            for (int k = 1; k <= 2 * R; ++k) {
+              aP = add2(aP, vP[k]);
+              aQ = add2(aQ, vQ[k]);
+              aX += vX[k];
+            }
+            const int X = x0 + ox;
+#pragma unroll
+            for (int k = 0; k < NOUT; ++k) {
+              if (k > 0) {
+                aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
+                aQ = sub2(add2(aQ, vQ[2 * R + k]), vQ[k - 1]);
+                aX = (aX + vX[2 * R + k]) - vX[k - 1];
+              }
+              const int Y = y0 + oy0 + k;
+              if (X < g.fW && Y < g.fH) {
+                // aP = (S_J, S_F), aQ = (S_JJ, S_FF), aX = S_FJ; variances clamped at 0
+                float2 v = fma2(mul2(aP, aP), ninv2, aQ);
+                v = make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f));
+                const float cross = fmaf(-aP.x * aP.y, inv_n, aX);
+                const float rD = rcp_approx(fmaf(v.x, v.y, eps));
+                const float A1 = 2.0f * cross * rD;
+                const float cc = cross * cross * rD;
+                const float A2 = cc * v.y * rD;
+                const size_t lin = ((size_t)zc * g.fH + Y) * g.fW + X;
+                a.gbuf[lin] = gs * (2.0f * A2 * aP.x - A1 * aP.y) * inv_n;
+                a.gbuf[N + lin] = -gs * A2;
+                a.gbuf[2 * N + lin] = gs * A1;
+                cc_acc += cc;
+              }
+            }
+          }
+          if ((s & 31) == 31) {
+            const float v = warp_sum(cc_acc);
+            if ((tid & 31) == 0) wsum[tid >> 5] += (double)v;
+            cc_acc = 0.0f;
+          }
+        }
+      }
+    }
+  }
+  {
+    const float v = warp_sum(cc_acc);
+    if ((tid & 31) == 0) wsum[tid >> 5] += (double)v;
+  }
+  __syncthreads();
+  if (tid < kPartialStride) {
+    double t = 0.0;
+    if (tid == kPCC)
+      for (int k = 0; k < kLnccRHThreads / 32; ++k) t += wsum[k];
+    a.partials[(size_t)blockIdx.x * kPartialStride + tid] = t;
+  }
+}
+
+template <typename FT, int BMAX, int R, bool DU>
+__global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_bw(const LnccArgs a) {
+  using S = LTS<R>;
+  constexpr int W = S::W, TY = S::TY, NOUT = S::NOUT, NSTG = S::NSTG, ZS = S::ZS, HH = S::HH, XG = S::XG;
+  constexpr bool MI = BMAX != 0;
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  __shared__ double wsum[kLnccRHThreads / 32][13];
+  float2* gP = reinterpret_cast<float2*>(sm);  // (g_J, g_JJ) on the halo plane
+  float* gX = sm + 2 * HH * ZS;                 // g_FJ
+  float2* gxP = reinterpret_cast<float2*>(sm + S::BW_G);
+  float* gxX = sm + S::BW_G + 2 * HH * kTX;
+  float* slope = sm + S::BW_TOTAL;  // LN_DU: three staging slots of an output plane's slope
+
+  const Geom& g = a.g;
+  const int tid = threadIdx.x;
+  const FT* __restrict__ F = static_cast<const FT*>(a.F);
+  const size_t plane = (size_t)g.fW * g.fH, N = (size_t)g.N;
+  if ((tid & 31) == 0)
+    for (int q = 0; q < 13; ++q) wsum[tid >> 5][q] = 0.0;
+  DuAcc<NOUT> dacc;
+  dacc.clear();
+  const int ox = tid & 31, oy0 = (tid >> 5) * NOUT;
+  int sidx[NSTG], soff[NSTG];
+  split_stage_idx<R>(tid, sidx);
+  float2 grP[W][NOUT];  // 2-D window sums of the g-terms at the own outputs, last w planes
+  float grX[W][NOUT];
+  float2 nP[NSTG];      // next g plane at the staged positions
+  float nX[NSTG];
+  float2 jf[NOUT], jfn[NOUT];  // (J, F) at the own outputs of this and of the next output plane
+  auto load_g = [&](int zp) {
+    const bool zin = zp >= 0 && zp < g.fD;
+    const size_t base = (size_t)zp * plane;
+#pragma unroll
+    for (int i = 0; i < NSTG; ++i) {
+      float2 v = make_float2(0.0f, 0.0f);
+      float x = 0.0f;
+      if (zin && soff[i] >= 0) {
+        const float* p = a.gbuf + base + soff[i];
+        v.x = ld_stream(p);
+        v.y = ld_stream(p + N);
+        x = ld_stream(p + 2 * N);
+      }
+      nP[i] = v;
+      nX[i] = x;
+    }
+  };
+
+  SegsBw seg(a);
+  int tx, ty, z0, z1;
+  while (seg.next(tx, ty, z0, z1)) {
+    const int x0 = tx * kTX, y0 = ty * TY;
+    const int nsteps = (z1 - z0) + 2 * R;
+    const bool full = x0 + kTX <= g.fW && y0 + TY <= g.fH && (g.fW & 3) == 0;
+    const size_t slope_plane = 3 * (size_t)g.fW * g.fH;
+    const float* slope_tile = DU ? a.dJdq + 3 * ((size_t)y0 * g.fW + x0) : nullptr;
+    int slot_rd = 2;
+    auto fold_du = [&] {
+      float cy[NOUT];
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) cy[k] = (float)(y0 + oy0 + k) - g.ctr[1];
+      dacc.fold(wsum[tid >> 5], tid & 31, (float)(x0 + ox) - g.ctr[0], cy);
+    };
+    // (J, F) at the own outputs of output plane zo (zero outside the grid)
+    auto load_jf = [&](int zo) {
+      const int X = x0 + ox;
+#pragma unroll
+      for (int k = 0; k < NOUT; ++k) {
+        const int Y = y0 + oy0 + k;
+        float2 v = make_float2(0.0f, 0.0f);
+        if (zo >= 0 && zo < g.fD && X < g.fW && Y < g.fH) {
+          const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
+          v.x = ld_stream(a.J + lin);
+          v.y = ld_stream(F + lin);
+        }
+        jfn[k] = v;
+      }
+    };
+    split_stage_off<R>(g, x0, y0, sidx, soff);
+    load_g(z0 - R);
+    for (int s0 = 0; s0 < nsteps; s0 += W) {
+#pragma unroll
+      for (int j = 0; j < W; ++j) {
+        const int s = s0 + j;
+        if (s < nsteps) {
+          const int zi = z0 - R + s;  // newest g plane; outputs at zo = zi - R
+          // the fetched plane goes to the halo plane; fetch the next, and the
+          // (J, F) and slope of the next step's output plane
+#pragma unroll
+          for (int i = 0; i < NSTG; ++i) {
+            if (sidx[i] >= 0) {
+              gP[sidx[i]] = nP[i];
+              gX[sidx[i]] = nX[i];
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < NOUT; ++k) jf[k] = jfn[k];
+          if (s + 1 < nsteps) load_g(zi + 1);
+          if (s + 1 >= 2 * R && s + 1 < nsteps) load_jf(zi + 1 - R);
+          if constexpr (DU) {
+            slot_rd = slot_rd == 2 ? 0 : slot_rd + 1;
+            const int sn = s + 1;
+            const float* src =
+                (sn >= 2 * R && sn < nsteps) ? slope_tile + (size_t)(zi + 1 - R) * slope_plane : nullptr;
+            stage_slope<TY, kLnccRHThreads>(slope + (slot_rd == 2 ? 0 : slot_rd + 1) * SlopeStage<TY>::SLOT, src,
+                                            g, x0, y0, full, tid);
+            slope_wait_prev();
+          }
+          __syncthreads();
+          {
+            // x sums of the g-terms onto the 32 output columns, 2 per item
+            constexpr int NI = 2 + 2 * R;
+            for (int it = tid; it < HH * XG; it += kLnccRHThreads) {
+              const int row = it / XG, g2 = it - row * XG;
+              float2 vP[NI];
+              float vX[NI];
+              const float4* sP4 = reinterpret_cast<const float4*>(gP + row * ZS + 2 * g2);
+              const float2* sX2 = reinterpret_cast<const float2*>(gX + row * ZS + 2 * g2);
+#pragma unroll
+              for (int k = 0; k < NI / 2; ++k) {
+                const float4 p = sP4[k];
+                const float2 x = sX2[k];
+                vP[2 * k] = make_float2(p.x, p.y);
+                vP[2 * k + 1] = make_float2(p.z, p.w);
+                vX[2 * k] = x.x;
+                vX[2 * k + 1] = x.y;
+              }
+              float2 aP = vP[0];
+              float aX = vX[0];
+#pragma unroll
+              for (int k = 1; k <= 2 * R; ++k) {
+                aP = add2(aP, vP[k]);
+                aX += vX[k];
+              }
+              const float2 bP = sub2(add2(aP, vP[2 * R + 1]), vP[0]);
+              const float bX = (aX + vX[2 * R + 1]) - vX[0];
+              *reinterpret_cast<float4*>(gxP + row * kTX + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
+              *reinterpret_cast<float2*>(gxX + row * kTX + 2 * g2) = make_float2(aX, bX);
+            }
+          }
+          __syncthreads();
+          {
+            // y sums at the own outputs -> register ring slot j
+            float2 vP[NOUT + 2 * R];
+            float vX[NOUT + 2 * R];
+#pragma unroll
+            for (int k = 0; k < NOUT + 2 * R; ++k) {
+              vP[k] = gxP[(oy0 + k) * kTX + ox];
+              vX[k] = gxX[(oy0 + k) * kTX + ox];
+            }
+            float2 aP = vP[0];
+            float aX = vX[0];
+#pragma unroll
+            for (int k = 1; k <= 2 * R; ++k) {
+              aP = add2(aP, vP[k]);
+              aX += vX[k];
+            }
+#pragma unroll
+            for (int k = 0; k < NOUT; ++k) {
+              if (k > 0) {
+                aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
+                aX = (aX + vX[2 * R + k]) - vX[k - 1];
+              }
+              grP[j][k] = aP;
+              grX[j][k] = aX;
+            }
+          }
+          // z sums over the ring (the w planes zo - R .. zo + R) -> dL/dJ at zo
+          if (s >= 2 * R) {
+            const int zo = zi - R;
+#pragma unroll
+            for (int k = 0; k < NOUT; ++k) {
+              float2 bP = grP[0][k];
+              float bX = grX[0][k];
+#pragma unroll
+              for (int q = 1; q < W; ++q) {
+                bP = add2(bP, grP[q][k]);
+                bX += grX[q][k];
+              }
+              const int X = x0 + ox, Y = y0 + oy0 + k;
+              if (X < g.fW && Y < g.fH) {
+                const size_t lin = ((size_t)zo * g.fH + Y) * g.fW + X;
+                const float jv = jf[k].x, fv = jf[k].y;
+                float gv = fmaf(fv, bX, fmaf(2.0f * jv, bP.y, bP.x));
+                if (MI) gv += mi_grad_ln<(MI ? BMAX : 32)>(a.T, a.bf, a.bj, fv, jv);
+                if constexpr (DU) {
+                  dacc.add(a, k, lin, slope + slot_rd * SlopeStage<TY>::SLOT + (oy0 + k) * SlopeStage<TY>::ROW + 3 * ox,
+                           (float)zo - g.ctr[2], gv);
+                } else if (a.dJ) {
+                  a.dJ[lin] = gv;
+                }
+              }
+            }
+          }
+          if constexpr (DU) {
+            if ((s & 31) == 31) fold_du();
+          }
+        }
+      }
+    }
+    if constexpr (DU) fold_du();  // the next segment has other columns and rows
+  }
+  if constexpr (DU) {
+    __syncthreads();
+    if (tid < 12) {
+      double t = 0.0;
+      for (int k = 0; k < kLnccRHThreads / 32; ++k) t += wsum[k][tid];
+      a.partials[(size_t)blockIdx.x * kPartialStride + tid] = t;
+    }
+  }
+}
+
 template <int R, bool DU>
 static size_t smem_of() {
   const size_t stage = (DU && !kLnccRecompute) ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0;
@@ -722,6 +1270,44 @@ static cudaError_t run_lncc(const LnccArgs& a, int grid, cudaStream_t s, int* oc
   return cudaGetLastError();
 }
 
+// Split variant: the forward and the backward kernel on the same grid (the
+// forward one writes every CTA's whole partial record, the backward one adds
+// the affine slots).  occ != nullptr: the smaller of their occupancies.
+template <typename FT, int BMAX, int R, bool DU>
+static cudaError_t run_split(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
+  auto k1 = k_lncc_fw<FT, R>;
+  auto k2 = k_lncc_bw<FT, BMAX, R, DU>;
+  const size_t m1 = (size_t)LTS<R>::FW_TOTAL * sizeof(float);
+  const size_t m2 = ((size_t)LTS<R>::BW_TOTAL + (DU ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0)) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m1);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m2);
+  if (e != cudaSuccess) return e;
+  if (occ) {
+    int o1 = 0, o2 = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o1, k1, kLnccRHThreads, m1);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, k2, kLnccRHThreads, m2);
+    *occ = o1 < o2 ? o1 : o2;
+    return e;
+  }
+  note_launch_begin("k_lncc_fw", s);
+  k1<<<grid, kLnccRHThreads, m1, s>>>(a);
+  note_launch_end(s);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  note_launch_begin("k_lncc_bw", s);
+  k2<<<grid, kLnccRHThreads, m2, s>>>(a);
+  note_launch_end(s);
+  return cudaGetLastError();
+}
+
+template <typename FT, int BMAX, int R, bool DU>
+static cudaError_t run_any(const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
+  if constexpr (kLnccSplit && !kLnccRecompute)
+    return run_split<FT, BMAX, R, DU>(a, grid, s, occ);
+  else
+    return run_lncc<FT, BMAX, R, DU>(a, grid, s, occ);
+}
+
 template <int R>
 static cudaError_t dispatch_r(int mode, int ft, int bmax, const LnccArgs& a, int grid, cudaStream_t s, int* occ) {
   // LN_DJ (the stand-alone LNCC gradient) carries no MI term; LN_DU (the
@@ -730,13 +1316,13 @@ static cudaError_t dispatch_r(int mode, int ft, int bmax, const LnccArgs& a, int
   if (mode == LN_DJ && bmax != 0) return e;
   FFDP_DT_SWITCH(ft, FT, {
     if (mode == LN_DJ)
-      e = run_lncc<FT, 0, R, false>(a, grid, s, occ);
+      e = run_any<FT, 0, R, false>(a, grid, s, occ);
     else if (bmax == 0)
-      e = run_lncc<FT, 0, R, true>(a, grid, s, occ);
+      e = run_any<FT, 0, R, true>(a, grid, s, occ);
     else if (bmax == 32)
-      e = run_lncc<FT, 32, R, true>(a, grid, s, occ);
+      e = run_any<FT, 32, R, true>(a, grid, s, occ);
     else
-      e = run_lncc<FT, 64, R, true>(a, grid, s, occ);
+      e = run_any<FT, 64, R, true>(a, grid, s, occ);
   });
   return e;
 }
