@@ -239,10 +239,13 @@ __global__ void __launch_bounds__(kWideThreads) k_wide_cc(const WideArgs a) {
   cc_d = warp_sum_d(cc_d);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = cc_d;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  // the whole record: cc, zeros elsewhere (the last pass adds the affine
+  // slots in the objective)
+  if (threadIdx.x < kPartialStride) {
     double t = 0.0;
-    for (int w = 0; w < kWideThreads / 32; ++w) t += red[w];
-    a.partials[(size_t)blockIdx.x * kPartialStride + kPCC] = t;
+    if (threadIdx.x == kPCC)
+      for (int w = 0; w < kWideThreads / 32; ++w) t += red[w];
+    a.partials[(size_t)blockIdx.x * kPartialStride + threadIdx.x] = t;
   }
 }
 
