@@ -775,26 +775,56 @@ struct LTS {
   static constexpr int NHALO = HH * HW - NCORE;
   static constexpr int NEXTRA = (NHALO + kLnccRHThreads - 1) / kLnccRHThreads;
   static constexpr int NSTG = NOUT + NEXTRA;
-  static constexpr int XG = kTX / 2;  // 2-output x items per row
   static_assert(NOUT * kLnccRHThreads == NCORE, "outputs per thread");
-  // row stride of the halo plane in the x pass: a row continues the bank
-  // sequence of the previous one for the 16-byte pair loads and the 8-byte
-  // scalar-pair loads (as in the register-history kernel)
-  static constexpr int zs_of(int s) { return (s % 2 == 0 && ((s / 2 - XG) % 16 + 16) % 16 == 0) ? s : zs_of(s + 1); }
-  static constexpr int ZS = zs_of(HW);
+  // The forward x pass takes items of four outputs, one per thread in a
+  // single round (rows padded to RB, a multiple of 8, per column group),
+  // consecutive threads on consecutive rows; the backward one, whose thread
+  // state leaves no room for eight pairs at once, items of two outputs
+  // (consecutive threads along a row, two rounds).  The row strides are odd
+  // multiples of 16 bytes (halo plane: 66 pairs; x sums: 34 pairs, 36
+  // scalars), so that the eight lanes of every 16-byte access phase fall on
+  // distinct banks in both.
+  static constexpr int ZS = 66, XS = 34, XSX = 36;
+  static_assert(HW <= ZS, "halo row fits the row stride");
+  static constexpr int XG4 = kTX / 4;
+  static constexpr int RB = (HH + 7) / 8 * 8;
+  static_assert(RB * XG4 <= kLnccRHThreads, "x items: one round");
   // forward: z sums (5 channels) on the halo plane, x sums (5) on HH x 32
   static constexpr int FW_Z = HH * ZS * 5;
-  static constexpr int FW_TOTAL = FW_Z + HH * kTX * 5;
+  static constexpr int FW_TOTAL = FW_Z + HH * (4 * XS + XSX);
   // backward: g-terms (3 channels) on the halo plane, x sums (3) on HH x 32
   static constexpr int BW_G = HH * ZS * 3;
-  static constexpr int BW_TOTAL = BW_G + HH * kTX * 3;
+  static constexpr int BW_TOTAL = BW_G + HH * (2 * XS + XSX);
+  static_assert(FW_Z % 4 == 0 && BW_G % 4 == 0 && BW_TOTAL % 4 == 0, "16-byte aligned regions");
 };
+
+// Box sums of width 2R + 1 at four consecutive outputs from v[0 .. 2R + 3],
+// as sums of shared partial sums (no running add-and-subtract: the moments'
+// variances cancel, and every subtraction of a sliding window would add its
+// rounding error to them).
+__device__ __forceinline__ float addv(float a, float b) { return a + b; }
+__device__ __forceinline__ float2 addv(float2 a, float2 b) { return add2(a, b); }
+template <int R, typename T>
+__device__ __forceinline__ void win4(const T* v, T o[4]) {
+  const T a = addv(v[1], v[2]);                 // in windows 0, 1
+  const T b = addv(v[2 * R + 1], v[2 * R + 2]);  // in windows 2, 3
+  o[0] = addv(v[0], a);
+  o[1] = addv(a, v[2 * R + 1]);
+  o[2] = addv(v[2], b);
+  o[3] = addv(b, v[2 * R + 3]);
+  if constexpr (R >= 2) {
+    T c = v[3];  // v[3 .. 2R]: in all four windows
+#pragma unroll
+    for (int k = 4; k <= 2 * R; ++k) c = addv(c, v[k]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = addv(o[q], c);
+  }
+}
 
 // Halo position h (outside the output core) of the R-halo plane: the top and
 // bottom R rows in full, then the R columns on either side of the core rows.
-template <int R>
+template <int R, class S>
 __device__ __forceinline__ void halo_pos_r(int h, int& row, int& col) {
-  using S = LTS<R>;
   constexpr int STRIP = R * S::HW;
   if (h < STRIP) {
     row = h / S::HW;
@@ -813,9 +843,8 @@ __device__ __forceinline__ void halo_pos_r(int h, int& row, int& col) {
 
 // Staged positions of a thread on the R-halo plane (its own outputs first):
 // shared-memory index (-1: no position).
-template <int R>
-__device__ __forceinline__ void split_stage_idx(int tid, int sidx[LTS<R>::NSTG]) {
-  using S = LTS<R>;
+template <int R, class S>
+__device__ __forceinline__ void split_stage_idx(int tid, int sidx[S::NSTG]) {
   const int ox = tid & 31, oy0 = (tid >> 5) * S::NOUT;
 #pragma unroll
   for (int i = 0; i < S::NSTG; ++i) {
@@ -826,7 +855,7 @@ __device__ __forceinline__ void split_stage_idx(int tid, int sidx[LTS<R>::NSTG])
     } else {
       const int h = tid + (i - S::NOUT) * kLnccRHThreads;
       if (h < S::NHALO) {
-        halo_pos_r<R>(h, row, col);
+        halo_pos_r<R, S>(h, row, col);
       } else {
         row = -1;
         col = 0;
@@ -838,10 +867,9 @@ __device__ __forceinline__ void split_stage_idx(int tid, int sidx[LTS<R>::NSTG])
 
 // In-plane offsets of the staged positions for the tile at (x0, y0): -1
 // outside the grid (read as zero), -2 no position.
-template <int R>
-__device__ __forceinline__ void split_stage_off(const Geom& g, int x0, int y0, const int sidx[LTS<R>::NSTG],
-                                                int soff[LTS<R>::NSTG]) {
-  using S = LTS<R>;
+template <int R, class S>
+__device__ __forceinline__ void split_stage_off(const Geom& g, int x0, int y0, const int sidx[S::NSTG],
+                                                int soff[S::NSTG]) {
 #pragma unroll
   for (int i = 0; i < S::NSTG; ++i) {
     soff[i] = -2;
@@ -856,16 +884,17 @@ __device__ __forceinline__ void split_stage_off(const Geom& g, int x0, int y0, c
 template <typename FT, int R>
 __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_fw(const LnccArgs a) {
   using S = LTS<R>;
-  constexpr int W = S::W, TY = S::TY, NOUT = S::NOUT, NSTG = S::NSTG, ZS = S::ZS, HH = S::HH, XG = S::XG;
+  constexpr int W = S::W, TY = S::TY, NOUT = S::NOUT, NSTG = S::NSTG, ZS = S::ZS, HH = S::HH;
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
   __shared__ double wsum[kLnccRHThreads / 32];
   float2* zP = reinterpret_cast<float2*>(sm);
   float2* zQ = zP + HH * ZS;
   float* zX = sm + 4 * HH * ZS;
+  constexpr int XS = S::XS, XSX = S::XSX, RB = S::RB;
   float2* xP = reinterpret_cast<float2*>(sm + S::FW_Z);
-  float2* xQ = xP + HH * kTX;
-  float* xX = sm + S::FW_Z + 4 * HH * kTX;
+  float2* xQ = xP + HH * XS;
+  float* xX = sm + S::FW_Z + 4 * HH * XS;
 
   const Geom& g = a.g;
   const int tid = threadIdx.x;
@@ -877,7 +906,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_f
   if ((tid & 31) == 0) wsum[tid >> 5] = 0.0;
   const int ox = tid & 31, oy0 = (tid >> 5) * NOUT;
   int sidx[NSTG], soff[NSTG];
-  split_stage_idx<R>(tid, sidx);
+  split_stage_idx<R, S>(tid, sidx);
   float2 hist[W][NSTG];
   float2 nxt[NSTG];
   auto load_plane = [&](int zp) {
@@ -899,7 +928,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_f
   while (seg.next(tx, ty, z0, z1)) {
     const int x0 = tx * kTX, y0 = ty * TY;
     const int nsteps = (z1 - z0) + 2 * R;
-    split_stage_off<R>(g, x0, y0, sidx, soff);
+    split_stage_off<R, S>(g, x0, y0, sidx, soff);
     load_plane(z0 - R);
     for (int s0 = 0; s0 < nsteps; s0 += W) {
 #pragma unroll
@@ -933,40 +962,39 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_f
           }
           __syncthreads();
           if (out) {
-            // x sums onto the 32 output columns of every halo row, 2 per item
-            constexpr int NI = 2 + 2 * R;
-            for (int it = tid; it < HH * XG; it += kLnccRHThreads) {
-              const int row = it / XG, g2 = it - row * XG;
-              float2 vP[NI], vQ[NI];
-              float vX[NI];
-              const float4* sP4 = reinterpret_cast<const float4*>(zP + row * ZS + 2 * g2);
-              const float4* sQ4 = reinterpret_cast<const float4*>(zQ + row * ZS + 2 * g2);
-              const float2* sX2 = reinterpret_cast<const float2*>(zX + row * ZS + 2 * g2);
+            // x sums onto the 32 output columns of every halo row, 4 per item
+            // (one channel pair at a time, to bound the live values)
+            constexpr int NI = 4 + 2 * R;
+            const int row = tid % RB, g4 = tid / RB;
+            if (g4 < S::XG4 && row < HH) {
+              auto pair4 = [&](const float2* src, float2* dst) {
+                const float4* s4 = reinterpret_cast<const float4*>(src + row * ZS + 4 * g4);
+                float2 v[NI];
+#pragma unroll
+                for (int k = 0; k < NI / 2; ++k) {
+                  const float4 p = s4[k];
+                  v[2 * k] = make_float2(p.x, p.y);
+                  v[2 * k + 1] = make_float2(p.z, p.w);
+                }
+                float2 o[4];
+                win4<R>(v, o);
+                float4* d4 = reinterpret_cast<float4*>(dst + row * XS + 4 * g4);
+                d4[0] = make_float4(o[0].x, o[0].y, o[1].x, o[1].y);
+                d4[1] = make_float4(o[2].x, o[2].y, o[3].x, o[3].y);
+              };
+              pair4(zP, xP);
+              pair4(zQ, xQ);
+              const float2* s2 = reinterpret_cast<const float2*>(zX + row * ZS + 4 * g4);
+              float v[NI];
 #pragma unroll
               for (int k = 0; k < NI / 2; ++k) {
-                const float4 p = sP4[k], q = sQ4[k];
-                const float2 x = sX2[k];
-                vP[2 * k] = make_float2(p.x, p.y);
-                vP[2 * k + 1] = make_float2(p.z, p.w);
-                vQ[2 * k] = make_float2(q.x, q.y);
-                vQ[2 * k + 1] = make_float2(q.z, q.w);
-                vX[2 * k] = x.x;
-                vX[2 * k + 1] = x.y;
+                const float2 x = s2[k];
+                v[2 * k] = x.x;
+                v[2 * k + 1] = x.y;
               }
-              float2 aP = vP[0], aQ = vQ[0];
-              float aX = vX[0];
-#pragma unroll
-              for (int k = 1; k <= 2 * R; ++k) {
-                aP = add2(aP, vP[k]);
-                aQ = add2(aQ, vQ[k]);
-                aX += vX[k];
-              }
-              const float2 bP = sub2(add2(aP, vP[2 * R + 1]), vP[0]);
-              const float2 bQ = sub2(add2(aQ, vQ[2 * R + 1]), vQ[0]);
-              const float bX = (aX + vX[2 * R + 1]) - vX[0];
-              *reinterpret_cast<float4*>(xP + row * kTX + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
-              *reinterpret_cast<float4*>(xQ + row * kTX + 2 * g2) = make_float4(aQ.x, aQ.y, bQ.x, bQ.y);
-              *reinterpret_cast<float2*>(xX + row * kTX + 2 * g2) = make_float2(aX, bX);
+              float o[4];
+              win4<R>(v, o);
+              *reinterpret_cast<float4*>(xX + row * XSX + 4 * g4) = make_float4(o[0], o[1], o[2], o[3]);
             }
           }
           __syncthreads();
@@ -977,25 +1005,32 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_f
             float vX[NOUT + 2 * R];
 #pragma unroll
             for (int k = 0; k < NOUT + 2 * R; ++k) {
-              vP[k] = xP[(oy0 + k) * kTX + ox];
-              vQ[k] = xQ[(oy0 + k) * kTX + ox];
-              vX[k] = xX[(oy0 + k) * kTX + ox];
+              vP[k] = xP[(oy0 + k) * XS + ox];
+              vQ[k] = xQ[(oy0 + k) * XS + ox];
+              vX[k] = xX[(oy0 + k) * XSX + ox];
             }
-            float2 aP = vP[0], aQ = vQ[0];
-            float aX = vX[0];
+            // window sums at the NOUT outputs: the rows shared by all of them
+            // once, then each output's own (no sliding; see win4)
+            float2 cP = vP[NOUT - 1], cQ = vQ[NOUT - 1];
+            float cX = vX[NOUT - 1];
 #pragma unroll
-            for (int k = 1; k <= 2 * R; ++k) {
-              aP = add2(aP, vP[k]);
-              aQ = add2(aQ, vQ[k]);
-              aX += vX[k];
+            for (int k = NOUT; k <= 2 * R; ++k) {
+              cP = add2(cP, vP[k]);
+              cQ = add2(cQ, vQ[k]);
+              cX += vX[k];
             }
             const int X = x0 + ox;
 #pragma unroll
             for (int k = 0; k < NOUT; ++k) {
-              if (k > 0) {
-                aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
-                aQ = sub2(add2(aQ, vQ[2 * R + k]), vQ[k - 1]);
-                aX = (aX + vX[2 * R + k]) - vX[k - 1];
+              float2 aP = cP, aQ = cQ;
+              float aX = cX;
+#pragma unroll
+              for (int r = k; r < k + 2 * R + 1; ++r) {
+                if (r < NOUT - 1 || r > 2 * R) {
+                  aP = add2(aP, vP[r]);
+                  aQ = add2(aQ, vQ[r]);
+                  aX += vX[r];
+                }
               }
               const int Y = y0 + oy0 + k;
               if (X < g.fW && Y < g.fH) {
@@ -1040,7 +1075,8 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_f
 template <typename FT, int BMAX, int R, bool DU>
 __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_bw(const LnccArgs a) {
   using S = LTS<R>;
-  constexpr int W = S::W, TY = S::TY, NOUT = S::NOUT, NSTG = S::NSTG, ZS = S::ZS, HH = S::HH, XG = S::XG;
+  constexpr int W = S::W, TY = S::TY, NOUT = S::NOUT, NSTG = S::NSTG, ZS = S::ZS, HH = S::HH;
+  constexpr int XS = S::XS, XSX = S::XSX;
   constexpr bool MI = BMAX != 0;
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
@@ -1048,7 +1084,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_b
   float2* gP = reinterpret_cast<float2*>(sm);  // (g_J, g_JJ) on the halo plane
   float* gX = sm + 2 * HH * ZS;                 // g_FJ
   float2* gxP = reinterpret_cast<float2*>(sm + S::BW_G);
-  float* gxX = sm + S::BW_G + 2 * HH * kTX;
+  float* gxX = sm + S::BW_G + 2 * HH * XS;
   float* slope = sm + S::BW_TOTAL;  // LN_DU: three staging slots of an output plane's slope
 
   const Geom& g = a.g;
@@ -1061,7 +1097,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_b
   dacc.clear();
   const int ox = tid & 31, oy0 = (tid >> 5) * NOUT;
   int sidx[NSTG], soff[NSTG];
-  split_stage_idx<R>(tid, sidx);
+  split_stage_idx<R, S>(tid, sidx);
   float2 grP[W][NOUT];  // 2-D window sums of the g-terms at the own outputs, last w planes
   float grX[W][NOUT];
   float2 nP[NSTG];      // next g plane at the staged positions
@@ -1115,7 +1151,7 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_b
         jfn[k] = v;
       }
     };
-    split_stage_off<R>(g, x0, y0, sidx, soff);
+    split_stage_off<R, S>(g, x0, y0, sidx, soff);
     load_g(z0 - R);
     for (int s0 = 0; s0 < nsteps; s0 += W) {
 #pragma unroll
@@ -1149,32 +1185,31 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_b
           {
             // x sums of the g-terms onto the 32 output columns, 2 per item
             constexpr int NI = 2 + 2 * R;
-            for (int it = tid; it < HH * XG; it += kLnccRHThreads) {
-              const int row = it / XG, g2 = it - row * XG;
+            for (int it = tid; it < HH * (kTX / 2); it += kLnccRHThreads) {
+              const int row = it / (kTX / 2), g2 = it - row * (kTX / 2);
+              const float4* s4 = reinterpret_cast<const float4*>(gP + row * ZS + 2 * g2);
+              const float2* s2 = reinterpret_cast<const float2*>(gX + row * ZS + 2 * g2);
               float2 vP[NI];
               float vX[NI];
-              const float4* sP4 = reinterpret_cast<const float4*>(gP + row * ZS + 2 * g2);
-              const float2* sX2 = reinterpret_cast<const float2*>(gX + row * ZS + 2 * g2);
 #pragma unroll
               for (int k = 0; k < NI / 2; ++k) {
-                const float4 p = sP4[k];
-                const float2 x = sX2[k];
+                const float4 p = s4[k];
+                const float2 x = s2[k];
                 vP[2 * k] = make_float2(p.x, p.y);
                 vP[2 * k + 1] = make_float2(p.z, p.w);
                 vX[2 * k] = x.x;
                 vX[2 * k + 1] = x.y;
               }
-              float2 aP = vP[0];
-              float aX = vX[0];
+              float2 cP = vP[1];
+              float cX = vX[1];
 #pragma unroll
-              for (int k = 1; k <= 2 * R; ++k) {
-                aP = add2(aP, vP[k]);
-                aX += vX[k];
+              for (int k = 2; k <= 2 * R; ++k) {
+                cP = add2(cP, vP[k]);
+                cX += vX[k];
               }
-              const float2 bP = sub2(add2(aP, vP[2 * R + 1]), vP[0]);
-              const float bX = (aX + vX[2 * R + 1]) - vX[0];
-              *reinterpret_cast<float4*>(gxP + row * kTX + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
-              *reinterpret_cast<float2*>(gxX + row * kTX + 2 * g2) = make_float2(aX, bX);
+              const float2 aP = add2(vP[0], cP), bP = add2(cP, vP[2 * R + 1]);
+              *reinterpret_cast<float4*>(gxP + row * XS + 2 * g2) = make_float4(aP.x, aP.y, bP.x, bP.y);
+              *reinterpret_cast<float2*>(gxX + row * XSX + 2 * g2) = make_float2(vX[0] + cX, cX + vX[2 * R + 1]);
             }
           }
           __syncthreads();
@@ -1184,21 +1219,27 @@ __global__ void __launch_bounds__(kLnccRHThreads, FFDP_LNCC_SPLIT_MINB) k_lncc_b
             float vX[NOUT + 2 * R];
 #pragma unroll
             for (int k = 0; k < NOUT + 2 * R; ++k) {
-              vP[k] = gxP[(oy0 + k) * kTX + ox];
-              vX[k] = gxX[(oy0 + k) * kTX + ox];
+              vP[k] = gxP[(oy0 + k) * XS + ox];
+              vX[k] = gxX[(oy0 + k) * XSX + ox];
             }
-            float2 aP = vP[0];
-            float aX = vX[0];
+            // the rows shared by all NOUT outputs once, then each output's own
+            float2 cP = vP[NOUT - 1];
+            float cX = vX[NOUT - 1];
 #pragma unroll
-            for (int k = 1; k <= 2 * R; ++k) {
-              aP = add2(aP, vP[k]);
-              aX += vX[k];
+            for (int k = NOUT; k <= 2 * R; ++k) {
+              cP = add2(cP, vP[k]);
+              cX += vX[k];
             }
 #pragma unroll
             for (int k = 0; k < NOUT; ++k) {
-              if (k > 0) {
-                aP = sub2(add2(aP, vP[2 * R + k]), vP[k - 1]);
-                aX = (aX + vX[2 * R + k]) - vX[k - 1];
+              float2 aP = cP;
+              float aX = cX;
+#pragma unroll
+              for (int r = k; r < k + 2 * R + 1; ++r) {
+                if (r < NOUT - 1 || r > 2 * R) {
+                  aP = add2(aP, vP[r]);
+                  aX += vX[r];
+                }
               }
               grP[j][k] = aP;
               grX[j][k] = aX;
@@ -1278,7 +1319,7 @@ static cudaError_t run_split(const LnccArgs& a, int grid, cudaStream_t s, int* o
   auto k1 = k_lncc_fw<FT, R>;
   auto k2 = k_lncc_bw<FT, BMAX, R, DU>;
   const size_t m1 = (size_t)LTS<R>::FW_TOTAL * sizeof(float);
-  const size_t m2 = ((size_t)LTS<R>::BW_TOTAL + (DU ? (size_t)SlopeStage<LT<R>::TY>::FLOATS : 0)) * sizeof(float);
+  const size_t m2 = ((size_t)LTS<R>::BW_TOTAL + (DU ? (size_t)SlopeStage<LTS<R>::TY>::FLOATS : 0)) * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m1);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)m2);
   if (e != cudaSuccess) return e;
